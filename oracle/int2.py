@@ -1,0 +1,170 @@
+"""Rotation fit, clip thresholds and grouped INT2 codes (oracle, test
+infrastructure only).
+
+Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10),
+maintainer reply, "How the rotation adapts to the latent":
+  * estimate the latent covariance Sigma = c^T c over the calibration tokens;
+  * eigendecompose it (eigh) and order eigenvectors by ascending eigenvalue, so
+    that low-variance directions fall in the same INT2 groups;
+  * the result is one [r x r] orthogonal matrix per layer;
+  * the clip thresholds are fit on the rotated latent;
+  * the cache holds the rotated + quantised latent and the up-projection runs on
+    the dequantised latent.
+
+Readings adopted where the page is silent:
+  * Sigma is exactly c^T c (no centring, no 1/N; 1/N would not move the
+    eigenvectors).
+  * Eigenvector signs: each column is flipped so that its largest-magnitude
+    entry is positive.
+  * Rotation is applied as a row vector: y = c . R, so column j of R is the
+    j-th eigenvector (ascending) and group 0 holds the lowest-variance dims.
+  * Clip threshold of group g: the 99th percentile (linear interpolation) of
+    |y| over all calibration tokens and the group's dims, fp64, stored fp32.
+  * Encoding, packing and dequantisation: ``int2_quant.c`` (fp32 order fixed
+    there).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+from . import attention
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "int2_quant.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle_int2.so")
+_lib = None
+
+
+def build_native(force: bool = False) -> str:
+    """Compile the plain-C encoder with gcc (no fused multiply-add contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _native():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build_native())
+        f32p = ctypes.POINTER(ctypes.c_float)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.oracle_rotate_chain.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_int, f32p]
+        lib.oracle_int2_encode.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, u8p, u16p]
+        lib.oracle_int2_decode.argtypes = [u8p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, f32p]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a, ty):
+    return a.ctypes.data_as(ctypes.POINTER(ty))
+
+
+# ---------------------------------------------------------------- calibration
+
+def latent_covariance(X: np.ndarray) -> np.ndarray:
+    """Sigma = X^T X over calibration latents X [N, r] (fp64)."""
+    X = np.asarray(X, dtype=np.float64)
+    return X.T @ X
+
+
+def fit_rotation(X: np.ndarray):
+    """Per-layer rotation: eigenvectors of Sigma, ascending eigenvalue.
+
+    Returns (R [r, r] fp64 with columns = eigenvectors, eigenvalues ascending).
+    """
+    Sigma = latent_covariance(X)
+    w, V = np.linalg.eigh(Sigma)               # ascending by contract of eigh
+    order = np.argsort(w, kind="stable")       # explicit: ascending eigenvalue
+    w, V = w[order], V[:, order]
+    idx = np.argmax(np.abs(V), axis=0)
+    signs = np.sign(V[idx, np.arange(V.shape[1])])
+    signs[signs == 0] = 1.0
+    return V * signs[None, :], w
+
+
+def clip_thresholds(X: np.ndarray, R: np.ndarray, group: int = 32, pct: float = 99.0) -> np.ndarray:
+    """T_g = pct-th percentile of |X R| over the calibration tokens and group g's dims."""
+    Y = np.asarray(X, dtype=np.float64) @ np.asarray(R, dtype=np.float64)
+    r = Y.shape[1]
+    return np.array([np.percentile(np.abs(Y[:, g * group:(g + 1) * group]), pct)
+                     for g in range(r // group)], dtype=np.float64)
+
+
+# ---------------------------------------------------------------- encoder (C)
+
+def rotate_fp32(c: np.ndarray, R32: np.ndarray) -> np.ndarray:
+    """y = c . R as the fp32 fused chain of the encoding definition."""
+    c = np.ascontiguousarray(c, dtype=np.float32)
+    R32 = np.ascontiguousarray(R32, dtype=np.float32)
+    n, r = c.shape
+    y = np.empty((n, r), dtype=np.float32)
+    _native().oracle_rotate_chain(_ptr(c, ctypes.c_float), _ptr(R32, ctypes.c_float), n, r,
+                                  _ptr(y, ctypes.c_float))
+    return y
+
+
+def encode(y: np.ndarray, T32: np.ndarray, group: int = 32):
+    """Rotated rows y [n, r] -> (codes [n, r/4] u8, sz [n, r/group, 2] fp16 bits)."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T32 = np.ascontiguousarray(T32, dtype=np.float32)
+    n, r = y.shape
+    codes = np.zeros((n, r // 4), dtype=np.uint8)
+    sz = np.zeros((n, r // group, 2), dtype=np.uint16)
+    _native().oracle_int2_encode(_ptr(y, ctypes.c_float), _ptr(T32, ctypes.c_float), n, r, group,
+                                 _ptr(codes, ctypes.c_uint8), _ptr(sz, ctypes.c_uint16))
+    return codes, sz
+
+
+def quantize(c: np.ndarray, R32: np.ndarray, T32: np.ndarray, group: int = 32):
+    """Rotate then encode: the full append-side transform of one batch of latents."""
+    return encode(rotate_fp32(c, R32), T32, group)
+
+
+def decode(codes: np.ndarray, sz: np.ndarray, group: int = 32) -> np.ndarray:
+    """Dequantised rotated latent c^ [n, r] fp32: fmaf(code, s, z)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sz = np.ascontiguousarray(sz, dtype=np.uint16)
+    n = codes.shape[0]
+    r = codes.shape[1] * 4
+    out = np.empty((n, r), dtype=np.float32)
+    _native().oracle_int2_decode(_ptr(codes, ctypes.c_uint8), _ptr(sz, ctypes.c_uint16), n, r, group,
+                                 _ptr(out, ctypes.c_float))
+    return out
+
+
+def unpack_codes(codes: np.ndarray) -> np.ndarray:
+    """[n, r/4] u8 -> [n, r] integer codes, element e at bits 2*(e%4) of byte e/4."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    shifts = np.array([0, 2, 4, 6], dtype=np.uint8)
+    return ((codes[:, :, None] >> shifts[None, None, :]) & 3).reshape(codes.shape[0], -1)
+
+
+# ---------------------------------------------------------------- attention
+
+def attention_rotated(q: np.ndarray, Chat: np.ndarray, KR: np.ndarray, R: np.ndarray,
+                      W_UV: np.ndarray, scale: float):
+    """Absorbed attention against a rotated latent c^ (fp64 after dequantisation).
+
+    Scores use the rotated query q~_lat . R (so that q~_lat . c = (q~_lat R) . (c R));
+    the latent output is taken back with o_lat = o_rot . R^T before W_UV.
+    q [q_len, H, r + d_R], Chat [L, r] (rotated basis), R [r, r].
+    """
+    R = np.asarray(R, dtype=np.float64)
+    r = R.shape[0]
+    q = q.astype(np.float64)
+    q_rot = np.concatenate([q[..., :r] @ R, q[..., r:]], axis=-1)
+    _, lse, o_rot = attention.absorbed(q_rot, Chat, KR, np.zeros((q.shape[1], r, 1)), scale,
+                                       return_latent=True)
+    o_lat = o_rot @ R.T
+    out = np.einsum("qhr,hrv->qhv", o_lat, np.asarray(W_UV, dtype=np.float64))
+    return out, lse

@@ -1,0 +1,335 @@
+"""Pins for the CPU oracle: facts the pages print, closed forms, invariants and
+brute force, each chosen so that a dropped term, a wrong index or a transposed
+operand in the oracle fails at least one of them. CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import attention, layout
+from oracle import int2 as oint2
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = (s.strip() for s in line.split("="))
+            vals[k] = float(v)
+    return vals
+
+
+# ----------------------------------------------------------------- footprint
+
+def test_footprint_matches_pages():
+    g = _golden("footprint.txt")
+    # DeepSeek V2/V3/V3.2: kv_lora_rank 512 + qk_rope_head_dim 64.
+    assert layout.footprint_elems(512, 64) == g["deepseek_v3_latent_elems_per_layer"]
+    # GLM-5.3-Flash: linear layers hold nothing, 11 latent layers x 640 x 2 B.
+    types = ["linear_attention"] * int(g["glm53_linear_layers"]) + ["full_attention"] * int(g["glm53_latent_layers"])
+    assert len(types) == g["glm53_layers_total"]
+    per_tok = layout.kv_bytes_per_token(types, 512, 64, 64, bytes_per_elem=int(g["glm53_bytes_per_elem"]))
+    assert layout.footprint_elems(512, 64, 64) == g["glm53_elems_per_latent_layer"]
+    assert per_tok == g["glm53_bytes_per_token"]
+    assert abs(per_tok * 2**20 / 1e9 - g["glm53_gb_at_1m_tokens"]) < 0.5
+    assert abs(g["glm53_after_gb"] * 1e9 / per_tok / 1e3 - g["glm53_after_tokens_k"]) < 5
+
+
+def test_footprint_ratios_match_pages():
+    g = _golden("footprint.txt")
+    # Old DeepSeek estimate: K and V at full hidden width (2 x 7168) per layer.
+    assert abs(2 * 7168 / layout.footprint_elems(512, 64) - g["deepseek_estimate_fall_factor"]) < 0.5
+    # Full-head K/V (H x (d_nope + d_rope + d_v)) over the latent, DS-V3 shapes.
+    ratio = 128 * (128 + 64 + 128) / layout.footprint_elems(512, 64)
+    assert abs(ratio - g["latent_kv_shrink_factor"]) / g["latent_kv_shrink_factor"] < 0.05
+    assert abs(g["full_head_kv_gb_32k"] / g["latent_kv_gb_32k"] - g["latent_kv_shrink_factor"]) / 70 < 0.05
+
+
+# ------------------------------------------------------- absorb == full head
+
+def test_absorbed_equals_full_head_tiny():
+    g = _golden("footprint.txt")
+    w = workloads.tiny(0)
+    for b in range(w.B):
+        qt = attention.absorb_query(w.q_nope[b], w.q_rope[b], w.W_UK)
+        o1, l1 = attention.absorbed(qt, w.latent[b], w.rope[b], w.W_UV, w.scale)
+        o2, l2 = attention.full_head(w.q_nope[b], w.q_rope[b], w.latent[b], w.rope[b],
+                                     w.W_UK, w.W_UV, w.scale)
+        assert np.max(np.abs(o1 - o2)) <= 10 * g["absorb_equivalence_error"]
+        assert np.max(np.abs(l1 - l2)) <= 10 * g["absorb_equivalence_error"]
+
+
+def test_absorbed_equals_full_head_dsv3_dims_causal():
+    rng = np.random.default_rng(7)
+    H, r, dR, dn, dv, L, ql = 16, 512, 64, 128, 128, 300, 4
+    C = rng.standard_normal((L, r)) * np.exp(rng.uniform(np.log(.1), np.log(3), r))
+    KR = rng.standard_normal((L, dR))
+    qn = rng.standard_normal((ql, H, dn))
+    qr = rng.standard_normal((ql, H, dR))
+    WUK = rng.standard_normal((H, dn, r)) / math.sqrt(r)
+    WUV = rng.standard_normal((H, r, dv)) / math.sqrt(r)
+    qt = attention.absorb_query(qn, qr, WUK)
+    o1, l1 = attention.absorbed(qt, C, KR, WUV, 1 / math.sqrt(192))
+    o2, l2 = attention.full_head(qn, qr, C, KR, WUK, WUV, 1 / math.sqrt(192))
+    assert np.max(np.abs(o1 - o2)) < 1e-12
+    assert np.max(np.abs(l1 - l2)) < 1e-12
+
+
+# ---------------------------------------------------------- brute force
+
+def _brute(q, C, KR, WUV, scale):
+    """Definition with explicit loops, written independently of the oracle."""
+    ql, H, D = q.shape
+    L, r = C.shape
+    dv = WUV.shape[2]
+    out = np.zeros((ql, H, dv))
+    lse = np.zeros((ql, H))
+    for i in range(ql):
+        for h in range(H):
+            n_vis = L - ql + i + 1
+            s = []
+            for t in range(n_vis):
+                acc = 0.0
+                for d in range(r):
+                    acc += q[i, h, d] * C[t, d]
+                for d in range(KR.shape[1]):
+                    acc += q[i, h, r + d] * KR[t, d]
+                s.append(scale * acc)
+            tot = sum(math.exp(x) for x in s)
+            lse[i, h] = math.log(tot)
+            for v in range(dv):
+                acc = 0.0
+                for t in range(n_vis):
+                    p = math.exp(s[t]) / tot
+                    for d in range(r):
+                        acc += p * C[t, d] * WUV[h, d, v]
+                out[i, h, v] = acc
+    return out, lse
+
+
+@pytest.mark.parametrize("L,ql", [(1, 1), (5, 1), (8, 3)])
+def test_brute_force_tiny(L, ql):
+    rng = np.random.default_rng(L * 10 + ql)
+    H, r, dR, dv = 2, 4, 2, 3
+    q = rng.standard_normal((ql, H, r + dR))
+    C = rng.standard_normal((L, r))
+    KR = rng.standard_normal((L, dR))
+    WUV = rng.standard_normal((H, r, dv))
+    o1, l1 = attention.absorbed(q, C, KR, WUV, 0.7)
+    o2, l2 = _brute(q, C, KR, WUV, 0.7)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------------------- closed forms
+
+def test_softmax_rows_sum_to_one():
+    w = workloads.dsv3(1, B=2, H=8, len_range=(100, 300), q_len=3)
+    for b in range(w.B):
+        P = attention.softmax_weights(w.q[b], w.latent[b], w.rope[b], w.scale)
+        assert np.max(np.abs(P.sum(-1) - 1.0)) < 1e-14
+        assert np.all(P >= 0)
+        # causal: row i has exactly L - q_len + i + 1 non-zero weights
+        L = w.latent[b].shape[0]
+        for i in range(3):
+            assert np.all(P[i, :, L - 3 + i + 1:] == 0)
+
+
+def test_single_token_closed_form():
+    rng = np.random.default_rng(3)
+    H, r, dR, dv = 4, 16, 8, 5
+    q = rng.standard_normal((1, H, r + dR))
+    C = rng.standard_normal((1, r))
+    KR = rng.standard_normal((1, dR))
+    WUV = rng.standard_normal((H, r, dv))
+    out, lse = attention.absorbed(q, C, KR, WUV, 0.3)
+    for h in range(H):
+        # one token: p = 1, o_h = (W_UV^h)^T c_0, lse = its scaled score
+        np.testing.assert_allclose(out[0, h], C[0] @ WUV[h], atol=1e-13)
+        s = 0.3 * (q[0, h, :r] @ C[0] + q[0, h, r:] @ KR[0])
+        assert abs(lse[0, h] - s) < 1e-13
+
+
+def test_identical_keys_uniform():
+    rng = np.random.default_rng(4)
+    H, r, dR, dv, L = 3, 8, 4, 6, 37
+    q = rng.standard_normal((1, H, r + dR))
+    C = np.repeat(rng.standard_normal((1, r)), L, 0)
+    KR = np.repeat(rng.standard_normal((1, dR)), L, 0)
+    WUV = rng.standard_normal((H, r, dv))
+    out, lse = attention.absorbed(q, C, KR, WUV, 0.5)
+    for h in range(H):
+        s = 0.5 * (q[0, h, :r] @ C[0] + q[0, h, r:] @ KR[0])
+        assert abs(lse[0, h] - (s + math.log(L))) < 1e-12
+        np.testing.assert_allclose(out[0, h], C[0] @ WUV[h], atol=1e-12)
+
+
+def test_dominant_key_selects_its_value():
+    rng = np.random.default_rng(5)
+    H, r, dR, dv, L = 2, 8, 4, 3, 20
+    C = rng.standard_normal((L, r))
+    KR = rng.standard_normal((L, dR))
+    WUV = rng.standard_normal((H, r, dv))
+    k7 = np.concatenate([C[7], KR[7]])
+    q = np.stack([k7 * 50.0, k7 * 50.0])[None]        # [1, H, D], aligned with token 7
+    out, _ = attention.absorbed(q, C, KR, WUV, 1.0)
+    for h in range(H):
+        np.testing.assert_allclose(out[0, h], C[7] @ WUV[h], atol=1e-9)
+
+
+def test_split_lse_identity():
+    """LSE over all tokens = logsumexp of the LSEs of two disjoint ranges, and the
+    output is the LSE-weighted mix of the two range outputs (q_len = 1)."""
+    w = workloads.dsv3(1, B=1, H=4, len_range=(500, 500))
+    C, KR, q = w.latent[0], w.rope[0], w.q[0]
+    o, l = attention.absorbed(q, C, KR, w.W_UV, w.scale)
+    o1, l1 = attention.absorbed(q, C[:123], KR[:123], w.W_UV, w.scale)
+    o2, l2 = attention.absorbed(q, C[123:], KR[123:], w.W_UV, w.scale)
+    lse = np.logaddexp(l1, l2)
+    np.testing.assert_allclose(l, lse, atol=1e-12)
+    mix = np.exp(l1 - lse)[..., None] * o1 + np.exp(l2 - lse)[..., None] * o2
+    np.testing.assert_allclose(o, mix, atol=1e-12)
+
+
+def test_row_subset_matches_full():
+    w = workloads.verify(3, B=1, q_len=4, len_range=(200, 200), H=8)
+    o, l = attention.absorbed(w.q[0], w.latent[0], w.rope[0], w.W_UV, w.scale)
+    rows = [(0, 0), (3, 7), (2, 5)]
+    os_, ls = attention.row_subset(w.q[0], w.latent[0], w.rope[0], w.W_UV, w.scale, rows)
+    for k, (i, h) in enumerate(rows):
+        np.testing.assert_allclose(os_[k], o[i, h], atol=1e-12)
+        assert abs(ls[k] - l[i, h]) < 1e-12
+
+
+# ----------------------------------------------------------------- paging
+
+def test_paged_roundtrip_and_permutation_invariance():
+    w = workloads.dsv3(1, B=3, H=4, len_range=(65, 300))
+    rows = [np.concatenate([w.latent[b], w.rope[b]], 1) for b in range(w.B)]
+    pool = layout.write_paged(w.num_blocks, 64, w.D, w.block_table, rows, [0] * w.B)
+    for b in range(w.B):
+        back = layout.read_paged(pool, w.block_table[b], int(w.seq_lens[b]), 64)
+        np.testing.assert_array_equal(back, rows[b])
+    # a different (identity) placement gives the same gathered rows
+    ident, n = workloads.make_paging(np.random.default_rng(0), w.seq_lens, 64, permute=False)
+    pool2 = layout.write_paged(n, 64, w.D, ident, rows, [0] * w.B)
+    for b in range(w.B):
+        np.testing.assert_array_equal(layout.read_paged(pool2, ident[b], int(w.seq_lens[b]), 64), rows[b])
+    # block ids really are permuted (the placement test is not vacuous)
+    assert not np.array_equal(w.block_table[w.block_table >= 0], np.arange(w.num_blocks))
+
+
+# --------------------------------------------------------------- rotation
+
+def test_rotation_recovers_known_eigenbasis():
+    """X = diag(sqrt d) Q^T has X^T X = Q diag(d) Q^T exactly: R must be Q with its
+    columns in ascending-d order, up to the sign rule."""
+    rng = np.random.default_rng(11)
+    n = 24
+    Q = workloads.haar_orthogonal(rng, n)
+    d = rng.permutation(np.linspace(1.0, 40.0, n))
+    X = np.sqrt(d)[:, None] * Q.T
+    R, w = oint2.fit_rotation(X)
+    order = np.argsort(d)
+    np.testing.assert_allclose(w, d[order], rtol=1e-12)
+    for j in range(n):
+        col = Q[:, order[j]]
+        col = col * np.sign(col[np.argmax(np.abs(col))])
+        np.testing.assert_allclose(R[:, j], col, atol=1e-10)
+        assert R[np.argmax(np.abs(R[:, j])), j] > 0
+
+
+def test_rotation_properties_on_calibration_set():
+    w = workloads.int2_rotated(4, B=1, H=4, len_range=(64, 64), n_calib=8192)
+    R, ev = oint2.fit_rotation(w.calib)
+    assert np.max(np.abs(R.T @ R - np.eye(512))) < 1e-12
+    Sig = oint2.latent_covariance(w.calib)
+    Dm = R.T @ Sig @ R
+    assert np.all(np.diff(np.diag(Dm)) >= 0)                        # ascending
+    off = Dm - np.diag(np.diag(Dm))
+    assert np.max(np.abs(off)) < 1e-9 * ev[-1]
+    # ascending eigenvalue -> group 0 holds the lowest-variance rotated dims
+    Y = w.calib @ R
+    var = Y.var(0)
+    assert var[:32].mean() < var[-32:].mean() / 50
+
+
+def test_rotation_is_lossless_before_quantisation():
+    w = workloads.int2_rotated(4, B=1, H=8, len_range=(150, 150), n_calib=4096)
+    R, _ = oint2.fit_rotation(w.calib)
+    C = w.latent[0].astype(np.float64)
+    Y = C @ R
+    o1, l1 = attention.absorbed(w.q[0], C, w.rope[0], w.W_UV, w.scale)
+    o2, l2 = oint2.attention_rotated(w.q[0], Y, w.rope[0], R, w.W_UV, w.scale)
+    assert np.max(np.abs(o1 - o2)) < 1e-12
+    assert np.max(np.abs(l1 - l2)) < 1e-12
+
+
+def test_clip_thresholds_clip_one_percent():
+    w = workloads.int2_rotated(4, B=1, H=4, len_range=(64, 64), n_calib=16384)
+    R, _ = oint2.fit_rotation(w.calib)
+    T = oint2.clip_thresholds(w.calib, R)
+    Y = np.abs(w.calib @ R)
+    for g in range(16):
+        frac = np.mean(Y[:, 32 * g:32 * g + 32] > T[g])
+        assert 0.009 <= frac <= 0.011
+    assert T[-1] > 3 * T[0]                              # thresholds grow with the group's variance
+
+
+# -------------------------------------------------------------- INT2 codes
+
+def test_int2_worked_example():
+    """Hand-worked encoding of two 4-element groups (r = 8, group 4)."""
+    y = np.array([[0.0, 1.0, 2.0, 3.0, -2.0, 0.5, 0.25, 2.0]], dtype=np.float32)
+    T = np.array([10.0, 1.0], dtype=np.float32)
+    codes, sz = oint2.encode(y, T, group=4)
+    # group 0: lo 0, hi 3, s 1, z 0 -> codes 0,1,2,3 -> 0b11_10_01_00
+    # group 1: clipped to [-1, .5, .25, 1]; s = fp16(2/3) = 0.66650390625, z = -1
+    #          (v - z)/s = 0, 2.2506, 1.8755, 3.0007 -> codes 0,2,2,3 -> 0b11_10_10_00
+    assert codes.tolist() == [[0xE4, 0xE8]]
+    s = sz.view(np.float16).astype(np.float64)
+    assert s[0, 0, 0] == 1.0 and s[0, 0, 1] == 0.0
+    assert s[0, 1, 0] == 0.66650390625 and s[0, 1, 1] == -1.0
+    deq = oint2.decode(codes, sz, group=4)
+    np.testing.assert_array_equal(deq[0], np.array(
+        [0, 1, 2, 3, -1, 0.3330078125, 0.3330078125, 0.99951171875], dtype=np.float32))
+    np.testing.assert_array_equal(oint2.unpack_codes(codes)[0], [0, 1, 2, 3, 0, 2, 2, 3])
+
+
+def test_int2_constant_group_has_zero_scale():
+    y = np.full((1, 8), 0.75, dtype=np.float32)
+    codes, sz = oint2.encode(y, np.array([5.0, 5.0], np.float32), group=4)
+    assert codes.tolist() == [[0, 0]]
+    assert np.all(sz.view(np.float16)[..., 0] == 0)
+    np.testing.assert_array_equal(oint2.decode(codes, sz, group=4), y)
+
+
+def test_int2_invariants_and_rotation_chain():
+    w = workloads.int2_rotated(4, B=2, H=4, len_range=(64, 64), n_calib=8192)
+    R, _ = oint2.fit_rotation(w.calib)
+    T = oint2.clip_thresholds(w.calib, R).astype(np.float32)
+    c = np.concatenate(w.new_latent)                         # [64, 512]
+    R32 = R.astype(np.float32)
+    y = oint2.rotate_fp32(c, R32)
+    # the fp32 chain is c . R (not c . R^T) to fp32 accuracy
+    y64 = c.astype(np.float64) @ R32.astype(np.float64)
+    assert np.max(np.abs(y - y64)) < 1e-4 * np.max(np.abs(y64))
+    assert np.max(np.abs(c.astype(np.float64) @ R32.T.astype(np.float64) - y64)) > 1e-2
+    codes, sz = oint2.encode(y, T)
+    u = oint2.unpack_codes(codes)
+    assert u.min() >= 0 and u.max() <= 3
+    s = sz.view(np.float16)[..., 0].astype(np.float32).repeat(32, 1)
+    z = sz.view(np.float16)[..., 1].astype(np.float32).repeat(32, 1)
+    deq = oint2.decode(codes, sz)
+    assert np.all(deq >= z - 1e-6) and np.all(deq <= z + 3 * s + 1e-5 * np.abs(z + 3 * s))
+    yc = np.clip(y, -T.repeat(32)[None], T.repeat(32)[None])
+    err = np.abs(deq - yc)
+    # rounding to the nearest level, plus the fp16 rounding of z and s
+    assert np.all(err <= s / 2 + 2e-3 * (np.abs(yc) + s) + 1e-6)
+    # python re-decoding agrees with the C decoder (codes * s + z is exact-then-rounded once)
+    np.testing.assert_array_equal(deq, (u.astype(np.float32) * s + z).astype(np.float32))
