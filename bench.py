@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark: MLA decode over a paged latent cache, DeepSeek-V3 shapes.
+
+One step = one pass of the whole decode path over one batch: append this step's
+new token of every sequence into the paged cache, then decode attention for
+all sequences (split schedule, attention kernel, split combine, W_UV
+up-projection). The workload: B=32, q_len=1, H=128, kv_lora_rank=512,
+qk_rope_head_dim=64, v_head_dim=128, per-sequence lengths ~ U[1024, 8192],
+block size 64 with a permuted block table, bf16. The new token written each
+step is the sequence's last position, so the cache (and the work) is identical
+every step.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle on the
+host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode KV-tokens/s, TFLOP/s and HBM GB/s as fraction of GB300 roofline"
+UNIT = "KV-tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------------ accounting
+
+def workload_config(w):
+    return {
+        "workload": (f"DeepSeek-V3-shaped MLA decode: B={w.B} q_len=1 H={w.H} kv_lora_rank={w.r} "
+                     f"qk_rope_head_dim={w.d_rope} v_head_dim={w.d_v} L~U[1024,8192] (sum {w.total_tokens}) "
+                     f"block_size={w.block_size} permuted block table, bf16"),
+        "global_batch": w.B,
+        "seq_len_sum": w.total_tokens,
+        "seq_len_mean": round(w.total_tokens / w.B, 1),
+        "cache_bytes": w.total_tokens * w.D * 2,
+        "l2": "flushed between timed steps (512 MiB write)",
+    }
+
+
+def algorithmic(w):
+    """Algorithmic bytes and flops of one decode step and of its attention kernel."""
+    tok = w.total_tokens
+    H, r, D, dv, B = w.H, w.r, w.D, w.d_v, w.B
+    kernel_bytes = tok * D * 2 + B * H * D * 2                 # cache read once + absorbed query
+    step_bytes = (kernel_bytes + H * r * dv * 2                # W_UV
+                  + B * H * dv * 2 + B * H * 4                 # out + lse
+                  + B * D * 2 * 2)                             # appended token: read + write
+    kernel_flops = 2 * tok * H * (D + r)                       # QK^T + PV
+    step_flops = kernel_flops + 2 * B * H * r * dv             # + W_UV up-projection
+    return kernel_bytes, step_bytes, kernel_flops, step_flops
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                elif isinstance(x, (int, float)):
+                    flat[pre[:-1]] = float(x)
+            walk(d)
+
+            def pick(*names):
+                for k, v in flat.items():
+                    if k.split(".")[-1] in names:
+                        return v
+                return None
+            hbm = pick("hbm_gbs", "hbm_GBs", "copy_gbs")
+            tf = pick("bf16_tflops", "bf16_tflops_burst")
+            tfs = pick("bf16_tflops_sustained")
+            if hbm and tf:
+                return {"hbm_gbs": hbm, "bf16_tflops": tf, "bf16_tflops_sustained": tfs or tf,
+                        "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_08_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        kv = dict(x.split("=", 1) for x in line.split())
+        if kv.get("kernel") == kernel and kv.get("source_sha") == src:
+            return float(kv["bytes_per_launch_full_workload"])
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            first = vis.split(",")[0].strip() if vis else str(self.dev)
+            if first:
+                cmd += ["-i", first]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for p in self.samples:
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_throughput(w, budget_s, max_tokens_per_call=None):
+    """Time the CPU oracle over sequences of the workload until ``budget_s`` of
+    work is done. Returns (tokens/s, tokens, seconds, description)."""
+    from oracle import attention
+    done_tok, t_total, calls = 0, 0.0, 0
+    b = 0
+    while t_total < budget_s or calls == 0:
+        L = w.latent[b].shape[0] if max_tokens_per_call is None else min(max_tokens_per_call, w.latent[b].shape[0])
+        t0 = time.perf_counter()
+        attention.absorbed(w.q[b], w.latent[b][:L], w.rope[b][:L], w.W_UV, w.scale)
+        t_total += time.perf_counter() - t0
+        done_tok += L
+        calls += 1
+        b = (b + 1) % w.B
+    return done_tok / t_total, done_tok, t_total, calls
+
+
+def cpu_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import workloads
+    w = workloads.dsv3(args.seed)
+    # size each step so the whole run stays within about two minutes
+    rate, _, _, _ = oracle_throughput(w, 2.0, max_tokens_per_call=2048)
+    per_step = int(max(64, min(8192, rate * 120.0 / max(1, args.steps + args.warmup))))
+    from oracle import attention
+    for k in range(args.warmup):
+        b = k % w.B
+        n = min(per_step, w.latent[b].shape[0])
+        attention.absorbed(w.q[b], w.latent[b][:n], w.rope[b][:n], w.W_UV, w.scale)
+    tok, t = 0, 0.0
+    for k in range(args.steps):
+        b = k % w.B
+        n = min(per_step, w.latent[b].shape[0])
+        t0 = time.perf_counter()
+        attention.absorbed(w.q[b], w.latent[b][:n], w.rope[b][:n], w.W_UV, w.scale)
+        t += time.perf_counter() - t0
+        tok += n
+    value = tok / t
+    sample = (f"each step: absorbed attention of one sequence's first <= {per_step} cached tokens, "
+              f"all {w.H} heads, fp64 numpy (cycling over the {w.B} sequences)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gb300(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    from mla_latent_kv_08_gb300 import build as _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    import mla_latent_kv_08_gb300 as mla
+    import workloads
+
+    dev = torch.device("cuda", local)
+    w = workloads.dsv3(args.seed)
+    shape = mla.Shape(num_heads=w.H, kv_lora_rank=w.r, rope_dim=w.d_rope, v_head_dim=w.d_v,
+                      block_size=w.block_size, num_blocks=w.num_blocks, kind=mla.MLA_KV_BF16)
+    bf = torch.bfloat16
+
+    def t(x, dtype=None):
+        tt = torch.from_numpy(np.ascontiguousarray(x))
+        return (tt.to(dtype) if dtype is not None else tt).to(dev)
+
+    cache = mla.Cache.allocate(shape, dev)
+    bt = t(w.block_table)
+    seq_lens = t(w.seq_lens.astype(np.int32))
+    # fill the cache (untimed) through the library's append
+    cu_all = t(np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32))
+    mla.mla_latent_append(cache, bt, t(np.zeros(w.B, np.int32)), cu_all,
+                          t(np.concatenate(w.latent), bf), t(np.concatenate(w.rope), bf))
+    # per-step inputs: the last token of each sequence (rewritten every step) and q
+    new_c = t(np.stack([x[-1] for x in w.latent]), bf)
+    new_r = t(np.stack([x[-1] for x in w.rope]), bf)
+    start = t((w.seq_lens - 1).astype(np.int32))
+    cu1 = t(np.arange(w.B + 1, dtype=np.int32))
+    q = t(w.q, bf)
+    W_UV = t(w.W_UV, bf)
+    out = torch.empty((w.B, 1, w.H, w.d_v), dtype=bf, device=dev)
+    lse = torch.empty((w.B, 1, w.H), dtype=torch.float32, device=dev)
+    ws = mla.alloc_workspace(shape, w.B, 1, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(qq=q, cc=new_c, rr=new_r):
+        mla.mla_latent_append(cache, bt, start, cu1, cc, rr, stream=stream)
+        mla.mla_decode(cache, bt, seq_lens, qq, W_UV, w.scale, out, lse, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    code, flags = mla.mla_get_status(ws)
+    if code != mla.MLA_OK:
+        raise RuntimeError(f"device status {code} flags {flags}")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    mla.mla_profile_enable(True)
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    att_ms, att_n, n_kernels = mla.mla_profile_read()
+    mla.mla_profile_enable(False)
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    att_avg_ms = att_ms / max(att_n, 1)
+
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(np.ascontiguousarray(w.q)).to(bf).pin_memory()
+        hc = new_c.cpu().pin_memory()
+        hr = new_r.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=bf).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        q_d = torch.empty_like(q)
+        c_d = torch.empty_like(new_c)
+        r_d = torch.empty_like(new_r)
+
+        def e2e_step():
+            q_d.copy_(hq, non_blocking=True)
+            c_d.copy_(hc, non_blocking=True)
+            r_d.copy_(hr, non_blocking=True)
+            step(q_d, c_d, r_d)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup // 4)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        ke = max(3, K // 4)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        for k in range(ke):
+            flush.zero_()
+            ev2[k][0].record(stream)
+            e2e_step()
+            ev2[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = sum(a.elapsed_time(b) for a, b in ev2) / ke
+        h2d = hq.numel() * 2 + hc.numel() * 2 + hr.numel() * 2
+        d2h = hout.numel() * 2 + hlse.numel() * 4
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+
+    if world > 1:
+        tt = torch.tensor([step_ms, att_avg_ms, e2e["ms"] if e2e else 0.0], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms, att_avg_ms = float(tt[0]), float(tt[1])
+        if e2e:
+            e2e["ms"] = float(tt[2])
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    kb, sb, kf, sf = algorithmic(w)
+    peaks = load_peaks()
+    tokens = w.total_tokens * world
+    value = tokens / (step_ms * 1e-3)
+    achieved = kb / (att_avg_ms * 1e-3) / 1e9
+    kernel_name = {mla.MLA_IMPL_SIMT: "decode_simt_kernel", mla.MLA_IMPL_TCGEN05: "decode_tc_kernel"}[
+        mla.mla_resolve_impl(shape, 1)]
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, tok, secs, calls = oracle_throughput(w, 12.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{calls} whole sequences of this workload ({tok} cached tokens, all heads), "
+                         f"fp64 numpy, {secs:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded numpy PCG64)",
+        "config": dict(workload_config(w), parallelism=f"replica x{world} (independent sequences)"),
+        "tflops": sf / (step_ms * 1e-3) / 1e12 * world,
+        "gbs": sb / (step_ms * 1e-3) / 1e9 * world,
+        # whole step against min(HBM bound, tensor bound): roofline time / measured time
+        "step_roofline_frac": max(sb / (peaks["hbm_gbs"] * 1e9),
+                                  sf / (peaks["bf16_tflops_sustained"] * 1e12)) / (step_ms * 1e-3),
+        "arithmetic_intensity": sf / sb,
+        "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(kernel_name),
+                     "algorithmic_bytes": kb, "launch_ms": att_avg_ms,
+                     "peak_source": peaks["source"],
+                     "tensor_tflops": kf / (att_avg_ms * 1e-3) / 1e12},
+        "gpu_launches": int(n_kernels),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if e2e:
+        line["e2e"] = {"value": tokens / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"]}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+/*
+ * mla.h - C ABI of the GB300 (sm_103a) MLA latent-cache decode library.
+ *
+ * Multi-head latent attention decode over a paged, compressed latent KV cache
+ * in the DeepSeek "absorb" form. Each cached token holds one shared latent c
+ * (kv_lora_rank = r elements) and one shared rope key k_R (qk_rope_head_dim =
+ * d_R elements); the query arrives already absorbed through W_UK, scores and
+ * softmax run against [c ; k_R], and the latent-space output is up-projected
+ * per head through W_UV.
+ *   Source: "GLM-5.2 speculative drafting: native MTP head beats GLM-4-9B, +
+ *   opt-in MLA-latent KV cache" (leyten/shard PR #5), TL;DR item 2; per-token
+ *   footprint r + d_R from "hf: size GLM-5.3-Flash's KV cache from its latent
+ *   layers only" (coder/llm-helper PR #64), PR description.
+ * An opt-in cache kind stores the latent rotated by a per-layer orthogonal
+ * covariance eigenbasis R and quantised to grouped INT2 (rope key kept bf16).
+ *   Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10),
+ *   maintainer reply, "How the rotation adapts to the latent".
+ *
+ * Definitions (per sequence b, query row i, head h, cached token t):
+ *   s = scale * (q[b,i,h,:] . [c_t ; kR_t])          (rotated kind: q_lat . R)
+ *   visible t: 0 <= t <= L_b - q_len + i               (causal draft window)
+ *   lse[b,i,h] = ln sum_visible exp(s)
+ *   olat = sum_t softmax(s)_t c_t                      (rotated kind: . R^T)
+ *   out[b,i,h,:] = olat . W_UV[h]                      ([r] x [r, d_v])
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers on the current CUDA device unless the
+ *     argument says "host". The caller owns every buffer; the library never
+ *     allocates device memory and never synchronises (mla_get_status is the
+ *     one call that waits, on the given stream).
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream. Work is enqueued on it and the call returns immediately.
+ *   - Row-major, densely packed layouts as stated per argument. Device buffers
+ *     must be 16-byte aligned.
+ *   - Host-side argument errors return before anything is launched. Device-side
+ *     problems (a block id outside [0, num_blocks), a sequence length outside
+ *     [q_len, max_blocks_per_seq * block_size]) never trap: the kernel records
+ *     a flag, skips the bad work and writes NaN to the affected output rows;
+ *     mla_get_status reports the flags.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID = -1,      /* bad argument (null pointer, shape, alignment)   */
+    MLA_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. forced impl)     */
+    MLA_ERR_BOUNDS = -3,       /* device flag: block id or length out of range     */
+    MLA_ERR_WORKSPACE = -4,    /* workspace smaller than mla_workspace_bytes()     */
+    MLA_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed             */
+    MLA_ERR_TIMEOUT = -6       /* device flag: a bounded wait gave up              */
+} mla_status;
+
+typedef enum {
+    MLA_KV_BF16 = 0,           /* latent + rope key, bf16, one row per token       */
+    MLA_KV_FP32 = 1,           /* latent + rope key, fp32, one row per token       */
+    MLA_KV_INT2_ROT = 2        /* rotated latent as grouped INT2 + bf16 rope key   */
+} mla_kv_kind;
+
+typedef enum {
+    MLA_IMPL_AUTO = 0,         /* tensor-core kernel where the shape allows it     */
+    MLA_IMPL_SIMT = 1,         /* generic CUDA-core kernel, any supported shape    */
+    MLA_IMPL_TCGEN05 = 2       /* tensor-core kernel; UNSUPPORTED if shape is not  */
+} mla_impl;
+
+/* Problem shape. All counts are element counts. */
+typedef struct {
+    int32_t num_heads;         /* H                                               */
+    int32_t kv_lora_rank;      /* r, multiple of 8 (INT2: of group_size and 4)    */
+    int32_t rope_dim;          /* d_R, multiple of 8 (may be 0 for FP32)          */
+    int32_t v_head_dim;        /* d_v                                             */
+    int32_t block_size;        /* tokens per cache block                          */
+    int32_t num_blocks;        /* physical blocks in the pool                     */
+    int32_t group_size;        /* INT2 group length along r (32); else ignored    */
+    int32_t kind;              /* mla_kv_kind                                     */
+    int32_t impl;              /* mla_impl                                        */
+    int32_t num_splits_hint;   /* 0: planner's choice; k>0: aim for about k split-
+                                  KV work units in total (1 = one per sequence)   */
+} mla_shape;
+
+/* The paged cache. Block p, slot j is token row p*block_size + j.
+ *   BF16/FP32:  latent     [num_blocks, block_size, r + d_R]  (c then k_R)
+ *   INT2_ROT:   codes      [num_blocks, block_size, r / 4]    uint8, element e
+ *                          of the row at bits 2*(e%4) of byte e/4
+ *               scale_zero [num_blocks, block_size, r / group_size, 2] fp16
+ *                          (scale, zero); value = fmaf(code, scale, zero)
+ *               rope       [num_blocks, block_size, d_R]      bf16
+ * Unused members are NULL. */
+typedef struct {
+    void *latent;
+    void *codes;
+    void *scale_zero;
+    void *rope;
+} mla_cache;
+
+/* Bytes of device workspace mla_decode / mla_verify need for B sequences with
+ * q_len query rows each, on the current device. 0 on a bad shape. */
+size_t mla_workspace_bytes(const mla_shape *shape, int32_t B, int32_t q_len);
+
+/* Write new tokens into the paged cache (append / quantise).
+ *   block_table [B, max_blocks_per_seq] int32: physical block of each logical
+ *               block of each sequence.
+ *   start_pos   [B] int32: position of the sequence's first new token.
+ *   cu_new      [B + 1] int32: prefix sums of new-token counts; new tokens of
+ *               sequence b are rows cu_new[b] .. cu_new[b+1]-1 of c_kv/k_rope.
+ *   num_new     host int: cu_new[B] (total new tokens, sizes the launch).
+ *   c_kv        [num_new, r]   bf16 (FP32 kind: fp32)
+ *   k_rope      [num_new, d_R] bf16 (FP32 kind: fp32)
+ *   R           INT2 only: [r, r] fp32 row-major, y = c . R (column j is the
+ *               j-th eigenvector in ascending eigenvalue order); else NULL.
+ *   clip        INT2 only: [r / group_size] fp32 clip thresholds; else NULL.
+ *   status      optional [1] int32 device word; flags are OR-ed into it.
+ * INT2 encoding per token and group g of group_size dims: y = fp32 fmaf chain
+ * over k ascending; y clipped to [-clip[g], clip[g]]; scale =
+ * fp16_rne((max - min) / 3), zero = fp16_rne(min); code = clamp(rint((y -
+ * zero) / scale), 0, 3), 0 when scale == 0.
+ *   Source: OSCAR issue #10, maintainer reply (rotated + quantised latent in
+ *   the cache, thresholds fit on the rotated latent). */
+mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache,
+                             const int32_t *block_table, int32_t max_blocks_per_seq,
+                             int32_t B, const int32_t *start_pos, const int32_t *cu_new,
+                             int32_t num_new, const void *c_kv, const void *k_rope,
+                             const float *R, const float *clip, int32_t *status,
+                             void *stream);
+
+/* Decode attention, one query row per sequence (q_len = 1).
+ *   seq_lens   [B] int32: tokens in the cache per sequence (>= 1).
+ *   q          [B, 1, H, r + d_R] absorbed query, bf16 (FP32 kind: fp32).
+ *   W_UV       [H, r, d_v] bf16 (FP32 kind: fp32).
+ *   R          INT2 only: [r, r] fp32 (as in append); else NULL.
+ *   scale      softmax scale applied to q . k.
+ *   out        [B, 1, H, d_v] bf16 (FP32 kind: fp32).
+ *   lse        [B, 1, H] fp32, natural log of the softmax denominator.
+ *   workspace  device scratch of at least mla_workspace_bytes(shape, B, 1).
+ * The call is stream-ordered after prior work on `stream` (e.g. an append). */
+mla_status mla_decode(const mla_shape *shape, const mla_cache *cache,
+                      const int32_t *block_table, int32_t max_blocks_per_seq,
+                      const int32_t *seq_lens, int32_t B, const void *q,
+                      const void *W_UV, const float *R, float scale, void *out,
+                      float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Speculative verify: q_len >= 1 draft rows per sequence, already appended, so
+ * row i of sequence b sees positions 0 .. seq_lens[b] - q_len + i. Arguments as
+ * mla_decode with q [B, q_len, H, r + d_R], out [B, q_len, H, d_v], lse
+ * [B, q_len, H], workspace >= mla_workspace_bytes(shape, B, q_len).
+ *   Source: "GLM-5.2 speculative drafting ..." (leyten/shard PR #5), TL;DR
+ *   item 1 (drafts verified by the target); the causal window is this
+ *   library's reading. */
+mla_status mla_verify(const mla_shape *shape, const mla_cache *cache,
+                      const int32_t *block_table, int32_t max_blocks_per_seq,
+                      const int32_t *seq_lens, int32_t B, int32_t q_len, const void *q,
+                      const void *W_UV, const float *R, float scale, void *out,
+                      float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Wait for `stream`, read the device flags of the last decode/verify that used
+ * `workspace` and return MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT. If
+ * raw_flags is not NULL it receives the raw flag word (host int). */
+mla_status mla_get_status(const void *workspace, int32_t *raw_flags, void *stream);
+
+/* Read a device status word written by mla_latent_append (same meaning). */
+mla_status mla_read_status_word(const int32_t *status, int32_t *raw_flags, void *stream);
+
+/* Static description of a status code. */
+const char *mla_status_string(mla_status status);
+
+/* Which implementation mla_decode would run for this shape on the current
+ * device (MLA_IMPL_SIMT or MLA_IMPL_TCGEN05), or a negative mla_status. */
+int32_t mla_resolve_impl(const mla_shape *shape, int32_t q_len);
+
+/* Diagnostics for benchmarking (host state, not thread-safe). While enabled,
+ * every decode/verify call records a CUDA event pair on its stream around its
+ * main attention kernel, and every entry point counts the kernels it launches.
+ * mla_profile_enable(1) (re)starts the record; mla_profile_read waits for the
+ * recorded events and returns the summed duration of the attention kernels in
+ * milliseconds, their launch count and the total kernel launch count (any
+ * output pointer may be NULL). Events are created by the library on first use
+ * (no device memory is allocated). */
+mla_status mla_profile_enable(int32_t enable);
+mla_status mla_profile_read(double *attention_ms, int32_t *attention_launches,
+                            int32_t *kernel_launches);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -1,0 +1,266 @@
+"""Python binding of the GB300 MLA latent-cache decode library (libmla_gb300.so).
+
+Argument marshalling only: every step of append, decode and verify runs in the
+library's CUDA kernels. PyTorch provides device memory and streams. The C ABI
+is declared in ``include/mla.h``; the functions here carry the same names.
+
+The library must be built (``python -m mla_latent_kv_08_gb300.build`` or
+``__graft_entry__.build()``); importing this package never falls back to
+anything else when it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmla_gb300.so")
+
+MLA_OK = 0
+MLA_ERR_INVALID = -1
+MLA_ERR_UNSUPPORTED = -2
+MLA_ERR_BOUNDS = -3
+MLA_ERR_WORKSPACE = -4
+MLA_ERR_CUDA = -5
+MLA_ERR_TIMEOUT = -6
+
+MLA_KV_BF16 = 0
+MLA_KV_FP32 = 1
+MLA_KV_INT2_ROT = 2
+
+MLA_IMPL_AUTO = 0
+MLA_IMPL_SIMT = 1
+MLA_IMPL_TCGEN05 = 2
+
+# Every symbol include/mla.h declares.
+EXPORTED = (
+    "mla_workspace_bytes", "mla_latent_append", "mla_decode", "mla_verify", "mla_get_status",
+    "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
+    "mla_profile_enable", "mla_profile_read",
+)
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+class mla_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_heads", "kv_lora_rank", "rope_dim", "v_head_dim", "block_size", "num_blocks",
+        "group_size", "kind", "impl", "num_splits_hint")]
+
+
+class mla_cache(ctypes.Structure):
+    _fields_ = [("latent", ctypes.c_void_p), ("codes", ctypes.c_void_p),
+                ("scale_zero", ctypes.c_void_p), ("rope", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmla_gb300.so and declare its signatures. Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m mla_latent_kv_08_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    sp = ctypes.POINTER(mla_shape)
+    cp = ctypes.POINTER(mla_cache)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.mla_workspace_bytes.argtypes = [sp, i32, i32]
+    lib.mla_workspace_bytes.restype = sz
+    lib.mla_latent_append.argtypes = [sp, cp, vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.mla_latent_append.restype = i32
+    lib.mla_decode.argtypes = [sp, cp, vp, i32, vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.mla_decode.restype = i32
+    lib.mla_verify.argtypes = [sp, cp, vp, i32, vp, i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.mla_verify.restype = i32
+    lib.mla_get_status.argtypes = [vp, i32p, vp]
+    lib.mla_get_status.restype = i32
+    lib.mla_read_status_word.argtypes = [vp, i32p, vp]
+    lib.mla_read_status_word.restype = i32
+    lib.mla_status_string.argtypes = [i32]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_resolve_impl.argtypes = [sp, i32]
+    lib.mla_resolve_impl.restype = i32
+    lib.mla_version.argtypes = []
+    lib.mla_version.restype = i32
+    lib.mla_profile_enable.argtypes = [i32]
+    lib.mla_profile_enable.restype = i32
+    lib.mla_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), i32p, i32p]
+    lib.mla_profile_read.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().mla_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != MLA_OK:
+        raise MlaError(code, where)
+
+
+# ---------------------------------------------------------------- shapes
+
+@dataclasses.dataclass
+class Shape:
+    """Problem shape (mirrors ``mla_shape``)."""
+
+    num_heads: int
+    kv_lora_rank: int
+    rope_dim: int
+    v_head_dim: int
+    block_size: int
+    num_blocks: int
+    kind: int = MLA_KV_BF16
+    group_size: int = 32
+    impl: int = MLA_IMPL_AUTO
+    num_splits_hint: int = 0
+
+    def c(self) -> mla_shape:
+        return mla_shape(self.num_heads, self.kv_lora_rank, self.rope_dim, self.v_head_dim,
+                         self.block_size, self.num_blocks, self.group_size, self.kind, self.impl,
+                         self.num_splits_hint)
+
+    @property
+    def D(self) -> int:
+        return self.kv_lora_rank + self.rope_dim
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+@dataclasses.dataclass
+class Cache:
+    """Device tensors of one paged latent cache (see ``mla_cache``)."""
+
+    shape: Shape
+    latent: object = None
+    codes: object = None
+    scale_zero: object = None
+    rope: object = None
+
+    def c(self) -> mla_cache:
+        return mla_cache(_ptr(self.latent), _ptr(self.codes), _ptr(self.scale_zero), _ptr(self.rope))
+
+    @classmethod
+    def allocate(cls, shape: Shape, device="cuda", zero: bool = True) -> "Cache":
+        """Allocate the pool for ``shape`` with torch (the library never allocates)."""
+        import torch
+        alloc = torch.zeros if zero else torch.empty
+        nb, bs, r, dR = shape.num_blocks, shape.block_size, shape.kv_lora_rank, shape.rope_dim
+        if shape.kind == MLA_KV_INT2_ROT:
+            return cls(shape,
+                       codes=alloc((nb, bs, r // 4), dtype=torch.uint8, device=device),
+                       scale_zero=alloc((nb, bs, r // shape.group_size, 2), dtype=torch.float16, device=device),
+                       rope=alloc((nb, bs, dR), dtype=torch.bfloat16, device=device))
+        dt = torch.float32 if shape.kind == MLA_KV_FP32 else torch.bfloat16
+        return cls(shape, latent=alloc((nb, bs, r + dR), dtype=dt, device=device))
+
+    def bytes_per_token(self) -> int:
+        s = self.shape
+        if s.kind == MLA_KV_INT2_ROT:
+            return s.kv_lora_rank // 4 + (s.kv_lora_rank // s.group_size) * 4 + 2 * s.rope_dim
+        return (4 if s.kind == MLA_KV_FP32 else 2) * (s.kv_lora_rank + s.rope_dim)
+
+
+# ---------------------------------------------------------------- entry points
+
+def mla_workspace_bytes(shape: Shape, B: int, q_len: int = 1) -> int:
+    n = load_library().mla_workspace_bytes(ctypes.byref(shape.c()), int(B), int(q_len))
+    if n == 0:
+        raise MlaError(MLA_ERR_INVALID, "mla_workspace_bytes")
+    return int(n)
+
+
+def alloc_workspace(shape: Shape, B: int, q_len: int = 1, device="cuda"):
+    import torch
+    return torch.empty(mla_workspace_bytes(shape, B, q_len), dtype=torch.uint8, device=device)
+
+
+def mla_latent_append(cache: Cache, block_table, start_pos, cu_new, c_kv, k_rope, R=None, clip=None,
+                      status=None, stream=None) -> None:
+    """Write len(c_kv) new tokens into the paged cache (see include/mla.h)."""
+    lib = load_library()
+    B = int(start_pos.shape[0])
+    code = lib.mla_latent_append(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+                                 int(block_table.shape[1]), B, _ptr(start_pos), _ptr(cu_new),
+                                 int(c_kv.shape[0]), _ptr(c_kv), _ptr(k_rope), _ptr(R), _ptr(clip),
+                                 _ptr(status), _stream(stream))
+    _check(code, "mla_latent_append")
+
+
+def mla_decode(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, workspace,
+               R=None, stream=None) -> None:
+    """Decode attention, q [B, 1, H, r + d_R] -> out [B, 1, H, d_v], lse [B, 1, H]."""
+    lib = load_library()
+    code = lib.mla_decode(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+                          int(block_table.shape[1]), _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(q),
+                          _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                          int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check(code, "mla_decode")
+
+
+def mla_verify(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, workspace,
+               R=None, stream=None) -> None:
+    """Speculative verify, q [B, q_len, H, r + d_R] with the causal draft window."""
+    lib = load_library()
+    code = lib.mla_verify(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+                          int(block_table.shape[1]), _ptr(seq_lens), int(seq_lens.shape[0]), int(q.shape[1]),
+                          _ptr(q), _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                          int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check(code, "mla_verify")
+
+
+def mla_get_status(workspace, stream=None):
+    """(status code, raw flag word) of the last decode/verify on this workspace."""
+    flags = ctypes.c_int32(0)
+    code = load_library().mla_get_status(_ptr(workspace), ctypes.byref(flags), _stream(stream))
+    return int(code), int(flags.value)
+
+
+def mla_read_status_word(status, stream=None):
+    flags = ctypes.c_int32(0)
+    code = load_library().mla_read_status_word(_ptr(status), ctypes.byref(flags), _stream(stream))
+    return int(code), int(flags.value)
+
+
+def mla_resolve_impl(shape: Shape, q_len: int = 1) -> int:
+    return int(load_library().mla_resolve_impl(ctypes.byref(shape.c()), int(q_len)))
+
+
+def mla_version() -> int:
+    return int(load_library().mla_version())
+
+
+def mla_profile_enable(enable: bool = True) -> None:
+    _check(load_library().mla_profile_enable(1 if enable else 0), "mla_profile_enable")
+
+
+def mla_profile_read():
+    """(summed attention-kernel ms, attention launches, total kernel launches)."""
+    ms = ctypes.c_double(0.0)
+    n_att = ctypes.c_int32(0)
+    n_all = ctypes.c_int32(0)
+    _check(load_library().mla_profile_read(ctypes.byref(ms), ctypes.byref(n_att), ctypes.byref(n_all)),
+           "mla_profile_read")
+    return float(ms.value), int(n_att.value), int(n_all.value)

@@ -1,0 +1,313 @@
+// C ABI entry points: argument checks, the workspace layout, implementation
+// choice and the launch sequence of append, decode and verify.
+#include "mla_internal.cuh"
+
+#include <string.h>
+
+namespace mla {
+
+static int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// ---- benchmarking diagnostics (see mla_profile_enable) ----------------------
+struct Profile {
+    bool on = false;
+    int32_t kernels = 0;
+    int32_t used = 0;
+    static constexpr int kMax = 1 << 14;
+    cudaEvent_t start[kMax];
+    cudaEvent_t stop[kMax];
+    int32_t created = 0;
+};
+static Profile g_prof;
+
+// Records the start event of the next pair; returns the pair index or -1.
+static int prof_begin(cudaStream_t st) {
+    if (!g_prof.on || g_prof.used >= Profile::kMax) return -1;
+    const int i = g_prof.used;
+    if (i >= g_prof.created) {
+        if (cudaEventCreate(&g_prof.start[i]) != cudaSuccess) return -1;
+        if (cudaEventCreate(&g_prof.stop[i]) != cudaSuccess) return -1;
+        g_prof.created = i + 1;
+    }
+    cudaEventRecord(g_prof.start[i], st);
+    g_prof.used = i + 1;
+    return i;
+}
+static void prof_end(int i, cudaStream_t st) {
+    if (i >= 0) cudaEventRecord(g_prof.stop[i], st);
+}
+static void prof_kernels(int n) {
+    if (g_prof.on) g_prof.kernels += n;
+}
+
+// Shape checks shared by every entry point.
+static mla_status check_shape(const mla_shape *s) {
+    if (!s) return MLA_ERR_INVALID;
+    if (s->num_heads < 1 || s->kv_lora_rank < 8 || s->kv_lora_rank % 8 || s->rope_dim < 0 ||
+        s->rope_dim % 8 || s->v_head_dim < 1 || s->block_size < 1 || s->num_blocks < 1)
+        return MLA_ERR_INVALID;
+    if (s->kind != MLA_KV_BF16 && s->kind != MLA_KV_FP32 && s->kind != MLA_KV_INT2_ROT)
+        return MLA_ERR_INVALID;
+    if (s->impl < MLA_IMPL_AUTO || s->impl > MLA_IMPL_TCGEN05 || s->num_splits_hint < 0)
+        return MLA_ERR_INVALID;
+    if (s->kind == MLA_KV_INT2_ROT) {
+        if (s->group_size < 4 || s->group_size % 4 || s->kv_lora_rank % s->group_size) return MLA_ERR_INVALID;
+        if (s->rope_dim < 8) return MLA_ERR_INVALID;
+    }
+    // generic kernel limits (shared-memory tiles sized from r and d_R)
+    if (s->kv_lora_rank > 1024 || s->rope_dim > 128) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+static ShapeArgs shape_args(const mla_shape *s) {
+    ShapeArgs a;
+    a.H = s->num_heads;
+    a.r = s->kv_lora_rank;
+    a.dR = s->rope_dim;
+    a.dv = s->v_head_dim;
+    a.bs = s->block_size;
+    a.num_blocks = s->num_blocks;
+    a.gs = s->group_size;
+    a.kind = s->kind;
+    return a;
+}
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
+    (void)q_len;
+    if (s->impl == MLA_IMPL_TCGEN05) return MLA_ERR_UNSUPPORTED;
+    return MLA_IMPL_SIMT;
+}
+
+static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {
+    (void)impl;
+    WsLayout w;
+    memset(&w, 0, sizeof w);
+    const int sms = device_sm_count();
+    int target = s->num_splits_hint > 0 ? s->num_splits_hint : (sms > 0 ? sms : 148);
+    w.target = target;
+    w.max_work = target + B;
+    const size_t rows = (size_t)q_len * s->num_heads;
+    size_t off = 0;
+    w.status = off;        off = up256(off + 2 * sizeof(int32_t));
+    w.work = off;          off = up256(off + sizeof(WorkItem) * (size_t)w.max_work);
+    w.split_start = off;   off = up256(off + sizeof(int32_t) * ((size_t)B + 1));
+    w.part_o = off;        off = up256(off + sizeof(float) * (size_t)w.max_work * rows * s->kv_lora_rank);
+    w.part_lse = off;      off = up256(off + sizeof(float) * (size_t)w.max_work * rows);
+    w.q_prep = off;
+    if (s->kind == MLA_KV_INT2_ROT)
+        off = up256(off + sizeof(float) * (size_t)B * rows * (s->kv_lora_rank + s->rope_dim));
+    w.total = off;
+    return w;
+}
+
+static mla_status run_attention(const mla_shape *s, const mla_cache *cache, const int32_t *block_table,
+                                int32_t max_blocks, const int32_t *seq_lens, int32_t B, int32_t q_len,
+                                const void *q, const void *W_UV, const float *R, float scale, void *out,
+                                float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    mla_status st = check_shape(s);
+    if (st != MLA_OK) return st;
+    if (!cache || !block_table || !seq_lens || !q || !W_UV || !out || !lse || !workspace) return MLA_ERR_INVALID;
+    if (B < 1 || q_len < 1 || max_blocks < 1) return MLA_ERR_INVALID;
+    if (!(scale == scale)) return MLA_ERR_INVALID;
+    const bool int2 = s->kind == MLA_KV_INT2_ROT;
+    if (int2) {
+        if (!cache->codes || !cache->scale_zero || !cache->rope || !R) return MLA_ERR_INVALID;
+        if (!aligned16(cache->codes) || !aligned16(cache->scale_zero) || !aligned16(cache->rope)) return MLA_ERR_INVALID;
+    } else {
+        if (!cache->latent || !aligned16(cache->latent)) return MLA_ERR_INVALID;
+    }
+    if (!aligned16(q) || !aligned16(workspace)) return MLA_ERR_INVALID;
+    const int32_t impl = resolve_impl(s, q_len);
+    if (impl < 0) return (mla_status)impl;
+    const WsLayout w = ws_layout(s, B, q_len, impl);
+    if (ws_bytes < w.total) return MLA_ERR_WORKSPACE;
+    cudaStream_t stream_ = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.s = shape_args(s);
+    p.B = B;
+    p.q_len = q_len;
+    p.max_blocks = max_blocks;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.latent = cache->latent;
+    p.codes = (const uint8_t *)cache->codes;
+    p.scale_zero = (const __half *)cache->scale_zero;
+    p.rope = (const __nv_bfloat16 *)cache->rope;
+    p.q = q;
+    p.q_prep = int2 ? (const float *)(ws + w.q_prep) : nullptr;
+    p.scale_log2 = scale * kLog2e;
+    p.status = (int32_t *)(ws + w.status);
+    p.num_work = (const int32_t *)(ws + w.status + sizeof(int32_t));
+    p.work = (const WorkItem *)(ws + w.work);
+    p.split_start = (const int32_t *)(ws + w.split_start);
+    p.part_o = (float *)(ws + w.part_o);
+    p.part_lse = (float *)(ws + w.part_lse);
+
+    if (launch_plan(p, w.target, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    if (int2 && launch_qprep(p, R, (float *)(ws + w.q_prep), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    const int ev = prof_begin(stream_);
+    if (launch_decode_simt(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    prof_end(ev, stream_);
+
+    CombineParams c;
+    memset(&c, 0, sizeof c);
+    c.s = p.s;
+    c.B = B;
+    c.q_len = q_len;
+    c.split_start = p.split_start;
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.R = int2 ? R : nullptr;
+    c.W_UV = W_UV;
+    c.out = out;
+    c.lse = lse;
+    if (launch_combine(c, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    prof_kernels(int2 ? 4 : 3);
+    return MLA_OK;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+size_t mla_workspace_bytes(const mla_shape *shape, int32_t B, int32_t q_len) {
+    if (check_shape(shape) != MLA_OK || B < 1 || q_len < 1) return 0;
+    const int32_t impl = resolve_impl(shape, q_len);
+    if (impl < 0) return 0;
+    return ws_layout(shape, B, q_len, impl).total;
+}
+
+mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                             int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
+                             const int32_t *cu_new, int32_t num_new, const void *c_kv, const void *k_rope,
+                             const float *R, const float *clip, int32_t *status, void *stream) {
+    mla_status st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    if (!cache || !block_table || !start_pos || !cu_new || B < 1 || max_blocks_per_seq < 1 || num_new < 0)
+        return MLA_ERR_INVALID;
+    if (num_new == 0) return MLA_OK;
+    if (!c_kv || !k_rope || !aligned16(c_kv) || !aligned16(k_rope)) return MLA_ERR_INVALID;
+    const bool int2 = shape->kind == MLA_KV_INT2_ROT;
+    if (int2) {
+        if (!cache->codes || !cache->scale_zero || !cache->rope || !R || !clip) return MLA_ERR_INVALID;
+    } else {
+        if (!cache->latent || !aligned16(cache->latent)) return MLA_ERR_INVALID;
+    }
+    AppendParams p;
+    memset(&p, 0, sizeof p);
+    p.s = shape_args(shape);
+    p.B = B;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_new = num_new;
+    p.block_table = block_table;
+    p.start_pos = start_pos;
+    p.cu_new = cu_new;
+    p.c_kv = c_kv;
+    p.k_rope = k_rope;
+    p.R = R;
+    p.clip = clip;
+    p.latent = cache->latent;
+    p.codes = (uint8_t *)cache->codes;
+    p.scale_zero = (__half *)cache->scale_zero;
+    p.rope = (__nv_bfloat16 *)cache->rope;
+    p.status = status;
+    if (launch_append(p, (cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
+    prof_kernels(1);
+    return MLA_OK;
+}
+
+mla_status mla_decode(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, const void *q,
+                      const void *W_UV, const float *R, float scale, void *out, float *lse, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    return run_attention(shape, cache, block_table, max_blocks_per_seq, seq_lens, B, 1, q, W_UV, R, scale, out,
+                         lse, workspace, workspace_bytes, stream);
+}
+
+mla_status mla_verify(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, int32_t q_len,
+                      const void *q, const void *W_UV, const float *R, float scale, void *out, float *lse,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    return run_attention(shape, cache, block_table, max_blocks_per_seq, seq_lens, B, q_len, q, W_UV, R, scale,
+                         out, lse, workspace, workspace_bytes, stream);
+}
+
+static mla_status flags_to_status(int32_t f) {
+    if (f & FLAG_TIMEOUT) return MLA_ERR_TIMEOUT;
+    if (f & (FLAG_BAD_BLOCK | FLAG_BAD_LENGTH)) return MLA_ERR_BOUNDS;
+    return MLA_OK;
+}
+
+mla_status mla_read_status_word(const int32_t *status, int32_t *raw_flags, void *stream) {
+    if (!status) return MLA_ERR_INVALID;
+    int32_t f = 0;
+    if (cudaMemcpyAsync(&f, status, sizeof f, cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (raw_flags) *raw_flags = f;
+    return flags_to_status(f);
+}
+
+mla_status mla_get_status(const void *workspace, int32_t *raw_flags, void *stream) {
+    // The flags word sits at offset 0 of every workspace layout.
+    return mla_read_status_word((const int32_t *)workspace, raw_flags, stream);
+}
+
+const char *mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported shape or implementation";
+        case MLA_ERR_BOUNDS: return "block id or sequence length out of range (device flag)";
+        case MLA_ERR_WORKSPACE: return "workspace too small";
+        case MLA_ERR_CUDA: return "CUDA launch or runtime error";
+        case MLA_ERR_TIMEOUT: return "bounded device wait gave up (device flag)";
+    }
+    return "unknown status";
+}
+
+int32_t mla_resolve_impl(const mla_shape *shape, int32_t q_len) {
+    mla_status st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    if (q_len < 1) return MLA_ERR_INVALID;
+    return resolve_impl(shape, q_len);
+}
+
+mla_status mla_profile_enable(int32_t enable) {
+    g_prof.on = enable != 0;
+    g_prof.used = 0;
+    g_prof.kernels = 0;
+    return MLA_OK;
+}
+
+mla_status mla_profile_read(double *attention_ms, int32_t *attention_launches, int32_t *kernel_launches) {
+    double total = 0.0;
+    for (int i = 0; i < g_prof.used; ++i) {
+        if (cudaEventSynchronize(g_prof.stop[i]) != cudaSuccess) return MLA_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]) != cudaSuccess) return MLA_ERR_CUDA;
+        total += ms;
+    }
+    if (attention_ms) *attention_ms = total;
+    if (attention_launches) *attention_launches = g_prof.used;
+    if (kernel_launches) *kernel_launches = g_prof.kernels;
+    return MLA_OK;
+}
+
+int32_t mla_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// Internal declarations shared by the library's translation units (not part
+// of the ABI). Kernel parameter blocks, the workspace layout and small device
+// helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Device status flags (OR-ed into the status word).
+enum : int32_t {
+    FLAG_BAD_BLOCK = 1,      // a block id outside [0, num_blocks) or a logical block past the table
+    FLAG_BAD_LENGTH = 2,     // a sequence length outside [q_len, max_blocks * block_size]
+    FLAG_TIMEOUT = 4,        // a bounded wait gave up
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Work item of the split-KV schedule: tokens [t0, t1) of sequence b, whose
+// partial result goes to partial slot `slot`.
+struct WorkItem {
+    int32_t b, t0, t1, slot;
+};
+
+// Byte offsets inside the caller's workspace.
+struct WsLayout {
+    size_t status;        // int32 flags word, then int32 num_work
+    size_t work;          // WorkItem[max_work]
+    size_t split_start;   // int32[B + 1]: first slot of each sequence
+    size_t part_o;        // fp32 [max_work][q_len * H][r]  normalised partial outputs
+    size_t part_lse;      // fp32 [max_work][q_len * H]     partial log2-sum-exp
+    size_t q_prep;        // fp32 [B * q_len * H][r + d_R]  rotated query (INT2 kind)
+    size_t total;
+    int32_t max_work;     // upper bound of schedule length
+    int32_t target;       // schedule target passed to the planner kernel
+};
+
+struct ShapeArgs {
+    int32_t H, r, dR, dv, bs, num_blocks, gs, kind;
+    __host__ __device__ int32_t D() const { return r + dR; }
+};
+
+// Everything a decode kernel reads.
+struct DecodeParams {
+    ShapeArgs s;
+    int32_t B, q_len, max_blocks;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const void *latent;          // BF16 / FP32 kinds
+    const uint8_t *codes;        // INT2
+    const __half *scale_zero;    // INT2
+    const __nv_bfloat16 *rope;   // INT2
+    const void *q;               // caller's absorbed query
+    const float *q_prep;         // INT2: rotated query (fp32), else nullptr
+    float scale_log2;            // scale * log2(e)
+    int32_t *status;             // -> flags word
+    const int32_t *num_work;
+    const WorkItem *work;
+    const int32_t *split_start;
+    float *part_o;
+    float *part_lse;
+};
+
+struct CombineParams {
+    ShapeArgs s;
+    int32_t B, q_len;
+    const int32_t *split_start;
+    const float *part_o;
+    const float *part_lse;
+    const float *R;              // INT2: [r, r], else nullptr
+    const void *W_UV;            // [H, r, dv]
+    void *out;                   // [B, q_len, H, dv]
+    float *lse;                  // [B, q_len, H]
+};
+
+struct AppendParams {
+    ShapeArgs s;
+    int32_t B, max_blocks, num_new;
+    const int32_t *block_table;
+    const int32_t *start_pos;
+    const int32_t *cu_new;
+    const void *c_kv;
+    const void *k_rope;
+    const float *R;
+    const float *clip;
+    void *latent;
+    uint8_t *codes;
+    __half *scale_zero;
+    __nv_bfloat16 *rope;
+    int32_t *status;
+};
+
+// ---- launchers (defined in mla_simt.cu) ------------------------------------
+cudaError_t launch_plan(const DecodeParams &p, int32_t target, int32_t max_work, cudaStream_t st);
+cudaError_t launch_qprep(const DecodeParams &p, const float *R, float *q_prep, cudaStream_t st);
+cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
+
+// ---- small device helpers ---------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ void raise_flag(int32_t *status, int32_t f) {
+    if (status) atomicOr(status, f);
+}
+
+}  // namespace mla

@@ -1,0 +1,685 @@
+// CUDA-core kernels of the library: the split-KV planner, the append /
+// quantise path, the query rotation, the generic decode and the split combine
+// with the W_UV up-projection.
+//
+// The generic decode handles every supported shape and cache kind; the
+// tensor-core decode (mla_tc.cu) replaces it for the DeepSeek-V3-shaped bf16
+// and INT2 caches. Both write the same partial format, so the planner and the
+// combine here serve both.
+#include "mla_internal.cuh"
+
+#include <math_constants.h>
+
+namespace mla {
+
+// ============================================================================
+// Planner: split every sequence into token ranges of `chunk` tokens, where
+// chunk = max(64, ceil64(sum_b L_b / target)). The number of work items is then
+// at most target + B. One CTA; the schedule lives in the workspace so the
+// decode launch never needs the lengths on the host.
+// ============================================================================
+__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t target, int32_t max_work) {
+    __shared__ long long s_total;
+    __shared__ int32_t s_chunk;
+    __shared__ int32_t s_carry;
+    __shared__ int32_t s_warp[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t cap = (int64_t)p.max_blocks * p.s.bs;
+    if (tid == 0) { s_total = 0; s_carry = 0; p.status[0] = 0; }
+    __syncthreads();
+    long long local = 0;
+    for (int b = tid; b < p.B; b += blockDim.x) {
+        int L = p.seq_lens[b];
+        if (L >= p.q_len && L <= cap) local += L;
+    }
+    atomicAdd((unsigned long long *)&s_total, (unsigned long long)local);
+    __syncthreads();
+    if (tid == 0) {
+        long long per = (s_total + target - 1) / target;
+        per = ((per + 63) / 64) * 64;
+        if (per < 64) per = 64;
+        if (per > 0x40000000LL) per = 0x40000000LL;
+        s_chunk = (int32_t)per;
+    }
+    __syncthreads();
+    const int32_t chunk = s_chunk;
+    // Block-wide exclusive scan of split counts, 1024 sequences per pass.
+    for (int base = 0; base < p.B; base += blockDim.x) {
+        const int b = base + tid;
+        int n = 0, L = 0;
+        if (b < p.B) {
+            L = p.seq_lens[b];
+            if (L >= p.q_len && L <= cap) n = (L + chunk - 1) / chunk;
+            else raise_flag(p.status, FLAG_BAD_LENGTH);
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int v = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+            int w = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int u = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += u;
+            }
+            s_warp[lane] = w - v;   // exclusive prefix of warp totals
+        }
+        __syncthreads();
+        const int start = s_carry + s_warp[warp] + incl - n;
+        if (b < p.B) {
+            ((int32_t *)p.split_start)[b] = start;
+            for (int k = 0; k < n && start + k < max_work; ++k) {
+                WorkItem it;
+                it.b = b;
+                it.t0 = k * chunk;
+                it.t1 = min((k + 1) * chunk, L);
+                it.slot = start + k;
+                ((WorkItem *)p.work)[start + k] = it;
+            }
+        }
+        __syncthreads();
+        if (tid == blockDim.x - 1) s_carry = start + n;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        ((int32_t *)p.split_start)[p.B] = s_carry;
+        ((int32_t *)p.num_work)[0] = min(s_carry, max_work);
+    }
+}
+
+cudaError_t launch_plan(const DecodeParams &p, int32_t target, int32_t max_work, cudaStream_t st) {
+    plan_kernel<<<1, 1024, 0, st>>>(p, target, max_work);
+    return cudaGetLastError();
+}
+
+// ============================================================================
+// Query rotation for the rotated-INT2 cache: q_prep[row] = [q_lat . R ; q_R],
+// fp32 accumulation. 32 query rows per CTA, each thread owns NC output dims.
+// ============================================================================
+template <int NC>
+__global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float *R, float *q_prep, int rows) {
+    extern __shared__ float sq[];                 // [32][r]
+    const int r = p.s.r, D = p.s.D();
+    const int row0 = blockIdx.x * 32;
+    const __nv_bfloat16 *q = (const __nv_bfloat16 *)p.q;
+    for (int idx = threadIdx.x; idx < 32 * r; idx += blockDim.x) {
+        int rr = idx / r, k = idx % r, row = row0 + rr;
+        sq[idx] = row < rows ? __bfloat162float(q[(size_t)row * D + k]) : 0.f;
+    }
+    __syncthreads();
+    float acc[32][NC];
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[rr][c] = 0.f;
+    for (int k = 0; k < r; ++k) {
+        float Rk[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            int j = threadIdx.x + 256 * c;
+            Rk[c] = j < r ? __ldg(R + (size_t)k * r + j) : 0.f;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+            float qv = sq[rr * r + k];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[rr][c] = fmaf(qv, Rk[c], acc[rr][c]);
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) {
+        int row = row0 + rr;
+        if (row >= rows) break;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            int j = threadIdx.x + 256 * c;
+            if (j < r) q_prep[(size_t)row * D + j] = acc[rr][c];
+        }
+        for (int j = threadIdx.x; j < p.s.dR; j += blockDim.x)
+            q_prep[(size_t)row * D + r + j] = __bfloat162float(q[(size_t)row * D + r + j]);
+    }
+}
+
+cudaError_t launch_qprep(const DecodeParams &p, const float *R, float *q_prep, cudaStream_t st) {
+    const int rows = p.B * p.q_len * p.s.H;
+    const size_t smem = (size_t)32 * p.s.r * sizeof(float);
+    dim3 grid((rows + 31) / 32);
+    if (p.s.r <= 256) {
+        cudaFuncSetAttribute(qprep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<1><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+    } else if (p.s.r <= 512) {
+        cudaFuncSetAttribute(qprep_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<2><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+    } else {
+        cudaFuncSetAttribute(qprep_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<4><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+    }
+    return cudaGetLastError();
+}
+
+// ============================================================================
+// Generic split-KV decode. One CTA = one work item x 16 query rows (a row is a
+// (draft position i, head h) pair). Per 32-token tile: gather the tile through
+// the block table into shared memory as fp32 (dequantising INT2), scores with
+// one lane per token, online softmax per row in log2 units, then P.C into
+// per-thread accumulators (thread owns latent dims tid + 256c for all rows).
+// Output: normalised partial latent output and its log2-sum-exp per row.
+// ============================================================================
+constexpr int kRB = 16;   // query rows per CTA
+constexpr int kTT = 32;   // tokens per tile
+
+template <int KIND>
+__device__ __forceinline__ void gather_tile(const DecodeParams &p, int b, int tb, int t1, float *sK,
+                                            int Dp, int *sValid) {
+    const int D = p.s.D(), r = p.s.r, dR = p.s.dR, bs = p.s.bs;
+    if (threadIdx.x < kTT) {
+        int t = tb + threadIdx.x;
+        int ok = 0;
+        if (t < t1) {
+            int lb = t / bs;
+            int blk = lb < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + lb] : -1;
+            if (blk >= 0 && blk < p.s.num_blocks) ok = 1 + blk;   // store blk+1
+            else raise_flag(p.status, FLAG_BAD_BLOCK);
+        }
+        sValid[threadIdx.x] = ok;
+    }
+    __syncthreads();
+    if (KIND == MLA_KV_BF16) {
+        const int nvec = D / 8;                       // 16-byte chunks per token row
+        for (int idx = threadIdx.x; idx < kTT * nvec; idx += blockDim.x) {
+            int tt = idx / nvec, v = idx % nvec;
+            int blk1 = sValid[tt];
+            float *dst = sK + tt * Dp + v * 8;
+            if (blk1) {
+                size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
+                uint4 u = *((const uint4 *)((const __nv_bfloat16 *)p.latent + row * D) + v);
+                const __nv_bfloat16 *h = (const __nv_bfloat16 *)&u;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dst[e] = __bfloat162float(h[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dst[e] = 0.f;
+            }
+        }
+    } else if (KIND == MLA_KV_FP32) {
+        const int nvec = D / 4;
+        for (int idx = threadIdx.x; idx < kTT * nvec; idx += blockDim.x) {
+            int tt = idx / nvec, v = idx % nvec;
+            int blk1 = sValid[tt];
+            float *dst = sK + tt * Dp + v * 4;
+            if (blk1) {
+                size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
+                float4 u = *((const float4 *)((const float *)p.latent + row * D) + v);
+                dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
+            } else {
+                dst[0] = dst[1] = dst[2] = dst[3] = 0.f;
+            }
+        }
+    } else {
+        // INT2: one thread per code byte (4 latent dims), then the bf16 rope key.
+        const int nbytes = r / 4, gs = p.s.gs, ng = r / gs;
+        for (int idx = threadIdx.x; idx < kTT * nbytes; idx += blockDim.x) {
+            int tt = idx / nbytes, k = idx % nbytes;
+            int blk1 = sValid[tt];
+            float *dst = sK + tt * Dp + 4 * k;
+            if (blk1) {
+                size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
+                unsigned byte = p.codes[row * nbytes + k];
+                int g = (4 * k) / gs;
+                float sc = __half2float(p.scale_zero[(row * ng + g) * 2 + 0]);
+                float zr = __half2float(p.scale_zero[(row * ng + g) * 2 + 1]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = __fmaf_rn((float)((byte >> (2 * e)) & 3u), sc, zr);
+            } else {
+                dst[0] = dst[1] = dst[2] = dst[3] = 0.f;
+            }
+        }
+        for (int idx = threadIdx.x; idx < kTT * dR; idx += blockDim.x) {
+            int tt = idx / dR, d = idx % dR;
+            int blk1 = sValid[tt];
+            float v = 0.f;
+            if (blk1) {
+                size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
+                v = __bfloat162float(p.rope[row * dR + d]);
+            }
+            sK[tt * Dp + r + d] = v;
+        }
+    }
+}
+
+template <int KIND, int NC>
+__global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
+    const int w = blockIdx.x;
+    if (w >= p.num_work[0]) return;
+    const WorkItem item = p.work[w];
+    const int b = item.b, t0 = item.t0, t1 = item.t1, slot = item.slot;
+    const int H = p.s.H, r = p.s.r, D = p.s.D(), Dp = D + 1;
+    const int rows_total = p.q_len * H;
+    const int row0 = blockIdx.y * kRB;
+    if (row0 >= rows_total) return;
+    const int L = p.seq_lens[b];
+
+    extern __shared__ float smem[];
+    float *sQ = smem;                     // [kRB][D]
+    float *sK = sQ + kRB * D;             // [kTT][Dp]
+    float *sP = sK + kTT * Dp;            // [kRB][kTT]
+    float *sA = sP + kRB * kTT;           // [kRB] rescale factors
+    float *sL = sA + kRB;                 // [kRB]
+    float *sM = sL + kRB;                 // [kRB]
+    int *sValid = (int *)(sM + kRB);      // [kTT]
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_bad = 0;
+    for (int idx = tid; idx < kRB * D; idx += blockDim.x) {
+        int rr = idx / D, d = idx % D, row = row0 + rr;
+        float v = 0.f;
+        if (row < rows_total) {
+            size_t off = ((size_t)b * rows_total + row) * D + d;   // q is [B][q_len][H][D]
+            if (KIND == MLA_KV_INT2_ROT) v = p.q_prep[off];
+            else if (KIND == MLA_KV_FP32) v = ((const float *)p.q)[off];
+            else v = __bfloat162float(((const __nv_bfloat16 *)p.q)[off]);
+        }
+        sQ[idx] = v;
+    }
+
+    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.f, 0.f};
+    int last_vis[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        int row = row0 + warp + 8 * j;
+        last_vis[j] = row < rows_total ? (L - p.q_len + row / H) : -1;
+    }
+    float acc[kRB][NC];
+#pragma unroll
+    for (int rr = 0; rr < kRB; ++rr)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[rr][c] = 0.f;
+
+    for (int tb = t0; tb < t1; tb += kTT) {
+        __syncthreads();                  // previous tile fully consumed
+        gather_tile<KIND>(p, b, tb, t1, sK, Dp, sValid);
+        __syncthreads();
+        if (tid < kTT && tb + tid < t1 && !sValid[tid]) s_bad = 1;
+        float sc[2];
+        {
+            // both rows of this warp against the lane's token, 4 independent chains
+            const float *q0 = sQ + warp * D, *q1 = sQ + (warp + 8) * D, *kr = sK + lane * Dp;
+            float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+            for (int d = 0; d < D; d += 2) {
+                const float k0 = kr[d], k1 = kr[d + 1];
+                a0 = fmaf(q0[d], k0, a0);
+                a1 = fmaf(q0[d + 1], k1, a1);
+                c0 = fmaf(q1[d], k0, c0);
+                c1 = fmaf(q1[d + 1], k1, c1);
+            }
+            sc[0] = a0 + a1;
+            sc[1] = c0 + c1;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int rr = warp + 8 * j;
+            const float s = sc[j];
+            const int t = tb + lane;
+            const bool vis = (t < t1) && (t <= last_vis[j]) && sValid[lane];
+            const float s2 = vis ? s * p.scale_log2 : -CUDART_INF_F;
+            const float m_new = fmaxf(m_run[j], warp_max(s2));
+            const float pr = vis ? exp2f(s2 - m_new) : 0.f;
+            const float alpha = (m_new == -CUDART_INF_F) ? 1.f : exp2f(m_run[j] - m_new);
+            l_run[j] = l_run[j] * alpha + warp_sum(pr);
+            m_run[j] = m_new;
+            sP[rr * kTT + lane] = pr;
+            if (lane == 0) sA[rr] = alpha;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int rr = 0; rr < kRB; ++rr) {
+            const float a = sA[rr];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[rr][c] *= a;
+        }
+        const int ntok = min(kTT, t1 - tb);
+        for (int tt = 0; tt < ntok; ++tt) {
+            float kv[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                int d = tid + 256 * c;
+                kv[c] = d < r ? sK[tt * Dp + d] : 0.f;
+            }
+#pragma unroll
+            for (int rr = 0; rr < kRB; ++rr) {
+                const float pr = sP[rr * kTT + tt];
+#pragma unroll
+                for (int c = 0; c < NC; ++c) acc[rr][c] = fmaf(pr, kv[c], acc[rr][c]);
+            }
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            sL[warp + 8 * j] = l_run[j];
+            sM[warp + 8 * j] = m_run[j];
+        }
+    }
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    for (int rr = 0; rr < kRB; ++rr) {
+        const int row = row0 + rr;
+        if (row >= rows_total) break;
+        const float l = sL[rr];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float *po = p.part_o + ((size_t)slot * rows_total + row) * r;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            int d = tid + 256 * c;
+            if (d < r) po[d] = acc[rr][c] * inv;
+        }
+        if (tid == 0)
+            p.part_lse[(size_t)slot * rows_total + row] =
+                bad ? CUDART_NAN_F : (l > 0.f ? sM[rr] + log2f(l) : -CUDART_INF_F);
+    }
+}
+
+template <int KIND>
+static cudaError_t launch_decode_kind(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
+    const int D = p.s.D();
+    const size_t smem = sizeof(float) * ((size_t)kRB * D + (size_t)kTT * (D + 1) + kRB * kTT + 3 * kRB) +
+                        sizeof(int) * kTT;
+    dim3 grid(max_work, (p.q_len * p.s.H + kRB - 1) / kRB);
+    if (p.s.r <= 256) {
+        cudaFuncSetAttribute(decode_simt_kernel<KIND, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_simt_kernel<KIND, 1><<<grid, 256, smem, st>>>(p);
+    } else if (p.s.r <= 512) {
+        cudaFuncSetAttribute(decode_simt_kernel<KIND, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_simt_kernel<KIND, 2><<<grid, 256, smem, st>>>(p);
+    } else {
+        cudaFuncSetAttribute(decode_simt_kernel<KIND, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_simt_kernel<KIND, 4><<<grid, 256, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
+    switch (p.s.kind) {
+        case MLA_KV_BF16: return launch_decode_kind<MLA_KV_BF16>(p, max_work, st);
+        case MLA_KV_FP32: return launch_decode_kind<MLA_KV_FP32>(p, max_work, st);
+        default: return launch_decode_kind<MLA_KV_INT2_ROT>(p, max_work, st);
+    }
+}
+
+// ============================================================================
+// Combine: merge the split partials of each (b, i, h) row by their log2-sum-
+// exp, rotate back (INT2: o_lat = o_rot . R^T) and up-project through W_UV^h.
+// One CTA = one head x 8 rows (b, i), so W_UV^h is read once per 8 rows.
+// ============================================================================
+constexpr int kCR = 8;
+
+template <bool FP32IO>
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+    extern __shared__ float cs[];
+    const int H = p.s.H, r = p.s.r, dv = p.s.dv;
+    const int h = blockIdx.x;
+    const int nrows = p.B * p.q_len;
+    const int rb0 = blockIdx.y * kCR;
+    float *so = cs;                       // [kCR][r]
+    float *st = so + kCR * r;             // [kCR][r] (INT2 rotation target)
+    float *slse = st + kCR * r;           // [kCR]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rows_total = p.q_len * H;
+
+    // warp w merges row rb0 + w
+    if (warp < kCR) {
+        const int rb = rb0 + warp;
+        float *dst = so + warp * r;
+        if (rb < nrows) {
+            const int b = rb / p.q_len, i = rb % p.q_len;
+            const int s0 = p.split_start[b], s1 = p.split_start[b + 1];
+            const int row = i * H + h;
+            float M = -CUDART_INF_F;
+            bool nan = (s1 <= s0);
+            for (int s = s0; s < s1; ++s) {
+                float v = p.part_lse[(size_t)s * rows_total + row];
+                if (isnan(v)) nan = true;
+                M = fmaxf(M, v);
+            }
+            float tot = 0.f;
+            for (int s = s0; s < s1; ++s) {
+                float v = p.part_lse[(size_t)s * rows_total + row];
+                tot += (v == -CUDART_INF_F) ? 0.f : exp2f(v - M);
+            }
+            const float inv = tot > 0.f ? 1.f / tot : 0.f;
+            for (int d = lane; d < r; d += 32) {
+                float a = 0.f;
+                for (int s = s0; s < s1; ++s) {
+                    float v = p.part_lse[(size_t)s * rows_total + row];
+                    float wgt = (v == -CUDART_INF_F) ? 0.f : exp2f(v - M) * inv;
+                    a = fmaf(wgt, p.part_o[((size_t)s * rows_total + row) * r + d], a);
+                }
+                dst[d] = nan ? CUDART_NAN_F : a;
+            }
+            if (lane == 0) slse[warp] = nan ? CUDART_NAN_F : (M + log2f(tot)) * kLn2;
+        } else {
+            for (int d = lane; d < r; d += 32) dst[d] = 0.f;
+        }
+    }
+    __syncthreads();
+    const float *src = so;
+    if (p.R) {
+        // o_lat[j] = sum_k R[j][k] o_rot[k]: a warp per (row, j), lanes over k.
+        for (int job = warp; job < kCR * r; job += 8) {
+            const int rr = job / r, j = job % r;
+            const float *Rj = p.R + (size_t)j * r;
+            float a = 0.f;
+            for (int k = lane; k < r; k += 32) a = fmaf(__ldg(Rj + k), so[rr * r + k], a);
+            a = warp_sum(a);
+            if (lane == 0) st[rr * r + j] = a;
+        }
+        __syncthreads();
+        src = st;
+    }
+    // out[v] = sum_k o_lat[k] W_UV[h][k][v]; thread -> (v, k-phase)
+    for (int v0 = 0; v0 < dv; v0 += 256) {
+        const int v = v0 + tid;
+        float a[kCR];
+#pragma unroll
+        for (int rr = 0; rr < kCR; ++rr) a[rr] = 0.f;
+        if (v < dv) {
+            for (int k = 0; k < r; ++k) {
+                float wv;
+                if (FP32IO) wv = __ldg((const float *)p.W_UV + ((size_t)h * r + k) * dv + v);
+                else wv = __bfloat162float(((const __nv_bfloat16 *)p.W_UV)[((size_t)h * r + k) * dv + v]);
+#pragma unroll
+                for (int rr = 0; rr < kCR; ++rr) a[rr] = fmaf(src[rr * r + k], wv, a[rr]);
+            }
+#pragma unroll
+            for (int rr = 0; rr < kCR; ++rr) {
+                const int rb = rb0 + rr;
+                if (rb >= nrows) break;
+                const size_t o = ((size_t)rb * H + h) * dv + v;
+                const float val = isnan(slse[rr]) ? CUDART_NAN_F : a[rr];
+                if (FP32IO) ((float *)p.out)[o] = val;
+                else ((__nv_bfloat16 *)p.out)[o] = __float2bfloat16_rn(val);
+            }
+        }
+    }
+    if (tid < kCR) {
+        const int rb = rb0 + tid;
+        if (rb < nrows) p.lse[(size_t)rb * H + h] = slse[tid];
+    }
+}
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t st) {
+    const size_t smem = sizeof(float) * ((size_t)2 * kCR * p.s.r + kCR);
+    dim3 grid(p.s.H, (p.B * p.q_len + kCR - 1) / kCR);
+    if (p.s.kind == MLA_KV_FP32) {
+        cudaFuncSetAttribute(combine_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        combine_kernel<true><<<grid, 256, smem, st>>>(p);
+    } else {
+        cudaFuncSetAttribute(combine_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        combine_kernel<false><<<grid, 256, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+// ============================================================================
+// Append. BF16 / FP32: one warp per new token, 16-byte vector copies of the
+// latent and rope key into the token's slot. INT2: 16 tokens per CTA; rotation
+// y = c . R as an fp32 fmaf chain over k ascending (the encoding definition's
+// order, which fixes the integer codes), then per (token, group) clip, range,
+// fp16 scale/zero, codes and 2-bit packing.
+// ============================================================================
+__device__ __forceinline__ int find_seq(const int32_t *cu_new, int B, int n) {
+    int lo = 0, hi = B - 1;                   // largest b with cu_new[b] <= n
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (cu_new[mid] <= n) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Returns the token row index (blk * bs + slot) or -1 after raising a flag.
+__device__ __forceinline__ long long locate_slot(const AppendParams &p, int n) {
+    const int b = find_seq(p.cu_new, p.B, n);
+    const int pos = p.start_pos[b] + (n - p.cu_new[b]);
+    const int lb = pos / p.s.bs;
+    if (pos < 0 || lb >= p.max_blocks) { raise_flag(p.status, FLAG_BAD_BLOCK); return -1; }
+    const int blk = p.block_table[(size_t)b * p.max_blocks + lb];
+    if (blk < 0 || blk >= p.s.num_blocks) { raise_flag(p.status, FLAG_BAD_BLOCK); return -1; }
+    return (long long)blk * p.s.bs + pos % p.s.bs;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
+    const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (n >= p.num_new) return;
+    long long row = 0;
+    if (lane == 0) row = locate_slot(p, n);
+    row = __shfl_sync(0xffffffffu, row, 0);
+    if (row < 0) return;
+    constexpr int E = 16 / sizeof(T);            // elements per 16-byte vector
+    const int r = p.s.r, dR = p.s.dR, D = r + dR;
+    uint4 *dst = (uint4 *)((T *)p.latent + (size_t)row * D);
+    const uint4 *src_c = (const uint4 *)((const T *)p.c_kv + (size_t)n * r);
+    const uint4 *src_r = (const uint4 *)((const T *)p.k_rope + (size_t)n * dR);
+    for (int v = lane; v < r / E; v += 32) dst[v] = src_c[v];
+    for (int v = lane; v < dR / E; v += 32) dst[r / E + v] = src_r[v];
+}
+
+constexpr int kAT = 16;   // tokens per INT2 append CTA
+
+template <int NC>
+__global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
+    extern __shared__ float sa[];
+    const int r = p.s.r, dR = p.s.dR, gs = p.s.gs, ng = r / gs;
+    float *sc = sa;                   // [kAT][r] latent (fp32)
+    float *sy = sc + kAT * r;         // [kAT][r] rotated
+    __shared__ long long s_row[kAT];
+    const int n0 = blockIdx.x * kAT;
+    const int tid = threadIdx.x;
+    if (tid < kAT) s_row[tid] = (n0 + tid < p.num_new) ? locate_slot(p, n0 + tid) : -1;
+    const __nv_bfloat16 *c = (const __nv_bfloat16 *)p.c_kv;
+    for (int idx = tid; idx < kAT * r; idx += blockDim.x) {
+        int t = idx / r, k = idx % r;
+        sc[idx] = (n0 + t < p.num_new) ? __bfloat162float(c[(size_t)(n0 + t) * r + k]) : 0.f;
+    }
+    __syncthreads();
+    float acc[kAT][NC];
+#pragma unroll
+    for (int t = 0; t < kAT; ++t)
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) acc[t][cc] = 0.f;
+    for (int k = 0; k < r; ++k) {
+        float Rk[NC];
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) {
+            int j = tid + 256 * cc;
+            Rk[cc] = j < r ? __ldg(p.R + (size_t)k * r + j) : 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < kAT; ++t) {
+            const float cv = sc[t * r + k];
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) acc[t][cc] = __fmaf_rn(cv, Rk[cc], acc[t][cc]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kAT; ++t)
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) {
+            int j = tid + 256 * cc;
+            if (j < r) sy[t * r + j] = acc[t][cc];
+        }
+    __syncthreads();
+    for (int job = tid; job < kAT * ng; job += blockDim.x) {
+        const int t = job / ng, g = job % ng;
+        const long long row = s_row[t];
+        if (row < 0) continue;
+        const float thr = p.clip[g];
+        const float *y = sy + t * r + g * gs;
+        float lo = CUDART_INF_F, hi = -CUDART_INF_F;
+        for (int j = 0; j < gs; ++j) {
+            float v = fminf(fmaxf(y[j], -thr), thr);
+            lo = fminf(lo, v);
+            hi = fmaxf(hi, v);
+        }
+        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+        const __half z16 = __float2half_rn(lo);
+        const float s = __half2float(s16), z = __half2float(z16);
+        uint8_t *dst = p.codes + (size_t)row * (r / 4) + g * (gs / 4);
+        for (int j4 = 0; j4 < gs / 4; ++j4) {
+            unsigned byte = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v = fminf(fmaxf(y[4 * j4 + e], -thr), thr);
+                int code = 0;
+                if (s != 0.f) {
+                    float qv = rintf(__fdiv_rn(__fsub_rn(v, z), s));
+                    code = qv < 0.f ? 0 : (qv > 3.f ? 3 : (int)qv);
+                }
+                byte |= (unsigned)code << (2 * e);
+            }
+            dst[j4] = (uint8_t)byte;
+        }
+        __half *szp = p.scale_zero + ((size_t)row * ng + g) * 2;
+        szp[0] = s16;
+        szp[1] = z16;
+    }
+    const __nv_bfloat16 *kr = (const __nv_bfloat16 *)p.k_rope;
+    for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
+        const int t = idx / dR, d = idx % dR;
+        const long long row = s_row[t];
+        if (row >= 0) p.rope[(size_t)row * dR + d] = kr[(size_t)(n0 + t) * dR + d];
+    }
+}
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
+    if (p.num_new == 0) return cudaSuccess;
+    if (p.s.kind == MLA_KV_BF16) {
+        append_copy_kernel<__nv_bfloat16><<<(p.num_new + 7) / 8, 256, 0, st>>>(p);
+    } else if (p.s.kind == MLA_KV_FP32) {
+        append_copy_kernel<float><<<(p.num_new + 7) / 8, 256, 0, st>>>(p);
+    } else {
+        const size_t smem = sizeof(float) * 2 * kAT * (size_t)p.s.r;
+        dim3 grid((p.num_new + kAT - 1) / kAT);
+        if (p.s.r <= 256) {
+            cudaFuncSetAttribute(append_int2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<1><<<grid, 256, smem, st>>>(p);
+        } else if (p.s.r <= 512) {
+            cudaFuncSetAttribute(append_int2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<2><<<grid, 256, smem, st>>>(p);
+        } else {
+            cudaFuncSetAttribute(append_int2_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<4><<<grid, 256, smem, st>>>(p);
+        }
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mla

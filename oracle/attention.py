@@ -77,11 +77,12 @@ def absorbed(q: np.ndarray, C: np.ndarray, KR: np.ndarray, W_UV: np.ndarray, sca
     q_len, H, D = q.shape
     L, r = C.shape
     K = np.concatenate([C, KR], axis=1)                      # [L, r + d_R]
-    S = scale * np.einsum("qhd,ld->qhl", q, K)               # [q_len, H, L]
+    S = scale * (q.reshape(q_len * H, D) @ K.T).reshape(q_len, H, L)
     vis = causal_visible(q_len, L)[:, None, :]
     P, lse = _softmax_stats(S, vis)
-    olat = np.einsum("qhl,lr->qhr", P, C)                    # latent-space output
-    out = np.einsum("qhr,hrv->qhv", olat, W_UV.astype(np.float64))
+    olat = (P.reshape(q_len * H, L) @ C).reshape(q_len, H, r)   # latent-space output
+    # per head: o_h = olat_h . W_UV^h
+    out = np.matmul(olat.transpose(1, 0, 2), W_UV.astype(np.float64)).transpose(1, 0, 2)
     if return_latent:
         return out, lse, olat
     return out, lse

@@ -44,12 +44,16 @@ static float f16_bits_to_f32(uint16_t b) {
 
 /* y[n][r] = c[n][r] . R[r][r], fp32 fused-multiply-add chain, ascending k. */
 void oracle_rotate_chain(const float *c, const float *R, int64_t n, int r, float *y) {
+    /* Each output keeps its own chain y_j <- fmaf(c_k, R[k][j], y_j) for
+     * k = 0, 1, ..., r-1; the loops visit k outermost only so that R is read
+     * row by row. */
     for (int64_t t = 0; t < n; ++t) {
         const float *ct = c + t * r;
-        for (int j = 0; j < r; ++j) {
-            float acc = 0.0f;
-            for (int k = 0; k < r; ++k) acc = fmaf(ct[k], R[(int64_t)k * r + j], acc);
-            y[t * r + j] = acc;
+        float *yt = y + t * r;
+        for (int j = 0; j < r; ++j) yt[j] = 0.0f;
+        for (int k = 0; k < r; ++k) {
+            const float *Rk = R + (int64_t)k * r;
+            for (int j = 0; j < r; ++j) yt[j] = fmaf(ct[k], Rk[j], yt[j]);
         }
     }
 }

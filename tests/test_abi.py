@@ -1,0 +1,90 @@
+"""The C-ABI library: it builds for sm_103a, loads without a GPU, exports every
+symbol include/mla.h declares, and its host-side checks reject bad arguments
+before anything is launched. No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_latent_kv_08_gb300 import build
+    build.build()
+    import mla_latent_kv_08_gb300 as mla
+    return mla.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    import mla_latent_kv_08_gb300 as mla
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(mla.EXPORTED) == names
+
+
+def test_status_strings_and_version(lib):
+    import mla_latent_kv_08_gb300 as mla
+    assert mla.mla_version() == 100
+    for code in range(-6, 1):
+        assert mla.status_string(code) != "unknown status"
+    assert mla.status_string(-99) == "unknown status"
+
+
+def _shape(**kw):
+    import mla_latent_kv_08_gb300 as mla
+    base = dict(num_heads=128, kv_lora_rank=512, rope_dim=64, v_head_dim=128, block_size=64, num_blocks=10)
+    base.update(kw)
+    return mla.Shape(**base)
+
+
+def test_shape_validation(lib):
+    import mla_latent_kv_08_gb300 as mla
+    assert mla.mla_resolve_impl(_shape()) in (mla.MLA_IMPL_SIMT, mla.MLA_IMPL_TCGEN05)
+    assert mla.mla_resolve_impl(_shape(kv_lora_rank=500)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(rope_dim=7)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=7)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, group_size=6)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kv_lora_rank=2048)) == mla.MLA_ERR_UNSUPPORTED
+    assert mla.mla_resolve_impl(_shape(), q_len=0) == mla.MLA_ERR_INVALID
+    # the generic kernel takes any supported shape, e.g. the tiny fp32 one
+    assert mla.mla_resolve_impl(_shape(num_heads=8, kv_lora_rank=64, rope_dim=16, v_head_dim=32,
+                                       block_size=256, kind=mla.MLA_KV_FP32)) == mla.MLA_IMPL_SIMT
+
+
+def test_workspace_size_scales(lib):
+    import mla_latent_kv_08_gb300 as mla
+    a = mla.mla_workspace_bytes(_shape(), 32, 1)
+    b = mla.mla_workspace_bytes(_shape(), 32, 8)
+    assert 0 < a < b
+    with pytest.raises(mla.MlaError):
+        mla.mla_workspace_bytes(_shape(kv_lora_rank=7), 32, 1)
+
+
+def test_null_arguments_rejected_before_launch(lib):
+    import mla_latent_kv_08_gb300 as mla
+    s = _shape().c()
+    cache = mla.mla_cache(None, None, None, None)
+    rc = lib.mla_decode(ctypes.byref(s), ctypes.byref(cache), None, 4, None, 2, None, None, None,
+                        ctypes.c_float(0.1), None, None, None, 0, None)
+    assert rc == mla.MLA_ERR_INVALID
+    rc = lib.mla_verify(ctypes.byref(s), ctypes.byref(cache), None, 4, None, 2, 3, None, None, None,
+                        ctypes.c_float(0.1), None, None, None, 0, None)
+    assert rc == mla.MLA_ERR_INVALID
+    rc = lib.mla_latent_append(ctypes.byref(s), ctypes.byref(cache), None, 4, 2, None, None, 5, None, None,
+                               None, None, None, None)
+    assert rc == mla.MLA_ERR_INVALID
+    rc = lib.mla_decode(None, ctypes.byref(cache), None, 4, None, 2, None, None, None,
+                        ctypes.c_float(0.1), None, None, None, 0, None)
+    assert rc == mla.MLA_ERR_INVALID
+    assert lib.mla_get_status(None, None, None) == mla.MLA_ERR_INVALID

@@ -1,0 +1,225 @@
+"""GPU parity: the library (through its C ABI) against the CPU oracle on the
+same seeded inputs. bf16 caches: max relative error 1e-2 per sequence and LSE
+absolute error 2e-3; fp32 cache: 1e-5 / 1e-5; cache bytes, INT2 codes, scales
+and packing bit-exact."""
+import math
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import attention, layout
+from oracle import int2 as oint2
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_seq(out, lse, w, b, ref_out, ref_lse, rel_tol, lse_tol):
+    e = gu.rel_err(out[b], ref_out)
+    le = float(np.max(np.abs(lse[b] - ref_lse)))
+    assert np.all(np.isfinite(out[b])), f"seq {b}: non-finite output"
+    assert e <= rel_tol, f"seq {b}: rel err {e:.3e} > {rel_tol}"
+    assert le <= lse_tol, f"seq {b}: lse err {le:.3e} > {lse_tol}"
+    return e, le
+
+
+# ------------------------------------------------------------------ tiny fp32
+
+def test_tiny_fp32_matches_absorbed_and_full_head(gpu_lib):
+    w = workloads.tiny(0)
+    q = np.stack([attention.absorb_query(w.q_nope[b], w.q_rope[b], w.W_UK) for b in range(w.B)])
+    shape = gu.shape_for(w)
+    cache, status = gu.fill_cache(w, shape)
+    out, lse, ws = gu.attend(w, shape, cache, q)
+    import mla_latent_kv_08_gb300 as mla
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    for b in range(w.B):
+        ro, rl = attention.absorbed(q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.FP32_REL_TOL, gu.FP32_LSE_TOL)
+        fo, fl = attention.full_head(w.q_nope[b], w.q_rope[b], w.latent[b], w.rope[b], w.W_UK, w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, fo, fl, gu.FP32_REL_TOL, gu.FP32_LSE_TOL)
+
+
+# ------------------------------------------------------------ append bytes
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+def test_append_layout_bit_exact(gpu_lib, kind):
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w = workloads.dsv3(11, B=5, H=8, len_range=(1, 333))
+    w.seq_lens[0] = 64        # exactly one block
+    w.latent[0] = w.latent[0][:64] if w.latent[0].shape[0] >= 64 else np.resize(w.latent[0], (64, 512))
+    w.rope[0] = np.resize(w.rope[0], (64, 64))
+    tab, nb = workloads.make_paging(np.random.default_rng(5), w.seq_lens, 64, spare_blocks=3)
+    w.block_table, w.num_blocks = tab, nb
+    shape = gu.shape_for(w, kind=mla.MLA_KV_FP32 if kind == "fp32" else mla.MLA_KV_BF16)
+    # split each sequence's tokens over two appends to exercise start_pos
+    cache = mla.Cache.allocate(shape)
+    half = [x.shape[0] // 2 for x in w.latent]
+    gu.append_tokens(cache, w, [x[:h] for x, h in zip(w.latent, half)], [x[:h] for x, h in zip(w.rope, half)],
+                     np.zeros(w.B, np.int32))
+    st = gu.append_tokens(cache, w, [x[h:] for x, h in zip(w.latent, half)], [x[h:] for x, h in zip(w.rope, half)],
+                          np.array(half, np.int32))
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    rows = [np.concatenate([w.latent[b], w.rope[b]], 1) for b in range(w.B)]
+    ref = layout.write_paged(nb, 64, w.D, tab, rows, [0] * w.B)
+    got = cache.latent.cpu()
+    if kind == "fp32":
+        np.testing.assert_array_equal(got.numpy().view(np.uint32), ref.astype(np.float32).view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got.view(torch.int16).numpy().view(np.uint16), workloads.bf16_bits(ref))
+
+
+def test_append_empty_is_noop(gpu_lib):
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w = workloads.dsv3(12, B=2, H=8, len_range=(10, 20))
+    shape = gu.shape_for(w)
+    cache = mla.Cache.allocate(shape)
+    gu.append_tokens(cache, w, [np.zeros((0, 512), np.float32)] * 2, [np.zeros((0, 64), np.float32)] * 2,
+                     np.zeros(2, np.int32))
+    torch.cuda.synchronize()
+    assert int(cache.latent.abs().sum().item()) == 0
+
+
+# ---------------------------------------------------------------- bf16 decode
+
+def test_dsv3_small_bf16(gpu_lib):
+    w = workloads.dsv3(1, B=6, H=128, len_range=(1, 900))
+    w.seq_lens[1] = 1
+    w.latent[1], w.rope[1] = w.latent[1][:1], w.rope[1][:1]
+    shape = gu.shape_for(w)
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, _ = gu.attend(w, shape, cache, w.q)
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+def test_split_count_does_not_change_result(gpu_lib):
+    w = workloads.dsv3(2, B=3, H=64, len_range=(2000, 3000))
+    res = []
+    for hint in (1, 7, 200):
+        shape = gu.shape_for(w, splits=hint)
+        cache, _ = gu.fill_cache(w, shape)
+        res.append(gu.attend(w, shape, cache, w.q)[:2])
+    for o, l in res[1:]:
+        assert np.max(np.abs(l - res[0][1])) < 1e-5
+        assert gu.rel_err(o, res[0][0]) < 8e-3      # bf16 output rounding of near-equal fp32 values
+    ro, rl = attention.absorbed(w.q[0], w.latent[0], w.rope[0], w.W_UV, w.scale)
+    _check_seq(res[2][0], res[2][1], w, 0, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+def test_verify_causal_window(gpu_lib):
+    w = workloads.verify(3, B=4, q_len=8, len_range=(8, 400), H=32)
+    w.seq_lens[0] = 8          # first draft row sees exactly one token
+    w.latent[0], w.rope[0] = w.latent[0][:8], w.rope[0][:8]
+    shape = gu.shape_for(w)
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, _ = gu.attend(w, shape, cache, w.q, q_len=8)
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+# ------------------------------------------------------------------ INT2
+
+def _int2_setup(B, H, len_range, n_calib=8192, seed=4):
+    w = workloads.int2_rotated(seed, B=B, H=H, len_range=len_range, n_calib=n_calib)
+    R, _ = oint2.fit_rotation(w.calib)
+    T = oint2.clip_thresholds(w.calib, R)
+    return w, R.astype(np.float32), T.astype(np.float32)
+
+
+def _int2_reference_pool(w, R32, T32, seqs, with_new=True):
+    """Oracle codes / scale-zero / rope for the given sequences, placed in a pool."""
+    out = {}
+    for b in seqs:
+        C = w.latent[b]
+        KR = w.rope[b]
+        if with_new:
+            C = np.concatenate([C, w.new_latent[b]])
+            KR = np.concatenate([KR, w.new_rope[b]])
+        codes, sz = oint2.quantize(C, R32, T32)
+        out[b] = (codes, sz, KR)
+    return out
+
+
+def test_int2_append_and_decode_small(gpu_lib):
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=4, H=32, len_range=(40, 300))
+    shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT)
+    cache = mla.Cache.allocate(shape)
+    st0 = gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32), R32, T32)
+    st1 = gu.append_tokens(cache, w, w.new_latent, w.new_rope, w.start_pos, R32, T32)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st0)[0] == mla.MLA_OK and mla.mla_read_status_word(st1)[0] == mla.MLA_OK
+    ref = _int2_reference_pool(w, R32, T32, range(w.B))
+    nb = w.num_blocks
+    lens_new = w.seq_lens + 32
+    ref_codes = layout.write_paged(nb, 64, 128, w.block_table, [ref[b][0] for b in range(w.B)], [0] * w.B, np.uint8)
+    ref_sz = layout.write_paged(nb, 64, 32, w.block_table, [ref[b][1].reshape(-1, 32) for b in range(w.B)],
+                                [0] * w.B, np.uint16)
+    ref_rope = layout.write_paged(nb, 64, 64, w.block_table, [workloads.bf16_bits(ref[b][2]) for b in range(w.B)],
+                                  [0] * w.B, np.uint16)
+    np.testing.assert_array_equal(cache.codes.cpu().numpy(), ref_codes)
+    np.testing.assert_array_equal(cache.scale_zero.cpu().view(torch.int16).numpy().view(np.uint16).reshape(nb, 64, 32), ref_sz)
+    np.testing.assert_array_equal(cache.rope.cpu().view(torch.int16).numpy().view(np.uint16), ref_rope)
+    # decode over the appended lengths against the oracle's own dequantised codes
+    w.seq_lens = lens_new.astype(np.int32)
+    out, lse, _ = gu.attend(w, shape, cache, w.q, R=R32)
+    for b in range(w.B):
+        Chat = oint2.decode(ref[b][0], ref[b][1])
+        ro, rl = oint2.attention_rotated(w.q[b], Chat, ref[b][2], R32, w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+# ------------------------------------------------------------ device checks
+
+def test_bad_block_id_sets_flag_and_nan_rows(gpu_lib):
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(13, B=3, H=16, len_range=(100, 200))
+    shape = gu.shape_for(w)
+    cache, _ = gu.fill_cache(w, shape)
+    w.block_table = w.block_table.copy()
+    w.block_table[1, 0] = w.num_blocks + 5          # out of range for decode only
+    out, lse, ws = gu.attend(w, shape, cache, w.q)
+    code, flags = mla.mla_get_status(ws)
+    assert code == mla.MLA_ERR_BOUNDS and flags & 1
+    assert np.all(np.isnan(out[1])) and np.all(np.isnan(lse[1]))
+    for b in (0, 2):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+def test_bad_length_sets_flag(gpu_lib):
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(14, B=2, H=16, len_range=(100, 120))
+    shape = gu.shape_for(w)
+    cache, _ = gu.fill_cache(w, shape)
+    good = w.seq_lens.copy()
+    w.seq_lens = np.array([good[0], w.block_table.shape[1] * 64 + 1], np.int32)
+    out, lse, ws = gu.attend(w, shape, cache, w.q)
+    code, flags = mla.mla_get_status(ws)
+    assert code == mla.MLA_ERR_BOUNDS and flags & 2
+    assert np.all(np.isnan(out[1]))
+    ro, rl = attention.absorbed(w.q[0], w.latent[0], w.rope[0], w.W_UV, w.scale)
+    _check_seq(out, lse, w, 0, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+def test_host_argument_errors_launch_nothing(gpu_lib):
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w = workloads.dsv3(15, B=2, H=16, len_range=(10, 20))
+    shape = gu.shape_for(w)
+    cache, _ = gu.fill_cache(w, shape)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mla.MlaError) as e:
+        gu_out = torch.empty((2, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((2, 1, 16), dtype=torch.float32, device="cuda")
+        mla.mla_decode(cache, gu.dev(w.block_table), gu.dev(w.seq_lens), gu.dev(w.q, torch.bfloat16),
+                       gu.dev(w.W_UV, torch.bfloat16), w.scale, gu_out, lse, small)
+    assert e.value.code == mla.MLA_ERR_WORKSPACE
