@@ -1,0 +1,553 @@
+// Tensor-core (tcgen05 / TMEM / TMA) split-KV decode for the DeepSeek-V3 latent
+// shape: kv_lora_rank 512, rope 64, bf16 cache, block size 64.
+//
+// Work decomposition. A work item is a token range [t0, t1) of one sequence
+// (from the planner) times a tile of 128 query rows (a row is a (draft
+// position, head) pair). Each work item runs on TWO CTAs that read the same
+// KV tiles; CTA `half` owns latent output dims [256*half, 256*half + 256).
+// The fp32 latent output of 128 rows x 512 dims alone is the whole 512-column
+// tensor memory of an SM, so the output is split across the pair and each CTA
+// computes the scores S = Q K^T on its own (the pair shares the KV tiles
+// through L2).
+//
+// Per CTA, per 64-token tile (one cache block):
+//   TMA     9 loads of [64 tokens x 64 dims] bf16, 128B-swizzled, into a stage
+//   MMA     S[128 x 64]  = Q[128 x 576] . K[64 x 576]^T   (36 x M128 N64 K16)
+//           Q dims 0..383 are read from tensor memory, 384..575 from smem
+//   softmax one thread per row: tcgen05.ld of S, scale, causal/length mask,
+//           running max in log2 units with a lazy rescale (only when the max
+//           grows by more than 8, so P <= 2^8), P -> bf16 smem (swizzled)
+//   MMA     O[128 x 256] += P[128 x 64] . V[64 x 256]     (4 x M128 N256 K16)
+//           V is the same smem tile read as an MN-major operand
+// Epilogue: O / l to the fp32 partial buffer, log2-sum-exp to the partial LSE;
+// the shared combine kernel merges splits and applies W_UV.
+//
+// Tensor memory columns: O [0,256), S [256,320), Q dims 0..383 [320,512).
+// Roles (256 threads): warp 0 lane 0 = TMA producer; warp 1 = TMEM owner, its
+// lane 0 issues MMAs; warps 4..7 = softmax / correction / epilogue (warp w
+// reads TMEM lanes 32*(w%4)..+31). All waits are bounded: a wait that gives up
+// records FLAG_TIMEOUT and the CTA winds down without trapping.
+#include "mla_internal.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+#include <string.h>
+
+namespace mla {
+namespace tc {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 64;             // tokens per tile == cache block size
+constexpr int kRows = 128;            // query rows per CTA (MMA M)
+constexpr int kD = 576;               // r + d_R
+constexpr int kKvBlocks = 9;          // 64-dim column blocks per token row
+constexpr int kQTmemBlocks = 6;       // Q column blocks held in TMEM (dims 0..383)
+constexpr int kQSmemBlocks = 3;       // Q column blocks read from smem (dims 384..575)
+constexpr int kStages = 2;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
+
+constexpr uint32_t kKvBlockBytes = kTile * 128;                     // 8 KB
+constexpr uint32_t kStageBytes = kKvBlocks * kKvBlockBytes;         // 72 KB
+constexpr uint32_t kQBlockBytes = kRows * 128;                      // 16 KB
+constexpr uint32_t kPBytes = kRows * 128;                           // 16 KB
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
+constexpr uint32_t kOffP = kOffQ + kQSmemBlocks * kQBlockBytes;     // 192 KB
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;                   // 224 KB
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;               // + barriers + alignment slack
+static_assert(kQTmemBlocks * kQBlockBytes <= kStages * kStageBytes, "Q staging must fit the stages");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bounded-wait safety net
+
+struct Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t s_full;
+    uint64_t s_free;
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t q_full;
+    uint64_t mma_fin;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+    int32_t bad_block;
+};
+
+struct TcParams {
+    DecodeParams p;
+    int32_t row_tiles;
+    uint32_t v_lbo, v_sbo;    // MN-major descriptor strides of the V operand
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+    return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity. On give-up it raises the
+// CTA abort flag and the global timeout flag and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Bars *bars, int32_t *status) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*(volatile int32_t *)&bars->abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                atomicExch(&bars->abort_flag, 1);
+                raise_flag(status, FLAG_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool aborted(Bars *bars) { return *(volatile int32_t *)&bars->abort_flag != 0; }
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+#define TMEM_LD32(taddr, v)                                                                                      \
+    asm volatile(                                                                                                \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"         \
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                               \
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),      \
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), \
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),            \
+          "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),            \
+          "=r"(v[30]), "=r"(v[31])                                                                               \
+        : "r"(taddr))
+
+#define TMEM_ST32(taddr, v)                                                                                      \
+    asm volatile(                                                                                                \
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"  \
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"                                     \
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),   \
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),           \
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),         \
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])          \
+        : "memory")
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Byte offset of element (row, col) in a [rows x 64] bf16 tile stored with the
+// 128-byte swizzle (16-byte chunk index XOR row % 8; 8-row atoms of 1 KB).
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+    return (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                 const TcParams tp) {
+    const DecodeParams &p = tp.p;
+    const int half = blockIdx.x;            // 0/1: which 256 latent output dims
+    const int g = blockIdx.y;               // query row tile
+    const int w = blockIdx.z;               // work item
+    if (w >= p.num_work[0]) return;
+    const WorkItem item = p.work[w];
+    const int b = item.b, t0 = item.t0, t1 = item.t1, slot = item.slot;
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    const int rows_seq = p.q_len * p.s.H;
+    const int L = p.seq_lens[b];
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    Bars *bars = (Bars *)(smem + kOffBar);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_free, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->p_full[i], 128);
+            mbar_init(&bars->pv_done[i], 1);
+        }
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->mma_fin, 1);
+        bars->abort_flag = 0;
+        bars->bad_block = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars->tmem_base)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    // ---- Q: TMA into smem (dims 0..383 staged in the KV stages), then rows to TMEM
+    const int q_row0 = b * rows_seq + g * kRows;
+    if (tid == 0) {
+        mbar_expect_tx(&bars->q_full, (kQTmemBlocks + kQSmemBlocks) * kQBlockBytes);
+        for (int c = 0; c < kQTmemBlocks + kQSmemBlocks; ++c) {
+            uint8_t *dst = c < kQTmemBlocks ? smem + kOffStage + c * kQBlockBytes
+                                            : smem + kOffQ + (c - kQTmemBlocks) * kQBlockBytes;
+            tma_load_2d(dst, &q_map, c * 64, q_row0, &bars->q_full);
+        }
+    }
+    if (warp < 4) {
+        const int row = 32 * warp + lane;
+        if (mbar_wait(&bars->q_full, 0, bars, p.status)) {
+            for (int c = 0; c < kQTmemBlocks; ++c) {
+                const uint8_t *blk = smem + kOffStage + c * kQBlockBytes;
+                uint32_t v[32];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 u = *(const uint4 *)(blk + sw128(row, ch));
+                    v[4 * ch + 0] = u.x;
+                    v[4 * ch + 1] = u.y;
+                    v[4 * ch + 2] = u.z;
+                    v[4 * ch + 3] = u.w;
+                }
+                const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + kColQ + 32 * c;
+                TMEM_ST32(taddr, v);
+            }
+            tmem_wait_st();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();              // Q in TMEM; the stages are free for KV
+    tc_fence_after();
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0 && !aborted(bars)) {
+            int issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % kStages;
+                if (t >= kStages && !mbar_wait(&bars->empty[s], ((t - kStages) / kStages) & 1, bars, p.status)) break;
+                const int lb = (t0 + t * kTile) / kTile;
+                int blk = lb < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + lb] : -1;
+                if (blk < 0 || blk >= p.s.num_blocks) {
+                    raise_flag(p.status, FLAG_BAD_BLOCK);
+                    atomicExch(&bars->bad_block, 1);
+                    blk = 0;
+                }
+                uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                mbar_expect_tx(&bars->full[s], kStageBytes);
+                for (int c = 0; c < kKvBlocks; ++c)
+                    tma_load_2d(stage + c * kKvBlockBytes, &kv_map, c * 64, blk * kTile, &bars->full[s]);
+                issued = t + 1;
+            }
+            // drain: never leave a copy in flight into this CTA's shared memory
+            for (int t = issued - kStages; t < issued; ++t)
+                if (t >= 0) mbar_wait(&bars->full[t % kStages], (t / kStages) & 1, bars, p.status);
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = idesc_bf16(128, 64, false);
+            const uint32_t id_pv = idesc_bf16(128, 256, true);
+            const uint32_t d_s = tmem + kColS, d_o = tmem + kColO;
+            int pv_issued = 0;
+            bool ok = true;
+            auto issue_pv = [&](int t) -> bool {
+                const int pb = t & 1;
+                if (!mbar_wait(&bars->p_full[pb], (t >> 1) & 1, bars, p.status)) return false;
+                tc_fence_after();
+                const int s = t % kStages;
+                const uint32_t pbase = smem_u32(smem + kOffP + pb * kPBytes);
+                const uint32_t vbase = smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint64_t a = sdesc(pbase + 32 * j, 16, 1024);
+                    const uint64_t bdesc = sdesc(vbase + 2048 * j, tp.v_lbo, tp.v_sbo);
+                    mma_ss(d_o, a, bdesc, id_pv, (t > 0 || j > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->pv_done[pb]);
+                mma_commit(&bars->empty[s]);
+                pv_issued = t + 1;
+                return true;
+            };
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t % kStages;
+                if (!mbar_wait(&bars->full[s], (t / kStages) & 1, bars, p.status)) { ok = false; break; }
+                if (t > 0 && !mbar_wait(&bars->s_free, (t - 1) & 1, bars, p.status)) { ok = false; break; }
+                // the sequence's final partial block: zero the slots past the end so
+                // that P = 0 never meets stale (possibly non-finite) cache bytes
+                const int tile_start = t0 + t * kTile;
+                const int valid = min(kTile, L - tile_start);
+                if (valid < kTile) {
+                    uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                    for (int c = 0; c < kKvBlocks; ++c)
+                        for (int rr = valid; rr < kTile; ++rr)
+                            for (int ch = 0; ch < 8; ++ch)
+                                *(uint4 *)(stage + c * kKvBlockBytes + sw128(rr, ch)) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async();
+                }
+                tc_fence_after();
+                const uint32_t kbase = smem_u32(smem + kOffStage + s * kStageBytes);
+                const uint32_t qbase = smem_u32(smem + kOffQ);
+#pragma unroll 4
+                for (int j = 0; j < 36; ++j) {
+                    const int c = j >> 2, k = j & 3;
+                    const uint64_t bdesc = sdesc(kbase + c * kKvBlockBytes + 32 * k, 16, 1024);
+                    if (c < kQTmemBlocks) {
+                        mma_ts(d_s, tmem + kColQ + 8 * j, bdesc, id_qk, j > 0 ? 1u : 0u);
+                    } else {
+                        const uint64_t a = sdesc(qbase + (c - kQTmemBlocks) * kQBlockBytes + 32 * k, 16, 1024);
+                        mma_ss(d_s, a, bdesc, id_qk, 1u);
+                    }
+                }
+                mma_commit(&bars->s_full);
+                if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
+            }
+            if (ok && ntiles > 0) issue_pv(ntiles - 1);
+            (void)pv_issued;
+            mma_commit(&bars->mma_fin);
+            mbar_wait(&bars->mma_fin, 0, bars, p.status);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ================================================= softmax / epilogue
+        const int wq = warp & 3;
+        const int row = 32 * wq + lane;
+        const int row_seq = g * kRows + row;
+        const bool row_valid = row_seq < rows_seq;
+        const int last_vis = L - p.q_len + (row_valid ? row_seq / p.s.H : 0);
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
+        float m_used = -CUDART_INF_F, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            if (!mbar_wait(&bars->s_full, t & 1, bars, p.status)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sv[64];
+            TMEM_LD32(lane_addr + kColS, sv);
+            TMEM_LD32(lane_addr + kColS + 32, (sv + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars->s_free);
+
+            const int tile_start = t0 + t * kTile;
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const int tok = tile_start + j;
+                const bool vis = row_valid && tok < t1 && tok <= last_vis;
+                const float s2 = vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
+                sv[j] = __float_as_uint(s2);
+                mx = fmaxf(mx, s2);
+            }
+            float alpha = 1.f;
+            bool rescale = false;
+            const float m_new = fmaxf(m_used, mx);
+            if (m_new > m_used + 8.f) {
+                alpha = exp2f(m_used - m_new);        // 0 when nothing was accumulated yet
+                m_used = m_new;
+                rescale = t > 0;
+            }
+            float sum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float a = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j]) - m_used);
+                const float c = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j + 1]) - m_used);
+                const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
+                // the sum uses the bf16-rounded probabilities the MMA will use
+                const float2 back = __bfloat1622float2(h);
+                sum += back.x + back.y;
+                pk[j] = *(const uint32_t *)&h;
+            }
+            l = l * alpha + sum;
+            const int pb = t & 1;
+            if (t >= 2 && !mbar_wait(&bars->pv_done[pb], ((t - 2) >> 1) & 1, bars, p.status)) { ok = false; break; }
+            if (rescale) {
+                // O *= alpha once PV(t-1) has landed; PV(t) waits for p_full below
+                if (!mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, p.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t ov[32];
+                    TMEM_LD32(lane_addr + kColO + 32 * c, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                    TMEM_ST32(lane_addr + kColO + 32 * c, ov);
+                }
+                tmem_wait_st();
+            }
+            uint8_t *pbuf = smem + kOffP + pb * kPBytes;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *(uint4 *)(pbuf + sw128(row, ch)) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[pb]);
+        }
+        // epilogue: wait for the last PV, then O / l -> partial buffer
+        if (ok && ntiles > 0) {
+            const int tl = ntiles - 1;
+            ok = mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status);
+        }
+        const bool bad = aborted(bars) || !ok || *(volatile int32_t *)&bars->bad_block;
+        tc_fence_after();
+        if (row_valid) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float *po = p.part_o + ((size_t)slot * rows_seq + row_seq) * p.s.r + 256 * half;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t ov[32];
+                if (ok) {
+                    TMEM_LD32(lane_addr + kColO + 32 * c, ov);
+                    tmem_wait_ld();
+                }
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    float4 f;
+                    f.x = ok ? __uint_as_float(ov[k + 0]) * inv : 0.f;
+                    f.y = ok ? __uint_as_float(ov[k + 1]) * inv : 0.f;
+                    f.z = ok ? __uint_as_float(ov[k + 2]) * inv : 0.f;
+                    f.w = ok ? __uint_as_float(ov[k + 3]) * inv : 0.f;
+                    *(float4 *)(po + 32 * c + k) = f;
+                }
+            }
+            if (half == 0)
+                p.part_lse[(size_t)slot * rows_seq + row_seq] =
+                    bad ? CUDART_NAN_F : (l > 0.f ? m_used + log2f(l) : -CUDART_INF_F);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, 576] matrix, 128-byte swizzled boxes of
+// [box_rows, 64].
+static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool tc_shape_supported(const ShapeArgs &s) {
+    return s.kind == MLA_KV_BF16 && s.r == 512 && s.dR == 64 && s.bs == tc::kTile;
+}
+
+cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
+    tc::TcParams tp;
+    tp.p = p;
+    tp.row_tiles = (p.q_len * p.s.H + tc::kRows - 1) / tc::kRows;
+    // MN-major V operand: 64-dim atoms 8 KB apart, 8-token groups 1 KB apart.
+    tp.v_lbo = tc::kKvBlockBytes;
+    tp.v_sbo = 1024;
+    if (const char *e = getenv("MLA_TC_VDESC_SWAP"))
+        if (e[0] == '1') { tp.v_lbo = 1024; tp.v_sbo = tc::kKvBlockBytes; }
+    CUtensorMap kv_map, q_map;
+    memset(&kv_map, 0, sizeof kv_map);
+    memset(&q_map, 0, sizeof q_map);
+    if (!tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&q_map, p.q, (uint64_t)p.B * p.q_len * p.s.H, tc::kRows)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(2, tp.row_tiles, max_work);
+    tc::decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, q_map, tp);
+    return cudaGetLastError();
+}
+
+}  // namespace mla
