@@ -83,7 +83,8 @@ static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
     (void)q_len;
-    if (s->impl == MLA_IMPL_TCGEN05) return MLA_ERR_UNSUPPORTED;
+    const bool tc_ok = tc_shape_supported(shape_args(s));
+    if (s->impl == MLA_IMPL_TCGEN05) return tc_ok ? MLA_IMPL_TCGEN05 : MLA_ERR_UNSUPPORTED;
     return MLA_IMPL_SIMT;
 }
 
@@ -158,7 +159,9 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     if (launch_plan(p, w.target, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
     if (int2 && launch_qprep(p, R, (float *)(ws + w.q_prep), stream_) != cudaSuccess) return MLA_ERR_CUDA;
     const int ev = prof_begin(stream_);
-    if (launch_decode_simt(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    const cudaError_t de = impl == MLA_IMPL_TCGEN05 ? launch_decode_tc(p, w.max_work, stream_)
+                                                    : launch_decode_simt(p, w.max_work, stream_);
+    if (de != cudaSuccess) return MLA_ERR_CUDA;
     prof_end(ev, stream_);
 
     CombineParams c;

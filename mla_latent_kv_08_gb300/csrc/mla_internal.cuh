@@ -102,6 +102,9 @@ cudaError_t launch_qprep(const DecodeParams &p, const float *R, float *q_prep, c
 cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
+// ---- tensor-core decode (defined in mla_tc.cu) -----------------------------
+bool tc_shape_supported(const ShapeArgs &s);
+cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 
 // ---- small device helpers ---------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {

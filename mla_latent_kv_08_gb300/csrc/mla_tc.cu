@@ -535,8 +535,6 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     // MN-major V operand: 64-dim atoms 8 KB apart, 8-token groups 1 KB apart.
     tp.v_lbo = tc::kKvBlockBytes;
     tp.v_sbo = 1024;
-    if (const char *e = getenv("MLA_TC_VDESC_SWAP"))
-        if (e[0] == '1') { tp.v_lbo = 1024; tp.v_sbo = tc::kKvBlockBytes; }
     CUtensorMap kv_map, q_map;
     memset(&kv_map, 0, sizeof kv_map);
     memset(&q_map, 0, sizeof q_map);
