@@ -159,6 +159,33 @@ mla_status mla_verify(const mla_shape *shape, const mla_cache *cache,
                       const void *W_UV, const float *R, float scale, void *out,
                       float *lse, void *workspace, size_t workspace_bytes, void *stream);
 
+/* mla_decode for callers that cannot allocate device memory at call time, such
+ * as an inference-engine plugin whose enqueue step must not allocate, or a
+ * serving process whose memory pool already holds the device's memory
+ * (cudaMalloc can block, synchronise the device, or simply fail there). The
+ * pages have no counterpart: this is a deployment convenience of the library.
+ *   Arguments are those of mla_decode without the workspace; the caller still
+ *   passes every input and output. Scratch comes from a fixed 32 MiB device
+ *   array inside the library, held on every GPU that loads it until the
+ *   process exits. No cudaMalloc, cudaFree or allocating library call is made.
+ *   If the planner's default split count does not fit 32 MiB, fewer splits
+ *   are used; if even one split per sequence does not fit (roughly B * q_len *
+ *   H * kv_lora_rank * 4 bytes above 32 MiB), MLA_ERR_WORKSPACE is returned and
+ *   nothing is launched.
+ *   status: optional [1] int32 device word that receives this call's flag word
+ *   (read it with mla_read_status_word); NULL to skip.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture. Every call shares the one array: calls that can overlap on the
+ *   GPU (other streams, other host threads) race on it and must be ordered by
+ *   the caller. The flag word is reset at the start of each call; all other
+ *   scratch is written before it is read. */
+mla_status mla_decode_noalloc(const mla_shape *shape, const mla_cache *cache,
+                              const int32_t *block_table, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, int32_t B, const void *q,
+                              const void *W_UV, const float *R, float scale, void *out,
+                              float *lse, int32_t *status, void *stream);
+
 /* Wait for `stream`, read the device flags of the last decode/verify that used
  * `workspace` and return MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT. If
  * raw_flags is not NULL it receives the raw flag word (host int). */

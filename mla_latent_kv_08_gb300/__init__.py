@@ -38,7 +38,7 @@ MLA_IMPL_TCGEN05 = 2
 EXPORTED = (
     "mla_workspace_bytes", "mla_latent_append", "mla_decode", "mla_verify", "mla_get_status",
     "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
-    "mla_profile_enable", "mla_profile_read",
+    "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc",
 )
 
 
@@ -92,6 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_resolve_impl.restype = i32
     lib.mla_version.argtypes = []
     lib.mla_version.restype = i32
+    lib.mla_decode_noalloc.argtypes = [sp, cp, vp, i32, vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+    lib.mla_decode_noalloc.restype = i32
     lib.mla_profile_enable.argtypes = [i32]
     lib.mla_profile_enable.restype = i32
     lib.mla_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), i32p, i32p]
@@ -229,6 +231,19 @@ def mla_verify(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, 
                           _ptr(q), _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
                           int(workspace.numel() * workspace.element_size()), _stream(stream))
     _check(code, "mla_verify")
+
+
+def mla_decode_noalloc(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, R=None,
+                       status=None, stream=None) -> None:
+    """mla_decode with the library's fixed internal scratch instead of a caller
+    workspace, for callers that cannot allocate device memory at call time (see
+    include/mla.h for the size limit and the ordering rule)."""
+    lib = load_library()
+    code = lib.mla_decode_noalloc(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+                                  int(block_table.shape[1]), _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(q),
+                                  _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(status),
+                                  _stream(stream))
+    _check(code, "mla_decode_noalloc")
 
 
 def mla_get_status(workspace, stream=None):
