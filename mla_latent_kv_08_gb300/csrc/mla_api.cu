@@ -85,7 +85,8 @@ int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
     (void)q_len;
     const bool tc_ok = tc_shape_supported(shape_args(s));
     if (s->impl == MLA_IMPL_TCGEN05) return tc_ok ? MLA_IMPL_TCGEN05 : MLA_ERR_UNSUPPORTED;
-    return MLA_IMPL_SIMT;
+    if (s->impl == MLA_IMPL_SIMT) return MLA_IMPL_SIMT;
+    return tc_ok ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
 }
 
 static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {

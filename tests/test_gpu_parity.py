@@ -223,3 +223,28 @@ def test_host_argument_errors_launch_nothing(gpu_lib):
         mla.mla_decode(cache, gu.dev(w.block_table), gu.dev(w.seq_lens), gu.dev(w.q, torch.bfloat16),
                        gu.dev(w.W_UV, torch.bfloat16), w.scale, gu_out, lse, small)
     assert e.value.code == mla.MLA_ERR_WORKSPACE
+
+
+# ----------------------------------------------------- tensor-core vs generic
+
+@pytest.mark.parametrize("H,q_len,lens", [(128, 1, (1, 700)), (64, 1, (60, 200)), (128, 4, (4, 300))])
+def test_tcgen05_and_simt_agree_with_oracle(gpu_lib, H, q_len, lens):
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(50 + H + q_len, B=3, H=H, len_range=lens, q_len=q_len)
+    res = {}
+    for impl in (mla.MLA_IMPL_TCGEN05, mla.MLA_IMPL_SIMT):
+        shape = gu.shape_for(w, impl=impl)
+        assert mla.mla_resolve_impl(shape, q_len) == impl
+        cache, _ = gu.fill_cache(w, shape)
+        res[impl] = gu.attend(w, shape, cache, w.q, q_len=q_len)[:2]
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        for impl, (o, l) in res.items():
+            _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+def test_auto_picks_tensor_cores_for_dsv3(gpu_lib):
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(1, B=2, H=128, len_range=(64, 64))
+    assert mla.mla_resolve_impl(gu.shape_for(w)) == mla.MLA_IMPL_TCGEN05
+    assert mla.mla_resolve_impl(gu.shape_for(w, kind=mla.MLA_KV_FP32)) == mla.MLA_IMPL_SIMT
