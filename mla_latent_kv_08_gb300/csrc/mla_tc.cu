@@ -266,7 +266,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     }
     if (warp < 4) {
         const int row = 32 * warp + lane;
-        if (mbar_wait(&bars->q_full, 0, bars, p.status)) {
+        // tcgen05.st is warp-collective (.sync.aligned): the branch must be warp-uniform
+        const bool q_ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, bars, p.status));
+        if (q_ok) {
             for (int c = 0; c < kQTmemBlocks; ++c) {
                 const uint8_t *blk = smem + kOffStage + c * kQBlockBytes;
                 uint32_t v[32];
@@ -387,8 +389,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
         float m_used = -CUDART_INF_F, l = 0.f;
         bool ok = true;
+        // Every branch around tcgen05.ld / tcgen05.st below is warp-uniform: those
+        // instructions are warp-collective (.sync.aligned).
         for (int t = 0; t < ntiles && ok; ++t) {
-            if (!mbar_wait(&bars->s_full, t & 1, bars, p.status)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, t & 1, bars, p.status))) { ok = false; break; }
             tc_fence_after();
             uint32_t sv[64];
             TMEM_LD32(lane_addr + kColS, sv);
@@ -422,17 +426,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 const float a = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j]) - m_used);
                 const float c = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j + 1]) - m_used);
                 const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
-                // the sum uses the bf16-rounded probabilities the MMA will use
-                const float2 back = __bfloat1622float2(h);
-                sum += back.x + back.y;
+                sum += a + c;          // fp32 row sum: the LSE does not see the bf16 rounding of P
                 pk[j] = *(const uint32_t *)&h;
             }
             l = l * alpha + sum;
             const int pb = t & 1;
-            if (t >= 2 && !mbar_wait(&bars->pv_done[pb], ((t - 2) >> 1) & 1, bars, p.status)) { ok = false; break; }
-            if (rescale) {
+            if (t >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[pb], ((t - 2) >> 1) & 1, bars, p.status))) {
+                ok = false;
+                break;
+            }
+            // Rows decide to rescale on their own; the warp corrects O together
+            // (alpha = 1 for rows that keep their max).
+            if (__any_sync(0xffffffffu, rescale)) {
                 // O *= alpha once PV(t-1) has landed; PV(t) waits for p_full below
-                if (!mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, p.status)) { ok = false; break; }
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, p.status))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
@@ -456,20 +467,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         // epilogue: wait for the last PV, then O / l -> partial buffer
         if (ok && ntiles > 0) {
             const int tl = ntiles - 1;
-            ok = mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status));
         }
         const bool bad = aborted(bars) || !ok || *(volatile int32_t *)&bars->bad_block;
         tc_fence_after();
-        if (row_valid) {
+        {
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            float *po = p.part_o + ((size_t)slot * rows_seq + row_seq) * p.s.r + 256 * half;
+            float *po = p.part_o + ((size_t)slot * rows_seq + (row_valid ? row_seq : 0)) * p.s.r + 256 * half;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
                 uint32_t ov[32];
-                if (ok) {
+                if (ok) {                      // warp-uniform
                     TMEM_LD32(lane_addr + kColO + 32 * c, ov);
                     tmem_wait_ld();
                 }
+                if (!row_valid) continue;
 #pragma unroll
                 for (int k = 0; k < 32; k += 4) {
                     float4 f;
@@ -480,6 +492,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     *(float4 *)(po + 32 * c + k) = f;
                 }
             }
+        }
+        if (row_valid) {
             if (half == 0)
                 p.part_lse[(size_t)slot * rows_seq + row_seq] =
                     bad ? CUDART_NAN_F : (l > 0.f ? m_used + log2f(l) : -CUDART_INF_F);
