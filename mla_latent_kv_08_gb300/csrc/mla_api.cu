@@ -84,17 +84,25 @@ static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
     (void)q_len;
     const bool tc_ok = tc_shape_supported(shape_args(s));
-    if (s->impl == MLA_IMPL_TCGEN05) return tc_ok ? MLA_IMPL_TCGEN05 : MLA_ERR_UNSUPPORTED;
+    if (s->impl == MLA_IMPL_TCGEN05) return tc_ok ? (int32_t)MLA_IMPL_TCGEN05 : (int32_t)MLA_ERR_UNSUPPORTED;
     if (s->impl == MLA_IMPL_SIMT) return MLA_IMPL_SIMT;
     return tc_ok ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
 }
 
 static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {
-    (void)impl;
     WsLayout w;
     memset(&w, 0, sizeof w);
-    const int sms = device_sm_count();
-    int target = s->num_splits_hint > 0 ? s->num_splits_hint : (sms > 0 ? sms : 148);
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+    int target;
+    if (impl == MLA_IMPL_TCGEN05) {
+        // one wave of persistent CTAs: 2 per stream per 128-row tile
+        const int row_tiles = (q_len * s->num_heads + 127) / 128;
+        target = sms / (2 * row_tiles);
+        if (target < 1) target = 1;
+        if (s->num_splits_hint > 0 && s->num_splits_hint < target) target = s->num_splits_hint;
+    } else {
+        target = s->num_splits_hint > 0 ? s->num_splits_hint : sms;
+    }
     w.target = target;
     w.max_work = target + B;
     const size_t rows = (size_t)q_len * s->num_heads;
@@ -102,6 +110,7 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
     w.status = off;        off = up256(off + 2 * sizeof(int32_t));
     w.work = off;          off = up256(off + sizeof(WorkItem) * (size_t)w.max_work);
     w.split_start = off;   off = up256(off + sizeof(int32_t) * ((size_t)B + 1));
+    w.stream_start = off;  off = up256(off + sizeof(int32_t) * ((size_t)target + 1));
     w.part_o = off;        off = up256(off + sizeof(float) * (size_t)w.max_work * rows * s->kv_lora_rank);
     w.part_lse = off;      off = up256(off + sizeof(float) * (size_t)w.max_work * rows);
     w.q_prep = off;
@@ -154,10 +163,12 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.num_work = (const int32_t *)(ws + w.status + sizeof(int32_t));
     p.work = (const WorkItem *)(ws + w.work);
     p.split_start = (const int32_t *)(ws + w.split_start);
+    p.stream_start = (const int32_t *)(ws + w.stream_start);
+    p.streams = w.target;
     p.part_o = (float *)(ws + w.part_o);
     p.part_lse = (float *)(ws + w.part_lse);
 
-    if (launch_plan(p, w.target, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_plan(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
     if (int2 && launch_qprep(p, R, (float *)(ws + w.q_prep), stream_) != cudaSuccess) return MLA_ERR_CUDA;
     const int ev = prof_begin(stream_);
     const cudaError_t de = impl == MLA_IMPL_TCGEN05 ? launch_decode_tc(p, w.max_work, stream_)

@@ -22,10 +22,12 @@ enum : int32_t {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Work item of the split-KV schedule: tokens [t0, t1) of sequence b, whose
-// partial result goes to partial slot `slot`.
+// Work item of the split-KV schedule: tokens [t0, t1) of sequence b, processed
+// by work stream `stream`. Its partial result goes to the slot equal to its
+// index in the schedule; the items of one sequence have consecutive indices,
+// and so do the items of one stream.
 struct WorkItem {
-    int32_t b, t0, t1, slot;
+    int32_t b, t0, t1, stream;
 };
 
 // Byte offsets inside the caller's workspace.
@@ -33,12 +35,13 @@ struct WsLayout {
     size_t status;        // int32 flags word, then int32 num_work
     size_t work;          // WorkItem[max_work]
     size_t split_start;   // int32[B + 1]: first slot of each sequence
+    size_t stream_start;  // int32[streams + 1]: first item of each stream
     size_t part_o;        // fp32 [max_work][q_len * H][r]  normalised partial outputs
     size_t part_lse;      // fp32 [max_work][q_len * H]     partial log2-sum-exp
     size_t q_prep;        // fp32 [B * q_len * H][r + d_R]  rotated query (INT2 kind)
     size_t total;
-    int32_t max_work;     // upper bound of schedule length
-    int32_t target;       // schedule target passed to the planner kernel
+    int32_t max_work;     // upper bound of schedule length (streams + B)
+    int32_t target;       // number of work streams
 };
 
 struct ShapeArgs {
@@ -63,6 +66,8 @@ struct DecodeParams {
     const int32_t *num_work;
     const WorkItem *work;
     const int32_t *split_start;
+    const int32_t *stream_start;
+    int32_t streams;
     float *part_o;
     float *part_lse;
 };
@@ -97,7 +102,7 @@ struct AppendParams {
 };
 
 // ---- launchers (defined in mla_simt.cu) ------------------------------------
-cudaError_t launch_plan(const DecodeParams &p, int32_t target, int32_t max_work, cudaStream_t st);
+cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 cudaError_t launch_qprep(const DecodeParams &p, const float *R, float *q_prep, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);

@@ -13,88 +13,111 @@
 namespace mla {
 
 // ============================================================================
-// Planner: split every sequence into token ranges of `chunk` tokens, where
-// chunk = max(64, ceil64(sum_b L_b / target)). The number of work items is then
-// at most target + B. One CTA; the schedule lives in the workspace so the
-// decode launch never needs the lengths on the host.
+// Planner. The cache of every valid sequence is cut into 64-token tiles (one
+// cache block); the concatenation of all sequences' tiles is split into
+// `streams` contiguous runs of T = ceil(total_tiles / streams) tiles. A work
+// item is the intersection of one sequence with one run, so every stream gets
+// the same number of tiles (the last tile of a sequence may be short) and the
+// schedule has at most streams + B items. Items are listed sequence by
+// sequence, which also lists them stream by stream. One CTA; the schedule lives
+// in the workspace, so no launch needs the lengths on the host.
 // ============================================================================
-__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t target, int32_t max_work) {
-    __shared__ long long s_total;
-    __shared__ int32_t s_chunk;
-    __shared__ int32_t s_carry;
-    __shared__ int32_t s_warp[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+constexpr int kPlanTile = 64;
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int x = s_warp[lane];
+        int w = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        s_warp[lane] = w - x;          // exclusive warp offsets
+        if (lane == 31) s_warp[32] = w;
+    }
+    __syncthreads();
+    const int excl = s_warp[warp] + incl - v;
+    total = s_warp[32];
+    __syncthreads();
+    return excl;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_work) {
+    __shared__ int s_warp[33];
+    __shared__ long long s_tiles;
+    const int tid = threadIdx.x;
     const int64_t cap = (int64_t)p.max_blocks * p.s.bs;
-    if (tid == 0) { s_total = 0; s_carry = 0; p.status[0] = 0; }
+    const int P = p.streams;
+    if (tid == 0) { s_tiles = 0; p.status[0] = 0; }
     __syncthreads();
     long long local = 0;
     for (int b = tid; b < p.B; b += blockDim.x) {
-        int L = p.seq_lens[b];
-        if (L >= p.q_len && L <= cap) local += L;
+        const int L = p.seq_lens[b];
+        if (L >= p.q_len && L <= cap) local += (L + kPlanTile - 1) / kPlanTile;
+        else raise_flag(p.status, FLAG_BAD_LENGTH);
     }
-    atomicAdd((unsigned long long *)&s_total, (unsigned long long)local);
+    atomicAdd((unsigned long long *)&s_tiles, (unsigned long long)local);
     __syncthreads();
-    if (tid == 0) {
-        long long per = (s_total + target - 1) / target;
-        per = ((per + 63) / 64) * 64;
-        if (per < 64) per = 64;
-        if (per > 0x40000000LL) per = 0x40000000LL;
-        s_chunk = (int32_t)per;
-    }
-    __syncthreads();
-    const int32_t chunk = s_chunk;
-    // Block-wide exclusive scan of split counts, 1024 sequences per pass.
+    const long long NB = s_tiles;
+    const long long T = NB > 0 ? (NB + P - 1) / P : 1;      // tiles per stream
+    int tile_carry = 0, item_carry = 0;
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + tid;
         int n = 0, L = 0;
         if (b < p.B) {
             L = p.seq_lens[b];
-            if (L >= p.q_len && L <= cap) n = (L + chunk - 1) / chunk;
-            else raise_flag(p.status, FLAG_BAD_LENGTH);
+            if (L >= p.q_len && L <= cap) n = (L + kPlanTile - 1) / kPlanTile;
         }
-        int incl = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) s_warp[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            int v = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
-            int w = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int u = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o) w += u;
-            }
-            s_warp[lane] = w - v;   // exclusive prefix of warp totals
-        }
-        __syncthreads();
-        const int start = s_carry + s_warp[warp] + incl - n;
+        int tot_tiles, tot_items;
+        const long long tb = tile_carry + block_exclusive_scan(n, s_warp, tot_tiles);
+        const long long first = tb / T;
+        const long long last = n > 0 ? (tb + n - 1) / T : first - 1;
+        const int cnt = (int)(last - first + 1);
+        const int start = item_carry + block_exclusive_scan(cnt, s_warp, tot_items);
         if (b < p.B) {
             ((int32_t *)p.split_start)[b] = start;
-            for (int k = 0; k < n && start + k < max_work; ++k) {
+            for (int k = 0; k < cnt && start + k < max_work; ++k) {
+                const long long s = first + k;
+                const long long lo = (s * T > tb ? s * T : tb) - tb;
+                const long long hi = ((s + 1) * T < tb + n ? (s + 1) * T : tb + n) - tb;
                 WorkItem it;
                 it.b = b;
-                it.t0 = k * chunk;
-                it.t1 = min((k + 1) * chunk, L);
-                it.slot = start + k;
+                it.t0 = (int)(lo * kPlanTile);
+                it.t1 = (int)min((long long)L, hi * kPlanTile);
+                it.stream = (int)s;
                 ((WorkItem *)p.work)[start + k] = it;
             }
         }
-        __syncthreads();
-        if (tid == blockDim.x - 1) s_carry = start + n;
-        __syncthreads();
+        tile_carry += tot_tiles;
+        item_carry += tot_items;
     }
+    const int total = min(item_carry, max_work);
     if (tid == 0) {
-        ((int32_t *)p.split_start)[p.B] = s_carry;
-        ((int32_t *)p.num_work)[0] = min(s_carry, max_work);
+        ((int32_t *)p.split_start)[p.B] = item_carry;
+        ((int32_t *)p.num_work)[0] = total;
+    }
+    __syncthreads();
+    // stream_start[s] = index of the first item whose stream is >= s
+    for (int i = tid; i <= total; i += blockDim.x) {
+        const int cur = i < total ? p.work[i].stream : P;
+        const int prev = i > 0 ? p.work[i - 1].stream : -1;
+        for (int s = prev + 1; s <= cur && s <= P; ++s) ((int32_t *)p.stream_start)[s] = i;
     }
 }
 
-cudaError_t launch_plan(const DecodeParams &p, int32_t target, int32_t max_work, cudaStream_t st) {
-    plan_kernel<<<1, 1024, 0, st>>>(p, target, max_work);
+cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
+    plan_kernel<<<1, 1024, 0, st>>>(p, max_work);
     return cudaGetLastError();
 }
 
@@ -258,7 +281,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
     const int w = blockIdx.x;
     if (w >= p.num_work[0]) return;
     const WorkItem item = p.work[w];
-    const int b = item.b, t0 = item.t0, t1 = item.t1, slot = item.slot;
+    const int b = item.b, t0 = item.t0, t1 = item.t1, slot = w;
     const int H = p.s.H, r = p.s.r, D = p.s.D(), Dp = D + 1;
     const int rows_total = p.q_len * H;
     const int row0 = blockIdx.y * kRB;

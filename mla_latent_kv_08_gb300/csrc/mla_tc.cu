@@ -61,6 +61,25 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bounded-wait safety net
 
+// Pipeline timestamps for performance analysis, compiled only with
+// -DMLA_TRACE: clock64 at each hand-off of one CTA (stream 0, half 0, row
+// tile 0) for its first kTraceTiles tiles. Product builds contain none of it.
+#ifdef MLA_TRACE
+constexpr int kTraceTiles = 64;
+__device__ long long g_trace[8][kTraceTiles];
+#define MLA_TRACE_POINT(ev, tile)                                                              \
+    do {                                                                                       \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (tile) < kTraceTiles)   \
+            g_trace[ev][tile] = clock64();                                                     \
+    } while (0)
+#else
+#define MLA_TRACE_POINT(ev, tile) \
+    do {                          \
+    } while (0)
+#endif
+// events: 0 TMA issued, 1 stage landed (MMA), 2 QK issued, 3 S seen (softmax),
+//         4 P ready (softmax), 5 PV issued, 6 PV stage released (producer saw empty)
+
 struct Bars {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -72,7 +91,6 @@ struct Bars {
     uint64_t mma_fin;
     uint32_t tmem_base;
     int32_t abort_flag;
-    int32_t bad_block;
 };
 
 struct TcParams {
@@ -205,19 +223,28 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 }
 
 // ---------------------------------------------------------------- the kernel
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+// Physical block of logical tile `lb` of sequence b, or -1.
+__device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
+    if (lb >= p.max_blocks) return -1;
+    const int blk = p.block_table[(size_t)b * p.max_blocks + lb];
+    return (blk >= 0 && blk < p.s.num_blocks) ? blk : -1;
+}
+
+constexpr int kPrefetchAhead = 4;   // tiles prefetched into L2 ahead of the TMA loads
+
 __global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                 const TcParams tp) {
+decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) {
     const DecodeParams &p = tp.p;
     const int half = blockIdx.x;            // 0/1: which 256 latent output dims
     const int g = blockIdx.y;               // query row tile
-    const int w = blockIdx.z;               // work item
-    if (w >= p.num_work[0]) return;
-    const WorkItem item = p.work[w];
-    const int b = item.b, t0 = item.t0, t1 = item.t1, slot = item.slot;
-    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    const int stream = blockIdx.z;          // work stream (persistent over its items)
+    const int i0 = p.stream_start[stream], i1 = p.stream_start[stream + 1];
+    if (i0 >= i1) return;
     const int rows_seq = p.q_len * p.s.H;
-    const int L = p.seq_lens[b];
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -235,10 +262,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             mbar_init(&bars->p_full[i], 128);
             mbar_init(&bars->pv_done[i], 1);
         }
-        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_full, 128);      // Q of the current item is in TMEM + smem
         mbar_init(&bars->mma_fin, 1);
         bars->abort_flag = 0;
-        bars->bad_block = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
@@ -254,249 +280,294 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    // ---- Q: TMA into smem (dims 0..383 staged in the KV stages), then rows to TMEM
-    const int q_row0 = b * rows_seq + g * kRows;
-    if (tid == 0) {
-        mbar_expect_tx(&bars->q_full, (kQTmemBlocks + kQSmemBlocks) * kQBlockBytes);
-        for (int c = 0; c < kQTmemBlocks + kQSmemBlocks; ++c) {
-            uint8_t *dst = c < kQTmemBlocks ? smem + kOffStage + c * kQBlockBytes
-                                            : smem + kOffQ + (c - kQTmemBlocks) * kQBlockBytes;
-            tma_load_2d(dst, &q_map, c * 64, q_row0, &bars->q_full);
-        }
-    }
-    if (warp < 4) {
-        const int row = 32 * warp + lane;
-        // tcgen05.st is warp-collective (.sync.aligned): the branch must be warp-uniform
-        const bool q_ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, bars, p.status));
-        if (q_ok) {
-            for (int c = 0; c < kQTmemBlocks; ++c) {
-                const uint8_t *blk = smem + kOffStage + c * kQBlockBytes;
-                uint32_t v[32];
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 u = *(const uint4 *)(blk + sw128(row, ch));
-                    v[4 * ch + 0] = u.x;
-                    v[4 * ch + 1] = u.y;
-                    v[4 * ch + 2] = u.z;
-                    v[4 * ch + 3] = u.w;
-                }
-                const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + kColQ + 32 * c;
-                TMEM_ST32(taddr, v);
-            }
-            tmem_wait_st();
-        }
-    }
-    tc_fence_before();
-    __syncthreads();              // Q in TMEM; the stages are free for KV
-    tc_fence_after();
-
     if (warp == 0) {
-        // ================================================= TMA producer
-        if (lane == 0 && !aborted(bars)) {
-            int issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % kStages;
-                if (t >= kStages && !mbar_wait(&bars->empty[s], ((t - kStages) / kStages) & 1, bars, p.status)) break;
-                const int lb = (t0 + t * kTile) / kTile;
-                int blk = lb < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + lb] : -1;
-                if (blk < 0 || blk >= p.s.num_blocks) {
-                    raise_flag(p.status, FLAG_BAD_BLOCK);
-                    atomicExch(&bars->bad_block, 1);
-                    blk = 0;
+        // ================================================= TMA producer (+ L2 prefetch)
+        if (lane == 0) {
+            const bool prefetcher = half == 0 && g == 0;
+            // look-ahead cursor for the L2 prefetch, PF tiles ahead of the loads
+            int pi = i0, pt = 0, ahead = 0;
+            auto advance_prefetch = [&]() {
+                while (pi < i1 && ahead < kPrefetchAhead) {
+                    const WorkItem it = p.work[pi];
+                    const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+                    if (pt >= nt) { ++pi; pt = 0; continue; }
+                    const int blk = block_of(p, it.b, it.t0 / kTile + pt);
+                    if (blk >= 0)
+                        prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * kD, kStageBytes);
+                    ++pt;
+                    ++ahead;
                 }
-                uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                mbar_expect_tx(&bars->full[s], kStageBytes);
-                for (int c = 0; c < kKvBlocks; ++c)
-                    tma_load_2d(stage + c * kKvBlockBytes, &kv_map, c * 64, blk * kTile, &bars->full[s]);
-                issued = t + 1;
+            };
+            int T = 0;
+            bool ok = true;
+            for (int i = i0; i < i1 && ok; ++i) {
+                const WorkItem it = p.work[i];
+                const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+                for (int t = 0; t < nt; ++t, ++T) {
+                    if (prefetcher) advance_prefetch();
+                    const int s = T % kStages;
+                    if (T >= kStages && !mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    MLA_TRACE_POINT(6, T);
+                    int blk = block_of(p, it.b, it.t0 / kTile + t);
+                    if (blk < 0) {            // the softmax marks the item's rows NaN
+                        raise_flag(p.status, FLAG_BAD_BLOCK);
+                        blk = 0;
+                    }
+                    uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                    mbar_expect_tx(&bars->full[s], kStageBytes);
+                    for (int c = 0; c < kKvBlocks; ++c)
+                        tma_load_2d(stage + c * kKvBlockBytes, &kv_map, c * 64, blk * kTile, &bars->full[s]);
+                    MLA_TRACE_POINT(0, T);
+                    if (prefetcher && ahead > 0) --ahead;
+                }
             }
             // drain: never leave a copy in flight into this CTA's shared memory
-            for (int t = issued - kStages; t < issued; ++t)
-                if (t >= 0) mbar_wait(&bars->full[t % kStages], (t / kStages) & 1, bars, p.status);
+            for (int u = T - kStages; u < T; ++u)
+                if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
         }
     } else if (warp == 1) {
-        // ================================================= MMA issuer
-        if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16(128, 64, false);
-            const uint32_t id_pv = idesc_bf16(128, 256, true);
-            const uint32_t d_s = tmem + kColS, d_o = tmem + kColO;
-            int pv_issued = 0;
-            bool ok = true;
-            auto issue_pv = [&](int t) -> bool {
-                const int pb = t & 1;
-                if (!mbar_wait(&bars->p_full[pb], (t >> 1) & 1, bars, p.status)) return false;
+        // ================================================= MMA issuer (lane 0 issues; the warp
+        // stays converged so that it can zero stale tail slots together)
+        const uint32_t id_qk = idesc_bf16(128, 64, false);
+        const uint32_t id_pv = idesc_bf16(128, 256, true);
+        const uint32_t d_s = tmem + kColS, d_o = tmem + kColO;
+        bool ok = true;
+        int T = 0;
+        auto issue_pv = [&](int Tp, bool first_of_item) -> bool {
+            const int pb = Tp & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, p.status))) return false;
+            if (lane == 0) {
                 tc_fence_after();
-                const int s = t % kStages;
+                const int s = Tp % kStages;
                 const uint32_t pbase = smem_u32(smem + kOffP + pb * kPBytes);
                 const uint32_t vbase = smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint64_t a = sdesc(pbase + 32 * j, 16, 1024);
                     const uint64_t bdesc = sdesc(vbase + 2048 * j, tp.v_lbo, tp.v_sbo);
-                    mma_ss(d_o, a, bdesc, id_pv, (t > 0 || j > 0) ? 1u : 0u);
+                    mma_ss(d_o, a, bdesc, id_pv, (first_of_item && j == 0) ? 0u : 1u);
                 }
                 mma_commit(&bars->pv_done[pb]);
                 mma_commit(&bars->empty[s]);
-                pv_issued = t + 1;
-                return true;
-            };
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int s = t % kStages;
-                if (!mbar_wait(&bars->full[s], (t / kStages) & 1, bars, p.status)) { ok = false; break; }
-                if (t > 0 && !mbar_wait(&bars->s_free, (t - 1) & 1, bars, p.status)) { ok = false; break; }
+                MLA_TRACE_POINT(5, Tp);
+            }
+            __syncwarp();
+            return true;
+        };
+        int item_no = 0;
+        for (int i = i0; i < i1 && ok; ++i, ++item_no) {
+            const WorkItem it = p.work[i];
+            const int L = p.seq_lens[it.b];
+            const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, item_no & 1, bars, p.status))) { ok = false; break; }
+            for (int t = 0; t < nt; ++t, ++T) {
+                const int s = T % kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status))) { ok = false; break; }
+                if (lane == 0) MLA_TRACE_POINT(1, T);
+                if (T > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->s_free, (T - 1) & 1, bars, p.status))) { ok = false; break; }
                 // the sequence's final partial block: zero the slots past the end so
                 // that P = 0 never meets stale (possibly non-finite) cache bytes
-                const int tile_start = t0 + t * kTile;
+                const int tile_start = it.t0 + t * kTile;
                 const int valid = min(kTile, L - tile_start);
                 if (valid < kTile) {
                     uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                    for (int c = 0; c < kKvBlocks; ++c)
-                        for (int rr = valid; rr < kTile; ++rr)
-                            for (int ch = 0; ch < 8; ++ch)
-                                *(uint4 *)(stage + c * kKvBlockBytes + sw128(rr, ch)) = make_uint4(0, 0, 0, 0);
-                    fence_proxy_async();
-                }
-                tc_fence_after();
-                const uint32_t kbase = smem_u32(smem + kOffStage + s * kStageBytes);
-                const uint32_t qbase = smem_u32(smem + kOffQ);
-#pragma unroll 4
-                for (int j = 0; j < 36; ++j) {
-                    const int c = j >> 2, k = j & 3;
-                    const uint64_t bdesc = sdesc(kbase + c * kKvBlockBytes + 32 * k, 16, 1024);
-                    if (c < kQTmemBlocks) {
-                        mma_ts(d_s, tmem + kColQ + 8 * j, bdesc, id_qk, j > 0 ? 1u : 0u);
-                    } else {
-                        const uint64_t a = sdesc(qbase + (c - kQTmemBlocks) * kQBlockBytes + 32 * k, 16, 1024);
-                        mma_ss(d_s, a, bdesc, id_qk, 1u);
+                    const int jobs = (kTile - valid) * kKvBlocks * 8;
+                    for (int jb = lane; jb < jobs; jb += 32) {
+                        const int rr = valid + jb / (kKvBlocks * 8), rem = jb % (kKvBlocks * 8);
+                        *(uint4 *)(stage + (rem >> 3) * kKvBlockBytes + sw128(rr, rem & 7)) = make_uint4(0, 0, 0, 0);
                     }
+                    fence_proxy_async();
+                    __syncwarp();
                 }
-                mma_commit(&bars->s_full);
-                if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t kbase = smem_u32(smem + kOffStage + s * kStageBytes);
+                    const uint32_t qbase = smem_u32(smem + kOffQ);
+#pragma unroll 4
+                    for (int j = 0; j < 36; ++j) {
+                        const int c = j >> 2, k = j & 3;
+                        const uint64_t bdesc = sdesc(kbase + c * kKvBlockBytes + 32 * k, 16, 1024);
+                        if (c < kQTmemBlocks) {
+                            mma_ts(d_s, tmem + kColQ + 8 * j, bdesc, id_qk, j > 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t a = sdesc(qbase + (c - kQTmemBlocks) * kQBlockBytes + 32 * k, 16, 1024);
+                            mma_ss(d_s, a, bdesc, id_qk, 1u);
+                        }
+                    }
+                    mma_commit(&bars->s_full);
+                    MLA_TRACE_POINT(2, T);
+                }
+                __syncwarp();
+                if (t > 0 && !issue_pv(T - 1, t == 1)) { ok = false; break; }
             }
-            if (ok && ntiles > 0) issue_pv(ntiles - 1);
-            (void)pv_issued;
+            if (ok && nt > 0 && !issue_pv(T - 1, nt == 1)) ok = false;
+        }
+        if (lane == 0) {
             mma_commit(&bars->mma_fin);
             mbar_wait(&bars->mma_fin, 0, bars, p.status);
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ================================================= softmax / epilogue
+        // ================================================= Q loads, softmax, epilogue
+        // Every branch around tcgen05.ld / tcgen05.st below is warp-uniform: those
+        // instructions are warp-collective (.sync.aligned).
         const int wq = warp & 3;
         const int row = 32 * wq + lane;
         const int row_seq = g * kRows + row;
         const bool row_valid = row_seq < rows_seq;
-        const int last_vis = L - p.q_len + (row_valid ? row_seq / p.s.H : 0);
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
-        float m_used = -CUDART_INF_F, l = 0.f;
         bool ok = true;
-        // Every branch around tcgen05.ld / tcgen05.st below is warp-uniform: those
-        // instructions are warp-collective (.sync.aligned).
-        for (int t = 0; t < ntiles && ok; ++t) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, t & 1, bars, p.status))) { ok = false; break; }
-            tc_fence_after();
-            uint32_t sv[64];
-            TMEM_LD32(lane_addr + kColS, sv);
-            TMEM_LD32(lane_addr + kColS + 32, (sv + 32));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars->s_free);
+        int T = 0;
+        for (int i = i0; i < i1 && ok; ++i) {
+            const WorkItem it = p.work[i];
+            const int L = p.seq_lens[it.b];
+            const int t0 = it.t0, t1 = it.t1;
+            const int nt = (t1 - t0 + kTile - 1) / kTile;
+            const int last_vis = L - p.q_len + (row_valid ? row_seq / p.s.H : 0);
+            // ---- Q of this item: dims 0..383 -> TMEM (A operand), 384..575 -> smem.
+            // The previous item's last QK has completed (its s_full was awaited).
+            {
+                const uint4 *src = (const uint4 *)((const __nv_bfloat16 *)p.q +
+                                                   ((size_t)it.b * rows_seq + (row_valid ? row_seq : 0)) * kD);
+#pragma unroll 1
+                for (int c = 0; c < kQTmemBlocks; ++c) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 u = row_valid ? __ldg(src + c * 8 + ch) : make_uint4(0, 0, 0, 0);
+                        v[4 * ch + 0] = u.x;
+                        v[4 * ch + 1] = u.y;
+                        v[4 * ch + 2] = u.z;
+                        v[4 * ch + 3] = u.w;
+                    }
+                    TMEM_ST32(lane_addr + kColQ + 32 * c, v);
+                }
+#pragma unroll
+                for (int c = 0; c < kQSmemBlocks; ++c)
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 u = row_valid ? __ldg(src + (kQTmemBlocks + c) * 8 + ch) : make_uint4(0, 0, 0, 0);
+                        *(uint4 *)(smem + kOffQ + c * kQBlockBytes + sw128(row, ch)) = u;
+                    }
+                tmem_wait_st();
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive(&bars->q_full);
+            }
+            float m_used = -CUDART_INF_F, l = 0.f;
+            bool bad_item = false;     // a block id of this item is out of range
+            for (int t = 0; t < nt && ok; ++t, ++T) {
+                bad_item |= block_of(p, it.b, t0 / kTile + t) < 0;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, T & 1, bars, p.status))) { ok = false; break; }
+                tc_fence_after();
+                if (row == 0) MLA_TRACE_POINT(3, T);
+                uint32_t sv[64];
+                TMEM_LD32(lane_addr + kColS, sv);
+                TMEM_LD32(lane_addr + kColS + 32, (sv + 32));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars->s_free);
 
-            const int tile_start = t0 + t * kTile;
-            float mx = -CUDART_INF_F;
+                const int tile_start = t0 + t * kTile;
+                float mx = -CUDART_INF_F;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const int tok = tile_start + j;
-                const bool vis = row_valid && tok < t1 && tok <= last_vis;
-                const float s2 = vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
-                sv[j] = __float_as_uint(s2);
-                mx = fmaxf(mx, s2);
-            }
-            float alpha = 1.f;
-            bool rescale = false;
-            const float m_new = fmaxf(m_used, mx);
-            if (m_new > m_used + 8.f) {
-                alpha = exp2f(m_used - m_new);        // 0 when nothing was accumulated yet
-                m_used = m_new;
-                rescale = t > 0;
-            }
-            float sum = 0.f;
-            uint32_t pk[32];
+                for (int j = 0; j < 64; ++j) {
+                    const int tok = tile_start + j;
+                    const bool vis = row_valid && tok < t1 && tok <= last_vis;
+                    const float s2 = vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
+                    sv[j] = __float_as_uint(s2);
+                    mx = fmaxf(mx, s2);
+                }
+                float alpha = 1.f;
+                bool rescale = false;
+                const float m_new = fmaxf(m_used, mx);
+                if (m_new > m_used + 8.f) {
+                    alpha = exp2f(m_used - m_new);        // 0 when nothing was accumulated yet
+                    m_used = m_new;
+                    rescale = t > 0;
+                }
+                float sum = 0.f;
+                uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float a = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j]) - m_used);
-                const float c = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j + 1]) - m_used);
-                const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
-                sum += a + c;          // fp32 row sum: the LSE does not see the bf16 rounding of P
-                pk[j] = *(const uint32_t *)&h;
-            }
-            l = l * alpha + sum;
-            const int pb = t & 1;
-            if (t >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[pb], ((t - 2) >> 1) & 1, bars, p.status))) {
-                ok = false;
-                break;
-            }
-            // Rows decide to rescale on their own; the warp corrects O together
-            // (alpha = 1 for rows that keep their max).
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O *= alpha once PV(t-1) has landed; PV(t) waits for p_full below
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, p.status))) {
+                for (int j = 0; j < 32; ++j) {
+                    const float a = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j]) - m_used);
+                    const float c = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j + 1]) - m_used);
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
+                    sum += a + c;          // fp32 row sum: the LSE does not see the bf16 rounding of P
+                    pk[j] = *(const uint32_t *)&h;
+                }
+                l = l * alpha + sum;
+                const int pb = T & 1;
+                if (T >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[pb], ((T - 2) >> 1) & 1, bars, p.status))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                // Rows decide to rescale on their own; the warp corrects O together
+                // (alpha = 1 for rows that keep their max).
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O *= alpha once PV(T-1) has landed; PV(T) waits for p_full below
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, bars, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t ov[32];
+                        TMEM_LD32(lane_addr + kColO + 32 * c, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                        TMEM_ST32(lane_addr + kColO + 32 * c, ov);
+                    }
+                    tmem_wait_st();
+                }
+                uint8_t *pbuf = smem + kOffP + pb * kPBytes;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *(uint4 *)(pbuf + sw128(row, ch)) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive(&bars->p_full[pb]);
+                if (row == 0) MLA_TRACE_POINT(4, T);
+            }
+            // ---- epilogue of this item: wait for its last PV, then O / l -> partial slot i
+            if (ok && nt > 0) {
+                const int tl = T - 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status));
+            }
+            const bool bad = aborted(bars) || !ok || bad_item;
+            tc_fence_after();
+            {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                float *po = p.part_o + ((size_t)i * rows_seq + (row_valid ? row_seq : 0)) * p.s.r + 256 * half;
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
                     uint32_t ov[32];
-                    TMEM_LD32(lane_addr + kColO + 32 * c, ov);
-                    tmem_wait_ld();
+                    if (ok) {                      // warp-uniform
+                        TMEM_LD32(lane_addr + kColO + 32 * c, ov);
+                        tmem_wait_ld();
+                    }
+                    if (!row_valid) continue;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                    TMEM_ST32(lane_addr + kColO + 32 * c, ov);
-                }
-                tmem_wait_st();
-            }
-            uint8_t *pbuf = smem + kOffP + pb * kPBytes;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *(uint4 *)(pbuf + sw128(row, ch)) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(&bars->p_full[pb]);
-        }
-        // epilogue: wait for the last PV, then O / l -> partial buffer
-        if (ok && ntiles > 0) {
-            const int tl = ntiles - 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status));
-        }
-        const bool bad = aborted(bars) || !ok || *(volatile int32_t *)&bars->bad_block;
-        tc_fence_after();
-        {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            float *po = p.part_o + ((size_t)slot * rows_seq + (row_valid ? row_seq : 0)) * p.s.r + 256 * half;
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                uint32_t ov[32];
-                if (ok) {                      // warp-uniform
-                    TMEM_LD32(lane_addr + kColO + 32 * c, ov);
-                    tmem_wait_ld();
-                }
-                if (!row_valid) continue;
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    float4 f;
-                    f.x = ok ? __uint_as_float(ov[k + 0]) * inv : 0.f;
-                    f.y = ok ? __uint_as_float(ov[k + 1]) * inv : 0.f;
-                    f.z = ok ? __uint_as_float(ov[k + 2]) * inv : 0.f;
-                    f.w = ok ? __uint_as_float(ov[k + 3]) * inv : 0.f;
-                    *(float4 *)(po + 32 * c + k) = f;
+                    for (int k = 0; k < 32; k += 4) {
+                        float4 f;
+                        f.x = ok ? __uint_as_float(ov[k + 0]) * inv : 0.f;
+                        f.y = ok ? __uint_as_float(ov[k + 1]) * inv : 0.f;
+                        f.z = ok ? __uint_as_float(ov[k + 2]) * inv : 0.f;
+                        f.w = ok ? __uint_as_float(ov[k + 3]) * inv : 0.f;
+                        *(float4 *)(po + 32 * c + k) = f;
+                    }
                 }
             }
-        }
-        if (row_valid) {
-            if (half == 0)
-                p.part_lse[(size_t)slot * rows_seq + row_seq] =
+            if (row_valid && half == 0)
+                p.part_lse[(size_t)i * rows_seq + row_seq] =
                     bad ? CUDART_NAN_F : (l > 0.f ? m_used + log2f(l) : -CUDART_INF_F);
+            tc_fence_before();     // O reads complete before the next item's first PV
         }
     }
     tc_fence_before();
@@ -549,17 +620,22 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     // MN-major V operand: 64-dim atoms 8 KB apart, 8-token groups 1 KB apart.
     tp.v_lbo = tc::kKvBlockBytes;
     tp.v_sbo = 1024;
-    CUtensorMap kv_map, q_map;
+    CUtensorMap kv_map;
     memset(&kv_map, 0, sizeof kv_map);
-    memset(&q_map, 0, sizeof q_map);
     if (!tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile)) return cudaErrorInvalidValue;
-    if (!tc::make_map(&q_map, p.q, (uint64_t)p.B * p.q_len * p.s.H, tc::kRows)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(2, tp.row_tiles, max_work);
-    tc::decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, q_map, tp);
+    (void)max_work;
+    dim3 grid(2, tp.row_tiles, p.streams);
+    tc::decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, tp);
     return cudaGetLastError();
 }
 
 }  // namespace mla
+
+#ifdef MLA_TRACE
+extern "C" int mla_trace_read(long long *host, int n) {
+    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);
+}
+#endif
