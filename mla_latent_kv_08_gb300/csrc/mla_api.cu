@@ -188,7 +188,8 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     c.W_UV = W_UV;
     c.out = out;
     c.lse = lse;
-    if (launch_combine(c, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    const bool comb_tc = impl == MLA_IMPL_TCGEN05 && combine_tc_supported(p.s);
+    if ((comb_tc ? launch_combine_tc(c, stream_) : launch_combine(c, stream_)) != cudaSuccess) return MLA_ERR_CUDA;
     prof_kernels(int2 ? 4 : 3);
     return MLA_OK;
 }

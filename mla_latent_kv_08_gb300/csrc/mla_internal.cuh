@@ -110,6 +110,9 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 // ---- tensor-core decode (defined in mla_tc.cu) -----------------------------
 bool tc_shape_supported(const ShapeArgs &s);
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st);
+// ---- tensor-core combine + W_UV (defined in mla_combine_tc.cu) --------------
+bool combine_tc_supported(const ShapeArgs &s);
+cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st);
 
 // ---- small device helpers ---------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {

@@ -28,6 +28,7 @@
 // reads TMEM lanes 32*(w%4)..+31). All waits are bounded: a wait that gives up
 // records FLAG_TIMEOUT and the CTA winds down without trapping.
 #include "mla_internal.cuh"
+#include "mla_ptx.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -66,7 +67,8 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bou
 // tile 0) for its first kTraceTiles tiles. Product builds contain none of it.
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 64;
-__device__ long long g_trace[8][kTraceTiles];
+__device__ long long g_trace[16][kTraceTiles];
+__device__ unsigned long long g_cta_time[4096][3];   // start, end (globaltimer ns), tiles
 #define MLA_TRACE_POINT(ev, tile)                                                              \
     do {                                                                                       \
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (tile) < kTraceTiles)   \
@@ -78,7 +80,8 @@ __device__ long long g_trace[8][kTraceTiles];
     } while (0)
 #endif
 // events: 0 TMA issued, 1 stage landed (MMA), 2 QK issued, 3 S seen (softmax),
-//         4 P ready (softmax), 5 PV issued, 6 PV stage released (producer saw empty)
+//         4 P ready (softmax), 5 PV issued, 6 PV stage released (producer saw empty),
+//         7 S in registers, 8 exponentials done, 9 previous P buffer free (softmax)
 
 struct Bars {
     uint64_t full[kStages];
@@ -100,127 +103,14 @@ struct TcParams {
 };
 
 // ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
-    return (uint32_t)__cvta_generic_to_shared(ptr);
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
+using namespace ptx;
+
 // Bounded wait for the phase with the given parity. On give-up it raises the
 // CTA abort flag and the global timeout flag and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Bars *bars, int32_t *status) {
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (*(volatile int32_t *)&bars->abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
-                atomicExch(&bars->abort_flag, 1);
-                raise_flag(status, FLAG_TIMEOUT);
-                return false;
-            }
-        }
-    }
+    return mbar_wait_bounded(bar, parity, &bars->abort_flag, status, FLAG_TIMEOUT, kTimeoutNs);
 }
 __device__ __forceinline__ bool aborted(Bars *bars) { return *(volatile int32_t *)&bars->abort_flag != 0; }
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulate.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-#define TMEM_LD32(taddr, v)                                                                                      \
-    asm volatile(                                                                                                \
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"         \
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                               \
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),      \
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), \
-          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),            \
-          "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),            \
-          "=r"(v[30]), "=r"(v[31])                                                                               \
-        : "r"(taddr))
-
-#define TMEM_ST32(taddr, v)                                                                                      \
-    asm volatile(                                                                                                \
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"  \
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"                                     \
-        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),   \
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),           \
-        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),         \
-        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])          \
-        : "memory")
-
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Byte offset of element (row, col) in a [rows x 64] bf16 tile stored with the
-// 128-byte swizzle (16-byte chunk index XOR row % 8; 8-row atoms of 1 KB).
-__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
-    return (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
-}
 
 // ---------------------------------------------------------------- the kernel
 __device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
@@ -245,6 +135,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
     const int i0 = p.stream_start[stream], i1 = p.stream_start[stream + 1];
     if (i0 >= i1) return;
     const int rows_seq = p.q_len * p.s.H;
+#ifdef MLA_TRACE
+    const unsigned cta_id = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    if (threadIdx.x == 0 && cta_id < 4096) g_cta_time[cta_id][0] = globaltimer();
+#endif
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -282,57 +176,61 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
 
     if (warp == 0) {
         // ================================================= TMA producer (+ L2 prefetch)
-        if (lane == 0) {
-            const bool prefetcher = half == 0 && g == 0;
-            // look-ahead cursor for the L2 prefetch, PF tiles ahead of the loads
-            int pi = i0, pt = 0, ahead = 0;
-            auto advance_prefetch = [&]() {
-                while (pi < i1 && ahead < kPrefetchAhead) {
-                    const WorkItem it = p.work[pi];
-                    const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
-                    if (pt >= nt) { ++pi; pt = 0; continue; }
-                    const int blk = block_of(p, it.b, it.t0 / kTile + pt);
-                    if (blk >= 0)
-                        prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * kD, kStageBytes);
-                    ++pt;
-                    ++ahead;
-                }
-            };
-            int T = 0;
-            bool ok = true;
-            for (int i = i0; i < i1 && ok; ++i) {
-                const WorkItem it = p.work[i];
+        // The warp runs converged: lane 0 waits and arms the barrier, lanes 0..8
+        // each issue one of the tile's nine boxes.
+        const bool prefetcher = half == 0 && g == 0;
+        int pi = i0, pt = 0, ahead = 0;        // L2 prefetch cursor, kPrefetchAhead tiles ahead
+        auto advance_prefetch = [&]() {
+            while (pi < i1 && ahead < kPrefetchAhead) {
+                const WorkItem it = p.work[pi];
                 const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
-                for (int t = 0; t < nt; ++t, ++T) {
-                    if (prefetcher) advance_prefetch();
-                    const int s = T % kStages;
-                    if (T >= kStages && !mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    MLA_TRACE_POINT(6, T);
-                    int blk = block_of(p, it.b, it.t0 / kTile + t);
-                    if (blk < 0) {            // the softmax marks the item's rows NaN
-                        raise_flag(p.status, FLAG_BAD_BLOCK);
-                        blk = 0;
-                    }
-                    uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                    mbar_expect_tx(&bars->full[s], kStageBytes);
-                    for (int c = 0; c < kKvBlocks; ++c)
-                        tma_load_2d(stage + c * kKvBlockBytes, &kv_map, c * 64, blk * kTile, &bars->full[s]);
+                if (pt >= nt) { ++pi; pt = 0; continue; }
+                const int blk = block_of(p, it.b, it.t0 / kTile + pt);
+                if (blk >= 0)
+                    prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * kD, kStageBytes);
+                ++pt;
+                ++ahead;
+            }
+        };
+        int T = 0;
+        bool ok = true;
+        for (int i = i0; i < i1 && ok; ++i) {
+            const WorkItem it = p.work[i];
+            const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+            int next_blk = block_of(p, it.b, it.t0 / kTile);     // loaded one tile ahead
+            for (int t = 0; t < nt; ++t, ++T) {
+                if (prefetcher && lane == 0) advance_prefetch();
+                int blk = next_blk;
+                if (t + 1 < nt) next_blk = block_of(p, it.b, it.t0 / kTile + t + 1);
+                const int s = T % kStages;
+                if (T >= kStages &&
+                    !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) MLA_TRACE_POINT(6, T);
+                if (blk < 0) {            // the softmax marks the item's rows NaN
+                    if (lane == 0) raise_flag(p.status, FLAG_BAD_BLOCK);
+                    blk = 0;
+                }
+                uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                if (lane == 0) mbar_expect_tx(&bars->full[s], kStageBytes);
+                __syncwarp();
+                if (lane < kKvBlocks)
+                    tma_load_2d(stage + lane * kKvBlockBytes, &kv_map, lane * 64, blk * kTile, &bars->full[s]);
+                if (lane == 0) {
                     MLA_TRACE_POINT(0, T);
                     if (prefetcher && ahead > 0) --ahead;
                 }
             }
-            // drain: never leave a copy in flight into this CTA's shared memory
-            for (int u = T - kStages; u < T; ++u)
-                if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
         }
+        // drain: never leave a copy in flight into this CTA's shared memory
+        for (int u = T - kStages; u < T; ++u)
+            if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
+        __syncwarp();
     } else if (warp == 1) {
         // ================================================= MMA issuer (lane 0 issues; the warp
         // stays converged so that it can zero stale tail slots together)
-        const uint32_t id_qk = idesc_bf16(128, 64, false);
-        const uint32_t id_pv = idesc_bf16(128, 256, true);
         const uint32_t d_s = tmem + kColS, d_o = tmem + kColO;
         bool ok = true;
         int T = 0;
@@ -342,14 +240,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             if (lane == 0) {
                 tc_fence_after();
                 const int s = Tp % kStages;
-                const uint32_t pbase = smem_u32(smem + kOffP + pb * kPBytes);
-                const uint32_t vbase = smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint64_t a = sdesc(pbase + 32 * j, 16, 1024);
-                    const uint64_t bdesc = sdesc(vbase + 2048 * j, tp.v_lbo, tp.v_sbo);
-                    mma_ss(d_o, a, bdesc, id_pv, (first_of_item && j == 0) ? 0u : 1u);
-                }
+                const uint64_t a0 = sdesc(smem_u32(smem + kOffP + pb * kPBytes), 16, 1024);
+                const uint64_t b0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes,
+                                          tp.v_lbo, tp.v_sbo);
+                constexpr uint32_t kIdPv = idesc_bf16(128, 256, true);
+                // descriptor start addresses advance in 16-byte units
+                if (first_of_item) mma_ss_k<kIdPv, 0>(d_o, a0, b0);
+                else mma_ss_k<kIdPv, 1>(d_o, a0, b0);
+                mma_ss_k<kIdPv, 1>(d_o, a0 + 2, b0 + 128);
+                mma_ss_k<kIdPv, 1>(d_o, a0 + 4, b0 + 256);
+                mma_ss_k<kIdPv, 1>(d_o, a0 + 6, b0 + 384);
                 mma_commit(&bars->pv_done[pb]);
                 mma_commit(&bars->empty[s]);
                 MLA_TRACE_POINT(5, Tp);
@@ -382,26 +282,51 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     fence_proxy_async();
                     __syncwarp();
                 }
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t kbase = smem_u32(smem + kOffStage + s * kStageBytes);
-                    const uint32_t qbase = smem_u32(smem + kOffQ);
-#pragma unroll 4
-                    for (int j = 0; j < 36; ++j) {
-                        const int c = j >> 2, k = j & 3;
-                        const uint64_t bdesc = sdesc(kbase + c * kKvBlockBytes + 32 * k, 16, 1024);
-                        if (c < kQTmemBlocks) {
-                            mma_ts(d_s, tmem + kColQ + 8 * j, bdesc, id_qk, j > 0 ? 1u : 0u);
-                        } else {
-                            const uint64_t a = sdesc(qbase + (c - kQTmemBlocks) * kQBlockBytes + 32 * k, 16, 1024);
-                            mma_ss(d_s, a, bdesc, id_qk, 1u);
+                // QK(T) in six groups of six K-steps. PV(T-1) of the same item is
+                // slipped in between groups as soon as its P is ready, so that the
+                // stage it reads is released early; otherwise it follows QK(T).
+                bool pv_pending = t > 0;
+                const int pb_prev = (T - 1) & 1;
+                tc_fence_after();
+                const uint64_t kd = sdesc(smem_u32(smem + kOffStage + s * kStageBytes), 16, 1024);
+                const uint64_t qd = sdesc(smem_u32(smem + kOffQ), 16, 1024);
+                const uint32_t qt = tmem + kColQ;
+                constexpr uint32_t kIdQk = idesc_bf16(128, 64, false);
+#pragma unroll
+                for (int grp = 0; grp < 6; ++grp) {
+                    if (lane == 0) {
+                        // K-step j: column block j/4, 32-byte step j%4 inside the swizzle
+                        // atom; descriptor start addresses advance in 16-byte units.
+#pragma unroll
+                        for (int jj = 0; jj < 6; ++jj) {
+                            const int j = grp * 6 + jj;
+                            const uint64_t bd = kd + (uint64_t)(((j >> 2) * kKvBlockBytes + 32 * (j & 3)) >> 4);
+                            if (j == 0) {
+                                mma_ts_k<kIdQk, 0>(d_s, qt, bd);
+                            } else if (j < 4 * kQTmemBlocks) {
+                                mma_ts_k<kIdQk, 1>(d_s, qt + 8 * j, bd);
+                            } else {
+                                mma_ss_k<kIdQk, 1>(
+                                    d_s, qd + (uint64_t)((((j >> 2) - kQTmemBlocks) * kQBlockBytes + 32 * (j & 3)) >> 4), bd);
+                            }
                         }
                     }
+                    __syncwarp();
+                    if (pv_pending && grp < 5) {
+                        const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_try(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
+                        if (ready) {
+                            if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
+                            pv_pending = false;
+                        }
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) {
                     mma_commit(&bars->s_full);
                     MLA_TRACE_POINT(2, T);
                 }
                 __syncwarp();
-                if (t > 0 && !issue_pv(T - 1, t == 1)) { ok = false; break; }
+                if (pv_pending && !issue_pv(T - 1, t == 1)) { ok = false; break; }
             }
             if (ok && nt > 0 && !issue_pv(T - 1, nt == 1)) ok = false;
         }
@@ -470,14 +395,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bars->s_free);
+                if (row == 0) MLA_TRACE_POINT(7, T);
 
                 const int tile_start = t0 + t * kTile;
+                // tokens j < n_vis of this tile are visible to this row
+                const int n_vis = row_valid ? max(0, min(t1, last_vis + 1) - tile_start) : 0;
                 float mx = -CUDART_INF_F;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
-                    const int tok = tile_start + j;
-                    const bool vis = row_valid && tok < t1 && tok <= last_vis;
-                    const float s2 = vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
+                    const float s2 = j < n_vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
                     sv[j] = __float_as_uint(s2);
                     mx = fmaxf(mx, s2);
                 }
@@ -489,22 +415,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     m_used = m_new;
                     rescale = t > 0;
                 }
-                float sum = 0.f;
+                // exponent base: the running max, or +inf for a row with nothing
+                // visible yet (every exponent is then -inf and P = 0)
+                const float mb = m_used == -CUDART_INF_F ? CUDART_INF_F : m_used;
+                float sum0 = 0.f, sum1 = 0.f;
                 uint32_t pk[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float a = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j]) - m_used);
-                    const float c = m_used == -CUDART_INF_F ? 0.f : exp2f(__uint_as_float(sv[2 * j + 1]) - m_used);
+                    const float a = ex2(__uint_as_float(sv[2 * j]) - mb);
+                    const float c = ex2(__uint_as_float(sv[2 * j + 1]) - mb);
                     const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
-                    sum += a + c;          // fp32 row sum: the LSE does not see the bf16 rounding of P
+                    sum0 += a;             // fp32 row sum: the LSE does not see the bf16 rounding of P
+                    sum1 += c;
                     pk[j] = *(const uint32_t *)&h;
                 }
+                const float sum = sum0 + sum1;
+                if (row == 0) MLA_TRACE_POINT(8, T);
                 l = l * alpha + sum;
                 const int pb = T & 1;
                 if (T >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[pb], ((T - 2) >> 1) & 1, bars, p.status))) {
                     ok = false;
                     break;
                 }
+                if (row == 0) MLA_TRACE_POINT(9, T);
                 // Rows decide to rescale on their own; the warp corrects O together
                 // (alpha = 1 for rows that keep their max).
                 if (__any_sync(0xffffffffu, rescale)) {
@@ -572,6 +505,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
     }
     tc_fence_before();
     __syncthreads();
+#ifdef MLA_TRACE
+    if (threadIdx.x == 0 && cta_id < 4096) {
+        g_cta_time[cta_id][1] = globaltimer();
+        int nt = 0;
+        for (int i = i0; i < i1; ++i) nt += (p.work[i].t1 - p.work[i].t0 + kTile - 1) / kTile;
+        g_cta_time[cta_id][2] = ((unsigned long long)(i1 - i0) << 32) | (unsigned)nt;
+    }
+#endif
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
@@ -637,5 +578,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
 #ifdef MLA_TRACE
 extern "C" int mla_trace_read(long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);
+}
+extern "C" int mla_trace_cta(unsigned long long *host, int n) {
+    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 3 * (size_t)n);
 }
 #endif
