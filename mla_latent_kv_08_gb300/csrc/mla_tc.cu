@@ -38,7 +38,7 @@
 namespace mla {
 namespace tc {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;         // 4 control warps + 8 softmax warps
 constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
@@ -47,6 +47,7 @@ constexpr int kQTmemBlocks = 6;       // Q column blocks held in TMEM (dims 0..3
 constexpr int kQSmemBlocks = 3;       // Q column blocks read from smem (dims 384..575)
 constexpr int kStages = 2;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
+constexpr int kSoftmaxThreads = 256;  // warps 4..11: two warps per 32-row lane quarter
 
 constexpr uint32_t kKvBlockBytes = kTile * 128;                     // 8 KB
 constexpr uint32_t kStageBytes = kKvBlocks * kKvBlockBytes;         // 72 KB
@@ -56,7 +57,8 @@ constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
 constexpr uint32_t kOffP = kOffQ + kQSmemBlocks * kQBlockBytes;     // 192 KB
 constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;                   // 224 KB
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;               // + barriers + alignment slack
+constexpr uint32_t kOffXchg = kOffBar + 256;                        // [2][128] fp32 row values
+constexpr uint32_t kSmemBytes = kOffXchg + 1024 + 1024;             // + alignment slack
 static_assert(kQTmemBlocks * kQBlockBytes <= kStages * kStageBytes, "Q staging must fit the stages");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -92,6 +94,8 @@ struct Bars {
     uint64_t pv_done[2];
     uint64_t q_full;
     uint64_t mma_fin;
+    uint64_t xchg_full;       // both halves of every row wrote their value
+    uint64_t xchg_read;       // both halves read the other's value
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -151,13 +155,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->s_free, 128);
+        mbar_init(&bars->s_free, kSoftmaxThreads);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->p_full[i], 128);
+            mbar_init(&bars->p_full[i], kSoftmaxThreads);
             mbar_init(&bars->pv_done[i], 1);
         }
-        mbar_init(&bars->q_full, 128);      // Q of the current item is in TMEM + smem
+        mbar_init(&bars->q_full, kSoftmaxThreads);   // Q of the current item is in TMEM + smem
         mbar_init(&bars->mma_fin, 1);
+        mbar_init(&bars->xchg_full, kSoftmaxThreads);
+        mbar_init(&bars->xchg_read, kSoftmaxThreads);
         bars->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -337,15 +343,32 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
         __syncwarp();
     } else if (warp >= 4) {
         // ================================================= Q loads, softmax, epilogue
-        // Every branch around tcgen05.ld / tcgen05.st below is warp-uniform: those
-        // instructions are warp-collective (.sync.aligned).
+        // Warps 4..11: warp w owns rows 32*(w%4)..+31 (its TMEM lane quarter) and
+        // half hs = (w-4)/4 of each row: score columns 32*hs..+31, output columns
+        // 128*hs..+127. The two halves of a row agree on the running max through
+        // shared memory once per tile. Every branch around tcgen05.ld / tcgen05.st
+        // is warp-uniform: those instructions are warp-collective (.sync.aligned).
         const int wq = warp & 3;
+        const int hs = (warp - 4) >> 2;
         const int row = 32 * wq + lane;
         const int row_seq = g * kRows + row;
         const bool row_valid = row_seq < rows_seq;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
+        float *xchg = (float *)(smem + kOffXchg);       // [2][128]
         bool ok = true;
         int T = 0;
+        int nx = 0;                                     // exchanges done
+        // Swap one value per row with the other half of the row (bounded waits).
+        auto exchange = [&](float v, float &other) -> bool {
+            if (nx > 0 && !mbar_wait(&bars->xchg_read, (nx - 1) & 1, bars, p.status)) return false;
+            xchg[hs * 128 + row] = v;
+            mbar_arrive(&bars->xchg_full);
+            if (!mbar_wait(&bars->xchg_full, nx & 1, bars, p.status)) return false;
+            other = xchg[(hs ^ 1) * 128 + row];
+            mbar_arrive(&bars->xchg_read);
+            ++nx;
+            return true;
+        };
         for (int i = i0; i < i1 && ok; ++i) {
             const WorkItem it = p.work[i];
             const int L = p.seq_lens[it.b];
@@ -358,7 +381,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 const uint4 *src = (const uint4 *)((const __nv_bfloat16 *)p.q +
                                                    ((size_t)it.b * rows_seq + (row_valid ? row_seq : 0)) * kD);
 #pragma unroll 1
-                for (int c = 0; c < kQTmemBlocks; ++c) {
+                for (int c = 3 * hs; c < 3 * hs + 3; ++c) {
                     uint32_t v[32];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -370,8 +393,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     }
                     TMEM_ST32(lane_addr + kColQ + 32 * c, v);
                 }
-#pragma unroll
-                for (int c = 0; c < kQSmemBlocks; ++c)
+                for (int c = hs; c < kQSmemBlocks; c += 2)
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
                         const uint4 u = row_valid ? __ldg(src + (kQTmemBlocks + c) * 8 + ch) : make_uint4(0, 0, 0, 0);
@@ -382,30 +404,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 tc_fence_before();
                 mbar_arrive(&bars->q_full);
             }
-            float m_used = -CUDART_INF_F, l = 0.f;
+            float m_used = -CUDART_INF_F, l = 0.f;       // l: this half's share of the row sum
             bool bad_item = false;     // a block id of this item is out of range
             for (int t = 0; t < nt && ok; ++t, ++T) {
                 bad_item |= block_of(p, it.b, t0 / kTile + t) < 0;
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, T & 1, bars, p.status))) { ok = false; break; }
                 tc_fence_after();
-                if (row == 0) MLA_TRACE_POINT(3, T);
-                uint32_t sv[64];
-                TMEM_LD32(lane_addr + kColS, sv);
-                TMEM_LD32(lane_addr + kColS + 32, (sv + 32));
+                if (row == 0 && hs == 0) MLA_TRACE_POINT(3, T);
+                uint32_t sv[32];
+                TMEM_LD32(lane_addr + kColS + 32 * hs, sv);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bars->s_free);
-                if (row == 0) MLA_TRACE_POINT(7, T);
+                if (row == 0 && hs == 0) MLA_TRACE_POINT(7, T);
 
-                const int tile_start = t0 + t * kTile;
-                // tokens j < n_vis of this tile are visible to this row
+                const int tile_start = t0 + t * kTile + 32 * hs;
+                // tokens j < n_vis of this half-tile are visible to this row
                 const int n_vis = row_valid ? max(0, min(t1, last_vis + 1) - tile_start) : 0;
                 float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     const float s2 = j < n_vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
                     sv[j] = __float_as_uint(s2);
                     mx = fmaxf(mx, s2);
+                }
+                // the row's max over both halves
+                {
+                    float other = -CUDART_INF_F;
+                    if (!__all_sync(0xffffffffu, exchange(mx, other))) { ok = false; break; }
+                    mx = fmaxf(mx, other);
                 }
                 float alpha = 1.f;
                 bool rescale = false;
@@ -419,9 +446,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 // visible yet (every exponent is then -inf and P = 0)
                 const float mb = m_used == -CUDART_INF_F ? CUDART_INF_F : m_used;
                 float sum0 = 0.f, sum1 = 0.f;
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     const float a = ex2(__uint_as_float(sv[2 * j]) - mb);
                     const float c = ex2(__uint_as_float(sv[2 * j + 1]) - mb);
                     const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
@@ -429,17 +456,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     sum1 += c;
                     pk[j] = *(const uint32_t *)&h;
                 }
-                const float sum = sum0 + sum1;
-                if (row == 0) MLA_TRACE_POINT(8, T);
-                l = l * alpha + sum;
+                if (row == 0 && hs == 0) MLA_TRACE_POINT(8, T);
+                l = l * alpha + (sum0 + sum1);
                 const int pb = T & 1;
                 if (T >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[pb], ((T - 2) >> 1) & 1, bars, p.status))) {
                     ok = false;
                     break;
                 }
-                if (row == 0) MLA_TRACE_POINT(9, T);
-                // Rows decide to rescale on their own; the warp corrects O together
-                // (alpha = 1 for rows that keep their max).
+                if (row == 0 && hs == 0) MLA_TRACE_POINT(9, T);
+                // Rows decide to rescale on their own; the warp corrects its O columns
+                // together (alpha = 1 for rows that keep their max).
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O *= alpha once PV(T-1) has landed; PV(T) waits for p_full below
                     if (!__all_sync(0xffffffffu,
@@ -449,7 +475,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 4 * hs; c < 4 * hs + 4; ++c) {
                         uint32_t ov[32];
                         TMEM_LD32(lane_addr + kColO + 32 * c, ov);
                         tmem_wait_ld();
@@ -461,28 +487,33 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 }
                 uint8_t *pbuf = smem + kOffP + pb * kPBytes;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *(uint4 *)(pbuf + sw128(row, ch)) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                for (int ch = 0; ch < 4; ++ch)
+                    *(uint4 *)(pbuf + sw128(row, 4 * hs + ch)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
                 fence_proxy_async();
                 tc_fence_before();
                 mbar_arrive(&bars->p_full[pb]);
-                if (row == 0) MLA_TRACE_POINT(4, T);
+                if (row == 0 && hs == 0) MLA_TRACE_POINT(4, T);
             }
             // ---- epilogue of this item: wait for its last PV, then O / l -> partial slot i
             if (ok && nt > 0) {
                 const int tl = T - 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status));
             }
+            // the row sum over both halves
+            float l_other = 0.f;
+            if (ok) ok = __all_sync(0xffffffffu, exchange(l, l_other));
+            const float l_row = l + l_other;
             const bool bad = aborted(bars) || !ok || bad_item;
             tc_fence_after();
             {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                float *po = p.part_o + ((size_t)i * rows_seq + (row_valid ? row_seq : 0)) * p.s.r + 256 * half;
+                const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                float *po = p.part_o + ((size_t)i * rows_seq + (row_valid ? row_seq : 0)) * p.s.r + 256 * half + 128 * hs;
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t ov[32];
                     if (ok) {                      // warp-uniform
-                        TMEM_LD32(lane_addr + kColO + 32 * c, ov);
+                        TMEM_LD32(lane_addr + kColO + 128 * hs + 32 * c, ov);
                         tmem_wait_ld();
                     }
                     if (!row_valid) continue;
@@ -497,9 +528,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     }
                 }
             }
-            if (row_valid && half == 0)
+            if (row_valid && half == 0 && hs == 0)
                 p.part_lse[(size_t)i * rows_seq + row_seq] =
-                    bad ? CUDART_NAN_F : (l > 0.f ? m_used + log2f(l) : -CUDART_INF_F);
+                    bad ? CUDART_NAN_F : (l_row > 0.f ? m_used + log2f(l_row) : -CUDART_INF_F);
             tc_fence_before();     // O reads complete before the next item's first PV
         }
     }
