@@ -114,8 +114,14 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
     w.part_o = off;        off = up256(off + sizeof(float) * (size_t)w.max_work * rows * s->kv_lora_rank);
     w.part_lse = off;      off = up256(off + sizeof(float) * (size_t)w.max_work * rows);
     w.q_prep = off;
-    if (s->kind == MLA_KV_INT2_ROT)
-        off = up256(off + sizeof(float) * (size_t)B * rows * (s->kv_lora_rank + s->rope_dim));
+    if (s->kind == MLA_KV_INT2_ROT) {
+        const size_t nrow = (size_t)B * rows;
+        off = up256(off + sizeof(float) * nrow * (s->kv_lora_rank + s->rope_dim));
+        w.o_rot = off;  off = up256(off + sizeof(float) * nrow * s->kv_lora_rank);
+        w.o_lat = off;  off = up256(off + sizeof(float) * nrow * s->kv_lora_rank);
+        w.lse2 = off;   off = up256(off + sizeof(float) * nrow);
+        w.ident = off;  off = up256(off + sizeof(int32_t) * ((size_t)B + 1));
+    }
     w.total = off;
     return w;
 }
@@ -169,7 +175,20 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.part_lse = (float *)(ws + w.part_lse);
 
     if (launch_plan(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-    if (int2 && launch_qprep(p, R, (float *)(ws + w.q_prep), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    const bool tc = impl == MLA_IMPL_TCGEN05;
+    if (int2) {
+        // the rotated query: fp32 for the CUDA-core kernel; fp16 (the MMA operand type
+        // of this cache kind) from the tensor-core GEMM for the tensor-core kernel,
+        // which then reads it in place of q
+        if (tc) {
+            if (launch_rot_query(R, q, ws + w.q_prep, B * q_len * s->num_heads, s->kv_lora_rank + s->rope_dim,
+                                 p.status, stream_) != cudaSuccess)
+                return MLA_ERR_CUDA;
+            p.q = ws + w.q_prep;
+        } else if (launch_qprep(p, R, ws + w.q_prep, false, stream_) != cudaSuccess) {
+            return MLA_ERR_CUDA;
+        }
+    }
     const int ev = prof_begin(stream_);
     const cudaError_t de = impl == MLA_IMPL_TCGEN05 ? launch_decode_tc(p, w.max_work, stream_)
                                                     : launch_decode_simt(p, w.max_work, stream_);
@@ -188,9 +207,23 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     c.W_UV = W_UV;
     c.out = out;
     c.lse = lse;
-    const bool comb_tc = impl == MLA_IMPL_TCGEN05 && combine_tc_supported(p.s);
-    if ((comb_tc ? launch_combine_tc(c, stream_) : launch_combine(c, stream_)) != cudaSuccess) return MLA_ERR_CUDA;
-    prof_kernels(int2 ? 4 : 3);
+    const bool comb_tc = tc && combine_tc_supported(p.s);
+    if (int2 && comb_tc) {
+        // merge splits, rotate back on the tensor cores (o_lat = o_rot . R^T), then the
+        // W_UV up-projection reads the merged rows as one-split partials
+        float *o_rot = (float *)(ws + w.o_rot), *o_lat = (float *)(ws + w.o_lat), *lse2 = (float *)(ws + w.lse2);
+        int32_t *ident = (int32_t *)(ws + w.ident);
+        if (launch_rot_output(c, R, o_rot, o_lat, lse2, ident, p.status, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+        c.split_start = ident;
+        c.part_o = o_lat;
+        c.part_lse = lse2;
+        c.R = nullptr;
+        if (launch_combine_tc(c, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+        prof_kernels(6);
+    } else {
+        if ((comb_tc ? launch_combine_tc(c, stream_) : launch_combine(c, stream_)) != cudaSuccess) return MLA_ERR_CUDA;
+        prof_kernels(int2 ? 4 : 3);
+    }
     return MLA_OK;
 }
 

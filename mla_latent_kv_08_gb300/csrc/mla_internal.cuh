@@ -39,6 +39,10 @@ struct WsLayout {
     size_t part_o;        // fp32 [max_work][q_len * H][r]  normalised partial outputs
     size_t part_lse;      // fp32 [max_work][q_len * H]     partial log2-sum-exp
     size_t q_prep;        // fp32 [B * q_len * H][r + d_R]  rotated query (INT2 kind)
+    size_t o_rot;         // fp32 [B * q_len * H][r]  merged rotated output (INT2, tensor cores)
+    size_t o_lat;         // fp32 [B * q_len * H][r]  o_rot . R^T
+    size_t lse2;          // fp32 [B * q_len * H]     merged log2-sum-exp
+    size_t ident;         // int32 [B + 1]           one slot per sequence
     size_t total;
     int32_t max_work;     // upper bound of schedule length (streams + B)
     int32_t target;       // number of work streams
@@ -103,7 +107,7 @@ struct AppendParams {
 
 // ---- launchers (defined in mla_simt.cu) ------------------------------------
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st);
-cudaError_t launch_qprep(const DecodeParams &p, const float *R, float *q_prep, cudaStream_t st);
+cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bool out_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
@@ -113,6 +117,12 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
 // ---- tensor-core combine + W_UV (defined in mla_combine_tc.cu) --------------
 bool combine_tc_supported(const ShapeArgs &s);
 cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st);
+// ---- tensor-core rotations of the rotated-INT2 cache (defined in mla_rot_tc.cu)
+bool rot_tc_supported(const ShapeArgs &s);
+cudaError_t launch_rot_query(const float *R, const void *q_bf16, void *q_rot_f16, int rows, int D, int32_t *status,
+                             cudaStream_t st);
+cudaError_t launch_rot_output(const CombineParams &c, const float *R, float *o_rot, float *o_lat, float *lse2,
+                              int32_t *ident, int32_t *status, cudaStream_t st);
 
 // ---- small device helpers ---------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {

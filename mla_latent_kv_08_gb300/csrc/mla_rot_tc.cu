@@ -1,0 +1,309 @@
+// The two rotations of the rotated-INT2 cache on the tensor cores:
+//   q_rot[m, :] = q_lat[m, :] . R          (query prep, before attention)
+//   o_lat[m, :] = o_rot[m, :] . R^T        (after the split merge, before W_UV)
+// as one GEMM kernel Y[M x 512] = X[M x 512] . op(R), op = identity or transpose,
+// with kv_lora_rank 512. X (bf16 query rows or fp32 merged outputs) and R (fp32)
+// are converted to fp16 by the threads that stage them in shared memory; the
+// MMA accumulates in fp32 in tensor memory. A CTA computes a [128 x 256] tile of
+// Y over eight 64-wide K chunks, double-buffered.
+//
+// Also here: the merge of split partials into one latent row per (sequence,
+// draft position, head), which precedes the second rotation.
+#include "mla_internal.cuh"
+#include "mla_ptx.cuh"
+
+#include <math_constants.h>
+
+namespace mla {
+namespace rot {
+
+using namespace ptx;
+
+constexpr int kThreads = 256;
+constexpr int kK = 512;                         // kv_lora_rank
+constexpr int kTm = 128, kTn = 256, kKc = 64;   // tile M, tile N, K chunk
+constexpr uint32_t kABytes = kTm * 128;         // [128 rows x 64 k] fp16
+constexpr uint32_t kBBytes = kTn * 128;         // [256 j x 64 k] fp16 (either layout)
+constexpr uint32_t kStage = kABytes + kBBytes;  // 48 KB
+constexpr uint32_t kOffBar = 2 * kStage;
+constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+struct RotParams {
+    const void *X;
+    int ldx;              // elements per X row
+    const float *R;       // [512, 512] row-major
+    void *Y;
+    int ldy;              // elements per Y row
+    int M;
+    int copy_rope;        // > 0: copy X[:, 512 : 512 + copy_rope] (bf16) to Y as fp16
+    int32_t *status;
+};
+
+__device__ __forceinline__ uint4 pack8_f16(const float *v) {
+    const __half2 h0 = __floats2half2_rn(v[0], v[1]);
+    const __half2 h1 = __floats2half2_rn(v[2], v[3]);
+    const __half2 h2 = __floats2half2_rn(v[4], v[5]);
+    const __half2 h3 = __floats2half2_rn(v[6], v[7]);
+    return make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1, *(const uint32_t *)&h2, *(const uint32_t *)&h3);
+}
+
+// X_FP32: X is fp32 (else bf16). TRANS: op(R) = R^T (else R). Y_F16: Y is fp16 (else fp32).
+template <bool X_FP32, bool TRANS, bool Y_F16>
+__global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const RotParams rp) {
+    const int m0 = blockIdx.x * kTm, j0 = blockIdx.y * kTn;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bar = (uint64_t *)(smem + kOffBar);        // [2] MMA done per stage
+    uint32_t *tmem_slot = (uint32_t *)(bar + 2);
+    int32_t *abort_flag = (int32_t *)(bar + 3);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(256)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // fp16 A and B, fp32 D, M 128, N 256; B MN-major for op(R) = R (R's rows are k)
+    const uint32_t idesc = (1u << 4) | ((TRANS ? 0u : 1u) << 16) | ((uint32_t)(kTn >> 3) << 17) |
+                           ((uint32_t)(kTm >> 4) << 24);
+    bool ok = true;
+    for (int kc = 0; kc < kK / kKc; ++kc) {
+        const int st = kc & 1;
+        uint8_t *A = smem + st * kStage, *Bm = A + kABytes;
+        if (kc >= 2 && !__syncthreads_and(mbar_wait_bounded(&bar[st], ((kc - 2) >> 1) & 1, abort_flag,
+                                                           rp.status, FLAG_TIMEOUT, kTimeoutNs))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // A: rows m0.., k = 64 kc + 8 ch .. +7 -> fp16, K-major swizzled
+        for (int job = tid; job < kTm * 8; job += kThreads) {
+            const int r = job >> 3, ch = job & 7, m = m0 + r;
+            float v[8];
+            if (m < rp.M) {
+                const size_t base = (size_t)m * rp.ldx + kc * kKc + 8 * ch;
+                if (X_FP32) {
+                    const float4 a = *(const float4 *)((const float *)rp.X + base);
+                    const float4 b = *(const float4 *)((const float *)rp.X + base + 4);
+                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                } else {
+                    const uint4 u = *(const uint4 *)((const __nv_bfloat16 *)rp.X + base);
+                    const __nv_bfloat162 *h = (const __nv_bfloat162 *)&u;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h[e]);
+                        v[2 * e] = f.x;
+                        v[2 * e + 1] = f.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = 0.f;
+            }
+            *(uint4 *)(A + sw128(r, ch)) = pack8_f16(v);
+        }
+        // B: fp16 copy of the R elements this chunk needs
+        for (int job = tid; job < kTn * 8; job += kThreads) {
+            float v[8];
+            if (TRANS) {
+                // B[j][k] = R[j][k]: K-major, row j, chunk ch
+                const int j = job >> 3, ch = job & 7;
+                const float *src = rp.R + (size_t)(j0 + j) * kK + kc * kKc + 8 * ch;
+                const float4 a = *(const float4 *)src, b = *(const float4 *)(src + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                *(uint4 *)(Bm + sw128(j, ch)) = pack8_f16(v);
+            } else {
+                // B[j][k] = R[k][j]: MN-major, 64-j atoms of [64 k rows x 128 B]
+                const int k = job & 63, rest = job >> 6, atom = rest >> 3, ch = rest & 7;
+                const float *src = rp.R + (size_t)(kc * kKc + k) * kK + j0 + 64 * atom + 8 * ch;
+                const float4 a = *(const float4 *)src, b = *(const float4 *)(src + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                *(uint4 *)(Bm + atom * (kKc * 128) + sw128(k, ch)) = pack8_f16(v);
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t a0 = sdesc(smem_u32(A), 16, 1024);
+            const uint64_t b0 = TRANS ? sdesc(smem_u32(Bm), 16, 1024) : sdesc(smem_u32(Bm), kKc * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kKc / 16; ++kk) {
+                const uint64_t bd = b0 + (uint64_t)((TRANS ? 32 * kk : 2048 * kk) >> 4);
+                mma_ss(tmem, a0 + (uint64_t)((32 * kk) >> 4), bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bar[st]);
+        }
+    }
+    // the last two chunks' MMAs (stages 0 and 1 of the final round)
+    if (ok) {
+        const int last = kK / kKc - 1;
+        ok = mbar_wait_bounded(&bar[last & 1], (last >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs) &&
+             mbar_wait_bounded(&bar[(last - 1) & 1], ((last - 1) >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
+                               kTimeoutNs);
+    }
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+    if (warp < 4) {
+        const int m = m0 + 32 * warp + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+        for (int c = 0; c < kTn / 32; ++c) {
+            uint32_t v[32];
+            if (ok) {
+                TMEM_LD32(taddr + 32 * c, v);
+                tmem_wait_ld();
+            }
+            if (m >= rp.M) continue;
+            const int j = j0 + 32 * c;
+            if (Y_F16) {
+                __half *dst = (__half *)rp.Y + (size_t)m * rp.ldy + j;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = ok ? __uint_as_float(v[8 * q + e]) : CUDART_NAN_F;
+                    *(uint4 *)(dst + 8 * q) = pack8_f16(f);
+                }
+            } else {
+                float *dst = (float *)rp.Y + (size_t)m * rp.ldy + j;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float4 f;
+                    f.x = ok ? __uint_as_float(v[4 * q + 0]) : CUDART_NAN_F;
+                    f.y = ok ? __uint_as_float(v[4 * q + 1]) : CUDART_NAN_F;
+                    f.z = ok ? __uint_as_float(v[4 * q + 2]) : CUDART_NAN_F;
+                    f.w = ok ? __uint_as_float(v[4 * q + 3]) : CUDART_NAN_F;
+                    *(float4 *)(dst + 4 * q) = f;
+                }
+            }
+        }
+    }
+    // the query's rope part passes through unrotated (bf16 -> fp16)
+    if (rp.copy_rope > 0 && blockIdx.y == 0) {
+        for (int job = tid; job < kTm * rp.copy_rope; job += kThreads) {
+            const int r = job / rp.copy_rope, d = job % rp.copy_rope, m = m0 + r;
+            if (m < rp.M) {
+                const float f = __bfloat162float(((const __nv_bfloat16 *)rp.X)[(size_t)m * rp.ldx + kK + d]);
+                ((__half *)rp.Y)[(size_t)m * rp.ldy + kK + d] = __float2half_rn(f);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+    }
+}
+
+template <bool X_FP32, bool TRANS, bool Y_F16>
+static cudaError_t launch_t(const RotParams &rp, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(rot_gemm_kernel<X_FP32, TRANS, Y_F16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((rp.M + kTm - 1) / kTm, kK / kTn);
+    rot_gemm_kernel<X_FP32, TRANS, Y_F16><<<grid, kThreads, kSmemBytes, st>>>(rp);
+    return cudaGetLastError();
+}
+
+// Merge the split partials of each (b, i, h) row into o_rot[(b * q_len + i) * H + h]
+// and its log2-sum-exp; write an identity schedule (sequence b -> slot b) so
+// that the up-projection reads the merged rows as one-split partials.
+__global__ void __launch_bounds__(256) merge_rows_kernel(CombineParams c, float *o_rot, float *lse2, int32_t *ident) {
+    const int H = c.s.H, rows_seq = c.q_len * H;
+    const int total = c.B * rows_seq;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b <= c.B; b += blockDim.x) ident[b] = b;
+    for (int rowg = blockIdx.x * 8 + warp; rowg < total; rowg += gridDim.x * 8) {
+        const int b = rowg / rows_seq, row = rowg % rows_seq;
+        const int s0 = c.split_start[b], s1 = c.split_start[b + 1];
+        bool nan = s1 <= s0;
+        float M = -CUDART_INF_F;
+        for (int s = s0; s < s1; ++s) {
+            const float v = c.part_lse[(size_t)s * rows_seq + row];
+            nan |= isnan(v);
+            M = fmaxf(M, v);
+        }
+        float acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+        float tot = 0.f;
+        for (int s = s0; s < s1; ++s) {
+            const float v = c.part_lse[(size_t)s * rows_seq + row];
+            const float w = v == -CUDART_INF_F ? 0.f : exp2f(v - M);
+            tot += w;
+            const float4 *po = (const float4 *)(c.part_o + ((size_t)s * rows_seq + row) * kK);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = po[lane + 32 * q];
+                acc[4 * q + 0] = fmaf(w, f.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(w, f.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w, f.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w, f.w, acc[4 * q + 3]);
+            }
+        }
+        const float inv = tot > 0.f ? 1.f / tot : 0.f;
+        float4 *dst = (float4 *)(o_rot + (size_t)rowg * kK);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float4 f;
+            f.x = nan ? CUDART_NAN_F : acc[4 * q + 0] * inv;
+            f.y = nan ? CUDART_NAN_F : acc[4 * q + 1] * inv;
+            f.z = nan ? CUDART_NAN_F : acc[4 * q + 2] * inv;
+            f.w = nan ? CUDART_NAN_F : acc[4 * q + 3] * inv;
+            dst[lane + 32 * q] = f;
+        }
+        if (lane == 0) lse2[rowg] = nan ? CUDART_NAN_F : M + log2f(tot);
+    }
+}
+
+}  // namespace rot
+
+bool rot_tc_supported(const ShapeArgs &s) { return s.r == rot::kK; }
+
+cudaError_t launch_rot_query(const float *R, const void *q_bf16, void *q_rot_f16, int rows, int D, int32_t *status,
+                             cudaStream_t st) {
+    rot::RotParams rp;
+    rp.X = q_bf16;
+    rp.ldx = D;
+    rp.R = R;
+    rp.Y = q_rot_f16;
+    rp.ldy = D;
+    rp.M = rows;
+    rp.copy_rope = D - rot::kK;
+    rp.status = status;
+    return rot::launch_t<false, false, true>(rp, st);
+}
+
+cudaError_t launch_rot_output(const CombineParams &c, const float *R, float *o_rot, float *o_lat, float *lse2,
+                              int32_t *ident, int32_t *status, cudaStream_t st) {
+    const int rows = c.B * c.q_len * c.s.H;
+    rot::merge_rows_kernel<<<min((rows + 7) / 8, 4096), 256, 0, st>>>(c, o_rot, lse2, ident);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    rot::RotParams rp;
+    rp.X = o_rot;
+    rp.ldx = rot::kK;
+    rp.R = R;
+    rp.Y = o_lat;
+    rp.ldy = rot::kK;
+    rp.M = rows;
+    rp.copy_rope = 0;
+    rp.status = status;
+    return rot::launch_t<true, true, false>(rp, st);
+}
+
+}  // namespace mla

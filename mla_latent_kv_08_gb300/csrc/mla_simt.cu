@@ -125,8 +125,9 @@ cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st
 // Query rotation for the rotated-INT2 cache: q_prep[row] = [q_lat . R ; q_R],
 // fp32 accumulation. 32 query rows per CTA, each thread owns NC output dims.
 // ============================================================================
-template <int NC>
-__global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float *R, float *q_prep, int rows) {
+// OUT: 0 fp32 (CUDA-core decode), 1 fp16 (tensor-core decode of the INT2 cache).
+template <int NC, int OUT>
+__global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float *R, void *q_prep, int rows) {
     extern __shared__ float sq[];                 // [32][r]
     const int r = p.s.r, D = p.s.D();
     const int row0 = blockIdx.x * 32;
@@ -162,28 +163,39 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float 
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             int j = threadIdx.x + 256 * c;
-            if (j < r) q_prep[(size_t)row * D + j] = acc[rr][c];
+            if (j < r) {
+                if (OUT == 1) ((__half *)q_prep)[(size_t)row * D + j] = __float2half_rn(acc[rr][c]);
+                else ((float *)q_prep)[(size_t)row * D + j] = acc[rr][c];
+            }
         }
-        for (int j = threadIdx.x; j < p.s.dR; j += blockDim.x)
-            q_prep[(size_t)row * D + r + j] = __bfloat162float(q[(size_t)row * D + r + j]);
+        for (int j = threadIdx.x; j < p.s.dR; j += blockDim.x) {
+            const float v = __bfloat162float(q[(size_t)row * D + r + j]);
+            if (OUT == 1) ((__half *)q_prep)[(size_t)row * D + r + j] = __float2half_rn(v);
+            else ((float *)q_prep)[(size_t)row * D + r + j] = v;
+        }
     }
 }
 
-cudaError_t launch_qprep(const DecodeParams &p, const float *R, float *q_prep, cudaStream_t st) {
+template <int OUT>
+static cudaError_t launch_qprep_t(const DecodeParams &p, const float *R, void *q_prep, cudaStream_t st) {
     const int rows = p.B * p.q_len * p.s.H;
     const size_t smem = (size_t)32 * p.s.r * sizeof(float);
     dim3 grid((rows + 31) / 32);
     if (p.s.r <= 256) {
-        cudaFuncSetAttribute(qprep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        qprep_kernel<1><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+        cudaFuncSetAttribute(qprep_kernel<1, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<1, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
     } else if (p.s.r <= 512) {
-        cudaFuncSetAttribute(qprep_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        qprep_kernel<2><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+        cudaFuncSetAttribute(qprep_kernel<2, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<2, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
     } else {
-        cudaFuncSetAttribute(qprep_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        qprep_kernel<4><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+        cudaFuncSetAttribute(qprep_kernel<4, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<4, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bool out_f16, cudaStream_t st) {
+    return out_f16 ? launch_qprep_t<1>(p, R, q_prep, st) : launch_qprep_t<0>(p, R, q_prep, st);
 }
 
 // ============================================================================

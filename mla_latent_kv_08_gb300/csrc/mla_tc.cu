@@ -52,15 +52,23 @@ constexpr int kSoftmaxThreads = 256;  // warps 4..11: two warps per 32-row lane 
 constexpr uint32_t kKvBlockBytes = kTile * 128;                     // 8 KB
 constexpr uint32_t kStageBytes = kKvBlocks * kKvBlockBytes;         // 72 KB
 constexpr uint32_t kQBlockBytes = kRows * 128;                      // 16 KB
-constexpr uint32_t kPBytes = kRows * 128;                           // 16 KB
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
-constexpr uint32_t kOffP = kOffQ + kQSmemBlocks * kQBlockBytes;     // 192 KB
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;                   // 224 KB
+// INT2 raw stage: one block's codes [64 x 128 B], scale/zero [64 x 64 B] and
+// rope keys [64 x 128 B], copied verbatim and expanded into a stage by the
+// dequantising warps.
+constexpr uint32_t kRawCodes = kTile * 128, kRawSz = kTile * 64, kRawRope = kTile * 128;
+constexpr uint32_t kRawBytes = kRawCodes + kRawSz + kRawRope;       // 20 KB
+constexpr uint32_t kOffRaw = kOffQ + kQSmemBlocks * kQBlockBytes;   // 192 KB
+constexpr uint32_t kOffBar = kOffRaw + kRawBytes;                   // 212 KB
 constexpr uint32_t kOffXchg = kOffBar + 256;                        // [2][128] fp32 row values
 constexpr uint32_t kSmemBytes = kOffXchg + 1024 + 1024;             // + alignment slack
-static_assert(kQTmemBlocks * kQBlockBytes <= kStages * kStageBytes, "Q staging must fit the stages");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// P (bf16 [128 rows x 64 tokens], 16 KB) of tile T is written into two column
+// blocks of tile T's own stage that only QK reads (the other half's V dims),
+// once QK(T) is done; PV(T) is their last reader.
+__host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u; }
+constexpr int kDequantThreads = 64;   // warps 2..3 (rotated-INT2 cache)
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bounded-wait safety net
 
@@ -96,6 +104,8 @@ struct Bars {
     uint64_t mma_fin;
     uint64_t xchg_full;       // both halves of every row wrote their value
     uint64_t xchg_read;       // both halves read the other's value
+    uint64_t raw_full;        // INT2: raw block landed
+    uint64_t raw_empty;       // INT2: raw block expanded
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -130,8 +140,10 @@ __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
 
 constexpr int kPrefetchAhead = 4;   // tiles prefetched into L2 ahead of the TMA loads
 
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) {
+    constexpr bool kInt2 = KIND == MLA_KV_INT2_ROT;
     const DecodeParams &p = tp.p;
     const int half = blockIdx.x;            // 0/1: which 256 latent output dims
     const int g = blockIdx.y;               // query row tile
@@ -151,9 +163,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->full[s], kInt2 ? kDequantThreads : 1);
             mbar_init(&bars->empty[s], 1);
         }
+        mbar_init(&bars->raw_full, 1);
+        mbar_init(&bars->raw_empty, kDequantThreads);
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->s_free, kSoftmaxThreads);
         for (int i = 0; i < 2; ++i) {
@@ -181,9 +195,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
-        // ================================================= TMA producer (+ L2 prefetch)
-        // The warp runs converged: lane 0 waits and arms the barrier, lanes 0..8
-        // each issue one of the tile's nine boxes.
+        // ================================================= producer (+ L2 prefetch)
+        // bf16 cache: the warp runs converged; lane 0 waits and arms the stage
+        // barrier, lanes 0..8 each issue one of the tile's nine TMA boxes.
+        // INT2 cache: lanes 0..2 copy the block's codes, scale/zero pairs and rope
+        // keys into the raw stage for the dequantising warps.
         const bool prefetcher = half == 0 && g == 0;
         int pi = i0, pt = 0, ahead = 0;        // L2 prefetch cursor, kPrefetchAhead tiles ahead
         auto advance_prefetch = [&]() {
@@ -192,8 +208,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
                 if (pt >= nt) { ++pi; pt = 0; continue; }
                 const int blk = block_of(p, it.b, it.t0 / kTile + pt);
-                if (blk >= 0)
-                    prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * kD, kStageBytes);
+                if (blk >= 0) {
+                    if (kInt2) {
+                        prefetch_l2(p.codes + (size_t)blk * kRawCodes, kRawCodes);
+                        prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * kRawSz, kRawSz);
+                        prefetch_l2((const uint8_t *)p.rope + (size_t)blk * kRawRope, kRawRope);
+                    } else {
+                        prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * kD, kStageBytes);
+                    }
+                }
                 ++pt;
                 ++ahead;
             }
@@ -208,22 +231,39 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 if (prefetcher && lane == 0) advance_prefetch();
                 int blk = next_blk;
                 if (t + 1 < nt) next_blk = block_of(p, it.b, it.t0 / kTile + t + 1);
-                const int s = T % kStages;
-                if (T >= kStages &&
-                    !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) MLA_TRACE_POINT(6, T);
                 if (blk < 0) {            // the softmax marks the item's rows NaN
                     if (lane == 0) raise_flag(p.status, FLAG_BAD_BLOCK);
                     blk = 0;
                 }
-                uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                if (lane == 0) mbar_expect_tx(&bars->full[s], kStageBytes);
-                __syncwarp();
-                if (lane < kKvBlocks)
-                    tma_load_2d(stage + lane * kKvBlockBytes, &kv_map, lane * 64, blk * kTile, &bars->full[s]);
+                if (kInt2) {
+                    if (T >= 1 && !__all_sync(0xffffffffu, mbar_wait(&bars->raw_empty, (T - 1) & 1, bars, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *raw = smem + kOffRaw;
+                    if (lane == 0) mbar_expect_tx(&bars->raw_full, kRawBytes);
+                    __syncwarp();
+                    if (lane == 0) bulk_load(raw, p.codes + (size_t)blk * kRawCodes, kRawCodes, &bars->raw_full);
+                    if (lane == 1)
+                        bulk_load(raw + kRawCodes, (const uint8_t *)p.scale_zero + (size_t)blk * kRawSz, kRawSz,
+                                  &bars->raw_full);
+                    if (lane == 2)
+                        bulk_load(raw + kRawCodes + kRawSz, (const uint8_t *)p.rope + (size_t)blk * kRawRope, kRawRope,
+                                  &bars->raw_full);
+                } else {
+                    const int s = T % kStages;
+                    if (T >= kStages &&
+                        !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) MLA_TRACE_POINT(6, T);
+                    uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                    if (lane == 0) mbar_expect_tx(&bars->full[s], kStageBytes);
+                    __syncwarp();
+                    if (lane < kKvBlocks)
+                        tma_load_2d(stage + lane * kKvBlockBytes, &kv_map, lane * 64, blk * kTile, &bars->full[s]);
+                }
                 if (lane == 0) {
                     MLA_TRACE_POINT(0, T);
                     if (prefetcher && ahead > 0) --ahead;
@@ -231,9 +271,90 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             }
         }
         // drain: never leave a copy in flight into this CTA's shared memory
-        for (int u = T - kStages; u < T; ++u)
-            if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
+        if (kInt2) {
+            if (T >= 1) mbar_wait(&bars->raw_full, (T - 1) & 1, bars, p.status);
+        } else {
+            for (int u = T - kStages; u < T; ++u)
+                if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
+        }
         __syncwarp();
+    } else if (kInt2 && (warp == 2 || warp == 3)) {
+        // ================================================= INT2 expansion into the stage
+        // value = fmaf(code, scale, zero) in fp32, rounded to fp16 (the MMA operand
+        // type of this cache kind), written in the 128B-swizzled layout the MMAs
+        // read; the bf16 rope key is converted to fp16; slots past the sequence end
+        // are zeroed.
+        const int dt = tid - 64;
+        int T = 0;
+        bool ok = true;
+        for (int i = i0; i < i1 && ok; ++i) {
+            const WorkItem it = p.work[i];
+            const int L = p.seq_lens[it.b];
+            const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+            for (int t = 0; t < nt; ++t, ++T) {
+                const int s = T % kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->raw_full, T & 1, bars, p.status))) { ok = false; break; }
+                if (T >= kStages &&
+                    !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
+                    ok = false;
+                    break;
+                }
+                const int valid = min(kTile, L - (it.t0 + t * kTile));
+                const uint8_t *raw = smem + kOffRaw;
+                const uint8_t *codes = raw;
+                const __half *sz = (const __half *)(raw + kRawCodes);
+                const uint4 *rope = (const uint4 *)(raw + kRawCodes + kRawSz);
+                uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                // latent: a lane expands one 32-dim group of one row (8 code bytes, one
+                // scale/zero pair) into four 16-byte chunks; a warp covers two rows per
+                // pass, so its code reads are 256 contiguous bytes.
+                const int half_lane = lane >> 4, grp = lane & 15;
+                for (int rr = 2 * (warp - 2) + half_lane; rr < kTile; rr += 4) {
+                    uint4 outc[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                     make_uint4(0, 0, 0, 0)};
+                    if (rr < valid) {
+                        const uint2 cb = *(const uint2 *)(codes + rr * 128 + 8 * grp);
+                        const __half2 szp = *(const __half2 *)(sz + (rr * 16 + grp) * 2);
+                        const float sc = __low2float(szp), zr = __high2float(szp);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const unsigned two = ((q4 < 2 ? cb.x : cb.y) >> (16 * (q4 & 1))) & 0xffffu;
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = __fmaf_rn((float)((two >> (2 * e)) & 3u), sc, zr);
+                            const __half2 h0 = __floats2half2_rn(v[0], v[1]);
+                            const __half2 h1 = __floats2half2_rn(v[2], v[3]);
+                            const __half2 h2 = __floats2half2_rn(v[4], v[5]);
+                            const __half2 h3 = __floats2half2_rn(v[6], v[7]);
+                            outc[q4] = make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1,
+                                                  *(const uint32_t *)&h2, *(const uint32_t *)&h3);
+                        }
+                    }
+                    // group grp = latent chunks 4*grp .. 4*grp+3 = column block grp/2, chunks 4*(grp%2)..
+                    uint8_t *blk = stage + (grp >> 1) * kKvBlockBytes;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * (grp & 1) + q4)) = outc[q4];
+                }
+                // rope key: bf16 -> fp16 (exact for values inside fp16's range), 8 chunks a row
+                for (int job = dt; job < kTile * 8; job += kDequantThreads) {
+                    const int rr = job >> 3, ch = job & 7;
+                    uint4 out = make_uint4(0, 0, 0, 0);
+                    if (rr < valid) {
+                        const uint4 u = rope[rr * 8 + ch];
+                        const __nv_bfloat162 *bh = (const __nv_bfloat162 *)&u;
+                        __half2 hh[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) hh[e] = __float22half2_rn(__bfloat1622float2(bh[e]));
+                        out = make_uint4(*(const uint32_t *)&hh[0], *(const uint32_t *)&hh[1], *(const uint32_t *)&hh[2],
+                                         *(const uint32_t *)&hh[3]);
+                    }
+                    *(uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch)) = out;
+                }
+                fence_proxy_async();
+                mbar_arrive(&bars->raw_empty);
+                mbar_arrive(&bars->full[s]);
+            }
+        }
     } else if (warp == 1) {
         // ================================================= MMA issuer (lane 0 issues; the warp
         // stays converged so that it can zero stale tail slots together)
@@ -246,10 +367,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             if (lane == 0) {
                 tc_fence_after();
                 const int s = Tp % kStages;
-                const uint64_t a0 = sdesc(smem_u32(smem + kOffP + pb * kPBytes), 16, 1024);
+                const uint64_t a0 =
+                    sdesc(smem_u32(smem + kOffStage + s * kStageBytes + p_block(half) * kKvBlockBytes), 16, 1024);
                 const uint64_t b0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes,
                                           tp.v_lbo, tp.v_sbo);
-                constexpr uint32_t kIdPv = idesc_bf16(128, 256, true);
+                // INT2 cache: the operands are fp16 (the dequantised latent, P); bf16 otherwise
+                constexpr uint32_t kIdPv = kInt2 ? idesc_f16(128, 256, true) : idesc_bf16(128, 256, true);
                 // descriptor start addresses advance in 16-byte units
                 if (first_of_item) mma_ss_k<kIdPv, 0>(d_o, a0, b0);
                 else mma_ss_k<kIdPv, 1>(d_o, a0, b0);
@@ -278,7 +401,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 // that P = 0 never meets stale (possibly non-finite) cache bytes
                 const int tile_start = it.t0 + t * kTile;
                 const int valid = min(kTile, L - tile_start);
-                if (valid < kTile) {
+                if (!kInt2 && valid < kTile) {
                     uint8_t *stage = smem + kOffStage + s * kStageBytes;
                     const int jobs = (kTile - valid) * kKvBlocks * 8;
                     for (int jb = lane; jb < jobs; jb += 32) {
@@ -297,7 +420,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 const uint64_t kd = sdesc(smem_u32(smem + kOffStage + s * kStageBytes), 16, 1024);
                 const uint64_t qd = sdesc(smem_u32(smem + kOffQ), 16, 1024);
                 const uint32_t qt = tmem + kColQ;
-                constexpr uint32_t kIdQk = idesc_bf16(128, 64, false);
+                constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
 #pragma unroll
                 for (int grp = 0; grp < 6; ++grp) {
                     if (lane == 0) {
@@ -451,18 +574,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 for (int j = 0; j < 16; ++j) {
                     const float a = ex2(__uint_as_float(sv[2 * j]) - mb);
                     const float c = ex2(__uint_as_float(sv[2 * j + 1]) - mb);
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
-                    sum0 += a;             // fp32 row sum: the LSE does not see the bf16 rounding of P
+                    if (kInt2) {
+                        const __half2 h = __floats2half2_rn(a, c);
+                        pk[j] = *(const uint32_t *)&h;
+                    } else {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
+                        pk[j] = *(const uint32_t *)&h;
+                    }
+                    sum0 += a;             // fp32 row sum: the LSE does not see the rounding of P
                     sum1 += c;
-                    pk[j] = *(const uint32_t *)&h;
                 }
                 if (row == 0 && hs == 0) MLA_TRACE_POINT(8, T);
                 l = l * alpha + (sum0 + sum1);
                 const int pb = T & 1;
-                if (T >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[pb], ((T - 2) >> 1) & 1, bars, p.status))) {
-                    ok = false;
-                    break;
-                }
                 if (row == 0 && hs == 0) MLA_TRACE_POINT(9, T);
                 // Rows decide to rescale on their own; the warp corrects its O columns
                 // together (alpha = 1 for rows that keep their max).
@@ -485,7 +609,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     }
                     tmem_wait_st();
                 }
-                uint8_t *pbuf = smem + kOffP + pb * kPBytes;
+                uint8_t *pbuf = smem + kOffStage + (T % kStages) * kStageBytes + p_block(half) * kKvBlockBytes;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch)
                     *(uint4 *)(pbuf + sw128(row, 4 * hs + ch)) =
@@ -582,10 +706,12 @@ static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t
 }  // namespace tc
 
 bool tc_shape_supported(const ShapeArgs &s) {
-    return s.kind == MLA_KV_BF16 && s.r == 512 && s.dR == 64 && s.bs == tc::kTile;
+    if (s.r != 512 || s.dR != 64 || s.bs != tc::kTile) return false;
+    return s.kind == MLA_KV_BF16 || (s.kind == MLA_KV_INT2_ROT && s.gs == 32);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
+    (void)max_work;
     tc::TcParams tp;
     tp.p = p;
     tp.row_tiles = (p.q_len * p.s.H + tc::kRows - 1) / tc::kRows;
@@ -594,13 +720,14 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     tp.v_sbo = 1024;
     CUtensorMap kv_map;
     memset(&kv_map, 0, sizeof kv_map);
-    if (!tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc::kSmemBytes);
+    const bool int2 = p.s.kind == MLA_KV_INT2_ROT;
+    if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile))
+        return cudaErrorInvalidValue;
+    auto kern = int2 ? tc::decode_tc_kernel<MLA_KV_INT2_ROT> : tc::decode_tc_kernel<MLA_KV_BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    (void)max_work;
     dim3 grid(2, tp.row_tiles, p.streams);
-    tc::decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, tp);
+    kern<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, tp);
     return cudaGetLastError();
 }
 

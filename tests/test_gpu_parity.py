@@ -147,11 +147,14 @@ def _int2_reference_pool(w, R32, T32, seqs, with_new=True):
     return out
 
 
-def test_int2_append_and_decode_small(gpu_lib):
+@pytest.mark.parametrize("impl_name,H", [("simt", 32), ("tcgen05", 32), ("tcgen05", 128)])
+def test_int2_append_and_decode_small(gpu_lib, impl_name, H):
     import mla_latent_kv_08_gb300 as mla
     import torch
-    w, R32, T32 = _int2_setup(B=4, H=32, len_range=(40, 300))
-    shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT)
+    w, R32, T32 = _int2_setup(B=4, H=H, len_range=(40, 300))
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT, impl=impl)
+    assert mla.mla_resolve_impl(shape) == impl
     cache = mla.Cache.allocate(shape)
     st0 = gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32), R32, T32)
     st1 = gu.append_tokens(cache, w, w.new_latent, w.new_rope, w.start_pos, R32, T32)
