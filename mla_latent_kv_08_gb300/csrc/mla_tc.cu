@@ -91,7 +91,8 @@ __device__ unsigned long long g_cta_time[4096][3];   // start, end (globaltimer 
 #endif
 // events: 0 TMA issued, 1 stage landed (MMA), 2 QK issued, 3 S seen (softmax),
 //         4 P ready (softmax), 5 PV issued, 6 PV stage released (producer saw empty),
-//         7 S in registers, 8 exponentials done, 9 previous P buffer free (softmax)
+//         7 S in registers, 8 exponentials done, 9 P about to be stored (softmax),
+//         10..15 QK issue group 0..5 issued (MMA)
 
 struct Bars {
     uint64_t full[kStages];
@@ -441,6 +442,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                         }
                     }
                     __syncwarp();
+                    if (lane == 0) MLA_TRACE_POINT(10 + grp, T);
                     if (pv_pending && grp < 5) {
                         const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_try(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
                         if (ready) {
