@@ -43,10 +43,20 @@ constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
 constexpr int kKvBlocks = 9;          // 64-dim column blocks per token row
-constexpr int kQTmemBlocks = 6;       // Q column blocks held in TMEM (dims 0..383)
-constexpr int kQSmemBlocks = 3;       // Q column blocks read from smem (dims 384..575)
 constexpr int kStages = 2;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
+constexpr uint32_t kColO = 0, kColS = 256;
+// Tensor-memory layout per cache kind. bf16: two S buffers (QK of the next tile
+// does not wait for the softmax of this one), Q dims 0..255 in TMEM, 256..575 in
+// smem. INT2 (whose raw stage needs shared memory): one S buffer, Q dims 0..383
+// in TMEM, 384..575 in smem.
+template <int KIND> struct Layout;
+template <> struct Layout<MLA_KV_BF16> {
+    static constexpr int kSBufs = 2, kQTmemBlocks = 4, kQSmemBlocks = 5;
+};
+template <> struct Layout<MLA_KV_INT2_ROT> {
+    static constexpr int kSBufs = 1, kQTmemBlocks = 6, kQSmemBlocks = 3;
+};
+constexpr int kMaxQSmemBlocks = 5;
 constexpr int kSoftmaxThreads = 256;  // warps 4..11: two warps per 32-row lane quarter
 
 constexpr uint32_t kKvBlockBytes = kTile * 128;                     // 8 KB
@@ -59,8 +69,9 @@ constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
 // dequantising warps.
 constexpr uint32_t kRawCodes = kTile * 128, kRawSz = kTile * 64, kRawRope = kTile * 128;
 constexpr uint32_t kRawBytes = kRawCodes + kRawSz + kRawRope;       // 20 KB
-constexpr uint32_t kOffRaw = kOffQ + kQSmemBlocks * kQBlockBytes;   // 192 KB
-constexpr uint32_t kOffBar = kOffRaw + kRawBytes;                   // 212 KB
+constexpr uint32_t kOffRaw = kOffQ + 3 * kQBlockBytes;              // 192 KB (INT2: after 3 Q blocks)
+constexpr uint32_t kOffBar = kOffQ + kMaxQSmemBlocks * kQBlockBytes; // 224 KB
+static_assert(kOffRaw + kRawBytes <= kOffBar, "INT2 raw stage must fit beside its Q blocks");
 constexpr uint32_t kOffXchg = kOffBar + 256;                        // [2][128] fp32 row values
 constexpr uint32_t kSmemBytes = kOffXchg + 1024 + 1024;             // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -95,10 +106,10 @@ __device__ unsigned long long g_cta_time[4096][3];   // start, end (globaltimer 
 //         10..15 QK issue group 0..5 issued (MMA)
 
 struct Bars {
-    uint64_t full[kStages];
+    uint64_t full[kStages];       // bf16: tile landed; INT2: stage expanded
     uint64_t empty[kStages];
-    uint64_t s_full;
-    uint64_t s_free;
+    uint64_t s_full[2];
+    uint64_t s_free[2];
     uint64_t p_full[2];
     uint64_t pv_done[2];
     uint64_t q_full;
@@ -139,12 +150,22 @@ __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
     return (blk >= 0 && blk < p.s.num_blocks) ? blk : -1;
 }
 
-constexpr int kPrefetchAhead = 4;   // tiles prefetched into L2 ahead of the TMA loads
+#ifndef MLA_PREFETCH_AHEAD
+#define MLA_PREFETCH_AHEAD 4
+#endif
+#ifndef MLA_PV_SLIP
+#define MLA_PV_SLIP 1
+#endif
+constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2 ahead of the TMA loads
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) {
     constexpr bool kInt2 = KIND == MLA_KV_INT2_ROT;
+    constexpr int kSBufs = Layout<KIND>::kSBufs;
+    constexpr int kQTmemBlocks = Layout<KIND>::kQTmemBlocks;
+    constexpr int kQSmemBlocks = Layout<KIND>::kQSmemBlocks;
+    constexpr uint32_t kColQ = kColS + 64 * kSBufs;
     const DecodeParams &p = tp.p;
     const int half = blockIdx.x;            // 0/1: which 256 latent output dims
     const int g = blockIdx.y;               // query row tile
@@ -169,8 +190,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
         }
         mbar_init(&bars->raw_full, 1);
         mbar_init(&bars->raw_empty, kDequantThreads);
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->s_free, kSoftmaxThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->s_free[i], kSoftmaxThreads);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->p_full[i], kSoftmaxThreads);
             mbar_init(&bars->pv_done[i], 1);
@@ -201,7 +224,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
         // barrier, lanes 0..8 each issue one of the tile's nine TMA boxes.
         // INT2 cache: lanes 0..2 copy the block's codes, scale/zero pairs and rope
         // keys into the raw stage for the dequantising warps.
-        const bool prefetcher = half == 0 && g == 0;
+        const bool prefetcher = kPrefetchAhead > 0 && half == 0 && g == 0;
         int pi = i0, pt = 0, ahead = 0;        // L2 prefetch cursor, kPrefetchAhead tiles ahead
         auto advance_prefetch = [&]() {
             while (pi < i1 && ahead < kPrefetchAhead) {
@@ -359,7 +382,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
     } else if (warp == 1) {
         // ================================================= MMA issuer (lane 0 issues; the warp
         // stays converged so that it can zero stale tail slots together)
-        const uint32_t d_s = tmem + kColS, d_o = tmem + kColO;
+        const uint32_t d_o = tmem + kColO;
         bool ok = true;
         int T = 0;
         auto issue_pv = [&](int Tp, bool first_of_item) -> bool {
@@ -395,9 +418,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, item_no & 1, bars, p.status))) { ok = false; break; }
             for (int t = 0; t < nt; ++t, ++T) {
                 const int s = T % kStages;
+                // Wait for this tile's stage; meanwhile issue the previous tile's PV as
+                // soon as its P is ready, so that its stage is released early.
+                bool pv_early = false;
+                if (t > 0) {
+                    const int pbp = (T - 1) & 1;
+                    int st = 0;                  // lane 0's view: 1 = stage landed, 2 = P ready
+                    if (lane == 0) {
+                        const unsigned long long tw0 = globaltimer();
+                        for (uint32_t it2 = 0;; ++it2) {
+                            if (mbar_try(&bars->p_full[pbp], ((T - 1) >> 1) & 1)) { st = 2; break; }
+                            if (mbar_try(&bars->full[s], (T / kStages) & 1)) { st = 1; break; }
+                            if ((it2 & 63u) == 63u && (aborted(bars) || globaltimer() - tw0 > kTimeoutNs)) break;
+                        }
+                    }
+                    st = __shfl_sync(0xffffffffu, st, 0);
+                    if (st == 2) {
+                        if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
+                        pv_early = true;
+                    }
+                }
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status))) { ok = false; break; }
                 if (lane == 0) MLA_TRACE_POINT(1, T);
-                if (T > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->s_free, (T - 1) & 1, bars, p.status))) { ok = false; break; }
+                // the S buffer this QK writes was read out by the softmax kSBufs tiles ago
+                if (T >= kSBufs &&
+                    !__all_sync(0xffffffffu, mbar_wait(&bars->s_free[T % kSBufs], ((T - kSBufs) / kSBufs) & 1, bars, p.status))) {
+                    ok = false;
+                    break;
+                }
                 // the sequence's final partial block: zero the slots past the end so
                 // that P = 0 never meets stale (possibly non-finite) cache bytes
                 const int tile_start = it.t0 + t * kTile;
@@ -415,21 +463,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 // QK(T) in six groups of six K-steps. PV(T-1) of the same item is
                 // slipped in between groups as soon as its P is ready, so that the
                 // stage it reads is released early; otherwise it follows QK(T).
-                bool pv_pending = t > 0;
+                bool pv_pending = t > 0 && !pv_early;
                 const int pb_prev = (T - 1) & 1;
                 tc_fence_after();
                 const uint64_t kd = sdesc(smem_u32(smem + kOffStage + s * kStageBytes), 16, 1024);
                 const uint64_t qd = sdesc(smem_u32(smem + kOffQ), 16, 1024);
                 const uint32_t qt = tmem + kColQ;
+                const uint32_t d_s = tmem + kColS + 64 * (T % kSBufs);
                 constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
 #pragma unroll
                 for (int grp = 0; grp < 6; ++grp) {
                     if (lane == 0) {
                         // K-step j: column block j/4, 32-byte step j%4 inside the swizzle
                         // atom; descriptor start addresses advance in 16-byte units.
+                        // Groups: K-steps [0,6) [6,12) [12,16) [16,22) [22,28) [28,36).
+                        constexpr int kGrpStart[7] = {0, 6, 12, 16, 22, 28, 36};
 #pragma unroll
-                        for (int jj = 0; jj < 6; ++jj) {
-                            const int j = grp * 6 + jj;
+                        for (int j = kGrpStart[grp]; j < kGrpStart[grp + 1]; ++j) {
                             const uint64_t bd = kd + (uint64_t)(((j >> 2) * kKvBlockBytes + 32 * (j & 3)) >> 4);
                             if (j == 0) {
                                 mma_ts_k<kIdQk, 0>(d_s, qt, bd);
@@ -443,7 +493,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                     }
                     __syncwarp();
                     if (lane == 0) MLA_TRACE_POINT(10 + grp, T);
-                    if (pv_pending && grp < 5) {
+                    if (MLA_PV_SLIP && pv_pending && grp < 5) {
                         const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_try(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
                         if (ready) {
                             if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
@@ -453,7 +503,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 }
                 if (!ok) break;
                 if (lane == 0) {
-                    mma_commit(&bars->s_full);
+                    mma_commit(&bars->s_full[T % kSBufs]);
                     MLA_TRACE_POINT(2, T);
                 }
                 __syncwarp();
@@ -506,7 +556,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 const uint4 *src = (const uint4 *)((const __nv_bfloat16 *)p.q +
                                                    ((size_t)it.b * rows_seq + (row_valid ? row_seq : 0)) * kD);
 #pragma unroll 1
-                for (int c = 3 * hs; c < 3 * hs + 3; ++c) {
+                for (int c = hs * (kQTmemBlocks / 2); c < (hs + 1) * (kQTmemBlocks / 2); ++c) {
                     uint32_t v[32];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -533,14 +583,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             bool bad_item = false;     // a block id of this item is out of range
             for (int t = 0; t < nt && ok; ++t, ++T) {
                 bad_item |= block_of(p, it.b, t0 / kTile + t) < 0;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, T & 1, bars, p.status))) { ok = false; break; }
+                const int sb = T % kSBufs;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (T / kSBufs) & 1, bars, p.status))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 if (row == 0 && hs == 0) MLA_TRACE_POINT(3, T);
                 uint32_t sv[32];
-                TMEM_LD32(lane_addr + kColS + 32 * hs, sv);
+                TMEM_LD32(lane_addr + kColS + 64 * sb + 32 * hs, sv);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&bars->s_free);
+                mbar_arrive(&bars->s_free[sb]);
                 if (row == 0 && hs == 0) MLA_TRACE_POINT(7, T);
 
                 const int tile_start = t0 + t * kTile + 32 * hs;
@@ -743,3 +797,4 @@ extern "C" int mla_trace_cta(unsigned long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 3 * (size_t)n);
 }
 #endif
+
