@@ -80,6 +80,16 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // once QK(T) is done; PV(T) is their last reader.
 __host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u; }
 constexpr int kDequantThreads = 64;   // warps 2..3 (rotated-INT2 cache)
+constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 32 dims] fp32
+// QK K-steps in six issue groups: [0,6) [6,12) [12,16) [16,22) [22,28) [28,36)
+__host__ __device__ constexpr int grp_start(int grp) {
+    return grp == 0 ? 0 : grp == 1 ? 6 : grp == 2 ? 12 : grp == 3 ? 16 : grp == 4 ? 22 : grp == 5 ? 28 : 36;
+}
+__host__ __device__ constexpr int first_smem_group(int first_smem_step) {
+    int g = 0;
+    while (grp_start(g + 1) <= first_smem_step) ++g;
+    return g;
+}
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bounded-wait safety net
 
@@ -89,13 +99,22 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bou
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 64;
 __device__ long long g_trace[16][kTraceTiles];
-__device__ unsigned long long g_cta_time[4096][3];   // start, end (globaltimer ns), tiles
+// per CTA: start, end (globaltimer ns), items<<32 | tiles, then for items 0 and 1:
+// first S seen, epilogue begin, epilogue end
+__device__ unsigned long long g_cta_time[4096][9];
+#define MLA_TRACE_ITEM(slot, item)                                                               \
+    do {                                                                                         \
+        if ((item) < 2 && cta_id < 4096) g_cta_time[cta_id][3 + 3 * (item) + (slot)] = globaltimer(); \
+    } while (0)
 #define MLA_TRACE_POINT(ev, tile)                                                              \
     do {                                                                                       \
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (tile) < kTraceTiles)   \
             g_trace[ev][tile] = clock64();                                                     \
     } while (0)
 #else
+#define MLA_TRACE_ITEM(slot, item) \
+    do {                           \
+    } while (0)
 #define MLA_TRACE_POINT(ev, tile) \
     do {                          \
     } while (0)
@@ -112,7 +131,10 @@ struct Bars {
     uint64_t s_free[2];
     uint64_t p_full[2];
     uint64_t pv_done[2];
-    uint64_t q_full;
+    uint64_t q_stage;         // a staging round of Q landed in the Q region (TMA)
+    uint64_t q_smem;          // the shared-memory part of Q landed (TMA)
+    uint64_t q_tmem;          // the tensor-memory part of Q is stored
+    uint64_t qreg_free;       // every softmax thread is done with the Q region
     uint64_t mma_fin;
     uint64_t xchg_full;       // both halves of every row wrote their value
     uint64_t xchg_read;       // both halves read the other's value
@@ -121,6 +143,8 @@ struct Bars {
     uint32_t tmem_base;
     int32_t abort_flag;
 };
+
+static_assert(sizeof(Bars) <= 256, "barriers must fit below the exchange area");
 
 struct TcParams {
     DecodeParams p;
@@ -160,12 +184,18 @@ constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) {
+decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                 const __grid_constant__ CUtensorMap o_map, const TcParams tp) {
     constexpr bool kInt2 = KIND == MLA_KV_INT2_ROT;
     constexpr int kSBufs = Layout<KIND>::kSBufs;
     constexpr int kQTmemBlocks = Layout<KIND>::kQTmemBlocks;
     constexpr int kQSmemBlocks = Layout<KIND>::kQSmemBlocks;
     constexpr uint32_t kColQ = kColS + 64 * kSBufs;
+    constexpr int kQRounds = (kQTmemBlocks + kQSmemBlocks - 1) / kQSmemBlocks;   // staging rounds of the TMEM part
+    constexpr int kEpiBoxes = (int)((kQSmemBlocks * kQBlockBytes) / (8 * kEpiBoxBytes));   // per warp at a time
+    static_assert(kEpiBoxes >= 1 && 4 % kEpiBoxes == 0, "epilogue boxes");
+    // the first QK group that reads Q from shared memory
+    constexpr int kFirstSmemGroup = first_smem_group(4 * kQTmemBlocks);
     const DecodeParams &p = tp.p;
     const int half = blockIdx.x;            // 0/1: which 256 latent output dims
     const int g = blockIdx.y;               // query row tile
@@ -198,7 +228,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             mbar_init(&bars->p_full[i], kSoftmaxThreads);
             mbar_init(&bars->pv_done[i], 1);
         }
-        mbar_init(&bars->q_full, kSoftmaxThreads);   // Q of the current item is in TMEM + smem
+        mbar_init(&bars->q_stage, 1);
+        mbar_init(&bars->q_smem, 1);
+        mbar_init(&bars->q_tmem, kSoftmaxThreads);
+        mbar_init(&bars->qreg_free, kSoftmaxThreads);
         mbar_init(&bars->mma_fin, 1);
         mbar_init(&bars->xchg_full, kSoftmaxThreads);
         mbar_init(&bars->xchg_read, kSoftmaxThreads);
@@ -415,7 +448,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             const WorkItem it = p.work[i];
             const int L = p.seq_lens[it.b];
             const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, item_no & 1, bars, p.status))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_tmem, item_no & 1, bars, p.status))) { ok = false; break; }
             for (int t = 0; t < nt; ++t, ++T) {
                 const int s = T % kStages;
                 // Wait for this tile's stage; meanwhile issue the previous tile's PV as
@@ -473,13 +506,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
 #pragma unroll
                 for (int grp = 0; grp < 6; ++grp) {
+                    // the item's first tile: its shared-memory Q part may still be landing
+                    if (grp == kFirstSmemGroup && t == 0 &&
+                        !__all_sync(0xffffffffu, mbar_wait(&bars->q_smem, item_no & 1, bars, p.status))) {
+                        ok = false;
+                        break;
+                    }
                     if (lane == 0) {
                         // K-step j: column block j/4, 32-byte step j%4 inside the swizzle
                         // atom; descriptor start addresses advance in 16-byte units.
                         // Groups: K-steps [0,6) [6,12) [12,16) [16,22) [22,28) [28,36).
-                        constexpr int kGrpStart[7] = {0, 6, 12, 16, 22, 28, 36};
 #pragma unroll
-                        for (int j = kGrpStart[grp]; j < kGrpStart[grp + 1]; ++j) {
+                        for (int j = grp_start(grp); j < grp_start(grp + 1); ++j) {
                             const uint64_t bd = kd + (uint64_t)(((j >> 2) * kKvBlockBytes + 32 * (j & 3)) >> 4);
                             if (j == 0) {
                                 mma_ts_k<kIdQk, 0>(d_s, qt, bd);
@@ -523,16 +561,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
         // 128*hs..+127. The two halves of a row agree on the running max through
         // shared memory once per tile. Every branch around tcgen05.ld / tcgen05.st
         // is warp-uniform: those instructions are warp-collective (.sync.aligned).
+        //
+        // The Q region of shared memory serves three uses in turn: staging the
+        // tensor-memory part of an item's Q (TMA in, tcgen05.st out), the
+        // epilogue's output boxes (written here, TMA-stored out) and the
+        // shared-memory part of Q that the QK MMAs read. qreg_free completes once
+        // every softmax thread is done with a staging or epilogue use; the TMA
+        // issuer (warp 4 lane 0) waits for it before loading into the region.
         const int wq = warp & 3;
         const int hs = (warp - 4) >> 2;
         const int row = 32 * wq + lane;
         const int row_seq = g * kRows + row;
         const bool row_valid = row_seq < rows_seq;
+        const bool issuer = warp == 4 && lane == 0;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
         float *xchg = (float *)(smem + kOffXchg);       // [2][128]
         bool ok = true;
         int T = 0;
         int nx = 0;                                     // exchanges done
+        int uses = 0;                                   // qreg_free phases this thread arrived on
+        int nstage = 0;                                 // q_stage phases consumed
         // Swap one value per row with the other half of the row (bounded waits).
         auto exchange = [&](float v, float &other) -> bool {
             if (nx > 0 && !mbar_wait(&bars->xchg_read, (nx - 1) & 1, bars, p.status)) return false;
@@ -544,41 +592,75 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             ++nx;
             return true;
         };
+        // TMA of Q part `round` of work item `item` into the Q region (issuer
+        // only). Rounds 0..kQRounds-1 stage the tensor-memory part, kQRounds
+        // loads the shared-memory part that the MMAs read.
+        auto issue_q = [&](int item, int round) -> bool {
+            if (!issuer) return true;
+            if (uses > 0 && !mbar_wait(&bars->qreg_free, (uses - 1) & 1, bars, p.status)) return false;
+            const int qrow = p.work[item].b * rows_seq + g * kRows;
+            int first, n;
+            uint64_t *bar;
+            if (round < kQRounds) {
+                first = round * kQSmemBlocks;
+                n = min(kQSmemBlocks, kQTmemBlocks - first);
+                bar = &bars->q_stage;
+            } else {
+                first = kQTmemBlocks;
+                n = kQSmemBlocks;
+                bar = &bars->q_smem;
+            }
+            mbar_expect_tx(bar, (uint32_t)n * kQBlockBytes);
+            for (int k = 0; k < n; ++k) tma_load_2d(smem + kOffQ + k * kQBlockBytes, &q_map, 64 * (first + k), qrow, bar);
+            return true;
+        };
+        // Staged round -> tensor memory: each thread moves its row's 64-dim
+        // blocks (those with block index % 2 == hs) with tcgen05.st.
+        auto stage_q = [&](int round) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_stage, nstage & 1, bars, p.status))) return false;
+            ++nstage;
+            const int first = round * kQSmemBlocks;
+            const int n = min(kQSmemBlocks, kQTmemBlocks - first);
+#pragma unroll 1
+            for (int k = hs; k < n; k += 2) {
+                uint32_t v[32];
+                const uint8_t *blk = smem + kOffQ + k * kQBlockBytes;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 u = *(const uint4 *)(blk + sw128(row, ch));
+                    v[4 * ch + 0] = u.x;
+                    v[4 * ch + 1] = u.y;
+                    v[4 * ch + 2] = u.z;
+                    v[4 * ch + 3] = u.w;
+                }
+                TMEM_ST32(lane_addr + kColQ + 32 * (first + k), v);
+            }
+            mbar_arrive(&bars->qreg_free);
+            ++uses;
+            return true;
+        };
+        // All staging rounds of `item` (round 0 already issued); then the
+        // tensor-memory part of Q is complete for the MMA warp.
+        auto load_q_tmem = [&](int item) -> bool {
+            for (int r = 0; r < kQRounds; ++r) {
+                if (r > 0 && !__all_sync(0xffffffffu, issue_q(item, r))) return false;
+                if (!stage_q(r)) return false;
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->q_tmem);
+            return true;
+        };
+        // ---- Q of the first item
+        ok = __all_sync(0xffffffffu, issue_q(i0, 0));
+        ok = ok && load_q_tmem(i0);
+        ok = ok && __all_sync(0xffffffffu, issue_q(i0, kQRounds));
         for (int i = i0; i < i1 && ok; ++i) {
             const WorkItem it = p.work[i];
             const int L = p.seq_lens[it.b];
             const int t0 = it.t0, t1 = it.t1;
             const int nt = (t1 - t0 + kTile - 1) / kTile;
             const int last_vis = L - p.q_len + (row_valid ? row_seq / p.s.H : 0);
-            // ---- Q of this item: dims 0..383 -> TMEM (A operand), 384..575 -> smem.
-            // The previous item's last QK has completed (its s_full was awaited).
-            {
-                const uint4 *src = (const uint4 *)((const __nv_bfloat16 *)p.q +
-                                                   ((size_t)it.b * rows_seq + (row_valid ? row_seq : 0)) * kD);
-#pragma unroll 1
-                for (int c = hs * (kQTmemBlocks / 2); c < (hs + 1) * (kQTmemBlocks / 2); ++c) {
-                    uint32_t v[32];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 u = row_valid ? __ldg(src + c * 8 + ch) : make_uint4(0, 0, 0, 0);
-                        v[4 * ch + 0] = u.x;
-                        v[4 * ch + 1] = u.y;
-                        v[4 * ch + 2] = u.z;
-                        v[4 * ch + 3] = u.w;
-                    }
-                    TMEM_ST32(lane_addr + kColQ + 32 * c, v);
-                }
-                for (int c = hs; c < kQSmemBlocks; c += 2)
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 u = row_valid ? __ldg(src + (kQTmemBlocks + c) * 8 + ch) : make_uint4(0, 0, 0, 0);
-                        *(uint4 *)(smem + kOffQ + c * kQBlockBytes + sw128(row, ch)) = u;
-                    }
-                tmem_wait_st();
-                fence_proxy_async();
-                tc_fence_before();
-                mbar_arrive(&bars->q_full);
-            }
             float m_used = -CUDART_INF_F, l = 0.f;       // l: this half's share of the row sum
             bool bad_item = false;     // a block id of this item is out of range
             for (int t = 0; t < nt && ok; ++t, ++T) {
@@ -590,6 +672,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 }
                 tc_fence_after();
                 if (row == 0 && hs == 0) MLA_TRACE_POINT(3, T);
+                if (row == 0 && hs == 0 && t == 0) MLA_TRACE_ITEM(0, i - i0);
                 uint32_t sv[32];
                 TMEM_LD32(lane_addr + kColS + 64 * sb + 32 * hs, sv);
                 tmem_wait_ld();
@@ -675,7 +758,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
                 mbar_arrive(&bars->p_full[pb]);
                 if (row == 0 && hs == 0) MLA_TRACE_POINT(4, T);
             }
-            // ---- epilogue of this item: wait for its last PV, then O / l -> partial slot i
+            // ---- end of this item. The Q region is free (the item's last QK has
+            // completed): stage the next item's tensor-memory Q while the last PV
+            // runs, then write this item's output through the region, then load
+            // the next item's shared-memory Q part.
+            const bool have_next = i + 1 < i1;
+            if (ok && have_next) ok = __all_sync(0xffffffffu, issue_q(i + 1, 0));
+            if (row == 0 && hs == 0) MLA_TRACE_ITEM(1, i - i0);
             if (ok && nt > 0) {
                 const int tl = T - 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[tl & 1], (tl >> 1) & 1, bars, p.status));
@@ -684,35 +773,62 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const TcParams tp) 
             float l_other = 0.f;
             if (ok) ok = __all_sync(0xffffffffu, exchange(l, l_other));
             const float l_row = l + l_other;
-            const bool bad = aborted(bars) || !ok || bad_item;
             tc_fence_after();
-            {
+            // O (fp32, this half's 256 latent dims) leaves tensor memory before the
+            // next item's staged Q enters it: both use the same lane quarter.
+            if (ok && have_next) ok = load_q_tmem(i + 1);
+            if (ok && have_next)        // every thread has read its staged Q out of the region
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->qreg_free, (uses - 1) & 1, bars, p.status));
+            const bool bad = aborted(bars) || !ok || bad_item;
+            // Epilogue: O / l -> partial slot i. Each warp writes [32 rows x 32 dims]
+            // fp32 boxes (128B-swizzled) into the region, kEpiBoxes at a time, and
+            // stores each with one TMA copy; rows past the sequence's rows are
+            // clipped by the tensor map.
+            if (ok) {
                 const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-                float *po = p.part_o + ((size_t)i * rows_seq + (row_valid ? row_seq : 0)) * p.s.r + 256 * half + 128 * hs;
+                uint8_t *boxes = smem + kOffQ + (warp - 4) * kEpiBoxes * kEpiBoxBytes;
+                const int y = g * kRows + 32 * wq;
+                const bool store = y < rows_seq;                 // warp-uniform
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t ov[32];
-                    if (ok) {                      // warp-uniform
-                        TMEM_LD32(lane_addr + kColO + 128 * hs + 32 * c, ov);
-                        tmem_wait_ld();
+                    const int bi = c % kEpiBoxes;
+                    if (bi == 0 && c > 0) {                      // the previous boxes were read
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
                     }
-                    if (!row_valid) continue;
+                    uint32_t ov[32];
+                    TMEM_LD32(lane_addr + kColO + 128 * hs + 32 * c, ov);
+                    tmem_wait_ld();
+                    uint8_t *box = boxes + bi * kEpiBoxBytes;
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
+                    for (int q4 = 0; q4 < 8; ++q4) {
                         float4 f;
-                        f.x = ok ? __uint_as_float(ov[k + 0]) * inv : 0.f;
-                        f.y = ok ? __uint_as_float(ov[k + 1]) * inv : 0.f;
-                        f.z = ok ? __uint_as_float(ov[k + 2]) * inv : 0.f;
-                        f.w = ok ? __uint_as_float(ov[k + 3]) * inv : 0.f;
-                        *(float4 *)(po + 32 * c + k) = f;
+                        f.x = __uint_as_float(ov[4 * q4 + 0]) * inv;
+                        f.y = __uint_as_float(ov[4 * q4 + 1]) * inv;
+                        f.z = __uint_as_float(ov[4 * q4 + 2]) * inv;
+                        f.w = __uint_as_float(ov[4 * q4 + 3]) * inv;
+                        *(float4 *)(box + sw128(lane, q4)) = f;
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0 && store) {
+                        tma_store_3d(&o_map, box, 256 * half + 128 * hs + 32 * c, y, i);
+                        bulk_commit();
                     }
                 }
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
             }
+            mbar_arrive(&bars->qreg_free);
+            ++uses;
             if (row_valid && half == 0 && hs == 0)
                 p.part_lse[(size_t)i * rows_seq + row_seq] =
                     bad ? CUDART_NAN_F : (l_row > 0.f ? m_used + log2f(l_row) : -CUDART_INF_F);
             tc_fence_before();     // O reads complete before the next item's first PV
+            if (ok && have_next) ok = __all_sync(0xffffffffu, issue_q(i + 1, kQRounds));
+            if (row == 0 && hs == 0) MLA_TRACE_ITEM(2, i - i0);
         }
+        if (lane == 0) bulk_wait_all();   // this warp's output stores have landed
     }
     tc_fence_before();
     __syncthreads();
@@ -744,19 +860,34 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 map over a row-major [rows, 576] matrix, 128-byte swizzled boxes of
-// [box_rows, 64].
-static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+// 2-D map over a row-major [rows, 576] matrix of 16-bit elements (bf16 or fp16),
+// 128-byte swizzled boxes of [box_rows, 64]. Rows past the end read as zero.
+static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows,
+                     CUtensorMapDataType dtype) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// 3-D fp32 map over the partial outputs [slots, rows_seq, r], boxes of
+// [32 rows x 32 dims] with the 128-byte swizzle (stores clip rows >= rows_seq).
+static bool make_out_map(CUtensorMap *map, float *base, int r, int rows_seq, int slots) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)r, (cuuint64_t)rows_seq, (cuuint64_t)slots};
+    cuuint64_t strides[2] = {(cuuint64_t)r * 4, (cuuint64_t)rows_seq * r * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
 }
 
 }  // namespace tc
@@ -767,23 +898,29 @@ bool tc_shape_supported(const ShapeArgs &s) {
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
-    (void)max_work;
     tc::TcParams tp;
     tp.p = p;
     tp.row_tiles = (p.q_len * p.s.H + tc::kRows - 1) / tc::kRows;
     // MN-major V operand: 64-dim atoms 8 KB apart, 8-token groups 1 KB apart.
     tp.v_lbo = tc::kKvBlockBytes;
     tp.v_sbo = 1024;
-    CUtensorMap kv_map;
+    CUtensorMap kv_map, q_map, o_map;
     memset(&kv_map, 0, sizeof kv_map);
     const bool int2 = p.s.kind == MLA_KV_INT2_ROT;
-    if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile))
+    if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile,
+                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return cudaErrorInvalidValue;
+    // the query: bf16 as given, or the fp16 rotated query of the INT2 cache
+    const int rows_seq = p.q_len * p.s.H;
+    if (!tc::make_map(&q_map, p.q, (uint64_t)p.B * rows_seq, tc::kRows,
+                      int2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return cudaErrorInvalidValue;
+    if (!tc::make_out_map(&o_map, p.part_o, p.s.r, rows_seq, max_work)) return cudaErrorInvalidValue;
     auto kern = int2 ? tc::decode_tc_kernel<MLA_KV_INT2_ROT> : tc::decode_tc_kernel<MLA_KV_BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);
-    kern<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, tp);
+    kern<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, q_map, o_map, tp);
     return cudaGetLastError();
 }
 
@@ -794,7 +931,7 @@ extern "C" int mla_trace_read(long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);
 }
 extern "C" int mla_trace_cta(unsigned long long *host, int n) {
-    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 3 * (size_t)n);
+    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 9 * (size_t)n);
 }
 #endif
 
