@@ -27,34 +27,49 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+// Non-blocking probe of the phase with the given parity (test_wait never
+// suspends the thread, unlike try_wait).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// (it resumes as soon as the phase completes), instead of spinning.
+__device__ __forceinline__ bool mbar_try_suspend(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase with the given parity. Gives up after
 // `timeout_ns` or as soon as *abort_flag is set; on a timeout it sets
 // *abort_flag and ORs `timeout_flag` into *status. Returns false on give-up.
+// Waiting threads sleep in try_wait rather than polling, which keeps the
+// shared-memory / barrier queues free for the warps that issue copies and MMAs.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *abort_flag,
                                                   int32_t *status, int32_t timeout_flag,
                                                   unsigned long long timeout_ns) {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (*(volatile int32_t *)abort_flag) return false;
-            if (globaltimer() - t0 > timeout_ns) {
-                atomicExch(abort_flag, 1);
-                if (status) atomicOr(status, timeout_flag);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_suspend(bar, parity, 1000u)) return true;
+        if (*(volatile int32_t *)abort_flag) return false;
+        if (globaltimer() - t0 > timeout_ns) {
+            atomicExch(abort_flag, 1);
+            if (status) atomicOr(status, timeout_flag);
+            return false;
         }
     }
 }

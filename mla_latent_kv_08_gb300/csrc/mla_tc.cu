@@ -94,11 +94,17 @@ __host__ __device__ constexpr int first_smem_group(int first_smem_step) {
 constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bounded-wait safety net
 
 // Pipeline timestamps for performance analysis, compiled only with
-// -DMLA_TRACE: clock64 at each hand-off of one CTA (stream 0, half 0, row
-// tile 0) for its first kTraceTiles tiles. Product builds contain none of it.
+// -DMLA_TRACE: clock64 at each hand-off of one CTA (stream MLA_TRACE_STREAM,
+// half MLA_TRACE_HALF, row tile 0) for its first kTraceTiles tiles. Product builds contain none of it.
 #ifdef MLA_TRACE
+#ifndef MLA_TRACE_STREAM
+#define MLA_TRACE_STREAM 0
+#endif
+#ifndef MLA_TRACE_HALF
+#define MLA_TRACE_HALF 0
+#endif
 constexpr int kTraceTiles = 64;
-__device__ long long g_trace[16][kTraceTiles];
+__device__ long long g_trace[24][kTraceTiles];
 // per CTA: start, end (globaltimer ns), items<<32 | tiles, then for items 0 and 1:
 // first S seen, epilogue begin, epilogue end
 __device__ unsigned long long g_cta_time[4096][9];
@@ -108,7 +114,7 @@ __device__ unsigned long long g_cta_time[4096][9];
     } while (0)
 #define MLA_TRACE_POINT(ev, tile)                                                              \
     do {                                                                                       \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (tile) < kTraceTiles)   \
+        if (blockIdx.x == MLA_TRACE_HALF && blockIdx.y == 0 && blockIdx.z == MLA_TRACE_STREAM && (tile) < kTraceTiles) \
             g_trace[ev][tile] = clock64();                                                     \
     } while (0)
 #else
@@ -122,7 +128,8 @@ __device__ unsigned long long g_cta_time[4096][9];
 // events: 0 TMA issued, 1 stage landed (MMA), 2 QK issued, 3 S seen (softmax),
 //         4 P ready (softmax), 5 PV issued, 6 PV stage released (producer saw empty),
 //         7 S in registers, 8 exponentials done, 9 P about to be stored (softmax),
-//         10..15 QK issue group 0..5 issued (MMA)
+//         10..15 QK issue group 0..5 issued (MMA), 16 S buffer free (MMA),
+//         17 first QK MMA issued, 18 about to issue it, 19 second issued (MMA)
 
 struct Bars {
     uint64_t full[kStages];       // bf16: tile landed; INT2: stage expanded
@@ -175,7 +182,7 @@ __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
 }
 
 #ifndef MLA_PREFETCH_AHEAD
-#define MLA_PREFETCH_AHEAD 4
+#define MLA_PREFETCH_AHEAD 2
 #endif
 #ifndef MLA_PV_SLIP
 #define MLA_PV_SLIP 1
@@ -285,7 +292,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
             int next_blk = block_of(p, it.b, it.t0 / kTile);     // loaded one tile ahead
             for (int t = 0; t < nt; ++t, ++T) {
-                if (prefetcher && lane == 0) advance_prefetch();
                 int blk = next_blk;
                 if (t + 1 < nt) next_blk = block_of(p, it.b, it.t0 / kTile + t + 1);
                 if (blk < 0) {            // the softmax marks the item's rows NaN
@@ -321,9 +327,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (lane < kKvBlocks)
                         tma_load_2d(stage + lane * kKvBlockBytes, &kv_map, lane * 64, blk * kTile, &bars->full[s]);
                 }
-                if (lane == 0) {
+                if (lane == 0) {                 // L2 prefetch after this tile's own loads
                     MLA_TRACE_POINT(0, T);
                     if (prefetcher && ahead > 0) --ahead;
+                    if (prefetcher) advance_prefetch();
                 }
             }
         }
@@ -460,8 +467,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (lane == 0) {
                         const unsigned long long tw0 = globaltimer();
                         for (uint32_t it2 = 0;; ++it2) {
-                            if (mbar_try(&bars->p_full[pbp], ((T - 1) >> 1) & 1)) { st = 2; break; }
-                            if (mbar_try(&bars->full[s], (T / kStages) & 1)) { st = 1; break; }
+                            if (mbar_test(&bars->p_full[pbp], ((T - 1) >> 1) & 1)) { st = 2; break; }
+                            if (mbar_test(&bars->full[s], (T / kStages) & 1)) { st = 1; break; }
                             if ((it2 & 63u) == 63u && (aborted(bars) || globaltimer() - tw0 > kTimeoutNs)) break;
                         }
                     }
@@ -479,6 +486,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     ok = false;
                     break;
                 }
+                if (lane == 0) MLA_TRACE_POINT(16, T);
                 // the sequence's final partial block: zero the slots past the end so
                 // that P = 0 never meets stale (possibly non-finite) cache bytes
                 const int tile_start = it.t0 + t * kTile;
@@ -520,7 +528,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         for (int j = grp_start(grp); j < grp_start(grp + 1); ++j) {
                             const uint64_t bd = kd + (uint64_t)(((j >> 2) * kKvBlockBytes + 32 * (j & 3)) >> 4);
                             if (j == 0) {
+                                MLA_TRACE_POINT(18, T);
                                 mma_ts_k<kIdQk, 0>(d_s, qt, bd);
+                                MLA_TRACE_POINT(17, T);
+                            } else if (j == 1) {
+                                mma_ts_k<kIdQk, 1>(d_s, qt + 8 * j, bd);
+                                MLA_TRACE_POINT(19, T);
                             } else if (j < 4 * kQTmemBlocks) {
                                 mma_ts_k<kIdQk, 1>(d_s, qt + 8 * j, bd);
                             } else {
@@ -532,7 +545,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     __syncwarp();
                     if (lane == 0) MLA_TRACE_POINT(10 + grp, T);
                     if (MLA_PV_SLIP && pv_pending && grp < 5) {
-                        const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_try(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
+                        const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_test(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
                         if (ready) {
                             if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
                             pv_pending = false;
@@ -683,13 +696,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 const int tile_start = t0 + t * kTile + 32 * hs;
                 // tokens j < n_vis of this half-tile are visible to this row
                 const int n_vis = row_valid ? max(0, min(t1, last_vis + 1) - tile_start) : 0;
+                // Scores stay unscaled where the scale is positive: the row max then
+                // commutes with the scaling (rounding is monotonic) and each exponent
+                // argument is a single fma, s * scale - max. Hidden slots become -inf
+                // (only partial tiles pay for the mask).
+                const bool pos_scale = p.scale_log2 > 0.f;
+                const float cs = pos_scale ? p.scale_log2 : 1.f;
+                if (!pos_scale || __any_sync(0xffffffffu, n_vis < 32)) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float v = pos_scale ? __uint_as_float(sv[j]) : __uint_as_float(sv[j]) * p.scale_log2;
+                        sv[j] = __float_as_uint(j < n_vis ? v : -CUDART_INF_F);
+                    }
+                }
                 float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float s2 = j < n_vis ? __uint_as_float(sv[j]) * p.scale_log2 : -CUDART_INF_F;
-                    sv[j] = __float_as_uint(s2);
-                    mx = fmaxf(mx, s2);
-                }
+                for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+                mx *= cs;
                 // the row's max over both halves
                 {
                     float other = -CUDART_INF_F;
@@ -704,15 +727,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     m_used = m_new;
                     rescale = t > 0;
                 }
-                // exponent base: the running max, or +inf for a row with nothing
-                // visible yet (every exponent is then -inf and P = 0)
-                const float mb = m_used == -CUDART_INF_F ? CUDART_INF_F : m_used;
+                // minus the exponent base: -(running max), or -inf for a row with
+                // nothing visible yet (every argument is then -inf and P = 0)
+                const float nmb = m_used == -CUDART_INF_F ? -CUDART_INF_F : -m_used;
                 float sum0 = 0.f, sum1 = 0.f;
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float a = ex2(__uint_as_float(sv[2 * j]) - mb);
-                    const float c = ex2(__uint_as_float(sv[2 * j + 1]) - mb);
+                    const float a = ex2(fmaf(__uint_as_float(sv[2 * j]), cs, nmb));
+                    const float c = ex2(fmaf(__uint_as_float(sv[2 * j + 1]), cs, nmb));
                     if (kInt2) {
                         const __half2 h = __floats2half2_rn(a, c);
                         pk[j] = *(const uint32_t *)&h;
@@ -928,7 +951,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
 
 #ifdef MLA_TRACE
 extern "C" int mla_trace_read(long long *host, int n) {
-    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);
+    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);   // [24][64]
 }
 extern "C" int mla_trace_cta(unsigned long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 9 * (size_t)n);
