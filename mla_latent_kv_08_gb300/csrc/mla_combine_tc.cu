@@ -54,23 +54,30 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
     uint32_t *tmem_slot = (uint32_t *)(bar_w + 2);
     int32_t *abort_flag = (int32_t *)(bar_w + 3);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
 
+    // set-up that overlaps the decode kernel's tail: barriers, TMEM, and W_UV^h
+    // ([512 x 128] bf16, contiguous) pulled into L2
     if (tid == 0) {
         mbar_init(bar_w, 1);
         mbar_init(bar_mma, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
-        mbar_expect_tx(bar_w, kWBytes);
-        for (int vb = 0; vb < 2; ++vb)
-            for (int kb = 0; kb < 8; ++kb)
-                tma_load_2d(smem + kOffW + (vb * 8 + kb) * kWBoxBytes, &w_map, 64 * vb, h * kR + 64 * kb, bar_w);
+        prefetch_l2((const uint8_t *)c.W_UV + (size_t)h * kWBytes, kWBytes);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(64)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    pdl_wait();                      // the split partials are complete from here on
+    if (tid == 0) {
+        mbar_expect_tx(bar_w, kWBytes);
+        for (int vb = 0; vb < 2; ++vb)
+            for (int kb = 0; kb < 8; ++kb)
+                tma_load_2d(smem + kOffW + (vb * 8 + kb) * kWBoxBytes, &w_map, 64 * vb, h * kR + 64 * kb, bar_w);
     }
 
     // ---- merge split partials: warp per row, each lane owns 16 latent dims
@@ -220,8 +227,7 @@ cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st) {
                                          (int)comb::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(c.s.H, (tp.rows + comb::kMaxRows - 1) / comb::kMaxRows);
-    comb::combine_tc_kernel<<<grid, comb::kThreads, comb::kSmemBytes, st>>>(map, tp);
-    return cudaGetLastError();
+    return launch_pdl(comb::combine_tc_kernel, grid, dim3(comb::kThreads), comb::kSmemBytes, st, map, tp);
 }
 
 }  // namespace mla

@@ -106,6 +106,28 @@ struct AppendParams {
 };
 
 // ---- launchers (defined in mla_simt.cu) ------------------------------------
+// Programmatic dependent launch. A kernel launched with launch_pdl may start while
+// the previous kernel of the stream is still running; it calls pdl_trigger() on entry
+// (so that the next kernel may be scheduled as soon as SMs free up) and pdl_wait()
+// before its first access to any buffer that another kernel writes or reads.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bool out_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st);

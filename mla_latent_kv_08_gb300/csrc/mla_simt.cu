@@ -56,6 +56,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &tot
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_work) {
     __shared__ int s_warp[33];
     __shared__ long long s_tiles;
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int64_t cap = (int64_t)p.max_blocks * p.s.bs;
     const int P = p.streams;
@@ -117,8 +119,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
 }
 
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
-    plan_kernel<<<1, 1024, 0, st>>>(p, max_work);
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, max_work);
 }
 
 // ============================================================================
@@ -591,6 +592,8 @@ __device__ __forceinline__ long long locate_slot(const AppendParams &p, int n) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (n >= p.num_new) return;
@@ -697,9 +700,9 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
     if (p.num_new == 0) return cudaSuccess;
     if (p.s.kind == MLA_KV_BF16) {
-        append_copy_kernel<__nv_bfloat16><<<(p.num_new + 7) / 8, 256, 0, st>>>(p);
+        return launch_pdl(append_copy_kernel<__nv_bfloat16>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     } else if (p.s.kind == MLA_KV_FP32) {
-        append_copy_kernel<float><<<(p.num_new + 7) / 8, 256, 0, st>>>(p);
+        return launch_pdl(append_copy_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     } else {
         const size_t smem = sizeof(float) * 2 * kAT * (size_t)p.s.r;
         dim3 grid((p.num_new + kAT - 1) / kAT);

@@ -170,9 +170,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Bars *
 __device__ __forceinline__ bool aborted(Bars *bars) { return *(volatile int32_t *)&bars->abort_flag != 0; }
 
 // ---------------------------------------------------------------- the kernel
-__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
 
 // Physical block of logical tile `lb` of sequence b, or -1.
 __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
@@ -207,8 +204,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     const int half = blockIdx.x;            // 0/1: which 256 latent output dims
     const int g = blockIdx.y;               // query row tile
     const int stream = blockIdx.z;          // work stream (persistent over its items)
-    const int i0 = p.stream_start[stream], i1 = p.stream_start[stream + 1];
-    if (i0 >= i1) return;
+    pdl_trigger();
     const int rows_seq = p.q_len * p.s.H;
 #ifdef MLA_TRACE
     const unsigned cta_id = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
@@ -257,6 +253,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // the set-up above overlaps the planner; its schedule is read only from here on
+    pdl_wait();
+    const int i0 = p.stream_start[stream], i1 = p.stream_start[stream + 1];
+    if (i0 >= i1) {                          // no work for this stream (CTA-uniform)
+        if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+        return;
+    }
 
     if (warp == 0) {
         // ================================================= producer (+ L2 prefetch)
@@ -943,8 +946,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);
-    kern<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(kv_map, q_map, o_map, tp);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(tc::kThreads), tc::kSmemBytes, st, kv_map, q_map, o_map, tp);
 }
 
 }  // namespace mla
