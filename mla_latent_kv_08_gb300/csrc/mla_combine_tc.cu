@@ -21,7 +21,7 @@ namespace comb {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kR = 512, kDv = 128;
 constexpr int kMaxRows = 64;                        // output rows per CTA (MMA N)
 constexpr uint32_t kWBoxBytes = 64 * 128;            // [64 k x 64 v] bf16
@@ -30,7 +30,7 @@ constexpr uint32_t kOffW = 0;
 constexpr uint32_t kOffO = kWBytes;                  // o_lat: 8 column blocks of [kMaxRows x 128 B]
 constexpr uint32_t kOBlockBytes = kMaxRows * 128;
 constexpr uint32_t kOffBar = kOffO + 8 * kOBlockBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
+constexpr uint32_t kSmemBytes = kOffBar + 64 + 8 * kMaxRows + 1024;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 struct CombTcParams {
@@ -80,38 +80,69 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
                 tma_load_2d(smem + kOffW + (vb * 8 + kb) * kWBoxBytes, &w_map, 64 * vb, h * kR + 64 * kb, bar_w);
     }
 
-    // ---- merge split partials: warp per row, each lane owns 16 latent dims
+    // ---- merge split partials: warp per row, each lane owns 16 latent dims. Every
+    // row's split range is read first; then a row costs one round trip: its log2-sum-
+    // exps and partials (up to four splits at a time) are loaded together and merged
+    // with a running maximum.
+    int2 *s_range = (int2 *)(smem + kOffBar + 64);   // [kMaxRows] split ranges
+    if (tid < nrows) {
+        const int b = (row0 + tid) / c.q_len;
+        s_range[tid] = make_int2(c.split_start[b], c.split_start[b + 1]);
+    }
+    __syncthreads();
     for (int rr = warp; rr < NR; rr += kThreads / 32) {
         const int grow = row0 + rr;
         float acc[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) acc[k] = 0.f;
         float lse_out = 0.f;
-        bool nan = false;
         if (rr < nrows) {
-            const int b = grow / c.q_len, i = grow % c.q_len;
-            const int s0 = c.split_start[b], s1 = c.split_start[b + 1];
+            const int i = grow % c.q_len;
+            const int2 sr = s_range[rr];
+            const int s0 = sr.x, s1 = sr.y;
             const int row = i * H + h;
-            nan = s1 <= s0;
-            float M = -CUDART_INF_F;
-            for (int s = s0; s < s1; ++s) {
-                const float v = c.part_lse[(size_t)s * rows_seq + row];
-                nan |= isnan(v);
-                M = fmaxf(M, v);
-            }
-            float tot = 0.f;
-            for (int s = s0; s < s1; ++s) {
-                const float v = c.part_lse[(size_t)s * rows_seq + row];
-                const float wgt = v == -CUDART_INF_F ? 0.f : exp2f(v - M);
-                tot += wgt;
-                const float4 *po = (const float4 *)(c.part_o + ((size_t)s * rows_seq + row) * kR);
+            bool nan = s1 <= s0;
+            float M = -CUDART_INF_F, tot = 0.f;
+            for (int sb = s0; sb < s1; sb += 4) {
+                float4 f[4][4];
+                float v[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 f = po[lane + 32 * q];
-                    acc[4 * q + 0] = fmaf(wgt, f.x, acc[4 * q + 0]);
-                    acc[4 * q + 1] = fmaf(wgt, f.y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(wgt, f.z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(wgt, f.w, acc[4 * q + 3]);
+                for (int k = 0; k < 4; ++k) {
+                    const int sp = sb + k;
+                    v[k] = -CUDART_INF_F;
+                    if (sp < s1) {
+                        const float4 *po = (const float4 *)(c.part_o + ((size_t)sp * rows_seq + row) * kR);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) f[k][q] = po[lane + 32 * q];
+                        v[k] = c.part_lse[(size_t)sp * rows_seq + row];
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) f[k][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float Mn = M;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    nan |= isnan(v[k]);
+                    Mn = fmaxf(Mn, v[k]);
+                }
+                // rescale what was merged so far (nothing, or the earlier splits)
+                const float a = M == -CUDART_INF_F ? 0.f : exp2f(M - Mn);
+                tot *= a;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) acc[k] *= a;
+                M = Mn;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float wgt = v[k] == -CUDART_INF_F ? 0.f : exp2f(v[k] - M);
+                    tot += wgt;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[4 * q + 0] = fmaf(wgt, f[k][q].x, acc[4 * q + 0]);
+                        acc[4 * q + 1] = fmaf(wgt, f[k][q].y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(wgt, f[k][q].z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(wgt, f[k][q].w, acc[4 * q + 3]);
+                    }
                 }
             }
             const float inv = tot > 0.f ? 1.f / tot : 0.f;
