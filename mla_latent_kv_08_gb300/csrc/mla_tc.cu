@@ -81,9 +81,12 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 __host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u; }
 constexpr int kDequantThreads = 64;   // warps 2..3 (rotated-INT2 cache)
 constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 32 dims] fp32
-// QK K-steps in six issue groups: [0,6) [6,12) [12,16) [16,22) [22,28) [28,36)
+// QK K-steps in two issue groups: [0,16) (Q from tensor memory in the bf16 kind)
+// and [16,36). Every group boundary costs the MMA warp a warp sync and a barrier
+// probe; with more, finer groups the decode ran slower.
+constexpr int kQkGroups = 2;
 __host__ __device__ constexpr int grp_start(int grp) {
-    return grp == 0 ? 0 : grp == 1 ? 6 : grp == 2 ? 12 : grp == 3 ? 16 : grp == 4 ? 22 : grp == 5 ? 28 : 36;
+    return grp == 0 ? 0 : grp == 1 ? 16 : 36;
 }
 __host__ __device__ constexpr int first_smem_group(int first_smem_step) {
     int g = 0;
@@ -504,7 +507,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     fence_proxy_async();
                     __syncwarp();
                 }
-                // QK(T) in six groups of six K-steps. PV(T-1) of the same item is
+                // QK(T) in kQkGroups issue groups. PV(T-1) of the same item is
                 // slipped in between groups as soon as its P is ready, so that the
                 // stage it reads is released early; otherwise it follows QK(T).
                 bool pv_pending = t > 0 && !pv_early;
@@ -516,7 +519,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 const uint32_t d_s = tmem + kColS + 64 * (T % kSBufs);
                 constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
 #pragma unroll
-                for (int grp = 0; grp < 6; ++grp) {
+                for (int grp = 0; grp < kQkGroups; ++grp) {
                     // the item's first tile: its shared-memory Q part may still be landing
                     if (grp == kFirstSmemGroup && t == 0 &&
                         !__all_sync(0xffffffffu, mbar_wait(&bars->q_smem, item_no & 1, bars, p.status))) {
@@ -526,7 +529,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (lane == 0) {
                         // K-step j: column block j/4, 32-byte step j%4 inside the swizzle
                         // atom; descriptor start addresses advance in 16-byte units.
-                        // Groups: K-steps [0,6) [6,12) [12,16) [16,22) [22,28) [28,36).
 #pragma unroll
                         for (int j = grp_start(grp); j < grp_start(grp + 1); ++j) {
                             const uint64_t bd = kd + (uint64_t)(((j >> 2) * kKvBlockBytes + 32 * (j & 3)) >> 4);
@@ -547,7 +549,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     }
                     __syncwarp();
                     if (lane == 0) MLA_TRACE_POINT(10 + grp, T);
-                    if (MLA_PV_SLIP && pv_pending && grp < 5) {
+                    if (MLA_PV_SLIP && pv_pending && grp < kQkGroups - 1) {
                         const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_test(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
                         if (ready) {
                             if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
