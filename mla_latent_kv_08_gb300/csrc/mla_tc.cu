@@ -38,7 +38,9 @@
 namespace mla {
 namespace tc {
 
-constexpr int kThreads = 384;         // 4 control warps + 8 softmax warps
+// Threads per CTA: warps 0..3 control (producer, MMA, two dequantisers), 4..11
+// softmax; the INT2 kind adds dequantising warps 12..15.
+template <int KIND> constexpr int threads_of() { return KIND == MLA_KV_INT2_ROT ? 512 : 384; }
 constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
@@ -79,7 +81,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // blocks of tile T's own stage that only QK reads (the other half's V dims),
 // once QK(T) is done; PV(T) is their last reader.
 __host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u; }
-constexpr int kDequantThreads = 64;   // warps 2..3 (rotated-INT2 cache)
+constexpr int kDequantWarps = 6;      // warps 2, 3, 12..15 (rotated-INT2 cache)
+constexpr int kDequantThreads = 32 * kDequantWarps;
 constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 32 dims] fp32
 // QK K-steps in two issue groups: [0,16) (Q from tensor memory in the bf16 kind)
 // and [16,36). Every group boundary costs the MMA warp a warp sync and a barrier
@@ -107,7 +110,7 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;           // 2 s: a bou
 #define MLA_TRACE_HALF 0
 #endif
 constexpr int kTraceTiles = 64;
-__device__ long long g_trace[24][kTraceTiles];
+__device__ long long g_trace[32][kTraceTiles];
 // per CTA: start, end (globaltimer ns), items<<32 | tiles, then for items 0 and 1:
 // first S seen, epilogue begin, epilogue end
 __device__ unsigned long long g_cta_time[4096][9];
@@ -132,7 +135,10 @@ __device__ unsigned long long g_cta_time[4096][9];
 //         4 P ready (softmax), 5 PV issued, 6 PV stage released (producer saw empty),
 //         7 S in registers, 8 exponentials done, 9 P about to be stored (softmax),
 //         10..15 QK issue group 0..5 issued (MMA), 16 S buffer free (MMA),
-//         17 first QK MMA issued, 18 about to issue it, 19 second issued (MMA)
+//         17 first QK MMA issued, 18 about to issue it, 19 second issued, 20 tail
+//         handled, 21 after the tcgen05 fence, 22 descriptors ready (MMA),
+//         INT2: 24 raw block copy issued (producer), 25 raw block seen, 26 stage
+//         free seen, 27 stage expanded (dequantising warp 2)
 
 struct Bars {
     uint64_t full[kStages];       // bf16: tile landed; INT2: stage expanded
@@ -190,7 +196,7 @@ __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
 constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2 ahead of the TMA loads
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<KIND>(), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                  const __grid_constant__ CUtensorMap o_map, const TcParams tp) {
     constexpr bool kInt2 = KIND == MLA_KV_INT2_ROT;
@@ -319,6 +325,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (lane == 2)
                         bulk_load(raw + kRawCodes + kRawSz, (const uint8_t *)p.rope + (size_t)blk * kRawRope, kRawRope,
                                   &bars->raw_full);
+                    if (lane == 0) MLA_TRACE_POINT(24, T);
                 } else {
                     const int s = T % kStages;
                     if (T >= kStages &&
@@ -348,13 +355,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
         }
         __syncwarp();
-    } else if (kInt2 && (warp == 2 || warp == 3)) {
+    } else if (kInt2 && (warp == 2 || warp == 3 || warp >= 12)) {
         // ================================================= INT2 expansion into the stage
-        // value = fmaf(code, scale, zero) in fp32, rounded to fp16 (the MMA operand
-        // type of this cache kind), written in the 128B-swizzled layout the MMAs
+        // value = code * scale + zero, rounded once to fp16 (the MMA operand type of
+        // this cache kind), written in the 128B-swizzled layout the MMAs
         // read; the bf16 rope key is converted to fp16; slots past the sequence end
         // are zeroed.
-        const int dt = tid - 64;
+        const int dw = warp < 4 ? warp - 2 : warp - 10;   // dequantising warp 0..5
+        const __half2 k1024 = __float2half2_rn(1024.f);
+        const int dt = 32 * dw + lane;
         int T = 0;
         bool ok = true;
         for (int i = i0; i < i1 && ok; ++i) {
@@ -364,38 +373,45 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             for (int t = 0; t < nt; ++t, ++T) {
                 const int s = T % kStages;
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars->raw_full, T & 1, bars, p.status))) { ok = false; break; }
+                if (dt == 0) MLA_TRACE_POINT(25, T);
                 if (T >= kStages &&
                     !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
                     ok = false;
                     break;
                 }
+                if (dt == 0) MLA_TRACE_POINT(26, T);
                 const int valid = min(kTile, L - (it.t0 + t * kTile));
                 const uint8_t *raw = smem + kOffRaw;
+                const uint4 *rope = (const uint4 *)(raw + kRawCodes + kRawSz);
                 const uint8_t *codes = raw;
                 const __half *sz = (const __half *)(raw + kRawCodes);
-                const uint4 *rope = (const uint4 *)(raw + kRawCodes + kRawSz);
                 uint8_t *stage = smem + kOffStage + s * kStageBytes;
                 // latent: a lane expands one 32-dim group of one row (8 code bytes, one
                 // scale/zero pair) into four 16-byte chunks; a warp covers two rows per
                 // pass, so its code reads are 256 contiguous bytes.
                 const int half_lane = lane >> 4, grp = lane & 15;
-                for (int rr = 2 * (warp - 2) + half_lane; rr < kTile; rr += 4) {
+                for (int rr = 2 * dw + half_lane; rr < kTile; rr += 2 * kDequantWarps) {
                     uint4 outc[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                                      make_uint4(0, 0, 0, 0)};
                     if (rr < valid) {
                         const uint2 cb = *(const uint2 *)(codes + rr * 128 + 8 * grp);
                         const __half2 szp = *(const __half2 *)(sz + (rr * 16 + grp) * 2);
-                        const float sc = __low2float(szp), zr = __high2float(szp);
+                        const __half2 s2 = __half2half2(__low2half(szp)), z2 = __half2half2(__high2half(szp));
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const unsigned two = ((q4 < 2 ? cb.x : cb.y) >> (16 * (q4 & 1))) & 0xffffu;
-                            float v[8];
+                            // two codes at a time in half2: 1024 + c has the bits 0x6400 | c,
+                            // so subtracting 1024 gives c exactly; then one fused c * s + z
+                            // rounded once to fp16 (the operand type)
+                            __half2 hh[4];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = __fmaf_rn((float)((two >> (2 * e)) & 3u), sc, zr);
-                            const __half2 h0 = __floats2half2_rn(v[0], v[1]);
-                            const __half2 h1 = __floats2half2_rn(v[2], v[3]);
-                            const __half2 h2 = __floats2half2_rn(v[4], v[5]);
-                            const __half2 h3 = __floats2half2_rn(v[6], v[7]);
+                            for (int e = 0; e < 4; ++e) {
+                                const unsigned pr = (two >> (4 * e)) & 0xFu;
+                                const unsigned wv = 0x64006400u | (pr & 3u) | ((pr & 0xCu) << 14);
+                                const __half2 c2 = __hsub2(*(const __half2 *)&wv, k1024);
+                                hh[e] = __hfma2(c2, s2, z2);
+                            }
+                            const __half2 h0 = hh[0], h1 = hh[1], h2 = hh[2], h3 = hh[3];
                             outc[q4] = make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1,
                                                   *(const uint32_t *)&h2, *(const uint32_t *)&h3);
                         }
@@ -423,6 +439,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 fence_proxy_async();
                 mbar_arrive(&bars->raw_empty);
                 mbar_arrive(&bars->full[s]);
+                if (dt == 0) MLA_TRACE_POINT(27, T);
             }
         }
     } else if (warp == 1) {
@@ -512,11 +529,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 // stage it reads is released early; otherwise it follows QK(T).
                 bool pv_pending = t > 0 && !pv_early;
                 const int pb_prev = (T - 1) & 1;
+                if (lane == 0) MLA_TRACE_POINT(20, T);
                 tc_fence_after();
+                if (lane == 0) MLA_TRACE_POINT(21, T);
                 const uint64_t kd = sdesc(smem_u32(smem + kOffStage + s * kStageBytes), 16, 1024);
                 const uint64_t qd = sdesc(smem_u32(smem + kOffQ), 16, 1024);
                 const uint32_t qt = tmem + kColQ;
                 const uint32_t d_s = tmem + kColS + 64 * (T % kSBufs);
+                if (lane == 0) MLA_TRACE_POINT(22, T);
                 constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
 #pragma unroll
                 for (int grp = 0; grp < kQkGroups; ++grp) {
@@ -572,7 +592,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             mbar_wait(&bars->mma_fin, 0, bars, p.status);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ================================================= Q loads, softmax, epilogue
         // Warps 4..11: warp w owns rows 32*(w%4)..+31 (its TMEM lane quarter) and
         // half hs = (w-4)/4 of each row: score columns 32*hs..+31, output columns
@@ -948,14 +968,15 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);
-    return launch_pdl(kern, grid, dim3(tc::kThreads), tc::kSmemBytes, st, kv_map, q_map, o_map, tp);
+    const int threads = int2 ? tc::threads_of<MLA_KV_INT2_ROT>() : tc::threads_of<MLA_KV_BF16>();
+    return launch_pdl(kern, grid, dim3(threads), tc::kSmemBytes, st, kv_map, q_map, o_map, tp);
 }
 
 }  // namespace mla
 
 #ifdef MLA_TRACE
 extern "C" int mla_trace_read(long long *host, int n) {
-    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);   // [24][64]
+    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);   // [32][64]
 }
 extern "C" int mla_trace_cta(unsigned long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 9 * (size_t)n);
