@@ -121,6 +121,7 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
         w.o_lat = off;  off = up256(off + sizeof(float) * nrow * s->kv_lora_rank);
         w.lse2 = off;   off = up256(off + sizeof(float) * nrow);
         w.ident = off;  off = up256(off + sizeof(int32_t) * ((size_t)B + 1));
+        w.r16 = off;    off = up256(off + sizeof(__half) * (size_t)s->kv_lora_rank * s->kv_lora_rank);
     }
     w.total = off;
     return w;
@@ -181,8 +182,8 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         // of this cache kind) from the tensor-core GEMM for the tensor-core kernel,
         // which then reads it in place of q
         if (tc) {
-            if (launch_rot_query(R, q, ws + w.q_prep, B * q_len * s->num_heads, s->kv_lora_rank + s->rope_dim,
-                                 p.status, stream_) != cudaSuccess)
+            if (launch_rot_query(R, (__half *)(ws + w.r16), q, ws + w.q_prep, B * q_len * s->num_heads,
+                                 s->kv_lora_rank + s->rope_dim, p.status, stream_) != cudaSuccess)
                 return MLA_ERR_CUDA;
             p.q = ws + w.q_prep;
         } else if (launch_qprep(p, R, ws + w.q_prep, false, stream_) != cudaSuccess) {
@@ -213,7 +214,9 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         // W_UV up-projection reads the merged rows as one-split partials
         float *o_rot = (float *)(ws + w.o_rot), *o_lat = (float *)(ws + w.o_lat), *lse2 = (float *)(ws + w.lse2);
         int32_t *ident = (int32_t *)(ws + w.ident);
-        if (launch_rot_output(c, R, o_rot, o_lat, lse2, ident, p.status, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_rot_output(c, (const __half *)(ws + w.r16), o_rot, o_lat, lse2, ident, p.status, stream_) !=
+            cudaSuccess)
+            return MLA_ERR_CUDA;
         c.split_start = ident;
         c.part_o = o_lat;
         c.part_lse = lse2;

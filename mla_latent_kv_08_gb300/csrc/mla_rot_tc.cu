@@ -2,17 +2,20 @@
 //   q_rot[m, :] = q_lat[m, :] . R          (query prep, before attention)
 //   o_lat[m, :] = o_rot[m, :] . R^T        (after the split merge, before W_UV)
 // as one GEMM kernel Y[M x 512] = X[M x 512] . op(R), op = identity or transpose,
-// with kv_lora_rank 512. X (bf16 query rows or fp32 merged outputs) and R (fp32)
-// are converted to fp16 by the threads that stage them in shared memory; the
-// MMA accumulates in fp32 in tensor memory. A CTA computes a [128 x 256] tile of
-// Y over eight 64-wide K chunks, double-buffered.
+// with kv_lora_rank 512. R is first converted once per call to fp16 (R16); the
+// GEMM's B tiles come from R16 by TMA, the A tiles (bf16 query rows or fp32
+// merged outputs) are converted to fp16 by the threads that stage them in
+// shared memory, and the MMA accumulates in fp32 in tensor memory. A CTA
+// computes a [128 x 128] tile of Y over eight 64-wide K chunks, double-buffered.
 //
 // Also here: the merge of split partials into one latent row per (sequence,
 // draft position, head), which precedes the second rotation.
 #include "mla_internal.cuh"
 #include "mla_ptx.cuh"
 
+#include <cudaTypedefs.h>
 #include <math_constants.h>
+#include <string.h>
 
 namespace mla {
 namespace rot {
@@ -21,10 +24,10 @@ using namespace ptx;
 
 constexpr int kThreads = 256;
 constexpr int kK = 512;                         // kv_lora_rank
-constexpr int kTm = 128, kTn = 256, kKc = 64;   // tile M, tile N, K chunk
+constexpr int kTm = 128, kTn = 128, kKc = 64;   // tile M, tile N, K chunk
 constexpr uint32_t kABytes = kTm * 128;         // [128 rows x 64 k] fp16
-constexpr uint32_t kBBytes = kTn * 128;         // [256 j x 64 k] fp16 (either layout)
-constexpr uint32_t kStage = kABytes + kBBytes;  // 48 KB
+constexpr uint32_t kBBytes = kTn * 128;         // [128 j x 64 k] fp16 (either layout)
+constexpr uint32_t kStage = kABytes + kBBytes;  // 32 KB
 constexpr uint32_t kOffBar = 2 * kStage;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
@@ -32,7 +35,6 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 struct RotParams {
     const void *X;
     int ldx;              // elements per X row
-    const float *R;       // [512, 512] row-major
     void *Y;
     int ldy;              // elements per Y row
     int M;
@@ -48,25 +50,42 @@ __device__ __forceinline__ uint4 pack8_f16(const float *v) {
     return make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1, *(const uint32_t *)&h2, *(const uint32_t *)&h3);
 }
 
+// R16 = fp16(R), round to nearest even, eight elements per thread.
+__global__ void __launch_bounds__(256) r_to_f16_kernel(const float *R, __half *R16, int n8) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
+        const float4 a = ((const float4 *)R)[2 * i], b = ((const float4 *)R)[2 * i + 1];
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        ((uint4 *)R16)[i] = pack8_f16(v);
+    }
+}
+
 // X_FP32: X is fp32 (else bf16). TRANS: op(R) = R^T (else R). Y_F16: Y is fp16 (else fp32).
+// r_map: R16 as [512 rows, 512 cols] fp16, 128B-swizzled boxes of [64 cols x 128
+// rows] (TRANS: B = R rows j, K-major) or [64 cols x 64 rows] (else: B = R rows k,
+// MN-major, two 64-wide j atoms per chunk).
 template <bool X_FP32, bool TRANS, bool Y_F16>
-__global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const RotParams rp) {
+__global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const __grid_constant__ CUtensorMap r_map,
+                                                               const RotParams rp) {
     const int m0 = blockIdx.x * kTm, j0 = blockIdx.y * kTn;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bar = (uint64_t *)(smem + kOffBar);        // [2] MMA done per stage
-    uint32_t *tmem_slot = (uint32_t *)(bar + 2);
-    int32_t *abort_flag = (int32_t *)(bar + 3);
+    uint64_t *bfull = bar + 2;                           // [2] B tile landed per stage
+    uint32_t *tmem_slot = (uint32_t *)(bar + 4);
+    int32_t *abort_flag = (int32_t *)(bar + 5);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[i], 1);
+            mbar_init(&bfull[i], 1);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(256)
+                     "r"(kTn)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -74,19 +93,44 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const RotParams r
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // fp16 A and B, fp32 D, M 128, N 256; B MN-major for op(R) = R (R's rows are k)
+    pdl_wait();
+    // fp16 A and B, fp32 D, M 128, N 128; B MN-major for op(R) = R (R's rows are k)
     const uint32_t idesc = (1u << 4) | ((TRANS ? 0u : 1u) << 16) | ((uint32_t)(kTn >> 3) << 17) |
                            ((uint32_t)(kTm >> 4) << 24);
+    int last_b[2] = {-1, -1};            // thread 0: last chunk whose B copy was issued, per stage
+    auto issue_b = [&](int kc) {         // thread 0: TMA of chunk kc's B tile into stage kc % 2
+        const int st = kc & 1;
+        last_b[st] = kc;
+        uint8_t *Bm = smem + st * kStage + kABytes;
+        mbar_expect_tx(&bfull[st], kBBytes);
+        if (TRANS) {
+            tma_load_2d(Bm, &r_map, kc * kKc, j0, &bfull[st]);
+        } else {
+            for (int atom = 0; atom < kTn / 64; ++atom)
+                tma_load_2d(Bm + atom * (kKc * 128), &r_map, j0 + 64 * atom, kc * kKc, &bfull[st]);
+        }
+    };
+    if (tid == 0) issue_b(0);
     bool ok = true;
     for (int kc = 0; kc < kK / kKc; ++kc) {
         const int st = kc & 1;
         uint8_t *A = smem + st * kStage, *Bm = A + kABytes;
+        // the stage's previous MMAs (chunk kc - 2) are done
         if (kc >= 2 && !__syncthreads_and(mbar_wait_bounded(&bar[st], ((kc - 2) >> 1) & 1, abort_flag,
                                                            rp.status, FLAG_TIMEOUT, kTimeoutNs))) {
             ok = false;
             break;
         }
         tc_fence_after();
+        // the next chunk's B tile goes into the other stage, whose MMAs (chunk kc - 1)
+        // must be done first
+        if (tid == 0 && kc + 1 < kK / kKc) {
+            if (kc >= 1 && !mbar_wait_bounded(&bar[st ^ 1], ((kc - 1) >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
+                                              kTimeoutNs))
+                ok = false;
+            else
+                issue_b(kc + 1);
+        }
         // A: rows m0.., k = 64 kc + 8 ch .. +7 -> fp16, K-major swizzled
         for (int job = tid; job < kTm * 8; job += kThreads) {
             const int r = job >> 3, ch = job & 7, m = m0 + r;
@@ -113,36 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const RotParams r
             }
             *(uint4 *)(A + sw128(r, ch)) = pack8_f16(v);
         }
-        // B: fp16 copy of the R elements this chunk needs
-        for (int job = tid; job < kTn * 8; job += kThreads) {
-            float v[8];
-            if (TRANS) {
-                // B[j][k] = R[j][k]: K-major, row j, chunk ch
-                const int j = job >> 3, ch = job & 7;
-                const float *src = rp.R + (size_t)(j0 + j) * kK + kc * kKc + 8 * ch;
-                const float4 a = *(const float4 *)src, b = *(const float4 *)(src + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-                *(uint4 *)(Bm + sw128(j, ch)) = pack8_f16(v);
-            } else {
-                // B[j][k] = R[k][j]: MN-major, 64-j atoms of [64 k rows x 128 B]
-                const int k = job & 63, rest = job >> 6, atom = rest >> 3, ch = rest & 7;
-                const float *src = rp.R + (size_t)(kc * kKc + k) * kK + j0 + 64 * atom + 8 * ch;
-                const float4 a = *(const float4 *)src, b = *(const float4 *)(src + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-                *(uint4 *)(Bm + atom * (kKc * 128) + sw128(k, ch)) = pack8_f16(v);
-            }
-        }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
         if (tid == 0) {
+            ok = mbar_wait_bounded(&bfull[st], (kc >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs);
             tc_fence_after();
             const uint64_t a0 = sdesc(smem_u32(A), 16, 1024);
             const uint64_t b0 = TRANS ? sdesc(smem_u32(Bm), 16, 1024) : sdesc(smem_u32(Bm), kKc * 128, 1024);
+            if (ok) {
 #pragma unroll
-            for (int kk = 0; kk < kKc / 16; ++kk) {
-                const uint64_t bd = b0 + (uint64_t)((TRANS ? 32 * kk : 2048 * kk) >> 4);
-                mma_ss(tmem, a0 + (uint64_t)((32 * kk) >> 4), bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kKc / 16; ++kk) {
+                    const uint64_t bd = b0 + (uint64_t)((TRANS ? 32 * kk : 2048 * kk) >> 4);
+                    mma_ss(tmem, a0 + (uint64_t)((32 * kk) >> 4), bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                }
             }
             mma_commit(&bar[st]);
         }
@@ -153,6 +184,15 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const RotParams r
         ok = mbar_wait_bounded(&bar[last & 1], (last >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs) &&
              mbar_wait_bounded(&bar[(last - 1) & 1], ((last - 1) >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
                                kTimeoutNs);
+    } else if (tid == 0) {
+        // never leave a B copy in flight into this CTA's shared memory: a stage's
+        // earlier copies landed before its later one was issued, so waiting for the
+        // last one of each stage is enough (bounded, and regardless of the abort flag)
+        int32_t *no_abort = abort_flag + 1;   // a flag of its own in the barrier area
+        *no_abort = 0;
+        for (int st = 0; st < 2; ++st)
+            if (last_b[st] >= 0)
+                mbar_wait_bounded(&bfull[st], (last_b[st] >> 1) & 1, no_abort, nullptr, 0, kTimeoutNs);
     }
     ok = __syncthreads_and(ok);
     tc_fence_after();
@@ -204,18 +244,42 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const RotParams r
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTn) : "memory");
     }
 }
 
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
 template <bool X_FP32, bool TRANS, bool Y_F16>
-static cudaError_t launch_t(const RotParams &rp, cudaStream_t st) {
+static cudaError_t launch_t(const __half *R16, const RotParams &rp, cudaStream_t st) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    CUtensorMap map;
+    memset(&map, 0, sizeof map);
+    cuuint64_t dims[2] = {(cuuint64_t)kK, (cuuint64_t)kK};
+    cuuint64_t strides[1] = {(cuuint64_t)kK * 2};
+    cuuint32_t box[2] = {64, TRANS ? (cuuint32_t)kTn : 64u};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(R16), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(rot_gemm_kernel<X_FP32, TRANS, Y_F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((rp.M + kTm - 1) / kTm, kK / kTn);
-    rot_gemm_kernel<X_FP32, TRANS, Y_F16><<<grid, kThreads, kSmemBytes, st>>>(rp);
-    return cudaGetLastError();
+    return launch_pdl(rot_gemm_kernel<X_FP32, TRANS, Y_F16>, grid, dim3(kThreads), kSmemBytes, st, map, rp);
 }
 
 // Merge the split partials of each (b, i, h) row into o_rot[(b * q_len + i) * H + h]
@@ -274,21 +338,24 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(CombineParams c, float 
 
 bool rot_tc_supported(const ShapeArgs &s) { return s.r == rot::kK; }
 
-cudaError_t launch_rot_query(const float *R, const void *q_bf16, void *q_rot_f16, int rows, int D, int32_t *status,
-                             cudaStream_t st) {
+cudaError_t launch_rot_query(const float *R, __half *R16, const void *q_bf16, void *q_rot_f16, int rows, int D,
+                             int32_t *status, cudaStream_t st) {
+    const int n8 = rot::kK * rot::kK / 8;
+    rot::r_to_f16_kernel<<<(n8 + 255) / 256, 256, 0, st>>>(R, R16, n8);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     rot::RotParams rp;
     rp.X = q_bf16;
     rp.ldx = D;
-    rp.R = R;
     rp.Y = q_rot_f16;
     rp.ldy = D;
     rp.M = rows;
     rp.copy_rope = D - rot::kK;
     rp.status = status;
-    return rot::launch_t<false, false, true>(rp, st);
+    return rot::launch_t<false, false, true>(R16, rp, st);
 }
 
-cudaError_t launch_rot_output(const CombineParams &c, const float *R, float *o_rot, float *o_lat, float *lse2,
+cudaError_t launch_rot_output(const CombineParams &c, const __half *R16, float *o_rot, float *o_lat, float *lse2,
                               int32_t *ident, int32_t *status, cudaStream_t st) {
     const int rows = c.B * c.q_len * c.s.H;
     rot::merge_rows_kernel<<<min((rows + 7) / 8, 4096), 256, 0, st>>>(c, o_rot, lse2, ident);
@@ -297,13 +364,12 @@ cudaError_t launch_rot_output(const CombineParams &c, const float *R, float *o_r
     rot::RotParams rp;
     rp.X = o_rot;
     rp.ldx = rot::kK;
-    rp.R = R;
     rp.Y = o_lat;
     rp.ldy = rot::kK;
     rp.M = rows;
     rp.copy_rope = 0;
     rp.status = status;
-    return rot::launch_t<true, true, false>(rp, st);
+    return rot::launch_t<true, true, false>(R16, rp, st);
 }
 
 }  // namespace mla
