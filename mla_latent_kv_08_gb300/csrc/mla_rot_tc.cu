@@ -6,7 +6,10 @@
 // GEMM's B tiles come from R16 by TMA, the A tiles (bf16 query rows or fp32
 // merged outputs) are converted to fp16 by the threads that stage them in
 // shared memory, and the MMA accumulates in fp32 in tensor memory. A CTA
-// computes a [128 x 128] tile of Y over eight 64-wide K chunks, double-buffered.
+// computes a [128 x 128] tile of Y over eight 64-wide K chunks: warps 1..7 convert
+// the whole A tile into shared memory chunk by chunk (one chunk of loads in flight
+// ahead), while warp 0 streams B through four stages and issues each chunk's MMAs
+// as soon as its A and B are there.
 //
 // Also here: the merge of split partials into one latent row per (sequence,
 // draft position, head), which precedes the second rotation.
@@ -22,15 +25,20 @@ namespace rot {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                   // warp 0: TMA + MMA issue; warps 1..7 convert A
+constexpr int kConvThreads = kThreads - 32;
 constexpr int kK = 512;                         // kv_lora_rank
 constexpr int kTm = 128, kTn = 128, kKc = 64;   // tile M, tile N, K chunk
-constexpr uint32_t kABytes = kTm * 128;         // [128 rows x 64 k] fp16
-constexpr uint32_t kBBytes = kTn * 128;         // [128 j x 64 k] fp16 (either layout)
-constexpr uint32_t kStage = kABytes + kBBytes;  // 32 KB
-constexpr uint32_t kOffBar = 2 * kStage;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
+constexpr int kChunks = kK / kKc;               // 8
+constexpr int kBStages = 4;
+constexpr uint32_t kABytes = kTm * 128;         // one chunk of A: [128 rows x 64 k] fp16
+constexpr uint32_t kBBytes = kTn * 128;         // one chunk of B: [128 j x 64 k] fp16 (either layout)
+constexpr uint32_t kOffA = 0;                   // all of A: 8 chunks, 128 KB
+constexpr uint32_t kOffB = kChunks * kABytes;   // kBStages B stages, 64 KB
+constexpr uint32_t kOffBar = kOffB + kBStages * kBBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr int kJobsPerConv = (kTm * 8 + kConvThreads - 1) / kConvThreads;   // 16-byte A chunks per thread
 
 struct RotParams {
     const void *X;
@@ -69,18 +77,23 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const __grid_cons
     const int m0 = blockIdx.x * kTm, j0 = blockIdx.y * kTn;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bar = (uint64_t *)(smem + kOffBar);        // [2] MMA done per stage
-    uint64_t *bfull = bar + 2;                           // [2] B tile landed per stage
-    uint32_t *tmem_slot = (uint32_t *)(bar + 4);
-    int32_t *abort_flag = (int32_t *)(bar + 5);
+    uint64_t *a_full = (uint64_t *)(smem + kOffBar);     // [kChunks] A chunk converted
+    uint64_t *b_full = a_full + kChunks;                 // [kBStages] B tile landed
+    uint64_t *b_free = b_full + kBStages;                // [kBStages] MMAs reading the stage done
+    uint64_t *mma_fin = b_free + kBStages;
+    uint32_t *tmem_slot = (uint32_t *)(mma_fin + 1);
+    int32_t *abort_flag = (int32_t *)(mma_fin + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar[i], 1);
-            mbar_init(&bfull[i], 1);
+        for (int i = 0; i < kChunks; ++i) mbar_init(&a_full[i], kConvThreads);
+        for (int i = 0; i < kBStages; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_free[i], 1);
         }
-        *abort_flag = 0;
+        mbar_init(mma_fin, 1);
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -94,56 +107,101 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_wait();
-    // fp16 A and B, fp32 D, M 128, N 128; B MN-major for op(R) = R (R's rows are k)
-    const uint32_t idesc = (1u << 4) | ((TRANS ? 0u : 1u) << 16) | ((uint32_t)(kTn >> 3) << 17) |
-                           ((uint32_t)(kTm >> 4) << 24);
-    int last_b[2] = {-1, -1};            // thread 0: last chunk whose B copy was issued, per stage
-    auto issue_b = [&](int kc) {         // thread 0: TMA of chunk kc's B tile into stage kc % 2
-        const int st = kc & 1;
-        last_b[st] = kc;
-        uint8_t *Bm = smem + st * kStage + kABytes;
-        mbar_expect_tx(&bfull[st], kBBytes);
-        if (TRANS) {
-            tma_load_2d(Bm, &r_map, kc * kKc, j0, &bfull[st]);
-        } else {
-            for (int atom = 0; atom < kTn / 64; ++atom)
-                tma_load_2d(Bm + atom * (kKc * 128), &r_map, j0 + 64 * atom, kc * kKc, &bfull[st]);
-        }
-    };
-    if (tid == 0) issue_b(0);
-    bool ok = true;
-    for (int kc = 0; kc < kK / kKc; ++kc) {
-        const int st = kc & 1;
-        uint8_t *A = smem + st * kStage, *Bm = A + kABytes;
-        // the stage's previous MMAs (chunk kc - 2) are done
-        if (kc >= 2 && !__syncthreads_and(mbar_wait_bounded(&bar[st], ((kc - 2) >> 1) & 1, abort_flag,
-                                                           rp.status, FLAG_TIMEOUT, kTimeoutNs))) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        // the next chunk's B tile goes into the other stage, whose MMAs (chunk kc - 1)
-        // must be done first
-        if (tid == 0 && kc + 1 < kK / kKc) {
-            if (kc >= 1 && !mbar_wait_bounded(&bar[st ^ 1], ((kc - 1) >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
-                                              kTimeoutNs))
-                ok = false;
-            else
-                issue_b(kc + 1);
-        }
-        // A: rows m0.., k = 64 kc + 8 ch .. +7 -> fp16, K-major swizzled
-        for (int job = tid; job < kTm * 8; job += kThreads) {
-            const int r = job >> 3, ch = job & 7, m = m0 + r;
-            float v[8];
-            if (m < rp.M) {
-                const size_t base = (size_t)m * rp.ldx + kc * kKc + 8 * ch;
-                if (X_FP32) {
-                    const float4 a = *(const float4 *)((const float *)rp.X + base);
-                    const float4 b = *(const float4 *)((const float *)rp.X + base + 4);
-                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    if (warp == 0) {
+        if (lane == 0) {
+            // fp16 A and B, fp32 D, M 128, N 128; B MN-major for op(R) = R (R's rows are k)
+            const uint32_t idesc = (1u << 4) | ((TRANS ? 0u : 1u) << 16) | ((uint32_t)(kTn >> 3) << 17) |
+                                   ((uint32_t)(kTm >> 4) << 24);
+            int last_b[kBStages];
+            auto issue_b = [&](int kc) {     // TMA of chunk kc's B tile into stage kc % kBStages
+                const int st = kc % kBStages;
+                uint8_t *Bm = smem + kOffB + st * kBBytes;
+                last_b[st] = kc;
+                mbar_expect_tx(&b_full[st], kBBytes);
+                if (TRANS) {
+                    tma_load_2d(Bm, &r_map, kc * kKc, j0, &b_full[st]);
                 } else {
-                    const uint4 u = *(const uint4 *)((const __nv_bfloat16 *)rp.X + base);
-                    const __nv_bfloat162 *h = (const __nv_bfloat162 *)&u;
+                    for (int atom = 0; atom < kTn / 64; ++atom)
+                        tma_load_2d(Bm + atom * (kKc * 128), &r_map, j0 + 64 * atom, kc * kKc, &b_full[st]);
+                }
+            };
+            for (int st = 0; st < kBStages; ++st) {
+                last_b[st] = -1;
+                if (st < kChunks) issue_b(st);
+            }
+            bool ok = true;
+            for (int kc = 0; kc < kChunks && ok; ++kc) {
+                const int st = kc % kBStages;
+                ok = mbar_wait_bounded(&a_full[kc], 0, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs) &&
+                     mbar_wait_bounded(&b_full[st], (kc / kBStages) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
+                                       kTimeoutNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t a0 = sdesc(smem_u32(smem + kOffA + kc * kABytes), 16, 1024);
+                const uint8_t *Bm = smem + kOffB + st * kBBytes;
+                const uint64_t b0 = TRANS ? sdesc(smem_u32(Bm), 16, 1024) : sdesc(smem_u32(Bm), kKc * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kKc / 16; ++kk) {
+                    const uint64_t bd = b0 + (uint64_t)((TRANS ? 32 * kk : 2048 * kk) >> 4);
+                    mma_ss(tmem, a0 + (uint64_t)((32 * kk) >> 4), bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&b_free[st]);
+                if (kc + kBStages < kChunks) {      // refill the stage once its MMAs are done
+                    ok = mbar_wait_bounded(&b_free[st], (kc / kBStages) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
+                                           kTimeoutNs);
+                    if (ok) issue_b(kc + kBStages);
+                }
+            }
+            mma_commit(mma_fin);
+            if (!ok) {
+                // never leave a B copy in flight into this CTA's shared memory: a stage's
+                // earlier copies landed before its later one was issued, so waiting for
+                // the last one of each stage is enough (bounded, regardless of the abort)
+                for (int st = 0; st < kBStages; ++st)
+                    if (last_b[st] >= 0)
+                        mbar_wait_bounded(&b_full[st], (last_b[st] / kBStages) & 1, abort_flag + 1, nullptr, 0,
+                                          kTimeoutNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // A: rows m0.., k = 64 kc + 8 ch .. +7 -> fp16, K-major swizzled; the next
+        // chunk's loads are issued before this chunk is converted and stored
+        const int ct = tid - 32;
+        uint4 ra[kJobsPerConv][2], rb[kJobsPerConv][2];
+        auto load = [&](int kc, uint4 (&r)[kJobsPerConv][2]) {
+#pragma unroll
+            for (int i = 0; i < kJobsPerConv; ++i) {
+                const int job = ct + kConvThreads * i, row = job >> 3, ch = job & 7, m = m0 + row;
+                r[i][0] = make_uint4(0, 0, 0, 0);
+                r[i][1] = make_uint4(0, 0, 0, 0);
+                if (job < kTm * 8 && m < rp.M) {
+                    const size_t base = (size_t)m * rp.ldx + kc * kKc + 8 * ch;
+                    if (X_FP32) {
+                        r[i][0] = *(const uint4 *)((const float *)rp.X + base);
+                        r[i][1] = *(const uint4 *)((const float *)rp.X + base + 4);
+                    } else {
+                        r[i][0] = *(const uint4 *)((const __nv_bfloat16 *)rp.X + base);
+                    }
+                }
+            }
+        };
+        auto store = [&](int kc, const uint4 (&r)[kJobsPerConv][2]) {
+            uint8_t *A = smem + kOffA + kc * kABytes;
+#pragma unroll
+            for (int i = 0; i < kJobsPerConv; ++i) {
+                const int job = ct + kConvThreads * i, row = job >> 3, ch = job & 7;
+                if (job >= kTm * 8) continue;
+                float v[8];
+                if (X_FP32) {
+                    const float *f0 = (const float *)&r[i][0], *f1 = (const float *)&r[i][1];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[e] = f0[e];
+                        v[4 + e] = f1[e];
+                    }
+                } else {
+                    const __nv_bfloat162 *h = (const __nv_bfloat162 *)&r[i][0];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = __bfloat1622float2(h[e]);
@@ -151,49 +209,22 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const __grid_cons
                         v[2 * e + 1] = f.y;
                     }
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                *(uint4 *)(A + sw128(row, ch)) = pack8_f16(v);
             }
-            *(uint4 *)(A + sw128(r, ch)) = pack8_f16(v);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        if (!__syncthreads_and(ok)) {
-            ok = false;
-            break;
-        }
-        if (tid == 0) {
-            ok = mbar_wait_bounded(&bfull[st], (kc >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs);
-            tc_fence_after();
-            const uint64_t a0 = sdesc(smem_u32(A), 16, 1024);
-            const uint64_t b0 = TRANS ? sdesc(smem_u32(Bm), 16, 1024) : sdesc(smem_u32(Bm), kKc * 128, 1024);
-            if (ok) {
-#pragma unroll
-                for (int kk = 0; kk < kKc / 16; ++kk) {
-                    const uint64_t bd = b0 + (uint64_t)((TRANS ? 32 * kk : 2048 * kk) >> 4);
-                    mma_ss(tmem, a0 + (uint64_t)((32 * kk) >> 4), bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-                }
-            }
-            mma_commit(&bar[st]);
+            fence_proxy_async();
+            mbar_arrive(&a_full[kc]);
+        };
+        load(0, ra);
+        for (int kc = 0; kc < kChunks; kc += 2) {
+            load(kc + 1, rb);
+            store(kc, ra);
+            if (kc + 2 < kChunks) load(kc + 2, ra);
+            store(kc + 1, rb);
         }
     }
-    // the last two chunks' MMAs (stages 0 and 1 of the final round)
-    if (ok) {
-        const int last = kK / kKc - 1;
-        ok = mbar_wait_bounded(&bar[last & 1], (last >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs) &&
-             mbar_wait_bounded(&bar[(last - 1) & 1], ((last - 1) >> 1) & 1, abort_flag, rp.status, FLAG_TIMEOUT,
-                               kTimeoutNs);
-    } else if (tid == 0) {
-        // never leave a B copy in flight into this CTA's shared memory: a stage's
-        // earlier copies landed before its later one was issued, so waiting for the
-        // last one of each stage is enough (bounded, and regardless of the abort flag)
-        int32_t *no_abort = abort_flag + 1;   // a flag of its own in the barrier area
-        *no_abort = 0;
-        for (int st = 0; st < 2; ++st)
-            if (last_b[st] >= 0)
-                mbar_wait_bounded(&bfull[st], (last_b[st] >> 1) & 1, no_abort, nullptr, 0, kTimeoutNs);
-    }
+    // everyone: the MMAs are done (or the CTA gave up)
+    bool ok = mbar_wait_bounded(mma_fin, 0, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs) &&
+              *(volatile int32_t *)abort_flag == 0;
     ok = __syncthreads_and(ok);
     tc_fence_after();
     if (warp < 4) {
