@@ -154,6 +154,7 @@ struct Bars {
     uint64_t mma_fin;
     uint64_t xchg_full;       // both halves of every row wrote their value
     uint64_t xchg_read;       // both halves read the other's value
+    uint64_t tail_done[kStages];  // bf16: the producer zeroed a partial tile's slots past the end
     uint64_t raw_full;        // INT2: raw block landed
     uint64_t raw_empty;       // INT2: raw block expanded
     uint32_t tmem_base;
@@ -229,6 +230,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->full[s], kInt2 ? kDequantThreads : 1);
             mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->tail_done[s], 1);
         }
         mbar_init(&bars->raw_full, 1);
         mbar_init(&bars->raw_empty, kDequantThreads);
@@ -302,6 +304,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         for (int i = i0; i < i1 && ok; ++i) {
             const WorkItem it = p.work[i];
             const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+            const int L = p.seq_lens[it.b];
             int next_blk = block_of(p, it.b, it.t0 / kTile);     // loaded one tile ahead
             for (int t = 0; t < nt; ++t, ++T) {
                 int blk = next_blk;
@@ -339,6 +342,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     __syncwarp();
                     if (lane < kKvBlocks)
                         tma_load_2d(stage + lane * kKvBlockBytes, &kv_map, lane * 64, blk * kTile, &bars->full[s]);
+                    // a sequence's final partial block: once it has landed, zero the slots
+                    // past the end so that P = 0 never meets stale (possibly non-finite)
+                    // cache bytes; the MMA thread waits for this on partial tiles only
+                    const int valid = min(kTile, L - (it.t0 + t * kTile));
+                    if (valid < kTile) {
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status))) {
+                            ok = false;
+                            break;
+                        }
+                        const int jobs = (kTile - valid) * kKvBlocks * 8;
+                        for (int jb = lane; jb < jobs; jb += 32) {
+                            const int rr = valid + jb / (kKvBlocks * 8), rem = jb % (kKvBlocks * 8);
+                            *(uint4 *)(stage + (rem >> 3) * kKvBlockBytes + sw128(rr, rem & 7)) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->tail_done[s]);
+                    }
                 }
                 if (lane == 0) {                 // L2 prefetch after this tile's own loads
                     MLA_TRACE_POINT(0, T);
@@ -443,15 +464,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             }
         }
     } else if (warp == 1) {
-        // ================================================= MMA issuer (lane 0 issues; the warp
-        // stays converged so that it can zero stale tail slots together)
-        const uint32_t d_o = tmem + kColO;
-        bool ok = true;
-        int T = 0;
-        auto issue_pv = [&](int Tp, bool first_of_item) -> bool {
-            const int pb = Tp & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, p.status))) return false;
-            if (lane == 0) {
+        // ================================================= MMA issuer: lane 0 alone runs
+        // the loop (plain bounded waits, no warp-wide votes or syncs per tile)
+        if (lane == 0) {
+            const uint32_t d_o = tmem + kColO;
+            bool ok = true;
+            int T = 0;
+            uint32_t tail_par = 0;                 // bit s: parity of the partial tiles seen in stage s
+            auto issue_pv = [&](int Tp, bool first_of_item) -> bool {
+                const int pb = Tp & 1;
+                if (!mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, p.status)) return false;
                 tc_fence_after();
                 const int s = Tp % kStages;
                 const uint64_t a0 =
@@ -469,84 +491,68 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 mma_commit(&bars->pv_done[pb]);
                 mma_commit(&bars->empty[s]);
                 MLA_TRACE_POINT(5, Tp);
-            }
-            __syncwarp();
-            return true;
-        };
-        int item_no = 0;
-        for (int i = i0; i < i1 && ok; ++i, ++item_no) {
-            const WorkItem it = p.work[i];
-            const int L = p.seq_lens[it.b];
-            const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_tmem, item_no & 1, bars, p.status))) { ok = false; break; }
-            for (int t = 0; t < nt; ++t, ++T) {
-                const int s = T % kStages;
-                // Wait for this tile's stage; meanwhile issue the previous tile's PV as
-                // soon as its P is ready, so that its stage is released early.
-                bool pv_early = false;
-                if (t > 0) {
-                    const int pbp = (T - 1) & 1;
-                    int st = 0;                  // lane 0's view: 1 = stage landed, 2 = P ready
-                    if (lane == 0) {
+                return true;
+            };
+            int item_no = 0;
+            for (int i = i0; i < i1 && ok; ++i, ++item_no) {
+                const WorkItem it = p.work[i];
+                const int L = p.seq_lens[it.b];
+                const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+                if (!mbar_wait(&bars->q_tmem, item_no & 1, bars, p.status)) { ok = false; break; }
+                for (int t = 0; t < nt; ++t, ++T) {
+                    const int s = T % kStages;
+                    // Wait for this tile's stage; meanwhile issue the previous tile's PV as
+                    // soon as its P is ready, so that its stage is released early.
+                    bool pv_early = false;
+                    if (t > 0) {
+                        const int pbp = (T - 1) & 1;
+                        int st = 0;                  // 1 = stage landed, 2 = P ready
                         const unsigned long long tw0 = globaltimer();
                         for (uint32_t it2 = 0;; ++it2) {
                             if (mbar_test(&bars->p_full[pbp], ((T - 1) >> 1) & 1)) { st = 2; break; }
                             if (mbar_test(&bars->full[s], (T / kStages) & 1)) { st = 1; break; }
                             if ((it2 & 63u) == 63u && (aborted(bars) || globaltimer() - tw0 > kTimeoutNs)) break;
                         }
+                        if (st == 2) {
+                            if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
+                            pv_early = true;
+                        }
                     }
-                    st = __shfl_sync(0xffffffffu, st, 0);
-                    if (st == 2) {
-                        if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
-                        pv_early = true;
-                    }
-                }
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status))) { ok = false; break; }
-                if (lane == 0) MLA_TRACE_POINT(1, T);
-                // the S buffer this QK writes was read out by the softmax kSBufs tiles ago
-                if (T >= kSBufs &&
-                    !__all_sync(0xffffffffu, mbar_wait(&bars->s_free[T % kSBufs], ((T - kSBufs) / kSBufs) & 1, bars, p.status))) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) MLA_TRACE_POINT(16, T);
-                // the sequence's final partial block: zero the slots past the end so
-                // that P = 0 never meets stale (possibly non-finite) cache bytes
-                const int tile_start = it.t0 + t * kTile;
-                const int valid = min(kTile, L - tile_start);
-                if (!kInt2 && valid < kTile) {
-                    uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                    const int jobs = (kTile - valid) * kKvBlocks * 8;
-                    for (int jb = lane; jb < jobs; jb += 32) {
-                        const int rr = valid + jb / (kKvBlocks * 8), rem = jb % (kKvBlocks * 8);
-                        *(uint4 *)(stage + (rem >> 3) * kKvBlockBytes + sw128(rr, rem & 7)) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async();
-                    __syncwarp();
-                }
-                // QK(T) in kQkGroups issue groups. PV(T-1) of the same item is
-                // slipped in between groups as soon as its P is ready, so that the
-                // stage it reads is released early; otherwise it follows QK(T).
-                bool pv_pending = t > 0 && !pv_early;
-                const int pb_prev = (T - 1) & 1;
-                if (lane == 0) MLA_TRACE_POINT(20, T);
-                tc_fence_after();
-                if (lane == 0) MLA_TRACE_POINT(21, T);
-                const uint64_t kd = sdesc(smem_u32(smem + kOffStage + s * kStageBytes), 16, 1024);
-                const uint64_t qd = sdesc(smem_u32(smem + kOffQ), 16, 1024);
-                const uint32_t qt = tmem + kColQ;
-                const uint32_t d_s = tmem + kColS + 64 * (T % kSBufs);
-                if (lane == 0) MLA_TRACE_POINT(22, T);
-                constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
-#pragma unroll
-                for (int grp = 0; grp < kQkGroups; ++grp) {
-                    // the item's first tile: its shared-memory Q part may still be landing
-                    if (grp == kFirstSmemGroup && t == 0 &&
-                        !__all_sync(0xffffffffu, mbar_wait(&bars->q_smem, item_no & 1, bars, p.status))) {
+                    if (!mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status)) { ok = false; break; }
+                    MLA_TRACE_POINT(1, T);
+                    // the S buffer this QK writes was read out by the softmax kSBufs tiles ago
+                    if (T >= kSBufs &&
+                        !mbar_wait(&bars->s_free[T % kSBufs], ((T - kSBufs) / kSBufs) & 1, bars, p.status)) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0) {
+                    MLA_TRACE_POINT(16, T);
+                    // a partial tile: the producer zeroes its slots past the end first
+                    if (!kInt2 && min(kTile, L - (it.t0 + t * kTile)) < kTile) {
+                        if (!mbar_wait(&bars->tail_done[s], (tail_par >> s) & 1u, bars, p.status)) { ok = false; break; }
+                        tail_par ^= 1u << s;
+                    }
+                    // QK(T) in kQkGroups issue groups. PV(T-1) of the same item is
+                    // slipped in between groups as soon as its P is ready, so that the
+                    // stage it reads is released early; otherwise it follows QK(T).
+                    bool pv_pending = t > 0 && !pv_early;
+                    const int pb_prev = (T - 1) & 1;
+                    MLA_TRACE_POINT(20, T);
+                    tc_fence_after();
+                    MLA_TRACE_POINT(21, T);
+                    const uint64_t kd = sdesc(smem_u32(smem + kOffStage + s * kStageBytes), 16, 1024);
+                    const uint64_t qd = sdesc(smem_u32(smem + kOffQ), 16, 1024);
+                    const uint32_t qt = tmem + kColQ;
+                    const uint32_t d_s = tmem + kColS + 64 * (T % kSBufs);
+                    MLA_TRACE_POINT(22, T);
+                    constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
+#pragma unroll
+                    for (int grp = 0; grp < kQkGroups; ++grp) {
+                        // the item's first tile: its shared-memory Q part may still be landing
+                        if (grp == kFirstSmemGroup && t == 0 && !mbar_wait(&bars->q_smem, item_no & 1, bars, p.status)) {
+                            ok = false;
+                            break;
+                        }
                         // K-step j: column block j/4, 32-byte step j%4 inside the swizzle
                         // atom; descriptor start addresses advance in 16-byte units.
 #pragma unroll
@@ -566,28 +572,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                                     d_s, qd + (uint64_t)((((j >> 2) - kQTmemBlocks) * kQBlockBytes + 32 * (j & 3)) >> 4), bd);
                             }
                         }
-                    }
-                    __syncwarp();
-                    if (lane == 0) MLA_TRACE_POINT(10 + grp, T);
-                    if (MLA_PV_SLIP && pv_pending && grp < kQkGroups - 1) {
-                        const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_test(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1) : 0, 0);
-                        if (ready) {
+                        MLA_TRACE_POINT(10 + grp, T);
+                        if (MLA_PV_SLIP && pv_pending && grp < kQkGroups - 1 &&
+                            mbar_test(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1)) {
                             if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
                             pv_pending = false;
                         }
                     }
-                }
-                if (!ok) break;
-                if (lane == 0) {
+                    if (!ok) break;
                     mma_commit(&bars->s_full[T % kSBufs]);
                     MLA_TRACE_POINT(2, T);
+                    if (pv_pending && !issue_pv(T - 1, t == 1)) { ok = false; break; }
                 }
-                __syncwarp();
-                if (pv_pending && !issue_pv(T - 1, t == 1)) { ok = false; break; }
+                if (ok && nt > 0 && !issue_pv(T - 1, nt == 1)) ok = false;
             }
-            if (ok && nt > 0 && !issue_pv(T - 1, nt == 1)) ok = false;
-        }
-        if (lane == 0) {
             mma_commit(&bars->mma_fin);
             mbar_wait(&bars->mma_fin, 0, bars, p.status);
         }
