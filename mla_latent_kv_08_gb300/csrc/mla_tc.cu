@@ -1,32 +1,42 @@
 // Tensor-core (tcgen05 / TMEM / TMA) split-KV decode for the DeepSeek-V3 latent
-// shape: kv_lora_rank 512, rope 64, bf16 cache, block size 64.
+// shape: kv_lora_rank 512, rope 64, block size 64; bf16 cache, or the rotated-INT2
+// cache expanded into fp16 operands on the fly.
 //
-// Work decomposition. A work item is a token range [t0, t1) of one sequence
-// (from the planner) times a tile of 128 query rows (a row is a (draft
-// position, head) pair). Each work item runs on TWO CTAs that read the same
-// KV tiles; CTA `half` owns latent output dims [256*half, 256*half + 256).
-// The fp32 latent output of 128 rows x 512 dims alone is the whole 512-column
-// tensor memory of an SM, so the output is split across the pair and each CTA
-// computes the scores S = Q K^T on its own (the pair shares the KV tiles
-// through L2).
+// Work decomposition. The planner cuts the concatenated 64-token tiles of all
+// sequences into equal runs ("streams"); a work item is one sequence's part of
+// one stream, times a tile of 128 query rows (a row is a (draft position, head)
+// pair). Each stream runs on a persistent pair of CTAs that read the same KV
+// tiles; CTA `half` owns latent output dims [256*half, 256*half + 256). The fp32
+// latent output of 128 rows x 512 dims alone is the whole 512-column tensor
+// memory of an SM, so the output is split across the pair and each CTA computes
+// the scores S = Q K^T on its own (the pair shares the KV tiles through L2).
 //
 // Per CTA, per 64-token tile (one cache block):
-//   TMA     9 loads of [64 tokens x 64 dims] bf16, 128B-swizzled, into a stage
-//   MMA     S[128 x 64]  = Q[128 x 576] . K[64 x 576]^T   (36 x M128 N64 K16)
-//           Q dims 0..383 are read from tensor memory, 384..575 from smem
-//   softmax one thread per row: tcgen05.ld of S, scale, causal/length mask,
-//           running max in log2 units with a lazy rescale (only when the max
-//           grows by more than 8, so P <= 2^8), P -> bf16 smem (swizzled)
+//   TMA     9 loads of [64 tokens x 64 dims], 128B-swizzled, into a stage (INT2:
+//           a bulk copy of the block's codes, scale/zero pairs and rope keys,
+//           expanded into the stage by six dequantising warps)
+//   MMA     S[128 x 64]  = Q[128 x 576] . K[64 x 576]^T   (36 x M128 N64 K16, in
+//           two issue groups; the first K-steps read Q from tensor memory)
+//   softmax two warps per 32-row lane quarter, one per half of the tile's
+//           columns: tcgen05.ld of S, causal/length mask, row max shared through
+//           an mbarrier exchange, running max in log2 units with a lazy rescale
+//           (only when the max grows by more than 8, so P <= 2^8), P -> the two
+//           stage blocks only QK reads (swizzled)
 //   MMA     O[128 x 256] += P[128 x 64] . V[64 x 256]     (4 x M128 N256 K16)
-//           V is the same smem tile read as an MN-major operand
-// Epilogue: O / l to the fp32 partial buffer, log2-sum-exp to the partial LSE;
-// the shared combine kernel merges splits and applies W_UV.
+//           V is the same smem tile read as an MN-major operand; PV(T-1) is
+//           slipped between the QK groups of tile T as soon as P(T-1) is ready
+// Per work item: Q arrives by TMA (its tensor-memory part staged through the Q
+// region of shared memory); the epilogue writes O / l to the fp32 partial
+// buffer by TMA stores and the log2-sum-exp to the partial LSE; the combine
+// kernel merges splits and applies W_UV.
 //
-// Tensor memory columns: O [0,256), S [256,320), Q dims 0..383 [320,512).
-// Roles (256 threads): warp 0 lane 0 = TMA producer; warp 1 = TMEM owner, its
-// lane 0 issues MMAs; warps 4..7 = softmax / correction / epilogue (warp w
-// reads TMEM lanes 32*(w%4)..+31). All waits are bounded: a wait that gives up
-// records FLAG_TIMEOUT and the CTA winds down without trapping.
+// Tensor memory columns: O [0,256), S [256,256+64*kSBufs), Q after S.
+// Roles: warp 0 = TMA producer (+ L2 prefetch, + zeroing of a partial tile's
+// slots past the end); warp 1 = TMEM owner, its lane 0 runs the MMA loop; warps
+// 2,3 (+12..15 for INT2) = dequantisers; warps 4..11 = Q loads, softmax,
+// correction and epilogue (warp w reads TMEM lanes 32*(w%4)..+31). All waits are
+// bounded: a wait that gives up records FLAG_TIMEOUT and the CTA winds down
+// without trapping.
 #include "mla_internal.cuh"
 #include "mla_ptx.cuh"
 

@@ -180,6 +180,64 @@ def test_int2_append_and_decode_small(gpu_lib, impl_name, H):
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+# ------------------------------------------------------------ stale pool bytes
+
+def _pool_fill(cache, value):
+    """Every pool byte set: latent/rope/scale_zero to `value`, codes to 0xFF or 0."""
+    import math
+    for name in ("latent", "rope", "scale_zero"):
+        t = getattr(cache, name, None)
+        if t is not None:
+            t.fill_(value)
+    if getattr(cache, "codes", None) is not None:
+        cache.codes.fill_(0xFF if math.isnan(value) else 0)
+
+
+@pytest.mark.parametrize("impl_name", ["tcgen05", "simt"])
+def test_stale_slots_past_the_end_do_not_leak(gpu_lib, impl_name):
+    """The slots of a sequence's last block past its length hold whatever the pool
+    held before (here NaN): the result must equal the one over a zero-filled pool,
+    bit for bit, and be finite (P = 0 must never meet the stale bytes)."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w = workloads.dsv3(21, B=4, H=128, len_range=(70, 700))
+    assert np.any(w.seq_lens % 64 != 0)
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    shape = gu.shape_for(w, impl=impl)
+    res = []
+    for fill in (0.0, float("nan")):
+        cache = mla.Cache.allocate(shape, zero=False)
+        _pool_fill(cache, fill)
+        gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32))
+        torch.cuda.synchronize()
+        res.append(gu.attend(w, shape, cache, w.q)[:2])
+    (o0, l0), (o1, l1) = res
+    assert np.isfinite(o1).all() and np.isfinite(l1).all()
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+
+
+def test_int2_stale_slots_past_the_end_do_not_leak(gpu_lib):
+    """As above for the rotated-INT2 cache on the tensor cores (NaN scale/zero and
+    rope bytes, 0xFF codes in the stale slots)."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=3, H=32, len_range=(40, 300))
+    assert np.any(w.seq_lens % 64 != 0)
+    shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT, impl=mla.MLA_IMPL_TCGEN05)
+    res = []
+    for fill in (0.0, float("nan")):
+        cache = mla.Cache.allocate(shape, zero=False)
+        _pool_fill(cache, fill)
+        gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32), R32, T32)
+        torch.cuda.synchronize()
+        res.append(gu.attend(w, shape, cache, w.q, R=R32)[:2])
+    (o0, l0), (o1, l1) = res
+    assert np.isfinite(o1).all() and np.isfinite(l1).all()
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+
+
 # ------------------------------------------------------------ device checks
 
 def test_bad_block_id_sets_flag_and_nan_rows(gpu_lib):
