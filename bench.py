@@ -51,6 +51,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, world, device=None):
+    """Each timing's maximum over the ranks: the slowest rank sets the job's time."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(tokens_per_rank, world, step_ms):
+    """Whole-job KV-tokens/s: every rank decodes its own copy of the workload (weak
+    scaling), all within the slowest rank's step time."""
+    return tokens_per_rank * world / (step_ms * 1e-3)
+
+
 # ------------------------------------------------------------------ accounting
 
 def workload_config(w):
@@ -378,11 +395,9 @@ def run_gb300(args):
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
 
     if world > 1:
-        tt = torch.tensor([step_ms, att_avg_ms, e2e["ms"] if e2e else 0.0], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms, att_avg_ms = float(tt[0]), float(tt[1])
+        step_ms, att_avg_ms, e2e_max = max_over_ranks([step_ms, att_avg_ms, e2e["ms"] if e2e else 0.0], world, dev)
         if e2e:
-            e2e["ms"] = float(tt[2])
+            e2e["ms"] = e2e_max
 
     if rank != 0:
         if world > 1:
@@ -392,7 +407,7 @@ def run_gb300(args):
     kb, sb, kf, sf = algorithmic(w)
     peaks = load_peaks()
     tokens = w.total_tokens * world
-    value = tokens / (step_ms * 1e-3)
+    value = job_throughput(w.total_tokens, world, step_ms)
     achieved = kb / (att_avg_ms * 1e-3) / 1e9
     kernel_name = {mla.MLA_IMPL_SIMT: "decode_simt_kernel", mla.MLA_IMPL_TCGEN05: "decode_tc_kernel"}[
         mla.mla_resolve_impl(shape, 1)]
