@@ -213,6 +213,17 @@ mla_status mla_profile_enable(int32_t enable);
 mla_status mla_profile_read(double *attention_ms, int32_t *attention_launches,
                             int32_t *kernel_launches);
 
+/* Self-test of the device-side failure detection (diagnostic; no attention).
+ * Launches one small kernel on `stream` that waits, with the same bounded
+ * mbarrier wait the attention kernels use, on a barrier that nothing arrives on;
+ * after `timeout_ns` the wait gives up, sets its CTA's abort flag and ORs the
+ * timeout flag into the device word `status` (a caller-owned int32, zeroed by
+ * the kernel first), and the kernel returns normally, leaving the context usable.
+ * Read the outcome with mla_read_status_word (MLA_ERR_TIMEOUT expected).
+ * timeout_ns must be in [1000, 100000000] (1 us .. 100 ms), else
+ * MLA_ERR_INVALID; MLA_ERR_CUDA if the launch fails. */
+mla_status mla_selftest_wait_timeout(uint64_t timeout_ns, int32_t *status, void *stream);
+
 /* Library ABI version (major * 100 + minor). */
 int32_t mla_version(void);
 

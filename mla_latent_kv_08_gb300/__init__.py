@@ -38,7 +38,7 @@ MLA_IMPL_TCGEN05 = 2
 EXPORTED = (
     "mla_workspace_bytes", "mla_latent_append", "mla_decode", "mla_verify", "mla_get_status",
     "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
-    "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc",
+    "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc", "mla_selftest_wait_timeout",
 )
 
 
@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_version.restype = i32
     lib.mla_decode_noalloc.argtypes = [sp, cp, vp, i32, vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
     lib.mla_decode_noalloc.restype = i32
+    lib.mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
+    lib.mla_selftest_wait_timeout.restype = i32
     lib.mla_profile_enable.argtypes = [i32]
     lib.mla_profile_enable.restype = i32
     lib.mla_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), i32p, i32p]
@@ -257,6 +259,12 @@ def mla_read_status_word(status, stream=None):
     flags = ctypes.c_int32(0)
     code = load_library().mla_read_status_word(_ptr(status), ctypes.byref(flags), _stream(stream))
     return int(code), int(flags.value)
+
+
+def mla_selftest_wait_timeout(timeout_ns: int, status, stream=None) -> None:
+    """Launch the bounded-wait self-test (see mla.h); read `status` afterwards."""
+    _check(load_library().mla_selftest_wait_timeout(int(timeout_ns), _ptr(status), _stream(stream)),
+           "mla_selftest_wait_timeout")
 
 
 def mla_resolve_impl(shape: Shape, q_len: int = 1) -> int:

@@ -88,3 +88,11 @@ def test_null_arguments_rejected_before_launch(lib):
                         ctypes.c_float(0.1), None, None, None, 0, None)
     assert rc == mla.MLA_ERR_INVALID
     assert lib.mla_get_status(None, None, None) == mla.MLA_ERR_INVALID
+
+
+def test_selftest_arguments_checked_before_launch(lib):
+    import mla_latent_kv_08_gb300 as mla
+    fake = ctypes.c_void_p(16)                     # never dereferenced: the arguments are refused first
+    assert lib.mla_selftest_wait_timeout(ctypes.c_uint64(2_000_000), None, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_selftest_wait_timeout(ctypes.c_uint64(10), fake, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_selftest_wait_timeout(ctypes.c_uint64(10 ** 9), fake, None) == mla.MLA_ERR_INVALID

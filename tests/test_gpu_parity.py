@@ -180,6 +180,27 @@ def test_int2_append_and_decode_small(gpu_lib, impl_name, H):
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+# ------------------------------------------------------------ failure detection
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable(gpu_lib):
+    """A wait on a barrier that nothing arrives on gives up after its limit, records
+    the timeout flag, and the kernel returns; a decode afterwards is still correct."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    mla.mla_selftest_wait_timeout(2_000_000, status)          # 2 ms
+    code, flags = mla.mla_read_status_word(status)
+    assert code == mla.MLA_ERR_TIMEOUT and flags == 4
+    w = workloads.dsv3(23, B=2, H=128, len_range=(100, 400))
+    shape = gu.shape_for(w)
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, ws = gu.attend(w, shape, cache, w.q)
+    assert mla.mla_get_status(ws) == (mla.MLA_OK, 0)
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 # ------------------------------------------------------------ stale pool bytes
 
 def _pool_fill(cache, value):
