@@ -180,6 +180,25 @@ def test_int2_append_and_decode_small(gpu_lib, impl_name, H):
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+# ------------------------------------------------------------ many sequences
+
+@pytest.mark.parametrize("impl_name", ["tcgen05", "simt"])
+def test_more_sequences_than_one_planner_block(gpu_lib, impl_name):
+    """B = 1100 short sequences (1..100 tokens): the planner's scans run over more than
+    one 1024-wide chunk, streams hold many items; every row matches the oracle."""
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(31, B=1100, H=16, len_range=(1, 100))
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    shape = gu.shape_for(w, impl=impl)
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, ws = gu.attend(w, shape, cache, w.q)
+    assert mla.mla_get_status(ws) == (mla.MLA_OK, 0)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    for b in list(range(0, w.B, 37)) + [w.B - 1]:
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 # ------------------------------------------------------------ failure detection
 
 def test_bounded_wait_gives_up_and_the_context_stays_usable(gpu_lib):
