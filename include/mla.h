@@ -204,7 +204,9 @@ int32_t mla_resolve_impl(const mla_shape *shape, int32_t q_len);
 /* Diagnostics for benchmarking (host state, not thread-safe). While enabled,
  * every decode/verify call records a CUDA event pair on its stream around its
  * main attention kernel, and every entry point counts the kernels it launches.
- * mla_profile_enable(1) (re)starts the record; mla_profile_read waits for the
+ * mla_profile_enable(1) (re)starts the record; mla_profile_enable(2) does the same
+ * but counts launches only (no event pairs between the kernels of a call);
+ * mla_profile_enable(0) stops recording. mla_profile_read waits for the
  * recorded events and returns the summed duration of the attention kernels in
  * milliseconds, their launch count and the total kernel launch count (any
  * output pointer may be NULL). Events are created by the library on first use

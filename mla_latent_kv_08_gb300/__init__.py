@@ -275,8 +275,11 @@ def mla_version() -> int:
     return int(load_library().mla_version())
 
 
-def mla_profile_enable(enable: bool = True) -> None:
-    _check(load_library().mla_profile_enable(1 if enable else 0), "mla_profile_enable")
+def mla_profile_enable(enable=True) -> None:
+    """True / 1: event pairs around attention kernels + launch counts; 2: launch counts
+    only; False / 0: off."""
+    mode = int(enable) if not isinstance(enable, bool) else (1 if enable else 0)
+    _check(load_library().mla_profile_enable(mode), "mla_profile_enable")
 
 
 def mla_profile_read():

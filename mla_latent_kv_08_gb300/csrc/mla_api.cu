@@ -18,6 +18,7 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // ---- benchmarking diagnostics (see mla_profile_enable) ----------------------
 struct Profile {
     bool on = false;
+    bool events = true;       // record the event pairs (mode 1) or only count launches (mode 2)
     int32_t kernels = 0;
     int32_t used = 0;
     static constexpr int kMax = 1 << 14;
@@ -29,7 +30,7 @@ static Profile g_prof;
 
 // Records the start event of the next pair; returns the pair index or -1.
 static int prof_begin(cudaStream_t st) {
-    if (!g_prof.on || g_prof.used >= Profile::kMax) return -1;
+    if (!g_prof.on || !g_prof.events || g_prof.used >= Profile::kMax) return -1;
     const int i = g_prof.used;
     if (i >= g_prof.created) {
         if (cudaEventCreate(&g_prof.start[i]) != cudaSuccess) return -1;
@@ -341,6 +342,7 @@ int32_t mla_resolve_impl(const mla_shape *shape, int32_t q_len) {
 
 mla_status mla_profile_enable(int32_t enable) {
     g_prof.on = enable != 0;
+    g_prof.events = enable != 2;
     g_prof.used = 0;
     g_prof.kernels = 0;
     return MLA_OK;
