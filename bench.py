@@ -43,6 +43,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", action="store_true",
+                    help="time the four parity workloads (one JSON line each) instead of the bench step")
     return ap.parse_args(argv)
 
 
@@ -459,10 +461,88 @@ def run_gb300(args):
     return 0
 
 
+def run_configs(args):
+    """One line per workload: a decode (or verify) call timed as a whole (no event
+    pairs inside), then the attention kernel alone in separate calls."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_08_gb300 import build as _build
+    _build.build()
+    import mla_latent_kv_08_gb300 as mla
+    import workloads
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    bf = torch.bfloat16
+
+    def t(x, dtype=None):
+        tt = torch.from_numpy(np.ascontiguousarray(x))
+        return (tt.to(dtype) if dtype is not None else tt).to(dev)
+
+    def run(name, w, kind, q_len, R=None, T=None, n=20):
+        shape = mla.Shape(num_heads=w.H, kv_lora_rank=w.r, rope_dim=w.d_rope, v_head_dim=w.d_v,
+                          block_size=w.block_size, num_blocks=w.num_blocks, kind=kind)
+        cache = mla.Cache.allocate(shape, dev)
+        cu = t(np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32))
+        Rd = None if R is None else t(R.astype(np.float32))
+        mla.mla_latent_append(cache, t(w.block_table), t(np.zeros(w.B, np.int32)), cu,
+                              t(np.concatenate(w.latent), bf), t(np.concatenate(w.rope), bf), R=Rd,
+                              clip=None if T is None else t(T.astype(np.float32)))
+        bt, sl = t(w.block_table), t(w.seq_lens.astype(np.int32))
+        q, W = t(w.q, bf), t(w.W_UV, bf)
+        out = torch.empty((w.B, q_len, w.H, w.d_v), dtype=bf, device=dev)
+        lse = torch.empty((w.B, q_len, w.H), dtype=torch.float32, device=dev)
+        ws = mla.alloc_workspace(shape, w.B, q_len, dev)
+        call = mla.mla_decode if q_len == 1 else mla.mla_verify
+        for _ in range(3):
+            call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)
+        torch.cuda.synchronize(dev)
+        tot = 0.0
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            tot += e0.elapsed_time(e1)
+        mla.mla_profile_enable(1)
+        for _ in range(n):
+            flush.zero_()
+            call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)
+        torch.cuda.synchronize(dev)
+        ms, na, _ = mla.mla_profile_read()
+        mla.mla_profile_enable(0)
+        code, flags = mla.mla_get_status(ws)
+        tok = int(w.seq_lens.sum())
+        D = w.r + w.d_rope
+        kb = tok * (D * 2 if kind == mla.MLA_KV_BF16 else w.r // 4 + (w.r // 32) * 4 + 2 * w.d_rope) + \
+            w.B * q_len * w.H * D * 2
+        fl = 2 * tok * q_len * w.H * (D + w.r)
+        att = ms / na
+        print(json.dumps({"config": name, "tokens": tok, "call_us": tot / n * 1e3, "attention_us": att * 1e3,
+                          "attention_GBs": kb / (att * 1e-3) / 1e9, "attention_TFLOPs": fl / (att * 1e-3) / 1e12,
+                          "call_KV_tokens_per_s": tok / (tot / n * 1e-3), "status": [code, flags],
+                          "impl": mla.mla_resolve_impl(shape, q_len)}), flush=True)
+
+    w = workloads.dsv3(1)
+    run("C1 DeepSeek-V3 decode, B=32, L~U[1024,8192]", w, mla.MLA_KV_BF16, 1)
+    w = workloads.long_context(2)
+    run("C2 long context, H=64, L=32768/131072", w, mla.MLA_KV_BF16, 1)
+    w = workloads.verify(3)
+    run("C3 speculative verify, q_len=8, L~U[4096,32768]", w, mla.MLA_KV_BF16, 8, n=5)
+    w = workloads.int2_rotated(4)
+    # timing only: any orthogonal R and positive thresholds exercise the same kernels
+    R = workloads.haar_orthogonal(np.random.Generator(np.random.PCG64(5)), w.r)
+    run("C4 rotated-INT2 decode", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs:
+        return run_configs(args)
     return run_gb300(args)
 
 
