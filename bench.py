@@ -530,6 +530,9 @@ def run_configs(args):
     run("C2 long context, H=64, L=32768/131072", w, mla.MLA_KV_BF16, 1)
     w = workloads.verify(3)
     run("C3 speculative verify, q_len=8, L~U[4096,32768]", w, mla.MLA_KV_BF16, 8, n=5)
+    # NEXT: one 512-token prefill chunk in latent form (the verify call, causal window)
+    w = workloads.verify(5, B=1, q_len=512, len_range=(8192, 8192))
+    run("C5 chunked prefill, one 512-token chunk at L=8192, H=128", w, mla.MLA_KV_BF16, 512, n=3)
     w = workloads.int2_rotated(4)
     # timing only: any orthogonal R and positive thresholds exercise the same kernels
     R = workloads.haar_orthogonal(np.random.Generator(np.random.PCG64(5)), w.r)

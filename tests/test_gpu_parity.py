@@ -180,6 +180,26 @@ def test_int2_append_and_decode_small(gpu_lib, impl_name, H):
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+# ------------------------------------------------------------ prefill chunks
+
+@pytest.mark.parametrize("impl_name", ["tcgen05", "simt"])
+@pytest.mark.parametrize("H,q_len,lens", [(16, 96, (200, 700)), (128, 40, (100, 400))])
+def test_prefill_chunk_in_latent_form(gpu_lib, impl_name, H, q_len, lens):
+    """Chunked prefill is the verify call with a long causal window: the chunk's
+    q_len tokens are already appended; row i sees positions 0 .. L - q_len + i
+    (many 128-row tiles, causal masks inside KV tiles)."""
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.verify(40 + q_len, B=2, q_len=q_len, len_range=lens, H=H)
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    shape = gu.shape_for(w, impl=impl)
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, ws = gu.attend(w, shape, cache, w.q, q_len=q_len)
+    assert mla.mla_get_status(ws) == (mla.MLA_OK, 0)
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 # ------------------------------------------------------------ many sequences
 
 @pytest.mark.parametrize("impl_name", ["tcgen05", "simt"])
