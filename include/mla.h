@@ -83,10 +83,16 @@ typedef struct {
     int32_t impl;              /* mla_impl                                        */
     int32_t num_splits_hint;   /* 0: planner's choice; k>0: aim for about k split-
                                   KV work units in total (1 = one per sequence)   */
+    int32_t index_dim;         /* BF16 / FP32 kinds: elements of an extra per-token
+                                  key stored after the rope key (e.g. a sparse-
+                                  attention indexer key: 64 gives the 640-element
+                                  row); a multiple of 8, <= 1024; 0 = none. INT2:
+                                  must be 0. Attention never reads it.           */
 } mla_shape;
 
 /* The paged cache. Block p, slot j is token row p*block_size + j.
- *   BF16/FP32:  latent     [num_blocks, block_size, r + d_R]  (c then k_R)
+ *   BF16/FP32:  latent     [num_blocks, block_size, r + d_R + index_dim]
+ *                          (c, then k_R, then the optional extra key)
  *   INT2_ROT:   codes      [num_blocks, block_size, r / 4]    uint8, element e
  *                          of the row at bits 2*(e%4) of byte e/4
  *               scale_zero [num_blocks, block_size, r / group_size, 2] fp16
@@ -225,6 +231,17 @@ mla_status mla_profile_read(double *attention_ms, int32_t *attention_launches,
  * timeout_ns must be in [1000, 100000000] (1 us .. 100 ms), else
  * MLA_ERR_INVALID; MLA_ERR_CUDA if the launch fails. */
 mla_status mla_selftest_wait_timeout(uint64_t timeout_ns, int32_t *status, void *stream);
+
+/* Write the extra per-token key (shape->index_dim elements, the caller's dtype:
+ * bf16, or fp32 for the FP32 kind) of the tokens described exactly as for
+ * mla_latent_append (block_table, start_pos, cu_new, num_new): index_key is
+ * [num_new, index_dim] row-major, 16-byte aligned; it goes to elements
+ * [r + d_R, r + d_R + index_dim) of each token's cache row. Errors as for
+ * mla_latent_append; MLA_ERR_INVALID when index_dim is 0 or the kind is INT2. */
+mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
+                                   const int32_t *cu_new, int32_t num_new, const void *index_key,
+                                   int32_t *status, void *stream);
 
 /* Library ABI version (major * 100 + minor). */
 int32_t mla_version(void);

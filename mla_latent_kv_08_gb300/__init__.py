@@ -39,6 +39,7 @@ EXPORTED = (
     "mla_workspace_bytes", "mla_latent_append", "mla_decode", "mla_verify", "mla_get_status",
     "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
     "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc", "mla_selftest_wait_timeout",
+    "mla_latent_append_index",
 )
 
 
@@ -51,7 +52,7 @@ class MlaError(RuntimeError):
 class mla_shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_heads", "kv_lora_rank", "rope_dim", "v_head_dim", "block_size", "num_blocks",
-        "group_size", "kind", "impl", "num_splits_hint")]
+        "group_size", "kind", "impl", "num_splits_hint", "index_dim")]
 
 
 class mla_cache(ctypes.Structure):
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_workspace_bytes.restype = sz
     lib.mla_latent_append.argtypes = [sp, cp, vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
     lib.mla_latent_append.restype = i32
+    lib.mla_latent_append_index.argtypes = [sp, cp, vp, i32, i32, vp, vp, i32, vp, vp, vp]
+    lib.mla_latent_append_index.restype = i32
     lib.mla_decode.argtypes = [sp, cp, vp, i32, vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
     lib.mla_decode.restype = i32
     lib.mla_verify.argtypes = [sp, cp, vp, i32, vp, i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
@@ -129,15 +132,21 @@ class Shape:
     group_size: int = 32
     impl: int = MLA_IMPL_AUTO
     num_splits_hint: int = 0
+    index_dim: int = 0
 
     def c(self) -> mla_shape:
         return mla_shape(self.num_heads, self.kv_lora_rank, self.rope_dim, self.v_head_dim,
                          self.block_size, self.num_blocks, self.group_size, self.kind, self.impl,
-                         self.num_splits_hint)
+                         self.num_splits_hint, self.index_dim)
 
     @property
     def D(self) -> int:
         return self.kv_lora_rank + self.rope_dim
+
+    @property
+    def E(self) -> int:
+        """Elements per cache row (BF16/FP32 kinds): latent, rope key, extra key."""
+        return self.D + self.index_dim
 
 
 def _ptr(t) -> Optional[int]:
@@ -178,13 +187,13 @@ class Cache:
                        scale_zero=alloc((nb, bs, r // shape.group_size, 2), dtype=torch.float16, device=device),
                        rope=alloc((nb, bs, dR), dtype=torch.bfloat16, device=device))
         dt = torch.float32 if shape.kind == MLA_KV_FP32 else torch.bfloat16
-        return cls(shape, latent=alloc((nb, bs, r + dR), dtype=dt, device=device))
+        return cls(shape, latent=alloc((nb, bs, r + dR + shape.index_dim), dtype=dt, device=device))
 
     def bytes_per_token(self) -> int:
         s = self.shape
         if s.kind == MLA_KV_INT2_ROT:
             return s.kv_lora_rank // 4 + (s.kv_lora_rank // s.group_size) * 4 + 2 * s.rope_dim
-        return (4 if s.kind == MLA_KV_FP32 else 2) * (s.kv_lora_rank + s.rope_dim)
+        return (4 if s.kind == MLA_KV_FP32 else 2) * (s.kv_lora_rank + s.rope_dim + s.index_dim)
 
 
 # ---------------------------------------------------------------- entry points
@@ -211,6 +220,17 @@ def mla_latent_append(cache: Cache, block_table, start_pos, cu_new, c_kv, k_rope
                                  int(c_kv.shape[0]), _ptr(c_kv), _ptr(k_rope), _ptr(R), _ptr(clip),
                                  _ptr(status), _stream(stream))
     _check(code, "mla_latent_append")
+
+
+def mla_latent_append_index(cache: Cache, block_table, start_pos, cu_new, index_key, status=None,
+                            stream=None) -> None:
+    """Write the extra per-token key of len(index_key) tokens (see include/mla.h)."""
+    lib = load_library()
+    code = lib.mla_latent_append_index(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+                                       int(block_table.shape[1]), int(start_pos.shape[0]), _ptr(start_pos),
+                                       _ptr(cu_new), int(index_key.shape[0]), _ptr(index_key), _ptr(status),
+                                       _stream(stream))
+    _check(code, "mla_latent_append_index")
 
 
 def mla_decode(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, workspace,

@@ -58,6 +58,8 @@ static mla_status check_shape(const mla_shape *s) {
         return MLA_ERR_INVALID;
     if (s->impl < MLA_IMPL_AUTO || s->impl > MLA_IMPL_TCGEN05 || s->num_splits_hint < 0)
         return MLA_ERR_INVALID;
+    if (s->index_dim < 0 || s->index_dim % 8 || s->index_dim > 1024) return MLA_ERR_INVALID;
+    if (s->kind == MLA_KV_INT2_ROT && s->index_dim != 0) return MLA_ERR_INVALID;
     if (s->kind == MLA_KV_INT2_ROT) {
         if (s->group_size < 4 || s->group_size % 4 || s->kv_lora_rank % s->group_size) return MLA_ERR_INVALID;
         if (s->rope_dim < 8) return MLA_ERR_INVALID;
@@ -77,6 +79,7 @@ static ShapeArgs shape_args(const mla_shape *s) {
     a.num_blocks = s->num_blocks;
     a.gs = s->group_size;
     a.kind = s->kind;
+    a.ix = s->kind == MLA_KV_INT2_ROT ? 0 : s->index_dim;
     return a;
 }
 
@@ -283,6 +286,34 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, con
     return MLA_OK;
 }
 
+mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
+                                   const int32_t *cu_new, int32_t num_new, const void *index_key,
+                                   int32_t *status, void *stream) {
+    mla_status st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    if (shape->kind == MLA_KV_INT2_ROT || shape->index_dim == 0) return MLA_ERR_INVALID;
+    if (!cache || !block_table || !start_pos || !cu_new || B < 1 || max_blocks_per_seq < 1 || num_new < 0)
+        return MLA_ERR_INVALID;
+    if (num_new == 0) return MLA_OK;
+    if (!index_key || !aligned16(index_key) || !cache->latent || !aligned16(cache->latent)) return MLA_ERR_INVALID;
+    AppendParams p;
+    memset(&p, 0, sizeof p);
+    p.s = shape_args(shape);
+    p.B = B;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_new = num_new;
+    p.block_table = block_table;
+    p.start_pos = start_pos;
+    p.cu_new = cu_new;
+    p.index_key = index_key;
+    p.latent = cache->latent;
+    p.status = status;
+    if (launch_append_index(p, (cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
+    prof_kernels(1);
+    return MLA_OK;
+}
+
 mla_status mla_decode(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
                       int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t B, const void *q,
                       const void *W_UV, const float *R, float scale, void *out, float *lse, void *workspace,
@@ -362,6 +393,6 @@ mla_status mla_profile_read(double *attention_ms, int32_t *attention_launches, i
     return MLA_OK;
 }
 
-int32_t mla_version(void) { return 100; }
+int32_t mla_version(void) { return 101; }
 
 }  // extern "C"

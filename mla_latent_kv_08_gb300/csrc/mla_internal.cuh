@@ -51,7 +51,9 @@ struct WsLayout {
 
 struct ShapeArgs {
     int32_t H, r, dR, dv, bs, num_blocks, gs, kind;
-    __host__ __device__ int32_t D() const { return r + dR; }
+    int32_t ix;                  // extra per-token key after the rope key (BF16/FP32 kinds)
+    __host__ __device__ int32_t D() const { return r + dR; }        // elements attention reads
+    __host__ __device__ int32_t E() const { return r + dR + ix; }   // cache row stride (BF16/FP32)
 };
 
 // Everything a decode kernel reads.
@@ -97,6 +99,7 @@ struct AppendParams {
     const int32_t *cu_new;
     const void *c_kv;
     const void *k_rope;
+    const void *index_key;       // mla_latent_append_index: [num_new, ix]; else nullptr
     const float *R;
     const float *clip;
     void *latent;
@@ -134,6 +137,7 @@ cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bo
 cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
+cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st);
 // ---- tensor-core decode (defined in mla_tc.cu) -----------------------------
 bool tc_shape_supported(const ShapeArgs &s);
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st);

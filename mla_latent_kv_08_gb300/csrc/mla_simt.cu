@@ -234,7 +234,7 @@ __device__ __forceinline__ void gather_tile(const DecodeParams &p, int b, int tb
             float *dst = sK + tt * Dp + v * 8;
             if (blk1) {
                 size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
-                uint4 u = *((const uint4 *)((const __nv_bfloat16 *)p.latent + row * D) + v);
+                uint4 u = *((const uint4 *)((const __nv_bfloat16 *)p.latent + row * p.s.E()) + v);
                 const __nv_bfloat16 *h = (const __nv_bfloat16 *)&u;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) dst[e] = __bfloat162float(h[e]);
@@ -251,7 +251,7 @@ __device__ __forceinline__ void gather_tile(const DecodeParams &p, int b, int tb
             float *dst = sK + tt * Dp + v * 4;
             if (blk1) {
                 size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
-                float4 u = *((const float4 *)((const float *)p.latent + row * D) + v);
+                float4 u = *((const float4 *)((const float *)p.latent + row * p.s.E()) + v);
                 dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
             } else {
                 dst[0] = dst[1] = dst[2] = dst[3] = 0.f;
@@ -602,12 +602,32 @@ __global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
     row = __shfl_sync(0xffffffffu, row, 0);
     if (row < 0) return;
     constexpr int E = 16 / sizeof(T);            // elements per 16-byte vector
-    const int r = p.s.r, dR = p.s.dR, D = r + dR;
-    uint4 *dst = (uint4 *)((T *)p.latent + (size_t)row * D);
+    const int r = p.s.r, dR = p.s.dR;
+    uint4 *dst = (uint4 *)((T *)p.latent + (size_t)row * p.s.E());
     const uint4 *src_c = (const uint4 *)((const T *)p.c_kv + (size_t)n * r);
     const uint4 *src_r = (const uint4 *)((const T *)p.k_rope + (size_t)n * dR);
     for (int v = lane; v < r / E; v += 32) dst[v] = src_c[v];
     for (int v = lane; v < dR / E; v += 32) dst[r / E + v] = src_r[v];
+}
+
+// The extra per-token key (index_dim elements) into elements [r + d_R, E) of each
+// token's row: one warp per token, 16-byte vectors.
+template <typename T>
+__global__ void __launch_bounds__(256) append_index_kernel(AppendParams p) {
+    pdl_trigger();
+    pdl_wait();
+    const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (n >= p.num_new) return;
+    long long row = 0;
+    if (lane == 0) row = locate_slot(p, n);
+    row = __shfl_sync(0xffffffffu, row, 0);
+    if (row < 0) return;
+    constexpr int V = 16 / sizeof(T);
+    const int ix = p.s.ix;
+    uint4 *dst = (uint4 *)((T *)p.latent + (size_t)row * p.s.E() + p.s.D());
+    const uint4 *src = (const uint4 *)((const T *)p.index_key + (size_t)n * ix);
+    for (int v = lane; v < ix / V; v += 32) dst[v] = src[v];
 }
 
 constexpr int kAT = 16;   // tokens per INT2 append CTA
@@ -695,6 +715,13 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
         const long long row = s_row[t];
         if (row >= 0) p.rope[(size_t)row * dR + d] = kr[(size_t)(n0 + t) * dR + d];
     }
+}
+
+cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st) {
+    if (p.num_new == 0) return cudaSuccess;
+    if (p.s.kind == MLA_KV_BF16)
+        return launch_pdl(append_index_kernel<__nv_bfloat16>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
+    return launch_pdl(append_index_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
 }
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {

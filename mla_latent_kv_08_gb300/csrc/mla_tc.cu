@@ -302,7 +302,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * kRawSz, kRawSz);
                         prefetch_l2((const uint8_t *)p.rope + (size_t)blk * kRawRope, kRawRope);
                     } else {
-                        prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * kD, kStageBytes);
+                        // the block's rows (index keys included: one contiguous range)
+                        prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * p.s.E(),
+                                    (uint32_t)kTile * p.s.E() * 2);
                     }
                 }
                 ++pt;
@@ -916,14 +918,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over a row-major [rows, 576] matrix of 16-bit elements (bf16 or fp16),
-// 128-byte swizzled boxes of [box_rows, 64]. Rows past the end read as zero.
+// 2-D map over the first 576 columns of a row-major [rows, row_elems] matrix of
+// 16-bit elements (bf16 or fp16), 128-byte swizzled boxes of [box_rows, 64]. Rows
+// past the end read as zero.
 static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows,
-                     CUtensorMapDataType dtype) {
+                     CUtensorMapDataType dtype, uint64_t row_elems = kD) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -964,7 +967,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     memset(&kv_map, 0, sizeof kv_map);
     const bool int2 = p.s.kind == MLA_KV_INT2_ROT;
     if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile,
-                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)p.s.E()))
         return cudaErrorInvalidValue;
     // the query: bf16 as given, or the fp16 rotated query of the INT2 cache
     const int rows_seq = p.q_len * p.s.H;

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     import mla_latent_kv_08_gb300 as mla
-    assert mla.mla_version() == 100
+    assert mla.mla_version() == 101
     for code in range(-6, 1):
         assert mla.status_string(code) != "unknown status"
     assert mla.status_string(-99) == "unknown status"
@@ -57,6 +57,11 @@ def test_shape_validation(lib):
     assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, group_size=6)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kv_lora_rank=2048)) == mla.MLA_ERR_UNSUPPORTED
     assert mla.mla_resolve_impl(_shape(), q_len=0) == mla.MLA_ERR_INVALID
+    # the extra per-token key: a multiple of 8 up to 1024, BF16/FP32 kinds only
+    assert mla.mla_resolve_impl(_shape(index_dim=64)) in (mla.MLA_IMPL_SIMT, mla.MLA_IMPL_TCGEN05)
+    assert mla.mla_resolve_impl(_shape(index_dim=12)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(index_dim=2048)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, index_dim=64)) == mla.MLA_ERR_INVALID
     # the generic kernel takes any supported shape, e.g. the tiny fp32 one
     assert mla.mla_resolve_impl(_shape(num_heads=8, kv_lora_rank=64, rope_dim=16, v_head_dim=32,
                                        block_size=256, kind=mla.MLA_KV_FP32)) == mla.MLA_IMPL_SIMT
@@ -96,3 +101,15 @@ def test_selftest_arguments_checked_before_launch(lib):
     assert lib.mla_selftest_wait_timeout(ctypes.c_uint64(2_000_000), None, None) == mla.MLA_ERR_INVALID
     assert lib.mla_selftest_wait_timeout(ctypes.c_uint64(10), fake, None) == mla.MLA_ERR_INVALID
     assert lib.mla_selftest_wait_timeout(ctypes.c_uint64(10 ** 9), fake, None) == mla.MLA_ERR_INVALID
+
+
+def test_index_append_refused_without_an_index_field(lib):
+    import mla_latent_kv_08_gb300 as mla
+    cache = mla.mla_cache(None, None, None, None)
+    fake = ctypes.c_void_p(256)                    # never dereferenced: refused before launch
+    s0 = _shape().c()                              # index_dim 0
+    assert lib.mla_latent_append_index(ctypes.byref(s0), ctypes.byref(cache), fake, 4, 2, fake, fake, 3, fake,
+                                       None, None) == mla.MLA_ERR_INVALID
+    s1 = _shape(index_dim=64).c()                  # no cache pointer
+    assert lib.mla_latent_append_index(ctypes.byref(s1), ctypes.byref(cache), fake, 4, 2, fake, fake, 3, fake,
+                                       None, None) == mla.MLA_ERR_INVALID

@@ -72,6 +72,60 @@ def test_append_layout_bit_exact(gpu_lib, kind):
         np.testing.assert_array_equal(got.view(torch.int16).numpy().view(np.uint16), workloads.bf16_bits(ref))
 
 
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+def test_index_key_layout_bit_exact(gpu_lib, kind):
+    """The extra per-token key (64 elements: the 640-element row of a latent layer
+    with an indexer key) lands after the rope key of each token's row."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w = workloads.dsv3(12, B=4, H=8, len_range=(1, 200))
+    rng = np.random.default_rng(12)
+    idx = [workloads.bf16_round(rng.standard_normal((int(L), 64)).astype(np.float32)) for L in w.seq_lens]
+    shape = gu.shape_for(w, kind=mla.MLA_KV_FP32 if kind == "fp32" else mla.MLA_KV_BF16)
+    shape.index_dim = 64
+    assert mla.Cache.allocate(shape).bytes_per_token() == (4 if kind == "fp32" else 2) * 640
+    cache = mla.Cache.allocate(shape)
+    gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32))
+    dt = torch.float32 if kind == "fp32" else torch.bfloat16
+    cu = np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_latent_append_index(cache, gu.dev(w.block_table), gu.dev(np.zeros(w.B, np.int32)), gu.dev(cu),
+                                gu.dev(np.concatenate(idx), dt), status=st)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    rows = [np.concatenate([w.latent[b], w.rope[b], idx[b]], 1) for b in range(w.B)]
+    ref = layout.write_paged(w.num_blocks, 64, 640, w.block_table, rows, [0] * w.B)
+    got = cache.latent.cpu()
+    if kind == "fp32":
+        np.testing.assert_array_equal(got.numpy().view(np.uint32), ref.astype(np.float32).view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got.view(torch.int16).numpy().view(np.uint16), workloads.bf16_bits(ref))
+
+
+@pytest.mark.parametrize("impl_name", ["tcgen05", "simt"])
+def test_index_key_is_never_read_by_attention(gpu_lib, impl_name):
+    """With NaN extra keys in every row, decode equals the decode of the same tokens
+    in a cache without the extra field, bit for bit (both follow the row stride)."""
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(13, B=3, H=128, len_range=(70, 600))
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    res = []
+    for index_dim in (0, 64):
+        shape = gu.shape_for(w, impl=impl)
+        shape.index_dim = index_dim
+        cache = mla.Cache.allocate(shape)
+        if index_dim:
+            cache.latent[..., 576:] = float("nan")
+        gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32))
+        res.append(gu.attend(w, shape, cache, w.q)[:2])
+    (o0, l0), (o1, l1) = res
+    assert np.isfinite(o1).all()
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+    ro, rl = attention.absorbed(w.q[0], w.latent[0], w.rope[0], w.W_UV, w.scale)
+    _check_seq(o1, l1, w, 0, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 def test_append_empty_is_noop(gpu_lib):
     import mla_latent_kv_08_gb300 as mla
     import torch
