@@ -86,10 +86,51 @@ def fit_rotation(X: np.ndarray):
     w, V = np.linalg.eigh(Sigma)               # ascending by contract of eigh
     order = np.argsort(w, kind="stable")       # explicit: ascending eigenvalue
     w, V = w[order], V[:, order]
+    return _sign_fix(V), w
+
+
+def _sign_fix(V: np.ndarray) -> np.ndarray:
+    """Flip each column so that its largest-magnitude entry is positive."""
     idx = np.argmax(np.abs(V), axis=0)
     signs = np.sign(V[idx, np.arange(V.shape[1])])
     signs[signs == 0] = 1.0
-    return V * signs[None, :], w
+    return V * signs[None, :]
+
+
+def projection_energy(W_UK: np.ndarray, W_UV: np.ndarray) -> np.ndarray:
+    """M = sum_h (W_UK^h^T W_UK^h + W_UV^h W_UV^h^T) [r, r] (fp64): how strongly a
+    latent direction reaches the keys and the values after the up-projection.
+    W_UK [H, d_n, r], W_UV [H, r, d_v]."""
+    K = np.asarray(W_UK, dtype=np.float64)
+    V = np.asarray(W_UV, dtype=np.float64)
+    return np.einsum("hnr,hns->rs", K, K) + np.einsum("hrv,hsv->rs", V, V)
+
+
+def fit_rotation_weighted(X: np.ndarray, W_UK: np.ndarray, W_UV: np.ndarray):
+    """Up-projection-aware variant of the per-layer rotation (the page names this as
+    the open refinement: shape the INT2 error in the latent directions that matter
+    after reconstruction, "MLA model support (GLM-5.1 / DeepSeek-style)", maintainer
+    reply). Reading taken: the eigenbasis, ascending, of G = S^1/2 M S^1/2 with S =
+    c^T c and M the projection energy above; same sign rule as fit_rotation. With
+    M a multiple of the identity it is fit_rotation's basis.
+
+    Returns (R [r, r] fp64, eigenvalues of G ascending)."""
+    S = latent_covariance(X)
+    ws, Vs = np.linalg.eigh(S)
+    S_half = (Vs * np.sqrt(np.maximum(ws, 0.0))[None, :]) @ Vs.T
+    G = S_half @ projection_energy(W_UK, W_UV) @ S_half
+    G = 0.5 * (G + G.T)
+    w, V = np.linalg.eigh(G)
+    order = np.argsort(w, kind="stable")
+    return _sign_fix(V[:, order]), w[order]
+
+
+def upprojected_error(C: np.ndarray, C_hat: np.ndarray, M: np.ndarray) -> float:
+    """Relative error energy of a reconstructed latent after the up-projection:
+    sum_t e_t M e_t^T / sum_t c_t M c_t^T with e = c_hat - c (fp64)."""
+    C = np.asarray(C, dtype=np.float64)
+    E = np.asarray(C_hat, dtype=np.float64) - C
+    return float(np.einsum("tr,rs,ts->", E, M, E) / np.einsum("tr,rs,ts->", C, M, C))
 
 
 def clip_thresholds(X: np.ndarray, R: np.ndarray, group: int = 32, pct: float = 99.0) -> np.ndarray:

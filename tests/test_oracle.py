@@ -333,3 +333,85 @@ def test_int2_invariants_and_rotation_chain():
     assert np.all(err <= s / 2 + 2e-3 * (np.abs(yc) + s) + 1e-6)
     # python re-decoding agrees with the C decoder (codes * s + z is exact-then-rounded once)
     np.testing.assert_array_equal(deq, (u.astype(np.float32) * s + z).astype(np.float32))
+
+
+# ------------------------------------------------- up-projection-aware rotation
+
+def test_projection_energy_closed_form():
+    rng = np.random.default_rng(3)
+    K = rng.standard_normal((3, 5, 8))
+    V = rng.standard_normal((3, 8, 4))
+    M = oint2.projection_energy(K, V)
+    # direct sum over heads, written out
+    ref = sum(K[h].T @ K[h] + V[h] @ V[h].T for h in range(3))
+    np.testing.assert_allclose(M, ref, rtol=1e-12)
+    # c M c^T is the energy c reaches the keys and values with
+    c = rng.standard_normal(8)
+    energy = sum(np.sum((K[h] @ c) ** 2) + np.sum((c @ V[h]) ** 2) for h in range(3))
+    assert abs(c @ M @ c - energy) < 1e-10 * energy
+
+
+def test_weighted_rotation_reduces_to_plain_for_isotropic_weights():
+    """M = I (W_UK the identity, no W_UV): G = S, so the basis is fit_rotation's."""
+    rng = np.random.default_rng(4)
+    r = 16
+    X = rng.standard_normal((4000, r)) * np.exp(rng.uniform(-1.5, 1.5, size=r))[None, :]
+    R0, w0 = oint2.fit_rotation(X)
+    R1, w1 = oint2.fit_rotation_weighted(X, np.eye(r)[None], np.zeros((1, r, 1)))
+    np.testing.assert_allclose(R1, R0, atol=1e-8)
+    np.testing.assert_allclose(w1, w0, rtol=1e-10)
+    assert np.max(np.abs(R1.T @ R1 - np.eye(r))) < 1e-12
+
+
+def test_weighted_rotation_follows_the_weights_for_white_latents():
+    """S = I (orthonormal calibration columns): G = M, the basis is M's eigenbasis."""
+    rng = np.random.default_rng(5)
+    r = 12
+    X, _ = np.linalg.qr(rng.standard_normal((500, r)))            # X^T X = I
+    K = rng.standard_normal((2, 6, r))
+    V = rng.standard_normal((2, r, 3))
+    R, w = oint2.fit_rotation_weighted(X, K, V)
+    M = oint2.projection_energy(K, V)
+    np.testing.assert_allclose(R.T @ M @ R, np.diag(w), atol=1e-9 * np.max(w))
+    assert np.all(np.diff(w) >= 0)
+
+
+def test_upprojected_error_closed_form():
+    rng = np.random.default_rng(6)
+    r = 10
+    A = rng.standard_normal((r, r))
+    M = A @ A.T
+    lam, U = np.linalg.eigh(M)
+    C = rng.standard_normal((50, r))
+    assert oint2.upprojected_error(C, C, M) == 0.0
+    # a perturbation of size d along eigenvector k of M on every token
+    d, k = 0.01, 3
+    err = oint2.upprojected_error(C, C + d * U[:, k][None, :], M)
+    assert abs(err - 50 * d * d * lam[k] / np.einsum("tr,rs,ts->", C, M, C)) < 1e-12
+
+
+def test_weighted_rotation_study():
+    """The up-projection-aware reading measured against the plain rotation on the INT2
+    workload's law (the comparison reported in the design notes): no gain with
+    isotropic synthetic weights, and a clear loss with anisotropic ones, because it
+    puts latent directions of very different variance into the same INT2 group."""
+    w = workloads.int2_rotated(4, B=4, H=32, len_range=(512, 768), n_calib=32768)
+    rng = np.random.default_rng(7)
+    r = w.r
+    K = rng.standard_normal((w.H, 128, r)) / np.sqrt(r)
+    V = np.asarray(w.W_UV, np.float64)
+    C = np.concatenate(w.latent).astype(np.float64)
+    scale = np.exp(rng.uniform(np.log(0.2), np.log(5.0), size=r))
+    res = {}
+    for label, (KK, VV) in (("isotropic", (K, V)),
+                            ("anisotropic", (K * scale[None, None, :], V * scale[None, :, None]))):
+        M = oint2.projection_energy(KK, VV)
+        for name, R in (("plain", oint2.fit_rotation(w.calib)[0]),
+                        ("weighted", oint2.fit_rotation_weighted(w.calib, KK, VV)[0])):
+            T = oint2.clip_thresholds(w.calib, R)
+            codes, sz = oint2.quantize(C.astype(np.float32), R.astype(np.float32), T.astype(np.float32))
+            Chat = oint2.decode(codes, sz).astype(np.float64) @ R.T
+            res[label, name] = oint2.upprojected_error(C, Chat, M)
+    print({k: round(v, 4) for k, v in res.items()})
+    assert res["isotropic", "weighted"] > 0.97 * res["isotropic", "plain"]
+    assert res["anisotropic", "weighted"] > 1.3 * res["anisotropic", "plain"]
