@@ -93,6 +93,10 @@ int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
     return tc_ok ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
 }
 
+// Tiles the planner charges per sequence start on the tensor-core path (a work item's
+// query load and epilogue cost about as much as two to three 64-token tiles).
+constexpr int kItemCostTc = 3;
+
 static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {
     WsLayout w;
     memset(&w, 0, sizeof w);
@@ -172,6 +176,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.scale_log2 = scale * kLog2e;
     p.status = (int32_t *)(ws + w.status);
     p.num_work = (const int32_t *)(ws + w.status + sizeof(int32_t));
+    p.item_cost = impl == MLA_IMPL_TCGEN05 ? kItemCostTc : 0;
     p.work = (const WorkItem *)(ws + w.work);
     p.split_start = (const int32_t *)(ws + w.split_start);
     p.stream_start = (const int32_t *)(ws + w.stream_start);

@@ -75,6 +75,7 @@ struct DecodeParams {
     const int32_t *split_start;
     const int32_t *stream_start;
     int32_t streams;
+    int32_t item_cost;           // planner: tiles charged per sequence start (its Q load, epilogue)
     float *part_o;
     float *part_lse;
 };

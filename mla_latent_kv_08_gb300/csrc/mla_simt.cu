@@ -63,16 +63,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
     const int P = p.streams;
     if (tid == 0) { s_tiles = 0; p.status[0] = 0; }
     __syncthreads();
+    // Cost axis: each sequence is charged item_cost units for its start (the query
+    // load and epilogue of a new work item) followed by one unit per tile; streams
+    // take equal cost ranges, so a stream that starts more sequences gets fewer tiles.
+    const int ic = p.item_cost;
     long long local = 0;
     for (int b = tid; b < p.B; b += blockDim.x) {
         const int L = p.seq_lens[b];
-        if (L >= p.q_len && L <= cap) local += (L + kPlanTile - 1) / kPlanTile;
+        if (L >= p.q_len && L <= cap) local += (L + kPlanTile - 1) / kPlanTile + ic;
         else raise_flag(p.status, FLAG_BAD_LENGTH);
     }
     atomicAdd((unsigned long long *)&s_tiles, (unsigned long long)local);
     __syncthreads();
-    const long long NB = s_tiles;
-    const long long T = NB > 0 ? (NB + P - 1) / P : 1;      // tiles per stream
+    const long long NC = s_tiles;
+    const long long T = NC > 0 ? (NC + P - 1) / P : 1;      // cost per stream
     int tile_carry = 0, item_carry = 0;
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + tid;
@@ -82,7 +86,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
             if (L >= p.q_len && L <= cap) n = (L + kPlanTile - 1) / kPlanTile;
         }
         int tot_tiles, tot_items;
-        const long long tb = tile_carry + block_exclusive_scan(n, s_warp, tot_tiles);
+        // tb: cost position of the sequence's first tile (after its start charge)
+        const long long tb = tile_carry + block_exclusive_scan(n > 0 ? n + ic : 0, s_warp, tot_tiles) + ic;
         const long long first = tb / T;
         const long long last = n > 0 ? (tb + n - 1) / T : first - 1;
         const int cnt = (int)(last - first + 1);
