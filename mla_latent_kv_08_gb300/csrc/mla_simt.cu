@@ -105,6 +105,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
                 it.stream = (int)s;
                 ((WorkItem *)p.work)[start + k] = it;
             }
+            // stream_start[s] = index of the first item whose stream is >= s. It lies
+            // in this sequence for the streams after the one holding the cost position
+            // just before the sequence, up to the sequence's last stream.
+            if (n > 0) {
+                const long long cb = tb - ic;
+                const long long prev = cb > 0 ? (cb - 1) / T : -1;
+                for (long long s = prev + 1; s <= last && s < P; ++s)
+                    ((int32_t *)p.stream_start)[s] = min(start + (int)(s > first ? s - first : 0), max_work);
+            }
         }
         tile_carry += tot_tiles;
         item_carry += tot_items;
@@ -114,13 +123,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
         ((int32_t *)p.split_start)[p.B] = item_carry;
         ((int32_t *)p.num_work)[0] = total;
     }
-    __syncthreads();
-    // stream_start[s] = index of the first item whose stream is >= s
-    for (int i = tid; i <= total; i += blockDim.x) {
-        const int cur = i < total ? p.work[i].stream : P;
-        const int prev = i > 0 ? p.work[i - 1].stream : -1;
-        for (int s = prev + 1; s <= cur && s <= P; ++s) ((int32_t *)p.stream_start)[s] = i;
-    }
+    // streams past the last sequence's last stream, and the end marker stream_start[P]
+    for (long long s = (NC > 0 ? (NC - 1) / T : -1) + 1 + tid; s <= P; s += blockDim.x)
+        ((int32_t *)p.stream_start)[s] = total;
 }
 
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
