@@ -423,3 +423,59 @@ def test_auto_picks_tensor_cores_for_dsv3(gpu_lib):
     w = workloads.dsv3(1, B=2, H=128, len_range=(64, 64))
     assert mla.mla_resolve_impl(gu.shape_for(w)) == mla.MLA_IMPL_TCGEN05
     assert mla.mla_resolve_impl(gu.shape_for(w, kind=mla.MLA_KV_FP32)) == mla.MLA_IMPL_SIMT
+
+
+@pytest.mark.parametrize("impl_name,kind", [("tcgen05", "bf16"), ("simt", "bf16"), ("tcgen05", "int2")])
+def test_decode_replays_from_a_cuda_graph(gpu_lib, impl_name, kind):
+    """A decode step captured as a CUDA graph (planner, attention and combine kernels
+    with their programmatic dependencies) and replayed after the query buffer was
+    rewritten in place gives bit-for-bit the eager result for the new query."""
+    import torch
+    impl = {"tcgen05": gu.mla.MLA_IMPL_TCGEN05, "simt": gu.mla.MLA_IMPL_SIMT}[impl_name]
+    R = T = None
+    if kind == "int2":
+        w, R, T = _int2_setup(B=4, H=128, len_range=(300, 1500))
+        shape = gu.shape_for(w, kind=gu.mla.MLA_KV_INT2_ROT, impl=impl)
+    else:
+        w = workloads.dsv3(4, B=5, H=128, len_range=(300, 1500))
+        shape = gu.shape_for(w, impl=impl)
+    cache, _ = gu.fill_cache(w, shape, R=R, T=T)
+    dt = gu.torch_dtype(w)
+    # the second query, rounded to the cache's dtype once so that the oracle sees
+    # exactly the values the kernels read
+    q2 = gu.dev(np.random.default_rng(44).standard_normal(w.q.shape).astype(np.float32), dt).float().cpu().numpy()
+    qd = gu.dev(w.q.astype(np.float32), dt)
+    W = gu.dev(w.W_UV.astype(np.float32), dt)
+    Rd = None if R is None else gu.dev(R.astype(np.float32))
+    bt = gu.dev(w.block_table)
+    sl = gu.dev(w.seq_lens.astype(np.int32))
+    out = torch.empty((w.B, 1, w.H, w.d_v), dtype=dt, device="cuda")
+    lse = torch.empty((w.B, 1, w.H), dtype=torch.float32, device="cuda")
+    ws = gu.mla.alloc_workspace(shape, w.B, 1)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        gu.mla.mla_decode(cache, bt, sl, qd, W, w.scale, out, lse, ws, R=Rd, stream=side)
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        gu.mla.mla_decode(cache, bt, sl, qd, W, w.scale, out, lse, ws, R=Rd, stream=side)
+    torch.cuda.synchronize()
+    # eager reference for the second query
+    qd.copy_(gu.dev(q2, dt))
+    gu.mla.mla_decode(cache, bt, sl, qd, W, w.scale, out, lse, ws, R=Rd)
+    torch.cuda.synchronize()
+    ref_o, ref_l = out.clone(), lse.clone()
+    out.zero_()
+    lse.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    code, flags = gu.mla.mla_get_status(ws)
+    assert code == gu.mla.MLA_OK, (code, flags)
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    if kind == "bf16":
+        o = out.float().cpu().numpy()
+        l = lse.cpu().numpy()
+        for b in range(w.B):
+            ro, rl = attention.absorbed(q2[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+            _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
