@@ -211,6 +211,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     c.B = B;
     c.q_len = q_len;
     c.split_start = p.split_start;
+    c.part_bf16 = impl == MLA_IMPL_TCGEN05;   // the tensor-core decode writes bf16 partials
     c.part_o = p.part_o;
     c.part_lse = p.part_lse;
     c.R = int2 ? R : nullptr;
@@ -227,6 +228,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
             cudaSuccess)
             return MLA_ERR_CUDA;
         c.split_start = ident;
+        c.part_bf16 = 0;                       // o_lat is fp32
         c.part_o = o_lat;
         c.part_lse = lse2;
         c.R = nullptr;

@@ -111,9 +111,16 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
                     const int sp = sb + k;
                     v[k] = -CUDART_INF_F;
                     if (sp < s1) {
-                        const float4 *po = (const float4 *)(c.part_o + ((size_t)sp * rows_seq + row) * kR);
+                        const size_t at = ((size_t)sp * rows_seq + row) * kR;
+                        if (c.part_bf16) {      // 4 bf16 per (lane, q): half the bytes of fp32
+                            const uint2 *po = (const uint2 *)((const __nv_bfloat16 *)c.part_o + at);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) f[k][q] = po[lane + 32 * q];
+                            for (int q = 0; q < 4; ++q) f[k][q] = bf16x4_to_float4(po[lane + 32 * q]);
+                        } else {
+                            const float4 *po = (const float4 *)((const float *)c.part_o + at);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) f[k][q] = po[lane + 32 * q];
+                        }
                         v[k] = c.part_lse[(size_t)sp * rows_seq + row];
                     } else {
 #pragma unroll

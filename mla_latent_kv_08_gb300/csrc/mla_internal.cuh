@@ -36,7 +36,8 @@ struct WsLayout {
     size_t work;          // WorkItem[max_work]
     size_t split_start;   // int32[B + 1]: first slot of each sequence
     size_t stream_start;  // int32[streams + 1]: first item of each stream
-    size_t part_o;        // fp32 [max_work][q_len * H][r]  normalised partial outputs
+    size_t part_o;        // [max_work][q_len * H][r] normalised partial outputs: bf16 from the
+                          // tensor-core decode, fp32 from the CUDA-core decode (sized for fp32)
     size_t part_lse;      // fp32 [max_work][q_len * H]     partial log2-sum-exp
     size_t q_prep;        // fp32 [B * q_len * H][r + d_R]  rotated query (INT2 kind)
     size_t o_rot;         // fp32 [B * q_len * H][r]  merged rotated output (INT2, tensor cores)
@@ -83,8 +84,9 @@ struct DecodeParams {
 struct CombineParams {
     ShapeArgs s;
     int32_t B, q_len;
+    int32_t part_bf16;           // part_o holds bf16 values (else fp32)
     const int32_t *split_start;
-    const float *part_o;
+    const void *part_o;
     const float *part_lse;
     const float *R;              // INT2: [r, r], else nullptr
     const void *W_UV;            // [H, r, dv]
@@ -164,6 +166,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+// Four bf16 values (8 bytes, memory order) widened to fp32.
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
 }
 __device__ __forceinline__ void raise_flag(int32_t *status, int32_t f) {
     if (status) atomicOr(status, f);

@@ -340,10 +340,11 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(CombineParams c, float 
             const float v = c.part_lse[(size_t)s * rows_seq + row];
             const float w = v == -CUDART_INF_F ? 0.f : exp2f(v - M);
             tot += w;
-            const float4 *po = (const float4 *)(c.part_o + ((size_t)s * rows_seq + row) * kK);
+            const size_t at = ((size_t)s * rows_seq + row) * kK;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 f = po[lane + 32 * q];
+                const float4 f = c.part_bf16 ? bf16x4_to_float4(((const uint2 *)((const __nv_bfloat16 *)c.part_o + at))[lane + 32 * q])
+                                             : ((const float4 *)((const float *)c.part_o + at))[lane + 32 * q];
                 acc[4 * q + 0] = fmaf(w, f.x, acc[4 * q + 0]);
                 acc[4 * q + 1] = fmaf(w, f.y, acc[4 * q + 1]);
                 acc[4 * q + 2] = fmaf(w, f.z, acc[4 * q + 2]);

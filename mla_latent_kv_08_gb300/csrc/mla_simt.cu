@@ -505,7 +505,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
                 for (int s = s0; s < s1; ++s) {
                     float v = p.part_lse[(size_t)s * rows_total + row];
                     float wgt = (v == -CUDART_INF_F) ? 0.f : exp2f(v - M) * inv;
-                    a = fmaf(wgt, p.part_o[((size_t)s * rows_total + row) * r + d], a);
+                    const size_t at = ((size_t)s * rows_total + row) * r + d;
+                    const float pv = p.part_bf16 ? __bfloat162float(((const __nv_bfloat16 *)p.part_o)[at])
+                                                 : ((const float *)p.part_o)[at];
+                    a = fmaf(wgt, pv, a);
                 }
                 dst[d] = nan ? CUDART_NAN_F : a;
             }

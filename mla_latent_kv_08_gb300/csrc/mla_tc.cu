@@ -26,7 +26,7 @@
 //           V is the same smem tile read as an MN-major operand; PV(T-1) is
 //           slipped between the QK groups of tile T as soon as P(T-1) is ready
 // Per work item: Q arrives by TMA (its tensor-memory part staged through the Q
-// region of shared memory); the epilogue writes O / l to the fp32 partial
+// region of shared memory); the epilogue writes O / l to the bf16 partial
 // buffer by TMA stores and the log2-sum-exp to the partial LSE; the combine
 // kernel merges splits and applies W_UV.
 //
@@ -93,7 +93,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 __host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u; }
 constexpr int kDequantWarps = 6;      // warps 2, 3, 12..15 (rotated-INT2 cache)
 constexpr int kDequantThreads = 32 * kDequantWarps;
-constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 32 dims] fp32
+constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 64 dims] bf16
 // QK K-steps in two issue groups: [0,16) (Q from tensor memory in the bf16 kind)
 // and [16,36). Every group boundary costs the MMA warp a warp sync and a barrier
 // probe; with more, finer groups the decode ran slower.
@@ -217,7 +217,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     constexpr uint32_t kColQ = kColS + 64 * kSBufs;
     constexpr int kQRounds = (kQTmemBlocks + kQSmemBlocks - 1) / kQSmemBlocks;   // staging rounds of the TMEM part
     constexpr int kEpiBoxes = (int)((kQSmemBlocks * kQBlockBytes) / (8 * kEpiBoxBytes));   // per warp at a time
-    static_assert(kEpiBoxes >= 1 && 4 % kEpiBoxes == 0, "epilogue boxes");
+    static_assert(kEpiBoxes >= 1 && 2 % kEpiBoxes == 0, "epilogue boxes");
     // the first QK group that reads Q from shared memory
     constexpr int kFirstSmemGroup = first_smem_group(4 * kQTmemBlocks);
     const DecodeParams &p = tp.p;
@@ -838,39 +838,45 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             if (ok && have_next)        // every thread has read its staged Q out of the region
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->qreg_free, (uses - 1) & 1, bars, p.status));
             const bool bad = aborted(bars) || !ok || bad_item;
-            // Epilogue: O / l -> partial slot i. Each warp writes [32 rows x 32 dims]
-            // fp32 boxes (128B-swizzled) into the region, kEpiBoxes at a time, and
-            // stores each with one TMA copy; rows past the sequence's rows are
-            // clipped by the tensor map.
+            // Epilogue: O / l -> partial slot i, rounded to bf16 (the combine rounds the
+            // merged rows to a bf16 MMA operand as well). Each warp writes [32 rows x 64
+            // dims] boxes (128B-swizzled) into the region, kEpiBoxes at a time, and
+            // stores each with one TMA copy; rows past the sequence's rows are clipped
+            // by the tensor map.
             if (ok) {
                 const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
                 uint8_t *boxes = smem + kOffQ + (warp - 4) * kEpiBoxes * kEpiBoxBytes;
                 const int y = g * kRows + 32 * wq;
                 const bool store = y < rows_seq;                 // warp-uniform
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     const int bi = c % kEpiBoxes;
                     if (bi == 0 && c > 0) {                      // the previous boxes were read
                         if (lane == 0) bulk_wait_read();
                         __syncwarp();
                     }
-                    uint32_t ov[32];
-                    TMEM_LD32(lane_addr + kColO + 128 * hs + 32 * c, ov);
-                    tmem_wait_ld();
                     uint8_t *box = boxes + bi * kEpiBoxBytes;
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {             // 32 of the box's 64 dims at a time
+                        uint32_t ov[32];
+                        TMEM_LD32(lane_addr + kColO + 128 * hs + 64 * c + 32 * hh, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        float4 f;
-                        f.x = __uint_as_float(ov[4 * q4 + 0]) * inv;
-                        f.y = __uint_as_float(ov[4 * q4 + 1]) * inv;
-                        f.z = __uint_as_float(ov[4 * q4 + 2]) * inv;
-                        f.w = __uint_as_float(ov[4 * q4 + 3]) * inv;
-                        *(float4 *)(box + sw128(lane, q4)) = f;
+                        for (int q = 0; q < 4; ++q) {            // 16-byte chunk 4 hh + q: 8 dims
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                                    __uint_as_float(ov[8 * q + 2 * e]) * inv, __uint_as_float(ov[8 * q + 2 * e + 1]) * inv);
+                                pk[e] = *(const uint32_t *)&h2;
+                            }
+                            *(uint4 *)(box + sw128(lane, 4 * hh + q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
                     }
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0 && store) {
-                        tma_store_3d(&o_map, box, 256 * half + 128 * hs + 32 * c, y, i);
+                        tma_store_3d(&o_map, box, 256 * half + 128 * hs + 64 * c, y, i);
                         bulk_commit();
                     }
                 }
@@ -934,16 +940,16 @@ static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t
     return r == CUDA_SUCCESS;
 }
 
-// 3-D fp32 map over the partial outputs [slots, rows_seq, r], boxes of
-// [32 rows x 32 dims] with the 128-byte swizzle (stores clip rows >= rows_seq).
-static bool make_out_map(CUtensorMap *map, float *base, int r, int rows_seq, int slots) {
+// 3-D bf16 map over the partial outputs [slots, rows_seq, r], boxes of
+// [32 rows x 64 dims] with the 128-byte swizzle (stores clip rows >= rows_seq).
+static bool make_out_map(CUtensorMap *map, void *base, int r, int rows_seq, int slots) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)r, (cuuint64_t)rows_seq, (cuuint64_t)slots};
-    cuuint64_t strides[2] = {(cuuint64_t)r * 4, (cuuint64_t)rows_seq * r * 4};
-    cuuint32_t box[3] = {32, 32, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)r * 2, (cuuint64_t)rows_seq * r * 2};
+    cuuint32_t box[3] = {64, 32, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;

@@ -479,3 +479,20 @@ def test_decode_replays_from_a_cuda_graph(gpu_lib, impl_name, kind):
         for b in range(w.B):
             ro, rl = attention.absorbed(q2[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
             _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+def test_tensor_core_decode_with_the_generic_combine(gpu_lib):
+    """d_v = 64: the tensor-core decode (bf16 split partials) feeds the CUDA-core
+    combine, which reads them in that format."""
+    import dataclasses
+    import mla_latent_kv_08_gb300 as mla
+    w = workloads.dsv3(9, B=4, H=128, len_range=(200, 2500))
+    w = dataclasses.replace(w, W_UV=np.ascontiguousarray(w.W_UV[:, :, :64]), d_v=64)
+    shape = gu.shape_for(w, impl=mla.MLA_IMPL_TCGEN05)
+    assert mla.mla_resolve_impl(shape) == mla.MLA_IMPL_TCGEN05
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, ws = gu.attend(w, shape, cache, w.q)
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
