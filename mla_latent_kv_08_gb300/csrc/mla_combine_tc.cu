@@ -2,8 +2,9 @@
 // kv_lora_rank 512, v_head_dim 128).
 //
 // One CTA per (head h, tile of up to 64 output rows), a row being a (sequence,
-// draft position) pair. While TMA streams W_UV^h ([512 x 128] bf16, 128 KB)
-// into shared memory, the threads merge each row's split partials by their
+// draft position) pair. TMA streams W_UV^h ([512 x 128] bf16, 128 KB) into shared
+// memory from the CTA's start, while the decode kernel is still finishing; once the
+// partials are complete, the threads merge each row's split partials (bf16 or fp32) by their
 // log2-sum-exp into the latent output o_lat (fp32 accumulate, stored bf16 as a
 // K-major 128B-swizzled operand) and write the row's LSE. One thread then
 // issues 32 tcgen05 MMAs, D[128 x NR] = W_UV^hT [128 x 512] . o_lat^T [512 x NR]
@@ -38,6 +39,22 @@ struct CombTcParams {
     int32_t rows;          // B * q_len
 };
 
+// Phase timestamps (globaltimer) per CTA for performance analysis, compiled only
+// with -DMLA_TRACE: entry, after the grid dependency wait, partials merged, W_UV
+// landed, MMAs done, end. Product builds contain none of it.
+#ifdef MLA_TRACE
+__device__ unsigned long long g_comb_time[1024][6];
+#define COMB_TRACE(slot)                                                                      \
+    do {                                                                                      \
+        const unsigned cid = blockIdx.y * gridDim.x + blockIdx.x;                             \
+        if (threadIdx.x == 0 && cid < 1024) g_comb_time[cid][slot] = globaltimer();            \
+    } while (0)
+#else
+#define COMB_TRACE(slot) \
+    do {                 \
+    } while (0)
+#endif
+
 __global__ void __launch_bounds__(kThreads, 1)
 combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams tp) {
     const CombineParams &c = tp.c;
@@ -55,16 +72,22 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
     int32_t *abort_flag = (int32_t *)(bar_w + 3);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
+    COMB_TRACE(0);
 
-    // set-up that overlaps the decode kernel's tail: barriers, TMEM, and W_UV^h
-    // ([512 x 128] bf16, contiguous) pulled into L2
+    // Set-up that overlaps the decode kernel's tail: barriers, TMEM, and the TMA of
+    // W_UV^h ([512 x 128] bf16) into shared memory. W_UV is an input no kernel of this
+    // call writes, and the planner lets the kernels after it launch only once every
+    // earlier kernel of the stream has completed, so it may be read before the wait.
     if (tid == 0) {
         mbar_init(bar_w, 1);
         mbar_init(bar_mma, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
-        prefetch_l2((const uint8_t *)c.W_UV + (size_t)h * kWBytes, kWBytes);
+        mbar_expect_tx(bar_w, kWBytes);
+        for (int vb = 0; vb < 2; ++vb)
+            for (int kb = 0; kb < 8; ++kb)
+                tma_load_2d(smem + kOffW + (vb * 8 + kb) * kWBoxBytes, &w_map, 64 * vb, h * kR + 64 * kb, bar_w);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -73,12 +96,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     pdl_wait();                      // the split partials are complete from here on
-    if (tid == 0) {
-        mbar_expect_tx(bar_w, kWBytes);
-        for (int vb = 0; vb < 2; ++vb)
-            for (int kb = 0; kb < 8; ++kb)
-                tma_load_2d(smem + kOffW + (vb * 8 + kb) * kWBoxBytes, &w_map, 64 * vb, h * kR + 64 * kb, bar_w);
-    }
+    COMB_TRACE(1);
 
     // ---- merge split partials: warp per row, each lane owns 16 latent dims. Every
     // row's split range is read first; then a row costs one round trip: its log2-sum-
@@ -175,10 +193,12 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    COMB_TRACE(2);
     const uint32_t tmem = *tmem_slot;
 
     if (tid == 0) {
         bool ok = mbar_wait_bounded(bar_w, 0, abort_flag, nullptr, 0, kTimeoutNs);
+        COMB_TRACE(3);
         if (ok) {
             tc_fence_after();
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(NR >> 3) << 17) |
@@ -197,6 +217,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
     __syncwarp();
     if (warp < 4) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_mma, 0, abort_flag, nullptr, 0, kTimeoutNs));
+        COMB_TRACE(4);
         tc_fence_after();
         const int v = 32 * warp + lane;              // TMEM lane = output dim
         const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -219,6 +240,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
     }
     tc_fence_before();
     __syncthreads();
+    COMB_TRACE(5);
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64) : "memory");
@@ -269,3 +291,9 @@ cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st) {
 }
 
 }  // namespace mla
+
+#ifdef MLA_TRACE
+extern "C" int mla_comb_trace_read(unsigned long long *host, int n) {
+    return (int)cudaMemcpyFromSymbol(host, mla::comb::g_comb_time, sizeof(unsigned long long) * 6 * (size_t)n);
+}
+#endif

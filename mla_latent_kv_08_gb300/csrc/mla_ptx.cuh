@@ -87,6 +87,21 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  ::"l"((uint64_t)map), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
+// As tma_store_3d, with an L2 cache policy (from l2_policy_evict_last) for the
+// written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *map, const void *src, int x, int y, int z,
+                                                  uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;"
+                 ::"l"((uint64_t)map), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "l"(policy)
+                 : "memory");
+}
+// L2 policy that keeps the accessed lines over evict-normal data (e.g. a stream
+// read once) until they are needed again.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the committed bulk stores of this thread have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

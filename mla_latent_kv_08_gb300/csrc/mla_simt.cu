@@ -24,7 +24,8 @@ namespace mla {
 // ============================================================================
 constexpr int kPlanTile = 64;
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, at
+// most 1024).
 __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -36,7 +37,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &tot
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int x = s_warp[lane];
+        int x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
         int w = x;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -53,11 +54,32 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &tot
     return excl;
 }
 
+#ifdef MLA_TRACE
+// planner timestamps (globaltimer): entry, after the grid dependency wait, end
+__device__ unsigned long long g_plan_time[3];
+__device__ __forceinline__ unsigned long long ptx_globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+extern "C" int mla_plan_trace_read(unsigned long long *host) {
+    return (int)cudaMemcpyFromSymbol(host, g_plan_time, sizeof g_plan_time);
+}
+#endif
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_work) {
     __shared__ int s_warp[33];
     __shared__ long long s_tiles;
-    pdl_trigger();
+#ifdef MLA_TRACE
+    if (threadIdx.x == 0) g_plan_time[0] = ptx_globaltimer();
+#endif
+    // Wait first, then let the decode kernel launch: everything after the planner
+    // (which may start work before its own wait, e.g. loading W_UV) then starts only
+    // once every kernel before the planner has completed.
     pdl_wait();
+    pdl_trigger();
+#ifdef MLA_TRACE
+    if (threadIdx.x == 0) g_plan_time[1] = ptx_globaltimer();
+#endif
     const int tid = threadIdx.x;
     const int64_t cap = (int64_t)p.max_blocks * p.s.bs;
     const int P = p.streams;
@@ -73,7 +95,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
         if (L >= p.q_len && L <= cap) local += (L + kPlanTile - 1) / kPlanTile + ic;
         else raise_flag(p.status, FLAG_BAD_LENGTH);
     }
-    atomicAdd((unsigned long long *)&s_tiles, (unsigned long long)local);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if ((tid & 31) == 0) atomicAdd((unsigned long long *)&s_tiles, (unsigned long long)local);   // one per warp
     __syncthreads();
     const long long NC = s_tiles;
     const long long T = NC > 0 ? (NC + P - 1) / P : 1;      // cost per stream
@@ -126,10 +150,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
     // streams past the last sequence's last stream, and the end marker stream_start[P]
     for (long long s = (NC > 0 ? (NC - 1) / T : -1) + 1 + tid; s <= P; s += blockDim.x)
         ((int32_t *)p.stream_start)[s] = total;
+#ifdef MLA_TRACE
+    __syncthreads();
+    if (tid == 0) g_plan_time[2] = ptx_globaltimer();
+#endif
 }
 
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
-    return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, max_work);
+    // one thread per sequence (whole warps, at most 1024): fewer threads, cheaper barriers
+    const int threads = p.B >= 1024 ? 1024 : ((p.B + 31) / 32) * 32;
+    return launch_pdl(plan_kernel, dim3(1), dim3(threads > 0 ? threads : 32), 0, st, p, max_work);
 }
 
 // ============================================================================

@@ -124,6 +124,7 @@ __device__ long long g_trace[32][kTraceTiles];
 // per CTA: start, end (globaltimer ns), items<<32 | tiles, then for items 0 and 1:
 // first S seen, epilogue begin, epilogue end
 __device__ unsigned long long g_cta_time[4096][9];
+__device__ unsigned long long g_cta_wait[4096];   // after the grid dependency wait
 #define MLA_TRACE_ITEM(slot, item)                                                               \
     do {                                                                                         \
         if ((item) < 2 && cta_id < 4096) g_cta_time[cta_id][3 + 3 * (item) + (slot)] = globaltimer(); \
@@ -276,6 +277,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     const uint32_t tmem = bars->tmem_base;
     // the set-up above overlaps the planner; its schedule is read only from here on
     pdl_wait();
+#ifdef MLA_TRACE
+    if (threadIdx.x == 0 && cta_id < 4096) g_cta_wait[cta_id] = globaltimer();
+#endif
     const int i0 = p.stream_start[stream], i1 = p.stream_start[stream + 1];
     if (i0 >= i1) {                          // no work for this stream (CTA-uniform)
         if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
@@ -845,6 +849,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             // by the tensor map.
             if (ok) {
                 const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                // the partials are read back by the combine right after this kernel:
+                // keep them in L2 over the KV stream, which is read once
+                const uint64_t keep = l2_policy_evict_last();
                 uint8_t *boxes = smem + kOffQ + (warp - 4) * kEpiBoxes * kEpiBoxBytes;
                 const int y = g * kRows + 32 * wq;
                 const bool store = y < rows_seq;                 // warp-uniform
@@ -876,7 +883,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0 && store) {
-                        tma_store_3d(&o_map, box, 256 * half + 128 * hs + 64 * c, y, i);
+                        tma_store_3d_hint(&o_map, box, 256 * half + 128 * hs + 64 * c, y, i, keep);
                         bulk_commit();
                     }
                 }
@@ -994,6 +1001,9 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
 #ifdef MLA_TRACE
 extern "C" int mla_trace_read(long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_trace, sizeof(long long) * (size_t)n);   // [32][64]
+}
+extern "C" int mla_trace_cta_wait(unsigned long long *host, int n) {
+    return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_wait, sizeof(unsigned long long) * (size_t)n);
 }
 extern "C" int mla_trace_cta(unsigned long long *host, int n) {
     return (int)cudaMemcpyFromSymbol(host, mla::tc::g_cta_time, sizeof(unsigned long long) * 9 * (size_t)n);
