@@ -209,3 +209,62 @@ def attention_rotated(q: np.ndarray, Chat: np.ndarray, KR: np.ndarray, R: np.nda
     o_lat = o_rot @ R.T
     out = np.einsum("qhr,hrv->qhv", o_lat, np.asarray(W_UV, dtype=np.float64))
     return out, lse
+
+
+# ---------------------------------------------------------------- rope-key variants
+# "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10), a later reply
+# about GLM-5.2 support: two designs "regarding ROPE+NOPE" were being benchmarked and
+# neither is described. The rotated-INT2 cache above keeps the rope key in bf16.
+# Readings adopted for the two alternatives built here (none of the details are on
+# the pages):
+#   * rope-INT2: the rope key is quantised too, unrotated (a RoPE'd key turns with
+#     the position, so a fixed covariance basis has no meaning for it), as two more
+#     INT2 groups of 32 with fp16 scale/zero and their own clip thresholds (the 99th
+#     percentile of |k_R| over calibration rope keys). The encoded row is
+#     [c . R ; k_R], 576 values in 18 groups; the latent groups are bit-identical to
+#     the bf16-rope cache's.
+#   * joint: [c ; k_R] is rotated as one 576-dim vector into the eigenbasis of
+#     Sigma_j = [c;k_R]^T [c;k_R] (ascending, same sign rule), clipped and encoded in
+#     18 groups. Scores use q . R_j; the output is o_j . R_j^T, whose first r dims are
+#     the latent output.
+
+def rope_thresholds(KR_calib: np.ndarray, group: int = 32, pct: float = 99.0) -> np.ndarray:
+    """Clip thresholds of the rope groups: pct-th percentile of |k_R| per group."""
+    d = np.asarray(KR_calib).shape[1]
+    return clip_thresholds(KR_calib, np.eye(d), group, pct)
+
+
+def quantize_rope_int2(c: np.ndarray, KR: np.ndarray, R32: np.ndarray, T32: np.ndarray,
+                       TR32: np.ndarray, group: int = 32):
+    """rope-INT2 encoding of tokens (c [n, r], k_R [n, d_R]): the row [c . R ; k_R]
+    (fp32 rotation chain for the latent part, the rope key as given) encoded in
+    groups with thresholds [T ; T_R]. Returns codes [n, (r+d_R)/4], sz [n, (r+d_R)/group, 2]."""
+    y = np.concatenate([rotate_fp32(c, R32), np.asarray(KR, dtype=np.float32)], axis=1)
+    T = np.concatenate([np.asarray(T32, np.float32), np.asarray(TR32, np.float32)])
+    return encode(y, T, group)
+
+
+def attention_rope_int2(q: np.ndarray, Y_hat: np.ndarray, R: np.ndarray, W_UV: np.ndarray,
+                        scale: float):
+    """Absorbed attention against a rope-INT2 cache: Y_hat [L, r + d_R] is the
+    dequantised row [c^ ; k_R^] (rotated latent, then the rope key)."""
+    r = np.asarray(R).shape[0]
+    return attention_rotated(q, Y_hat[:, :r], Y_hat[:, r:], R, W_UV, scale)
+
+
+def attention_joint(q: np.ndarray, Y_hat: np.ndarray, Rj: np.ndarray, W_UV: np.ndarray,
+                    scale: float):
+    """Absorbed attention against a jointly rotated cache: Y_hat [L, r + d_R] holds
+    [c ; k_R] . R_j (dequantised). Scores: (q . R_j) . Y_hat (= q . [c ; k_R] before
+    quantisation); output: o_j . R_j^T, of which the first r dims are o_lat."""
+    Rj = np.asarray(Rj, dtype=np.float64)
+    D = Rj.shape[0]
+    r = np.asarray(W_UV).shape[1]
+    q = q.astype(np.float64)
+    qj = q @ Rj
+    L = Y_hat.shape[0]
+    _, lse, oj = attention.absorbed(qj, Y_hat, np.zeros((L, 0)), np.zeros((q.shape[1], D, 1)), scale,
+                                    return_latent=True)
+    o_lat = (oj @ Rj.T)[..., :r]
+    out = np.einsum("qhr,hrv->qhv", o_lat, np.asarray(W_UV, dtype=np.float64))
+    return out, lse

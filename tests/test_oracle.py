@@ -415,3 +415,112 @@ def test_weighted_rotation_study():
     print({k: round(v, 4) for k, v in res.items()})
     assert res["isotropic", "weighted"] > 0.97 * res["isotropic", "plain"]
     assert res["anisotropic", "weighted"] > 1.3 * res["anisotropic", "plain"]
+
+
+# ------------------------------------------------------- rope-key variants (next-2)
+
+def _rope_setup(n=96, seed=21):
+    w = workloads.int2_rotated(seed, B=1, H=4, len_range=(n, n), n_calib=4096)
+    R, _ = oint2.fit_rotation(w.calib)
+    T = oint2.clip_thresholds(w.calib, R)
+    return w, R, T
+
+
+def test_rope_int2_latent_groups_match_the_bf16_rope_cache():
+    """Quantising the rope key as two more groups leaves the latent's 16 groups (codes
+    and scale/zero) bit-identical to the cache that keeps the rope key in bf16."""
+    w, R, T = _rope_setup()
+    C, KR = w.latent[0], w.rope[0]
+    TR = oint2.rope_thresholds(KR.astype(np.float64))
+    codes, sz = oint2.quantize(C, R.astype(np.float32), T.astype(np.float32))
+    c2, s2 = oint2.quantize_rope_int2(C, KR, R.astype(np.float32), T.astype(np.float32), TR.astype(np.float32))
+    assert c2.shape == (C.shape[0], 144) and s2.shape == (C.shape[0], 18, 2)
+    np.testing.assert_array_equal(c2[:, :128], codes)
+    np.testing.assert_array_equal(s2[:, :16], sz)
+
+
+def test_rope_int2_is_lossless_on_four_level_keys():
+    """Rope groups whose values are the four levels -1.5, -0.5, 0.5, 1.5 (clip 1.5)
+    encode with scale 1 and zero -1.5 exactly, decode exactly, and the attention over
+    the rope-INT2 row equals the attention over the bf16-rope cache."""
+    w, R, T = _rope_setup()
+    rng = np.random.default_rng(3)
+    n = w.latent[0].shape[0]
+    levels = np.array([-1.5, -0.5, 0.5, 1.5], np.float32)
+    KR = levels[rng.integers(0, 4, size=(n, 64))]
+    KR[:, [0, 32]] = -1.5
+    KR[:, [1, 33]] = 1.5                 # every token's two groups span the full range
+    TR = np.array([1.5, 1.5], np.float32)
+    c2, s2 = oint2.quantize_rope_int2(w.latent[0], KR, R.astype(np.float32), T.astype(np.float32), TR)
+    Y = oint2.decode(c2, s2)
+    np.testing.assert_array_equal(Y[:, 512:], KR)
+    np.testing.assert_array_equal(oint2.unpack_codes(c2)[:, 512:], (KR + 1.5).astype(np.int64))
+    o1, l1 = oint2.attention_rope_int2(w.q[0], Y.astype(np.float64), R, w.W_UV, w.scale)
+    o2, l2 = oint2.attention_rotated(w.q[0], Y[:, :512], KR, R, w.W_UV, w.scale)
+    assert np.max(np.abs(o1 - o2)) < 1e-12 and np.max(np.abs(l1 - l2)) < 1e-12
+
+
+def test_joint_rotation_attention_is_exact_without_quantisation():
+    """With the rotated row kept exact, the jointly rotated attention is the plain
+    absorbed attention: scores through q . R_j, output through o_j . R_j^T (a Haar
+    rotation, not symmetric, so an R_j / R_j^T swap anywhere fails)."""
+    rng = np.random.default_rng(5)
+    L, H, r, dR = 40, 4, 512, 64
+    C = rng.standard_normal((L, r))
+    KR = rng.standard_normal((L, dR))
+    q = rng.standard_normal((2, H, r + dR))
+    W = rng.standard_normal((H, r, 16)) / np.sqrt(r)
+    Rj = workloads.haar_orthogonal(rng, r + dR)
+    Y = np.concatenate([C, KR], 1) @ Rj
+    o1, l1 = oint2.attention_joint(q, Y, Rj, W, 0.05)
+    o2, l2 = attention.absorbed(q, C, KR, W, 0.05)
+    assert np.max(np.abs(o1 - o2)) < 1e-10 and np.max(np.abs(l1 - l2)) < 1e-10
+
+
+def test_rope_variants_study():
+    """Bytes and error of the three rope-key layouts on the INT2 workload's law (the
+    comparison reported in the design notes). Per token: bf16 rope key 128 B codes +
+    64 B scale/zero + 128 B rope = 320 B; rope-INT2 and joint 144 B + 72 B = 216 B.
+    INT2 costs each covered dim about the same relative error (~0.38 on this law), so
+    both variants add about 4 % to the score error of the bf16-rope cache."""
+    w = workloads.int2_rotated(4, B=4, H=32, len_range=(512, 768), n_calib=32768)
+    rng = np.random.default_rng(11)
+    KRcal = workloads.bf16_round(rng.standard_normal((32768, 64)).astype(np.float32)).astype(np.float64)
+    R, _ = oint2.fit_rotation(w.calib)
+    T = oint2.clip_thresholds(w.calib, R)
+    TR = oint2.rope_thresholds(KRcal)
+    Xj = np.concatenate([w.calib, KRcal], axis=1)
+    Rj, _ = oint2.fit_rotation(Xj)
+    Tj = oint2.clip_thresholds(Xj, Rj)
+    R32, T32, TR32, Rj32, Tj32 = (a.astype(np.float32) for a in (R, T, TR, Rj, Tj))
+    res = {}
+    for b in range(w.B):
+        C, KR, q = (a.astype(np.float64) for a in (w.latent[b], w.rope[b], w.q[b]))
+        K = np.concatenate([C, KR], 1)
+        S = q[0] @ K.T
+        ref, rl = attention.absorbed(q, C, KR, w.W_UV, w.scale)
+        codes, sz = oint2.quantize(C, R32, T32)
+        Ch = oint2.decode(codes, sz).astype(np.float64)
+        c2, s2 = oint2.quantize_rope_int2(C, KR, R32, T32, TR32)
+        Y2 = oint2.decode(c2, s2).astype(np.float64)
+        c3, s3 = oint2.quantize(K, Rj32, Tj32)
+        Y3 = oint2.decode(c3, s3).astype(np.float64)
+        layouts = (
+            ("bf16 rope", codes.nbytes + sz.nbytes + KR.shape[0] * 64 * 2, np.concatenate([Ch @ R.T, KR], 1),
+             oint2.attention_rotated(q, Ch, KR, R, w.W_UV, w.scale)),
+            ("rope-INT2", c2.nbytes + s2.nbytes, np.concatenate([Y2[:, :512] @ R.T, Y2[:, 512:]], 1),
+             oint2.attention_rope_int2(q, Y2, R, w.W_UV, w.scale)),
+            ("joint", c3.nbytes + s3.nbytes, Y3 @ Rj.T, oint2.attention_joint(q, Y3, Rj, w.W_UV, w.scale)),
+        )
+        for name, nbytes, Kh, (o, l) in layouts:
+            row = (nbytes / C.shape[0], np.linalg.norm(q[0] @ Kh.T - S) / np.linalg.norm(S),
+                   np.linalg.norm(Kh[:, 512:] - KR) / np.linalg.norm(KR),
+                   np.linalg.norm(o - ref) / np.linalg.norm(ref), float(np.max(np.abs(l - rl))))
+            res.setdefault(name, []).append(row)
+    m = {k: np.mean(np.array(v), axis=0) for k, v in res.items()}
+    print({k: [round(float(x), 4) for x in v] for k, v in m.items()})
+    assert m["bf16 rope"][0] == 320 and m["rope-INT2"][0] == 216 and m["joint"][0] == 216
+    assert m["bf16 rope"][2] == 0.0                      # rope key kept exactly
+    for name in ("rope-INT2", "joint"):
+        assert 0.3 < m[name][2] < 0.5                    # INT2 error on the rope dims
+        assert 1.0 < m[name][1] / m["bf16 rope"][1] < 1.1
