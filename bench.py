@@ -549,8 +549,13 @@ def run_configs(args):
         code, flags = mla.mla_get_status(ws)
         tok = int(w.seq_lens.sum())
         D = w.r + w.d_rope
-        kb = tok * (D * 2 if kind == mla.MLA_KV_BF16 else w.r // 4 + (w.r // 32) * 4 + 2 * w.d_rope) + \
-            w.B * q_len * w.H * D * 2
+        if kind == mla.MLA_KV_BF16:
+            per_tok = D * 2
+        elif kind == mla.MLA_KV_INT2_ROT:
+            per_tok = w.r // 4 + (w.r // 32) * 4 + 2 * w.d_rope
+        else:                                   # the rope key held as codes as well
+            per_tok = D // 4 + (D // 32) * 4
+        kb = tok * per_tok + w.B * q_len * w.H * D * 2
         fl = 2 * tok * q_len * w.H * (D + w.r)
         att = ms / na
         print(json.dumps({"config": name, "tokens": tok, "call_us": tot / n * 1e3, "attention_us": att * 1e3,
@@ -571,6 +576,9 @@ def run_configs(args):
     # timing only: any orthogonal R and positive thresholds exercise the same kernels
     R = workloads.haar_orthogonal(np.random.Generator(np.random.PCG64(5)), w.r)
     run("C4 rotated-INT2 decode", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0))
+    # next-2: the same workload with the rope key held as two more INT2 groups (216 B a token)
+    run("C6 rotated-INT2 decode, rope key as INT2 too", w, mla.MLA_KV_INT2_ROT_QR, 1, R=R,
+        T=np.full((w.r + w.d_rope) // 32, 4.0))
     return 0
 
 

@@ -15,6 +15,9 @@
  * covariance eigenbasis R and quantised to grouped INT2 (rope key kept bf16).
  *   Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10),
  *   maintainer reply, "How the rotation adapts to the latent".
+ * A variant of it quantises the rope key as well, unrotated, as further INT2
+ * groups (MLA_KV_INT2_ROT_QR): one of the rope/nope designs the same thread
+ * names as benchmarked, without details (a later reply on GLM-5.2 support).
  *
  * Definitions (per sequence b, query row i, head h, cached token t):
  *   s = scale * (q[b,i,h,:] . [c_t ; kR_t])          (rotated kind: q_lat . R)
@@ -61,7 +64,10 @@ typedef enum {
 typedef enum {
     MLA_KV_BF16 = 0,           /* latent + rope key, bf16, one row per token       */
     MLA_KV_FP32 = 1,           /* latent + rope key, fp32, one row per token       */
-    MLA_KV_INT2_ROT = 2        /* rotated latent as grouped INT2 + bf16 rope key   */
+    MLA_KV_INT2_ROT = 2,       /* rotated latent as grouped INT2 + bf16 rope key   */
+    MLA_KV_INT2_ROT_QR = 3     /* rotated latent and the (unrotated) rope key, both
+                                  as grouped INT2: [c . R ; k_R] in (r + d_R) /
+                                  group_size groups; d_R a multiple of group_size */
 } mla_kv_kind;
 
 typedef enum {
@@ -98,6 +104,9 @@ typedef struct {
  *               scale_zero [num_blocks, block_size, r / group_size, 2] fp16
  *                          (scale, zero); value = fmaf(code, scale, zero)
  *               rope       [num_blocks, block_size, d_R]      bf16
+ *   INT2_ROT_QR: codes      [num_blocks, block_size, (r + d_R) / 4] uint8 and
+ *               scale_zero [num_blocks, block_size, (r + d_R) / group_size, 2]
+ *                          fp16, as above over the row [c . R ; k_R]; rope unused
  * Unused members are NULL. */
 typedef struct {
     void *latent;
@@ -121,12 +130,15 @@ size_t mla_workspace_bytes(const mla_shape *shape, int32_t B, int32_t q_len);
  *   k_rope      [num_new, d_R] bf16 (FP32 kind: fp32)
  *   R           INT2 only: [r, r] fp32 row-major, y = c . R (column j is the
  *               j-th eigenvector in ascending eigenvalue order); else NULL.
- *   clip        INT2 only: [r / group_size] fp32 clip thresholds; else NULL.
+ *   clip        INT2 kinds: [r / group_size] fp32 clip thresholds (INT2_ROT_QR:
+ *               [(r + d_R) / group_size], the rope groups' after the latent's);
+ *               else NULL.
  *   status      optional [1] int32 device word; flags are OR-ed into it.
  * INT2 encoding per token and group g of group_size dims: y = fp32 fmaf chain
  * over k ascending; y clipped to [-clip[g], clip[g]]; scale =
  * fp16_rne((max - min) / 3), zero = fp16_rne(min); code = clamp(rint((y -
- * zero) / scale), 0, 3), 0 when scale == 0.
+ * zero) / scale), 0, 3), 0 when scale == 0. INT2_ROT_QR: the rope groups encode
+ * k_R as given (bf16 widened to fp32, not rotated) with their own thresholds.
  *   Source: OSCAR issue #10, maintainer reply (rotated + quantised latent in
  *   the cache, thresholds fit on the rotated latent). */
 mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache,

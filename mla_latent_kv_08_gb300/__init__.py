@@ -29,6 +29,7 @@ MLA_ERR_TIMEOUT = -6
 MLA_KV_BF16 = 0
 MLA_KV_FP32 = 1
 MLA_KV_INT2_ROT = 2
+MLA_KV_INT2_ROT_QR = 3
 
 MLA_IMPL_AUTO = 0
 MLA_IMPL_SIMT = 1
@@ -186,6 +187,11 @@ class Cache:
                        codes=alloc((nb, bs, r // 4), dtype=torch.uint8, device=device),
                        scale_zero=alloc((nb, bs, r // shape.group_size, 2), dtype=torch.float16, device=device),
                        rope=alloc((nb, bs, dR), dtype=torch.bfloat16, device=device))
+        if shape.kind == MLA_KV_INT2_ROT_QR:      # the rope key's codes follow the latent's
+            return cls(shape,
+                       codes=alloc((nb, bs, (r + dR) // 4), dtype=torch.uint8, device=device),
+                       scale_zero=alloc((nb, bs, (r + dR) // shape.group_size, 2), dtype=torch.float16,
+                                        device=device))
         dt = torch.float32 if shape.kind == MLA_KV_FP32 else torch.bfloat16
         return cls(shape, latent=alloc((nb, bs, r + dR + shape.index_dim), dtype=dt, device=device))
 
@@ -193,6 +199,9 @@ class Cache:
         s = self.shape
         if s.kind == MLA_KV_INT2_ROT:
             return s.kv_lora_rank // 4 + (s.kv_lora_rank // s.group_size) * 4 + 2 * s.rope_dim
+        if s.kind == MLA_KV_INT2_ROT_QR:
+            qd = s.kv_lora_rank + s.rope_dim
+            return qd // 4 + (qd // s.group_size) * 4
         return (4 if s.kind == MLA_KV_FP32 else 2) * (s.kv_lora_rank + s.rope_dim + s.index_dim)
 
 

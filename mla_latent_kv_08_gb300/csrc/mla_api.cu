@@ -54,15 +54,15 @@ static mla_status check_shape(const mla_shape *s) {
     if (s->num_heads < 1 || s->kv_lora_rank < 8 || s->kv_lora_rank % 8 || s->rope_dim < 0 ||
         s->rope_dim % 8 || s->v_head_dim < 1 || s->block_size < 1 || s->num_blocks < 1)
         return MLA_ERR_INVALID;
-    if (s->kind != MLA_KV_BF16 && s->kind != MLA_KV_FP32 && s->kind != MLA_KV_INT2_ROT)
-        return MLA_ERR_INVALID;
+    if (s->kind != MLA_KV_BF16 && s->kind != MLA_KV_FP32 && !is_int2(s->kind)) return MLA_ERR_INVALID;
     if (s->impl < MLA_IMPL_AUTO || s->impl > MLA_IMPL_TCGEN05 || s->num_splits_hint < 0)
         return MLA_ERR_INVALID;
     if (s->index_dim < 0 || s->index_dim % 8 || s->index_dim > 1024) return MLA_ERR_INVALID;
-    if (s->kind == MLA_KV_INT2_ROT && s->index_dim != 0) return MLA_ERR_INVALID;
-    if (s->kind == MLA_KV_INT2_ROT) {
+    if (is_int2(s->kind) && s->index_dim != 0) return MLA_ERR_INVALID;
+    if (is_int2(s->kind)) {
         if (s->group_size < 4 || s->group_size % 4 || s->kv_lora_rank % s->group_size) return MLA_ERR_INVALID;
         if (s->rope_dim < 8) return MLA_ERR_INVALID;
+        if (s->kind == MLA_KV_INT2_ROT_QR && s->rope_dim % s->group_size) return MLA_ERR_INVALID;
     }
     // generic kernel limits (shared-memory tiles sized from r and d_R)
     if (s->kv_lora_rank > 1024 || s->rope_dim > 128) return MLA_ERR_UNSUPPORTED;
@@ -79,7 +79,7 @@ static ShapeArgs shape_args(const mla_shape *s) {
     a.num_blocks = s->num_blocks;
     a.gs = s->group_size;
     a.kind = s->kind;
-    a.ix = s->kind == MLA_KV_INT2_ROT ? 0 : s->index_dim;
+    a.ix = is_int2(s->kind) ? 0 : s->index_dim;
     return a;
 }
 
@@ -122,7 +122,7 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
     w.part_o = off;        off = up256(off + sizeof(float) * (size_t)w.max_work * rows * s->kv_lora_rank);
     w.part_lse = off;      off = up256(off + sizeof(float) * (size_t)w.max_work * rows);
     w.q_prep = off;
-    if (s->kind == MLA_KV_INT2_ROT) {
+    if (is_int2(s->kind)) {
         const size_t nrow = (size_t)B * rows;
         off = up256(off + sizeof(float) * nrow * (s->kv_lora_rank + s->rope_dim));
         w.o_rot = off;  off = up256(off + sizeof(float) * nrow * s->kv_lora_rank);
@@ -144,10 +144,12 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     if (!cache || !block_table || !seq_lens || !q || !W_UV || !out || !lse || !workspace) return MLA_ERR_INVALID;
     if (B < 1 || q_len < 1 || max_blocks < 1) return MLA_ERR_INVALID;
     if (!(scale == scale)) return MLA_ERR_INVALID;
-    const bool int2 = s->kind == MLA_KV_INT2_ROT;
+    const bool int2 = is_int2(s->kind);
+    const bool rope_bf16 = s->kind == MLA_KV_INT2_ROT;      // INT2_ROT_QR holds the rope key as codes
     if (int2) {
-        if (!cache->codes || !cache->scale_zero || !cache->rope || !R) return MLA_ERR_INVALID;
-        if (!aligned16(cache->codes) || !aligned16(cache->scale_zero) || !aligned16(cache->rope)) return MLA_ERR_INVALID;
+        if (!cache->codes || !cache->scale_zero || (rope_bf16 && !cache->rope) || !R) return MLA_ERR_INVALID;
+        if (!aligned16(cache->codes) || !aligned16(cache->scale_zero) || (rope_bf16 && !aligned16(cache->rope)))
+            return MLA_ERR_INVALID;
     } else {
         if (!cache->latent || !aligned16(cache->latent)) return MLA_ERR_INVALID;
     }
@@ -264,9 +266,10 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, con
         return MLA_ERR_INVALID;
     if (num_new == 0) return MLA_OK;
     if (!c_kv || !k_rope || !aligned16(c_kv) || !aligned16(k_rope)) return MLA_ERR_INVALID;
-    const bool int2 = shape->kind == MLA_KV_INT2_ROT;
+    const bool int2 = is_int2(shape->kind);
     if (int2) {
-        if (!cache->codes || !cache->scale_zero || !cache->rope || !R || !clip) return MLA_ERR_INVALID;
+        if (!cache->codes || !cache->scale_zero || (shape->kind == MLA_KV_INT2_ROT && !cache->rope) || !R || !clip)
+            return MLA_ERR_INVALID;
     } else {
         if (!cache->latent || !aligned16(cache->latent)) return MLA_ERR_INVALID;
     }
@@ -299,7 +302,7 @@ mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cach
                                    int32_t *status, void *stream) {
     mla_status st = check_shape(shape);
     if (st != MLA_OK) return st;
-    if (shape->kind == MLA_KV_INT2_ROT || shape->index_dim == 0) return MLA_ERR_INVALID;
+    if (is_int2(shape->kind) || shape->index_dim == 0) return MLA_ERR_INVALID;
     if (!cache || !block_table || !start_pos || !cu_new || B < 1 || max_blocks_per_seq < 1 || num_new < 0)
         return MLA_ERR_INVALID;
     if (num_new == 0) return MLA_OK;

@@ -263,7 +263,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace comb
 
 bool combine_tc_supported(const ShapeArgs &s) {
-    return (s.kind == MLA_KV_BF16 || s.kind == MLA_KV_INT2_ROT) && s.r == comb::kR && s.dv == comb::kDv;
+    return (s.kind == MLA_KV_BF16 || is_int2(s.kind)) && s.r == comb::kR && s.dv == comb::kDv;
 }
 
 cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st) {

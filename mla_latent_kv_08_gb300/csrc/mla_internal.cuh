@@ -55,7 +55,13 @@ struct ShapeArgs {
     int32_t ix;                  // extra per-token key after the rope key (BF16/FP32 kinds)
     __host__ __device__ int32_t D() const { return r + dR; }        // elements attention reads
     __host__ __device__ int32_t E() const { return r + dR + ix; }   // cache row stride (BF16/FP32)
+    // INT2 kinds: dims held as codes per token (the latent; INT2_ROT_QR: + the rope key)
+    __host__ __device__ int32_t QD() const { return kind == MLA_KV_INT2_ROT_QR ? r + dR : r; }
 };
+
+__host__ __device__ constexpr bool is_int2(int32_t kind) {
+    return kind == MLA_KV_INT2_ROT || kind == MLA_KV_INT2_ROT_QR;
+}
 
 // Everything a decode kernel reads.
 struct DecodeParams {

@@ -298,8 +298,9 @@ __device__ __forceinline__ void gather_tile(const DecodeParams &p, int b, int tb
             }
         }
     } else {
-        // INT2: one thread per code byte (4 latent dims), then the bf16 rope key.
-        const int nbytes = r / 4, gs = p.s.gs, ng = r / gs;
+        // INT2: one thread per code byte (4 dims), then the bf16 rope key (INT2_ROT_QR:
+        // the rope key's codes follow the latent's in the row, so the bytes cover it).
+        const int nbytes = p.s.QD() / 4, gs = p.s.gs, ng = p.s.QD() / gs;
         for (int idx = threadIdx.x; idx < kTT * nbytes; idx += blockDim.x) {
             int tt = idx / nbytes, k = idx % nbytes;
             int blk1 = sValid[tt];
@@ -316,15 +317,17 @@ __device__ __forceinline__ void gather_tile(const DecodeParams &p, int b, int tb
                 dst[0] = dst[1] = dst[2] = dst[3] = 0.f;
             }
         }
-        for (int idx = threadIdx.x; idx < kTT * dR; idx += blockDim.x) {
-            int tt = idx / dR, d = idx % dR;
-            int blk1 = sValid[tt];
-            float v = 0.f;
-            if (blk1) {
-                size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
-                v = __bfloat162float(p.rope[row * dR + d]);
+        if (p.s.kind == MLA_KV_INT2_ROT) {
+            for (int idx = threadIdx.x; idx < kTT * dR; idx += blockDim.x) {
+                int tt = idx / dR, d = idx % dR;
+                int blk1 = sValid[tt];
+                float v = 0.f;
+                if (blk1) {
+                    size_t row = (size_t)(blk1 - 1) * bs + (tb + tt) % bs;
+                    v = __bfloat162float(p.rope[row * dR + d]);
+                }
+                sK[tt * Dp + r + d] = v;
             }
-            sK[tt * Dp + r + d] = v;
         }
     }
 }
@@ -679,8 +682,11 @@ template <int NC>
 __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
     extern __shared__ float sa[];
     const int r = p.s.r, dR = p.s.dR, gs = p.s.gs, ng = r / gs;
+    const bool rope_codes = p.s.kind == MLA_KV_INT2_ROT_QR;   // the rope key as INT2 groups too
+    const int QD = p.s.QD(), ng_all = QD / gs;
     float *sc = sa;                   // [kAT][r] latent (fp32)
     float *sy = sc + kAT * r;         // [kAT][r] rotated
+    float *sr = sy + kAT * r;         // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
     __shared__ long long s_row[kAT];
     const int n0 = blockIdx.x * kAT;
     const int tid = threadIdx.x;
@@ -690,6 +696,12 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
         int t = idx / r, k = idx % r;
         sc[idx] = (n0 + t < p.num_new) ? __bfloat162float(c[(size_t)(n0 + t) * r + k]) : 0.f;
     }
+    const __nv_bfloat16 *kr = (const __nv_bfloat16 *)p.k_rope;
+    if (rope_codes)
+        for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
+            int t = idx / dR, d = idx % dR;
+            sr[idx] = (n0 + t < p.num_new) ? __bfloat162float(kr[(size_t)(n0 + t) * dR + d]) : 0.f;
+        }
     __syncthreads();
     float acc[kAT][NC];
 #pragma unroll
@@ -718,12 +730,13 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
             if (j < r) sy[t * r + j] = acc[t][cc];
         }
     __syncthreads();
-    for (int job = tid; job < kAT * ng; job += blockDim.x) {
-        const int t = job / ng, g = job % ng;
+    // groups 0..ng-1: the rotated latent; INT2_ROT_QR: then the rope key's groups
+    for (int job = tid; job < kAT * ng_all; job += blockDim.x) {
+        const int t = job / ng_all, g = job % ng_all;
         const long long row = s_row[t];
         if (row < 0) continue;
         const float thr = p.clip[g];
-        const float *y = sy + t * r + g * gs;
+        const float *y = g < ng ? sy + t * r + g * gs : sr + t * dR + (g - ng) * gs;
         float lo = CUDART_INF_F, hi = -CUDART_INF_F;
         for (int j = 0; j < gs; ++j) {
             float v = fminf(fmaxf(y[j], -thr), thr);
@@ -733,7 +746,7 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
         const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
         const __half z16 = __float2half_rn(lo);
         const float s = __half2float(s16), z = __half2float(z16);
-        uint8_t *dst = p.codes + (size_t)row * (r / 4) + g * (gs / 4);
+        uint8_t *dst = p.codes + (size_t)row * (QD / 4) + g * (gs / 4);
         for (int j4 = 0; j4 < gs / 4; ++j4) {
             unsigned byte = 0;
 #pragma unroll
@@ -748,16 +761,16 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
             }
             dst[j4] = (uint8_t)byte;
         }
-        __half *szp = p.scale_zero + ((size_t)row * ng + g) * 2;
+        __half *szp = p.scale_zero + ((size_t)row * ng_all + g) * 2;
         szp[0] = s16;
         szp[1] = z16;
     }
-    const __nv_bfloat16 *kr = (const __nv_bfloat16 *)p.k_rope;
-    for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
-        const int t = idx / dR, d = idx % dR;
-        const long long row = s_row[t];
-        if (row >= 0) p.rope[(size_t)row * dR + d] = kr[(size_t)(n0 + t) * dR + d];
-    }
+    if (!rope_codes)
+        for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
+            const int t = idx / dR, d = idx % dR;
+            const long long row = s_row[t];
+            if (row >= 0) p.rope[(size_t)row * dR + d] = kr[(size_t)(n0 + t) * dR + d];
+        }
 }
 
 cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st) {
@@ -774,7 +787,7 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
     } else if (p.s.kind == MLA_KV_FP32) {
         return launch_pdl(append_copy_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     } else {
-        const size_t smem = sizeof(float) * 2 * kAT * (size_t)p.s.r;
+        const size_t smem = sizeof(float) * kAT * (2 * (size_t)p.s.r + (p.s.kind == MLA_KV_INT2_ROT_QR ? p.s.dR : 0));
         dim3 grid((p.num_new + kAT - 1) / kAT);
         if (p.s.r <= 256) {
             cudaFuncSetAttribute(append_int2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

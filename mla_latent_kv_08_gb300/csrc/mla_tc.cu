@@ -50,7 +50,7 @@ namespace tc {
 
 // Threads per CTA: warps 0..3 control (producer, MMA, two dequantisers), 4..11
 // softmax; the INT2 kind adds dequantising warps 12..15.
-template <int KIND> constexpr int threads_of() { return KIND == MLA_KV_INT2_ROT ? 512 : 384; }
+template <int KIND> constexpr int threads_of() { return is_int2(KIND) ? 512 : 384; }
 constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
@@ -68,6 +68,7 @@ template <> struct Layout<MLA_KV_BF16> {
 template <> struct Layout<MLA_KV_INT2_ROT> {
     static constexpr int kSBufs = 1, kQTmemBlocks = 6, kQSmemBlocks = 3;
 };
+template <> struct Layout<MLA_KV_INT2_ROT_QR> : Layout<MLA_KV_INT2_ROT> {};
 constexpr int kMaxQSmemBlocks = 5;
 constexpr int kSoftmaxThreads = 256;  // warps 4..11: two warps per 32-row lane quarter
 
@@ -80,7 +81,18 @@ constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
 // rope keys [64 x 128 B], copied verbatim and expanded into a stage by the
 // dequantising warps.
 constexpr uint32_t kRawCodes = kTile * 128, kRawSz = kTile * 64, kRawRope = kTile * 128;
-constexpr uint32_t kRawBytes = kRawCodes + kRawSz + kRawRope;       // 20 KB
+constexpr uint32_t kRawBytes = kRawCodes + kRawSz + kRawRope;       // 20 KB (the larger of the two kinds)
+// Raw stage per INT2 kind, bytes per token: codes, scale/zero pairs, bf16 rope key.
+// INT2_ROT_QR holds the rope key as two more groups of codes (none in bf16).
+template <int KIND> struct Raw {
+    static constexpr bool kQR = KIND == MLA_KV_INT2_ROT_QR;
+    static constexpr uint32_t kGroups = kQR ? 18 : 16;               // groups of 32 per token
+    static constexpr uint32_t kCodesRow = 8 * kGroups, kSzRow = 4 * kGroups, kRopeRow = kQR ? 0 : 128;
+    static constexpr uint32_t kCodes = kTile * kCodesRow, kSz = kTile * kSzRow, kRope = kTile * kRopeRow;
+    static constexpr uint32_t kBytes = kCodes + kSz + kRope;
+};
+static_assert(Raw<MLA_KV_INT2_ROT>::kBytes == kRawBytes && Raw<MLA_KV_INT2_ROT_QR>::kBytes <= kRawBytes,
+              "raw stage sizes");
 constexpr uint32_t kOffRaw = kOffQ + 3 * kQBlockBytes;              // 192 KB (INT2: after 3 Q blocks)
 constexpr uint32_t kOffBar = kOffQ + kMaxQSmemBlocks * kQBlockBytes; // 224 KB
 static_assert(kOffRaw + kRawBytes <= kOffBar, "INT2 raw stage must fit beside its Q blocks");
@@ -211,7 +223,8 @@ template <int KIND>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                  const __grid_constant__ CUtensorMap o_map, const TcParams tp) {
-    constexpr bool kInt2 = KIND == MLA_KV_INT2_ROT;
+    constexpr bool kInt2 = is_int2(KIND);
+    using RW = Raw<KIND>;
     constexpr int kSBufs = Layout<KIND>::kSBufs;
     constexpr int kQTmemBlocks = Layout<KIND>::kQTmemBlocks;
     constexpr int kQSmemBlocks = Layout<KIND>::kQSmemBlocks;
@@ -302,9 +315,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 const int blk = block_of(p, it.b, it.t0 / kTile + pt);
                 if (blk >= 0) {
                     if (kInt2) {
-                        prefetch_l2(p.codes + (size_t)blk * kRawCodes, kRawCodes);
-                        prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * kRawSz, kRawSz);
-                        prefetch_l2((const uint8_t *)p.rope + (size_t)blk * kRawRope, kRawRope);
+                        prefetch_l2(p.codes + (size_t)blk * RW::kCodes, RW::kCodes);
+                        prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz);
+                        if (RW::kRope) prefetch_l2((const uint8_t *)p.rope + (size_t)blk * RW::kRope, RW::kRope);
                     } else {
                         // the block's rows (index keys included: one contiguous range)
                         prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * p.s.E(),
@@ -335,15 +348,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         break;
                     }
                     uint8_t *raw = smem + kOffRaw;
-                    if (lane == 0) mbar_expect_tx(&bars->raw_full, kRawBytes);
+                    if (lane == 0) mbar_expect_tx(&bars->raw_full, RW::kBytes);
                     __syncwarp();
-                    if (lane == 0) bulk_load(raw, p.codes + (size_t)blk * kRawCodes, kRawCodes, &bars->raw_full);
+                    if (lane == 0) bulk_load(raw, p.codes + (size_t)blk * RW::kCodes, RW::kCodes, &bars->raw_full);
                     if (lane == 1)
-                        bulk_load(raw + kRawCodes, (const uint8_t *)p.scale_zero + (size_t)blk * kRawSz, kRawSz,
+                        bulk_load(raw + RW::kCodes, (const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz,
                                   &bars->raw_full);
-                    if (lane == 2)
-                        bulk_load(raw + kRawCodes + kRawSz, (const uint8_t *)p.rope + (size_t)blk * kRawRope, kRawRope,
-                                  &bars->raw_full);
+                    if (RW::kRope && lane == 2)
+                        bulk_load(raw + RW::kCodes + RW::kSz, (const uint8_t *)p.rope + (size_t)blk * RW::kRope,
+                                  RW::kRope, &bars->raw_full);
                     if (lane == 0) MLA_TRACE_POINT(24, T);
                 } else {
                     const int s = T % kStages;
@@ -419,59 +432,75 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 if (dt == 0) MLA_TRACE_POINT(26, T);
                 const int valid = min(kTile, L - (it.t0 + t * kTile));
                 const uint8_t *raw = smem + kOffRaw;
-                const uint4 *rope = (const uint4 *)(raw + kRawCodes + kRawSz);
+                const uint4 *rope = (const uint4 *)(raw + RW::kCodes + RW::kSz);
                 const uint8_t *codes = raw;
-                const __half *sz = (const __half *)(raw + kRawCodes);
+                const __half *sz = (const __half *)(raw + RW::kCodes);
                 uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                // latent: a lane expands one 32-dim group of one row (8 code bytes, one
-                // scale/zero pair) into four 16-byte chunks; a warp covers two rows per
-                // pass, so its code reads are 256 contiguous bytes.
+                // One 32-dim group of row rr (8 code bytes, one scale/zero pair) into four
+                // 16-byte chunks of fp16; zeros for slots past the sequence end.
+                auto expand_group = [&](int rr, int g, uint4 (&outc)[4]) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) outc[q4] = make_uint4(0, 0, 0, 0);
+                    if (rr >= valid) return;
+                    const uint2 cb = *(const uint2 *)(codes + rr * RW::kCodesRow + 8 * g);
+                    const __half2 szp = *(const __half2 *)(sz + (rr * RW::kGroups + g) * 2);
+                    const __half2 s2 = __half2half2(__low2half(szp)), z2 = __half2half2(__high2half(szp));
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const unsigned two = ((q4 < 2 ? cb.x : cb.y) >> (16 * (q4 & 1))) & 0xffffu;
+                        // two codes at a time in half2: 1024 + c has the bits 0x6400 | c,
+                        // so subtracting 1024 gives c exactly; then one fused c * s + z
+                        // rounded once to fp16 (the operand type)
+                        __half2 hh[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const unsigned pr = (two >> (4 * e)) & 0xFu;
+                            const unsigned wv = 0x64006400u | (pr & 3u) | ((pr & 0xCu) << 14);
+                            const __half2 c2 = __hsub2(*(const __half2 *)&wv, k1024);
+                            hh[e] = __hfma2(c2, s2, z2);
+                        }
+                        const __half2 h0 = hh[0], h1 = hh[1], h2 = hh[2], h3 = hh[3];
+                        outc[q4] = make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1, *(const uint32_t *)&h2,
+                                              *(const uint32_t *)&h3);
+                    }
+                };
+                // latent: a lane expands one group of one row; a warp covers two rows per
+                // pass, so its code reads are contiguous.
                 const int half_lane = lane >> 4, grp = lane & 15;
                 for (int rr = 2 * dw + half_lane; rr < kTile; rr += 2 * kDequantWarps) {
-                    uint4 outc[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                                     make_uint4(0, 0, 0, 0)};
-                    if (rr < valid) {
-                        const uint2 cb = *(const uint2 *)(codes + rr * 128 + 8 * grp);
-                        const __half2 szp = *(const __half2 *)(sz + (rr * 16 + grp) * 2);
-                        const __half2 s2 = __half2half2(__low2half(szp)), z2 = __half2half2(__high2half(szp));
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const unsigned two = ((q4 < 2 ? cb.x : cb.y) >> (16 * (q4 & 1))) & 0xffffu;
-                            // two codes at a time in half2: 1024 + c has the bits 0x6400 | c,
-                            // so subtracting 1024 gives c exactly; then one fused c * s + z
-                            // rounded once to fp16 (the operand type)
-                            __half2 hh[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const unsigned pr = (two >> (4 * e)) & 0xFu;
-                                const unsigned wv = 0x64006400u | (pr & 3u) | ((pr & 0xCu) << 14);
-                                const __half2 c2 = __hsub2(*(const __half2 *)&wv, k1024);
-                                hh[e] = __hfma2(c2, s2, z2);
-                            }
-                            const __half2 h0 = hh[0], h1 = hh[1], h2 = hh[2], h3 = hh[3];
-                            outc[q4] = make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1,
-                                                  *(const uint32_t *)&h2, *(const uint32_t *)&h3);
-                        }
-                    }
+                    uint4 outc[4];
+                    expand_group(rr, grp, outc);
                     // group grp = latent chunks 4*grp .. 4*grp+3 = column block grp/2, chunks 4*(grp%2)..
                     uint8_t *blk = stage + (grp >> 1) * kKvBlockBytes;
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * (grp & 1) + q4)) = outc[q4];
                 }
-                // rope key: bf16 -> fp16 (exact for values inside fp16's range), 8 chunks a row
-                for (int job = dt; job < kTile * 8; job += kDequantThreads) {
-                    const int rr = job >> 3, ch = job & 7;
-                    uint4 out = make_uint4(0, 0, 0, 0);
-                    if (rr < valid) {
-                        const uint4 u = rope[rr * 8 + ch];
-                        const __nv_bfloat162 *bh = (const __nv_bfloat162 *)&u;
-                        __half2 hh[4];
+                if (RW::kQR) {
+                    // rope key held as codes: groups 16 and 17 of the row -> the rope block
+                    for (int job = dt; job < kTile * 2; job += kDequantThreads) {
+                        const int rr = job >> 1, gr = job & 1;
+                        uint4 outc[4];
+                        expand_group(rr, 16 + gr, outc);
+                        uint8_t *blk = stage + 8 * kKvBlockBytes;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) hh[e] = __float22half2_rn(__bfloat1622float2(bh[e]));
-                        out = make_uint4(*(const uint32_t *)&hh[0], *(const uint32_t *)&hh[1], *(const uint32_t *)&hh[2],
-                                         *(const uint32_t *)&hh[3]);
+                        for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * gr + q4)) = outc[q4];
                     }
-                    *(uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch)) = out;
+                } else {
+                    // rope key: bf16 -> fp16 (exact for values inside fp16's range), 8 chunks a row
+                    for (int job = dt; job < kTile * 8; job += kDequantThreads) {
+                        const int rr = job >> 3, ch = job & 7;
+                        uint4 out = make_uint4(0, 0, 0, 0);
+                        if (rr < valid) {
+                            const uint4 u = rope[rr * 8 + ch];
+                            const __nv_bfloat162 *bh = (const __nv_bfloat162 *)&u;
+                            __half2 hh[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) hh[e] = __float22half2_rn(__bfloat1622float2(bh[e]));
+                            out = make_uint4(*(const uint32_t *)&hh[0], *(const uint32_t *)&hh[1], *(const uint32_t *)&hh[2],
+                                             *(const uint32_t *)&hh[3]);
+                        }
+                        *(uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch)) = out;
+                    }
                 }
                 fence_proxy_async();
                 mbar_arrive(&bars->raw_empty);
@@ -966,7 +995,7 @@ static bool make_out_map(CUtensorMap *map, void *base, int r, int rows_seq, int 
 
 bool tc_shape_supported(const ShapeArgs &s) {
     if (s.r != 512 || s.dR != 64 || s.bs != tc::kTile) return false;
-    return s.kind == MLA_KV_BF16 || (s.kind == MLA_KV_INT2_ROT && s.gs == 32);
+    return s.kind == MLA_KV_BF16 || (is_int2(s.kind) && s.gs == 32);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
@@ -978,7 +1007,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     tp.v_sbo = 1024;
     CUtensorMap kv_map, q_map, o_map;
     memset(&kv_map, 0, sizeof kv_map);
-    const bool int2 = p.s.kind == MLA_KV_INT2_ROT;
+    const bool int2 = is_int2(p.s.kind);
     if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile,
                                CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)p.s.E()))
         return cudaErrorInvalidValue;
@@ -988,7 +1017,9 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
                       int2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return cudaErrorInvalidValue;
     if (!tc::make_out_map(&o_map, p.part_o, p.s.r, rows_seq, max_work)) return cudaErrorInvalidValue;
-    auto kern = int2 ? tc::decode_tc_kernel<MLA_KV_INT2_ROT> : tc::decode_tc_kernel<MLA_KV_BF16>;
+    auto kern = p.s.kind == MLA_KV_INT2_ROT_QR ? tc::decode_tc_kernel<MLA_KV_INT2_ROT_QR>
+                : int2                        ? tc::decode_tc_kernel<MLA_KV_INT2_ROT>
+                                              : tc::decode_tc_kernel<MLA_KV_BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);

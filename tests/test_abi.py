@@ -62,6 +62,11 @@ def test_shape_validation(lib):
     assert mla.mla_resolve_impl(_shape(index_dim=12)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(index_dim=2048)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, index_dim=64)) == mla.MLA_ERR_INVALID
+    # the rope key as INT2 groups: d_R a multiple of the group size; both kernels
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT_QR)) == mla.MLA_IMPL_TCGEN05
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT_QR, impl=mla.MLA_IMPL_SIMT)) == mla.MLA_IMPL_SIMT
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT_QR, rope_dim=48)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT_QR, index_dim=64)) == mla.MLA_ERR_INVALID
     # the generic kernel takes any supported shape, e.g. the tiny fp32 one
     assert mla.mla_resolve_impl(_shape(num_heads=8, kv_lora_rank=64, rope_dim=16, v_head_dim=32,
                                        block_size=256, kind=mla.MLA_KV_FP32)) == mla.MLA_IMPL_SIMT

@@ -496,3 +496,44 @@ def test_tensor_core_decode_with_the_generic_combine(gpu_lib):
     for b in range(w.B):
         ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+@pytest.mark.parametrize("impl_name,H", [("simt", 32), ("tcgen05", 32), ("tcgen05", 128)])
+def test_int2_rope_codes_append_and_decode(gpu_lib, impl_name, H):
+    """INT2_ROT_QR (the rope key quantised as two more INT2 groups): codes and
+    scale/zero of every appended token bit-exact against the oracle's encoding, and the
+    decode against the oracle's attention over the dequantised rows."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=4, H=H, len_range=(40, 300))
+    rng = np.random.default_rng(12)
+    KRcal = workloads.bf16_round(rng.standard_normal((8192, 64)).astype(np.float32)).astype(np.float64)
+    TR32 = oint2.rope_thresholds(KRcal).astype(np.float32)
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT_QR, impl=impl)
+    assert mla.mla_resolve_impl(shape) == impl
+    cache = mla.Cache.allocate(shape)
+    assert cache.rope is None and cache.bytes_per_token() == 216
+    Tall = np.concatenate([T32, TR32])
+    st0 = gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32), R32, Tall)
+    st1 = gu.append_tokens(cache, w, w.new_latent, w.new_rope, w.start_pos, R32, Tall)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st0)[0] == mla.MLA_OK and mla.mla_read_status_word(st1)[0] == mla.MLA_OK
+    ref = []
+    for b in range(w.B):
+        C = np.concatenate([w.latent[b], w.new_latent[b]])
+        KR = np.concatenate([w.rope[b], w.new_rope[b]])
+        ref.append(oint2.quantize_rope_int2(C, KR, R32, T32, TR32))
+    nb = w.num_blocks
+    ref_codes = layout.write_paged(nb, 64, 144, w.block_table, [x[0] for x in ref], [0] * w.B, np.uint8)
+    ref_sz = layout.write_paged(nb, 64, 36, w.block_table, [x[1].reshape(-1, 36) for x in ref], [0] * w.B, np.uint16)
+    np.testing.assert_array_equal(cache.codes.cpu().numpy(), ref_codes)
+    np.testing.assert_array_equal(cache.scale_zero.cpu().view(torch.int16).numpy().view(np.uint16).reshape(nb, 64, 36),
+                                  ref_sz)
+    w.seq_lens = (w.seq_lens + 32).astype(np.int32)
+    out, lse, ws = gu.attend(w, shape, cache, w.q, R=R32)
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    for b in range(w.B):
+        Y = oint2.decode(ref[b][0], ref[b][1]).astype(np.float64)
+        ro, rl = oint2.attention_rope_int2(w.q[b], Y, R32, w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
