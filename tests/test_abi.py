@@ -118,3 +118,19 @@ def test_index_append_refused_without_an_index_field(lib):
     s1 = _shape(index_dim=64).c()                  # no cache pointer
     assert lib.mla_latent_append_index(ctypes.byref(s1), ctypes.byref(cache), fake, 4, 2, fake, fake, 3, fake,
                                        None, None) == mla.MLA_ERR_INVALID
+
+
+def test_cache_layout_bytes_per_kind():
+    """The binding allocates each cache kind as the header lays it out, and its per-token
+    footprint is the documented one (DeepSeek-V3 shape): bf16 1152 B, fp32 2304 B,
+    rotated INT2 with a bf16 rope key 320 B, and with the rope key as INT2 too 216 B."""
+    import mla_latent_kv_08_gb300 as mla
+    nb, bs = 3, 64
+    expect = {mla.MLA_KV_BF16: 1152, mla.MLA_KV_FP32: 2304, mla.MLA_KV_INT2_ROT: 320, mla.MLA_KV_INT2_ROT_QR: 216}
+    for kind, per_token in expect.items():
+        cache = mla.Cache.allocate(_shape(kind=kind, num_blocks=nb, block_size=bs), device="cpu")
+        assert cache.bytes_per_token() == per_token
+        parts = [x for x in (cache.latent, cache.codes, cache.scale_zero, cache.rope) if x is not None]
+        assert sum(x.numel() * x.element_size() for x in parts) == per_token * nb * bs
+    qr = mla.Cache.allocate(_shape(kind=mla.MLA_KV_INT2_ROT_QR, num_blocks=nb, block_size=bs), device="cpu")
+    assert qr.rope is None and tuple(qr.codes.shape) == (nb, bs, 144) and tuple(qr.scale_zero.shape) == (nb, bs, 18, 2)
