@@ -84,7 +84,8 @@ typedef struct {
     int32_t v_head_dim;        /* d_v                                             */
     int32_t block_size;        /* tokens per cache block                          */
     int32_t num_blocks;        /* physical blocks in the pool                     */
-    int32_t group_size;        /* INT2 group length along r (32); else ignored    */
+    int32_t group_size;        /* INT2 group length along r (and d_R for
+                                  INT2_ROT_QR), e.g. 32; else ignored             */
     int32_t kind;              /* mla_kv_kind                                     */
     int32_t impl;              /* mla_impl                                        */
     int32_t num_splits_hint;   /* 0: planner's choice; k>0: aim for about k split-
@@ -128,7 +129,7 @@ size_t mla_workspace_bytes(const mla_shape *shape, int32_t B, int32_t q_len);
  *   num_new     host int: cu_new[B] (total new tokens, sizes the launch).
  *   c_kv        [num_new, r]   bf16 (FP32 kind: fp32)
  *   k_rope      [num_new, d_R] bf16 (FP32 kind: fp32)
- *   R           INT2 only: [r, r] fp32 row-major, y = c . R (column j is the
+ *   R           INT2 kinds: [r, r] fp32 row-major, y = c . R (column j is the
  *               j-th eigenvector in ascending eigenvalue order); else NULL.
  *   clip        INT2 kinds: [r / group_size] fp32 clip thresholds (INT2_ROT_QR:
  *               [(r + d_R) / group_size], the rope groups' after the latent's);
@@ -152,7 +153,7 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache,
  *   seq_lens   [B] int32: tokens in the cache per sequence (>= 1).
  *   q          [B, 1, H, r + d_R] absorbed query, bf16 (FP32 kind: fp32).
  *   W_UV       [H, r, d_v] bf16 (FP32 kind: fp32).
- *   R          INT2 only: [r, r] fp32 (as in append); else NULL.
+ *   R          INT2 kinds: [r, r] fp32 (as in append); else NULL.
  *   scale      softmax scale applied to q . k.
  *   out        [B, 1, H, d_v] bf16 (FP32 kind: fp32).
  *   lse        [B, 1, H] fp32, natural log of the softmax denominator.
@@ -249,7 +250,7 @@ mla_status mla_selftest_wait_timeout(uint64_t timeout_ns, int32_t *status, void 
  * mla_latent_append (block_table, start_pos, cu_new, num_new): index_key is
  * [num_new, index_dim] row-major, 16-byte aligned; it goes to elements
  * [r + d_R, r + d_R + index_dim) of each token's cache row. Errors as for
- * mla_latent_append; MLA_ERR_INVALID when index_dim is 0 or the kind is INT2. */
+ * mla_latent_append; MLA_ERR_INVALID when index_dim is 0 or the kind is an INT2 one. */
 mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
                                    int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
                                    const int32_t *cu_new, int32_t num_new, const void *index_key,
