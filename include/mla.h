@@ -28,9 +28,12 @@
  *
  * Conventions for every entry point:
  *   - All pointers are DEVICE pointers on the current CUDA device unless the
- *     argument says "host". The caller owns every buffer; the library never
- *     allocates device memory and never synchronises (mla_get_status is the
- *     one call that waits, on the given stream).
+ *     argument says "host". The caller owns every buffer; no call allocates
+ *     device memory, and none synchronises (mla_get_status is the one call
+ *     that waits, on the given stream). The one piece of device memory the
+ *     library holds itself is the fixed 32 MiB scratch array of
+ *     mla_decode_noalloc, a static device variable that exists on every GPU
+ *     where the library's module is loaded, for as long as it stays loaded.
  *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *     stream. Work is enqueued on it and the call returns immediately.
  *   - Row-major, densely packed layouts as stated per argument. Device buffers
@@ -193,9 +196,12 @@ mla_status mla_verify(const mla_shape *shape, const mla_cache *cache,
  *   nothing is launched.
  *   status: optional [1] int32 device word that receives this call's flag word
  *   (read it with mla_read_status_word); NULL to skip.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any stream
- *   capture. Every call shares the one array: calls that can overlap on the
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture. Calls
+ *   outside capture look the address up again (cheap), so a module reload
+ *   after cudaDeviceReset is followed; calls while `stream` is capturing use
+ *   the address of the last call outside capture. Shape and implementation
+ *   errors are those of mla_decode. Every call shares the one array: calls that can overlap on the
  *   GPU (other streams, other host threads) race on it and must be ordered by
  *   the caller. The flag word is reset at the start of each call; all other
  *   scratch is written before it is read. */

@@ -24,17 +24,25 @@ static std::mutex g_noalloc_mu;
 static void *g_noalloc_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device. In host code the
-// array's name is only a stand-in, so the address is looked up once per device
-// (with that device current) and cached.
-static mla_status noalloc_scratch(void **out) {
+// array's name is only a stand-in, so the address is looked up with the device
+// current. The lookup is repeated on every call made outside stream capture
+// (cheap once the module is loaded, and it follows a module reload after
+// cudaDeviceReset); a call made while `stream` is capturing uses the address
+// cached by the last call outside capture, so the first call on a device must
+// come before any capture.
+static mla_status noalloc_scratch(cudaStream_t stream, void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MLA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return MLA_ERR_CUDA;
         g_noalloc_ptr[dev] = ptr;
+    } else if (!g_noalloc_ptr[dev]) {
+        return MLA_ERR_CUDA;           // no address looked up on this device before capture
     }
     *out = g_noalloc_ptr[dev];
     return MLA_OK;
@@ -49,12 +57,13 @@ extern "C" mla_status mla_decode_noalloc(const mla_shape *shape, const mla_cache
                                          void *stream) {
     using namespace mla;
     if (!shape || B < 1) return MLA_ERR_INVALID;
+    // The same shape and implementation checks as mla_decode, with its codes.
+    const int32_t impl = mla_resolve_impl(shape, 1);
+    if (impl < 0) return (mla_status)impl;
     // Pick the largest split target the fixed scratch can hold; the planner's
     // own choice (hint 0: one target per SM) is used when it fits.
     mla_shape s = *shape;
-    size_t need = mla_workspace_bytes(&s, B, 1);
-    if (need == 0) return MLA_ERR_INVALID;
-    if (need > kNoallocScratchBytes) {
+    if (mla_workspace_bytes(&s, B, 1) > kNoallocScratchBytes) {
         int lo = 1, hi = s.num_splits_hint > 0 ? s.num_splits_hint : 4096;
         s.num_splits_hint = 1;
         if (mla_workspace_bytes(&s, B, 1) > kNoallocScratchBytes) return MLA_ERR_WORKSPACE;
@@ -64,10 +73,9 @@ extern "C" mla_status mla_decode_noalloc(const mla_shape *shape, const mla_cache
             if (mla_workspace_bytes(&s, B, 1) <= kNoallocScratchBytes) lo = mid; else hi = mid - 1;
         }
         s.num_splits_hint = lo;
-        need = mla_workspace_bytes(&s, B, 1);
     }
     void *scratch = nullptr;
-    mla_status st = noalloc_scratch(&scratch);
+    mla_status st = noalloc_scratch((cudaStream_t)stream, &scratch);
     if (st != MLA_OK) return st;
     st = mla_decode(&s, cache, block_table, max_blocks_per_seq, seq_lens, B, q, W_UV, R, scale, out, lse,
                     scratch, kNoallocScratchBytes, stream);
@@ -76,6 +84,5 @@ extern "C" mla_status mla_decode_noalloc(const mla_shape *shape, const mla_cache
     if (status && cudaMemcpyAsync(status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
                                   (cudaStream_t)stream) != cudaSuccess)
         return MLA_ERR_CUDA;
-    (void)need;
     return MLA_OK;
 }
