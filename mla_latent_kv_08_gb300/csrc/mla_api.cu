@@ -106,6 +106,12 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
         // one wave of persistent CTAs: 2 per stream per 128-row tile
         const int row_tiles = (q_len * s->num_heads + 127) / 128;
         target = sms / (2 * row_tiles);
+        // the bf16 cache with q_len > 1 runs on 2-CTA clusters: no more streams than
+        // pairs that fit at once
+        if (s->kind == MLA_KV_BF16 && q_len > 1) {
+            const int pairs = pair_max_clusters();
+            if (pairs > 0 && pairs / row_tiles < target) target = pairs / row_tiles;
+        }
         if (target < 1) target = 1;
         if (s->num_splits_hint > 0 && s->num_splits_hint < target) target = s->num_splits_hint;
     } else {

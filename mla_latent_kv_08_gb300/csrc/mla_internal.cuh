@@ -150,6 +150,9 @@ cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st);
 // ---- tensor-core decode (defined in mla_tc.cu) -----------------------------
 bool tc_shape_supported(const ShapeArgs &s);
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st);
+// ---- paired tensor-core decode of the bf16 cache (defined in mla_pair.cu) ----
+cudaError_t launch_decode_pair(const DecodeParams &p, int32_t max_work, cudaStream_t st);
+int pair_max_clusters();   // 2-CTA clusters resident at once on the current device (0: unknown)
 // ---- tensor-core combine + W_UV (defined in mla_combine_tc.cu) --------------
 bool combine_tc_supported(const ShapeArgs &s);
 cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st);

@@ -209,5 +209,57 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 }
 
 
+
+// ---- clusters: rank, distributed shared memory, cluster barrier ------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 4-byte store into another CTA's shared memory that completes 4 transaction
+// bytes on an mbarrier of that CTA (both addresses shared::cluster).
+__device__ __forceinline__ void st_async_f32(uint32_t dst, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst), "r"(__float_as_uint(v)),
+                 "r"(bar)
+                 : "memory");
+}
+// 16-byte store into another CTA's shared memory completing 16 transaction bytes on
+// an mbarrier of that CTA (both addresses shared::cluster, 16-byte aligned).
+__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+                 : "memory");
+}
+// Bulk copy of this CTA's shared memory into another CTA's shared memory (async
+// proxy), completing `bytes` transaction bytes on the destination's mbarrier.
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// tcgen05.commit that arrives, once the issued MMAs complete, on the mbarrier at
+// the same shared-memory offset in each CTA of `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "h"(cta_mask)
+                 : "memory");
+}
+// Barrier among `count` threads (whole warps) on hardware barrier `id` (not 0).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 }  // namespace ptx
 }  // namespace mla
