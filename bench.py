@@ -512,9 +512,10 @@ def run_configs(args):
         tt = torch.from_numpy(np.ascontiguousarray(x))
         return (tt.to(dtype) if dtype is not None else tt).to(dev)
 
-    def run(name, w, kind, q_len, R=None, T=None, n=20):
+    def run(name, w, kind, q_len, R=None, T=None, n=20, fold=False):
         shape = mla.Shape(num_heads=w.H, kv_lora_rank=w.r, rope_dim=w.d_rope, v_head_dim=w.d_v,
-                          block_size=w.block_size, num_blocks=w.num_blocks, kind=kind)
+                          block_size=w.block_size, num_blocks=w.num_blocks, kind=kind,
+                          flags=mla.MLA_FLAG_WUV_FOLDED if fold else 0)
         cache = mla.Cache.allocate(shape, dev)
         cu = t(np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32))
         Rd = None if R is None else t(R.astype(np.float32))
@@ -523,6 +524,10 @@ def run_configs(args):
                               clip=None if T is None else t(T.astype(np.float32)))
         bt, sl = t(w.block_table), t(w.seq_lens.astype(np.int32))
         q, W = t(w.q, bf), t(w.W_UV, bf)
+        if fold:                    # once per layer: W'_UV = R^T . W_UV
+            Wf = torch.empty_like(W)
+            mla.mla_fold_rotation(shape, Rd, W, Wf)
+            W = Wf
         out = torch.empty((w.B, q_len, w.H, w.d_v), dtype=bf, device=dev)
         lse = torch.empty((w.B, q_len, w.H), dtype=torch.float32, device=dev)
         ws = mla.alloc_workspace(shape, w.B, q_len, dev)
@@ -575,10 +580,12 @@ def run_configs(args):
     w = workloads.int2_rotated(4)
     # timing only: any orthogonal R and positive thresholds exercise the same kernels
     R = workloads.haar_orthogonal(np.random.Generator(np.random.PCG64(5)), w.r)
-    run("C4 rotated-INT2 decode", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0))
+    run("C4 rotated-INT2 decode, W_UV folded with R^T", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0),
+        fold=True)
+    run("C4 rotated-INT2 decode, o.R^T per call", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0))
     # next-2: the same workload with the rope key held as two more INT2 groups (216 B a token)
-    run("C6 rotated-INT2 decode, rope key as INT2 too", w, mla.MLA_KV_INT2_ROT_QR, 1, R=R,
-        T=np.full((w.r + w.d_rope) // 32, 4.0))
+    run("C6 rotated-INT2 decode, rope key as INT2 too, W_UV folded", w, mla.MLA_KV_INT2_ROT_QR, 1, R=R,
+        T=np.full((w.r + w.d_rope) // 32, 4.0), fold=True)
     return 0
 
 

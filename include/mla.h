@@ -98,7 +98,17 @@ typedef struct {
                                   attention indexer key: 64 gives the 640-element
                                   row); a multiple of 8, <= 1024; 0 = none. INT2:
                                   must be 0. Attention never reads it.           */
+    int32_t flags;             /* OR of mla_flag values; 0 for none               */
 } mla_shape;
+
+typedef enum {
+    /* INT2 kinds only: the W_UV given to mla_decode / mla_verify is already the
+     * folded W'_UV[h] = R^T . W_UV[h] of mla_fold_rotation, so the latent-space
+     * output stays in the rotated basis and no o . R^T product is formed per call
+     * (out = o_rot . R^T . W_UV[h] = o_rot . W'_UV[h]). R is still required: the
+     * query is rotated by it on every call. */
+    MLA_FLAG_WUV_FOLDED = 1
+} mla_flag;
 
 /* The paged cache. Block p, slot j is token row p*block_size + j.
  *   BF16/FP32:  latent     [num_blocks, block_size, r + d_R + index_dim]
@@ -261,6 +271,21 @@ mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cach
                                    int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
                                    const int32_t *cu_new, int32_t num_new, const void *index_key,
                                    int32_t *status, void *stream);
+
+/* Fold the output rotation of a rotated-INT2 layer into its up-projection, once
+ * per layer: W_folded[h] = R^T . W_UV[h], i.e. W_folded[h][i][j] = sum_k R[k][i] *
+ * W_UV[h][k][j], fp32 accumulation, rounded to bf16. Pass W_folded as W_UV with
+ * MLA_FLAG_WUV_FOLDED set in shape->flags.
+ *   Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10),
+ *   maintainer reply: the up-projection runs on the dequantised latent, which the
+ *   cache holds in the rotated basis, so its product with R^T can be taken ahead.
+ *   shape  an INT2 kind (num_heads, kv_lora_rank, v_head_dim are read), else
+ *          MLA_ERR_INVALID.
+ *   R      [r, r] fp32 as in mla_latent_append.
+ *   W_UV   [H, r, d_v] bf16.
+ *   W_folded [H, r, d_v] bf16 output (must not alias W_UV). */
+mla_status mla_fold_rotation(const mla_shape *shape, const float *R, const void *W_UV, void *W_folded,
+                             void *stream);
 
 /* Library ABI version (major * 100 + minor). */
 int32_t mla_version(void);

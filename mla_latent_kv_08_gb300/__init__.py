@@ -34,13 +34,14 @@ MLA_KV_INT2_ROT_QR = 3
 MLA_IMPL_AUTO = 0
 MLA_IMPL_SIMT = 1
 MLA_IMPL_TCGEN05 = 2
+MLA_FLAG_WUV_FOLDED = 1
 
 # Every symbol include/mla.h declares.
 EXPORTED = (
     "mla_workspace_bytes", "mla_latent_append", "mla_decode", "mla_verify", "mla_get_status",
     "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
     "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc", "mla_selftest_wait_timeout",
-    "mla_latent_append_index",
+    "mla_latent_append_index", "mla_fold_rotation",
 )
 
 
@@ -53,7 +54,7 @@ class MlaError(RuntimeError):
 class mla_shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_heads", "kv_lora_rank", "rope_dim", "v_head_dim", "block_size", "num_blocks",
-        "group_size", "kind", "impl", "num_splits_hint", "index_dim")]
+        "group_size", "kind", "impl", "num_splits_hint", "index_dim", "flags")]
 
 
 class mla_cache(ctypes.Structure):
@@ -100,6 +101,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_noalloc.restype = i32
     lib.mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
     lib.mla_selftest_wait_timeout.restype = i32
+    lib.mla_fold_rotation.argtypes = [sp, vp, vp, vp, vp]
+    lib.mla_fold_rotation.restype = i32
     lib.mla_profile_enable.argtypes = [i32]
     lib.mla_profile_enable.restype = i32
     lib.mla_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), i32p, i32p]
@@ -134,11 +137,12 @@ class Shape:
     impl: int = MLA_IMPL_AUTO
     num_splits_hint: int = 0
     index_dim: int = 0
+    flags: int = 0
 
     def c(self) -> mla_shape:
         return mla_shape(self.num_heads, self.kv_lora_rank, self.rope_dim, self.v_head_dim,
                          self.block_size, self.num_blocks, self.group_size, self.kind, self.impl,
-                         self.num_splits_hint, self.index_dim)
+                         self.num_splits_hint, self.index_dim, self.flags)
 
     @property
     def D(self) -> int:
@@ -243,10 +247,11 @@ def mla_latent_append_index(cache: Cache, block_table, start_pos, cu_new, index_
 
 
 def mla_decode(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, workspace,
-               R=None, stream=None) -> None:
-    """Decode attention, q [B, 1, H, r + d_R] -> out [B, 1, H, d_v], lse [B, 1, H]."""
+               R=None, stream=None, shape: Optional[Shape] = None) -> None:
+    """Decode attention, q [B, 1, H, r + d_R] -> out [B, 1, H, d_v], lse [B, 1, H].
+    ``shape`` overrides ``cache.shape`` (e.g. to set flags for this call)."""
     lib = load_library()
-    code = lib.mla_decode(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+    code = lib.mla_decode(ctypes.byref((shape or cache.shape).c()), ctypes.byref(cache.c()), _ptr(block_table),
                           int(block_table.shape[1]), _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(q),
                           _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
                           int(workspace.numel() * workspace.element_size()), _stream(stream))
@@ -254,14 +259,21 @@ def mla_decode(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, 
 
 
 def mla_verify(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, workspace,
-               R=None, stream=None) -> None:
+               R=None, stream=None, shape: Optional[Shape] = None) -> None:
     """Speculative verify, q [B, q_len, H, r + d_R] with the causal draft window."""
     lib = load_library()
-    code = lib.mla_verify(ctypes.byref(cache.shape.c()), ctypes.byref(cache.c()), _ptr(block_table),
+    code = lib.mla_verify(ctypes.byref((shape or cache.shape).c()), ctypes.byref(cache.c()), _ptr(block_table),
                           int(block_table.shape[1]), _ptr(seq_lens), int(seq_lens.shape[0]), int(q.shape[1]),
                           _ptr(q), _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
                           int(workspace.numel() * workspace.element_size()), _stream(stream))
     _check(code, "mla_verify")
+
+
+def mla_fold_rotation(shape: Shape, R, W_UV, W_folded, stream=None) -> None:
+    """W_folded[h] = R^T . W_UV[h] (bf16), for decode with MLA_FLAG_WUV_FOLDED (see include/mla.h)."""
+    lib = load_library()
+    _check(lib.mla_fold_rotation(ctypes.byref(shape.c()), _ptr(R), _ptr(W_UV), _ptr(W_folded), _stream(stream)),
+           "mla_fold_rotation")
 
 
 def mla_decode_noalloc(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, R=None,

@@ -59,6 +59,8 @@ static mla_status check_shape(const mla_shape *s) {
         return MLA_ERR_INVALID;
     if (s->index_dim < 0 || s->index_dim % 8 || s->index_dim > 1024) return MLA_ERR_INVALID;
     if (is_int2(s->kind) && s->index_dim != 0) return MLA_ERR_INVALID;
+    if (s->flags & ~(int32_t)MLA_FLAG_WUV_FOLDED) return MLA_ERR_INVALID;
+    if ((s->flags & MLA_FLAG_WUV_FOLDED) && !is_int2(s->kind)) return MLA_ERR_INVALID;
     if (is_int2(s->kind)) {
         if (s->group_size < 4 || s->group_size % 4 || s->kv_lora_rank % s->group_size) return MLA_ERR_INVALID;
         if (s->rope_dim < 8) return MLA_ERR_INVALID;
@@ -227,7 +229,9 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     c.out = out;
     c.lse = lse;
     const bool comb_tc = tc && combine_tc_supported(p.s);
-    if (int2 && comb_tc) {
+    const bool folded = int2 && (s->flags & MLA_FLAG_WUV_FOLDED);
+    if (folded) c.R = nullptr;                 // W_UV already carries R^T
+    if (int2 && comb_tc && !folded) {
         // merge splits, rotate back on the tensor cores (o_lat = o_rot . R^T), then the
         // W_UV up-projection reads the merged rows as one-split partials
         float *o_rot = (float *)(ws + w.o_rot), *o_lat = (float *)(ws + w.o_lat), *lse2 = (float *)(ws + w.lse2);
@@ -409,6 +413,17 @@ mla_status mla_profile_read(double *attention_ms, int32_t *attention_launches, i
     return MLA_OK;
 }
 
-int32_t mla_version(void) { return 101; }
+mla_status mla_fold_rotation(const mla_shape *shape, const float *R, const void *W_UV, void *W_folded,
+                             void *stream) {
+    mla_status st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    if (!is_int2(shape->kind) || !R || !W_UV || !W_folded || W_UV == W_folded) return MLA_ERR_INVALID;
+    if (launch_fold_rotation(shape_args(shape), R, W_UV, W_folded, (cudaStream_t)stream) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    prof_kernels(1);
+    return MLA_OK;
+}
+
+int32_t mla_version(void) { return 102; }
 
 }  // extern "C"

@@ -147,6 +147,7 @@ cudaError_t launch_decode_simt(const DecodeParams &p, int32_t max_work, cudaStre
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st);
+cudaError_t launch_fold_rotation(const ShapeArgs &s, const float *R, const void *W_UV, void *W_folded, cudaStream_t st);
 // ---- tensor-core decode (defined in mla_tc.cu) -----------------------------
 bool tc_shape_supported(const ShapeArgs &s);
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st);

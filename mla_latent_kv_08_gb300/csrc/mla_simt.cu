@@ -804,3 +804,60 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
 }
 
 }  // namespace mla
+
+namespace mla {
+// ============================================================================
+// Output rotation folded into the up-projection: Wf[h] = R^T . W_UV[h] ([r, r]^T x
+// [r, d_v]), fp32 accumulation over k ascending, rounded to bf16. One-time per
+// layer. A CTA computes a 64 x 64 tile of one head's output, staging 32-row slabs
+// of R and W_UV in shared memory; thread (ty, tx) owns a 4 x 4 block.
+// ============================================================================
+__global__ void __launch_bounds__(256) fold_rotation_kernel(const float *R, const __nv_bfloat16 *W, __nv_bfloat16 *Wf,
+                                                            int r, int dv) {
+    __shared__ float sR[32][64 + 1];   // R[k0 + kk][i0 + ii]
+    __shared__ float sW[32][64 + 1];   // W[h][k0 + kk][j0 + jj]
+    const int h = blockIdx.z, i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const __nv_bfloat16 *Wh = W + (size_t)h * r * dv;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < r; k0 += 32) {
+        for (int e = threadIdx.x; e < 32 * 64; e += 256) {
+            const int kk = e >> 6, c = e & 63;
+            const int k = k0 + kk;
+            sR[kk][c] = (k < r && i0 + c < r) ? R[(size_t)k * r + i0 + c] : 0.f;
+            sW[kk][c] = (k < r && j0 + c < dv) ? __bfloat162float(Wh[(size_t)k * dv + j0 + c]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < 32; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a[u] = sR[kk][4 * ty + u];
+                b[u] = sW[kk][4 * tx + u];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(a[u], b[v], acc[u][v]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = i0 + 4 * ty + u;
+        if (i >= r) continue;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int j = j0 + 4 * tx + v;
+            if (j < dv) Wf[((size_t)h * r + i) * dv + j] = __float2bfloat16_rn(acc[u][v]);
+        }
+    }
+}
+
+cudaError_t launch_fold_rotation(const ShapeArgs &s, const float *R, const void *W_UV, void *W_folded, cudaStream_t st) {
+    dim3 grid((s.dv + 63) / 64, (s.r + 63) / 64, s.H);
+    fold_rotation_kernel<<<grid, 256, 0, st>>>(R, (const __nv_bfloat16 *)W_UV, (__nv_bfloat16 *)W_folded, s.r, s.dv);
+    return cudaGetLastError();
+}
+}  // namespace mla

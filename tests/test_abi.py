@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     import mla_latent_kv_08_gb300 as mla
-    assert mla.mla_version() == 101
+    assert mla.mla_version() == 102
     for code in range(-6, 1):
         assert mla.status_string(code) != "unknown status"
     assert mla.status_string(-99) == "unknown status"
@@ -57,6 +57,10 @@ def test_shape_validation(lib):
     assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, group_size=6)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kv_lora_rank=2048)) == mla.MLA_ERR_UNSUPPORTED
     assert mla.mla_resolve_impl(_shape(), q_len=0) == mla.MLA_ERR_INVALID
+    # flags: only MLA_FLAG_WUV_FOLDED exists, and it belongs to the INT2 kinds
+    assert mla.mla_resolve_impl(_shape(flags=2)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(flags=mla.MLA_FLAG_WUV_FOLDED)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, flags=mla.MLA_FLAG_WUV_FOLDED)) >= 0
     # the extra per-token key: a multiple of 8 up to 1024, BF16/FP32 kinds only
     assert mla.mla_resolve_impl(_shape(index_dim=64)) in (mla.MLA_IMPL_SIMT, mla.MLA_IMPL_TCGEN05)
     assert mla.mla_resolve_impl(_shape(index_dim=12)) == mla.MLA_ERR_INVALID
@@ -134,3 +138,17 @@ def test_cache_layout_bytes_per_kind():
         assert sum(x.numel() * x.element_size() for x in parts) == per_token * nb * bs
     qr = mla.Cache.allocate(_shape(kind=mla.MLA_KV_INT2_ROT_QR, num_blocks=nb, block_size=bs), device="cpu")
     assert qr.rope is None and tuple(qr.codes.shape) == (nb, bs, 144) and tuple(qr.scale_zero.shape) == (nb, bs, 18, 2)
+
+
+def test_fold_rotation_argument_checks(lib):
+    """mla_fold_rotation refuses non-INT2 kinds, null pointers and in-place output
+    before launching anything."""
+    import mla_latent_kv_08_gb300 as mla
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    q = ctypes.cast(ctypes.create_string_buffer(64), ctypes.c_void_p)
+    int2 = _shape(kind=mla.MLA_KV_INT2_ROT)
+    assert lib.mla_fold_rotation(ctypes.byref(_shape().c()), p, p, q, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_fold_rotation(ctypes.byref(int2.c()), None, p, q, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_fold_rotation(ctypes.byref(int2.c()), p, p, None, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_fold_rotation(ctypes.byref(int2.c()), p, q, q, None) == mla.MLA_ERR_INVALID

@@ -537,3 +537,68 @@ def test_int2_rope_codes_append_and_decode(gpu_lib, impl_name, H):
         Y = oint2.decode(ref[b][0], ref[b][1]).astype(np.float64)
         ro, rl = oint2.attention_rope_int2(w.q[b], Y, R32, w.W_UV, w.scale)
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+# ------------------------------------------------------------ folded output rotation
+
+def test_fold_rotation_matches_the_definition(gpu_lib):
+    """W_folded[h] = R^T . W_UV[h], rounded once to bf16: every element within one bf16
+    rounding (plus fp32 accumulation) of the fp64 product."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    rng = np.random.default_rng(3)
+    H, r, dv = 8, 512, 128
+    R = workloads.haar_orthogonal(np.random.Generator(np.random.PCG64(9)), r).astype(np.float32)
+    W = workloads.bf16_round(rng.standard_normal((H, r, dv)).astype(np.float32) / math.sqrt(r))
+    shape = mla.Shape(num_heads=H, kv_lora_rank=r, rope_dim=64, v_head_dim=dv, block_size=64, num_blocks=1,
+                      kind=mla.MLA_KV_INT2_ROT)
+    Wf = torch.empty((H, r, dv), dtype=torch.bfloat16, device="cuda")
+    mla.mla_fold_rotation(shape, gu.dev(R), gu.dev(W, torch.bfloat16), Wf)
+    torch.cuda.synchronize()
+    ref = np.einsum("ki,hkj->hij", R.astype(np.float64), W.astype(np.float64))
+    got = Wf.float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+@pytest.mark.parametrize("kind_name,impl_name,H", [("rot", "tcgen05", 128), ("rot", "simt", 32),
+                                                   ("rope", "tcgen05", 128), ("rope", "simt", 32)])
+def test_int2_decode_with_folded_up_projection(gpu_lib, kind_name, impl_name, H):
+    """MLA_FLAG_WUV_FOLDED: the decode with W'_UV = R^T . W_UV (no o . R^T per call)
+    matches the oracle, which rotates back and up-projects in fp64."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=3, H=H, len_range=(60, 700))
+    kind = mla.MLA_KV_INT2_ROT if kind_name == "rot" else mla.MLA_KV_INT2_ROT_QR
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    T = T32
+    if kind_name == "rope":
+        rng = np.random.default_rng(12)
+        KRcal = workloads.bf16_round(rng.standard_normal((8192, 64)).astype(np.float32)).astype(np.float64)
+        TR32 = oint2.rope_thresholds(KRcal).astype(np.float32)
+        T = np.concatenate([T32, TR32])
+    shape = gu.shape_for(w, kind=kind, impl=impl)
+    cache, st = gu.fill_cache(w, shape, R32, T)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    Wf = torch.empty((w.H, w.r, w.d_v), dtype=torch.bfloat16, device="cuda")
+    mla.mla_fold_rotation(shape, gu.dev(R32), gu.dev(w.W_UV, torch.bfloat16), Wf)
+    fshape = gu.shape_for(w, kind=kind, impl=impl)
+    fshape.flags = mla.MLA_FLAG_WUV_FOLDED
+    out = torch.empty((w.B, 1, w.H, w.d_v), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, 1, w.H), dtype=torch.float32, device="cuda")
+    ws = mla.alloc_workspace(fshape, w.B, 1)
+    mla.mla_decode(cache, gu.dev(w.block_table), gu.dev(w.seq_lens.astype(np.int32)), gu.dev(w.q, torch.bfloat16),
+                   Wf, w.scale, out, lse, ws, R=gu.dev(R32), shape=fshape)
+    torch.cuda.synchronize()
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    for b in range(w.B):
+        if kind_name == "rot":
+            codes, sz = oint2.quantize(w.latent[b], R32, T32)
+            ro, rl = oint2.attention_rotated(w.q[b], oint2.decode(codes, sz), w.rope[b], R32, w.W_UV, w.scale)
+        else:
+            codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
+            Y = oint2.decode(codes, sz).astype(np.float64)
+            ro, rl = oint2.attention_rope_int2(w.q[b], Y, R32, w.W_UV, w.scale)
+        _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
