@@ -15,9 +15,11 @@
  * covariance eigenbasis R and quantised to grouped INT2 (rope key kept bf16).
  *   Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10),
  *   maintainer reply, "How the rotation adapts to the latent".
- * A variant of it quantises the rope key as well, unrotated, as further INT2
- * groups (MLA_KV_INT2_ROT_QR): one of the rope/nope designs the same thread
- * names as benchmarked, without details (a later reply on GLM-5.2 support).
+ * Two variants also quantise the rope key, the two rope/nope designs the same
+ * thread names as benchmarked, without details (a later reply on GLM-5.2
+ * support): MLA_KV_INT2_ROT_QR keeps the rope key unrotated as further INT2
+ * groups; MLA_KV_INT2_JOINT rotates the latent and the rope key together by one
+ * eigenbasis of the whole row and quantises the result.
  *
  * Definitions (per sequence b, query row i, head h, cached token t):
  *   s = scale * (q[b,i,h,:] . [c_t ; kR_t])          (rotated kind: q_lat . R)
@@ -68,9 +70,13 @@ typedef enum {
     MLA_KV_BF16 = 0,           /* latent + rope key, bf16, one row per token       */
     MLA_KV_FP32 = 1,           /* latent + rope key, fp32, one row per token       */
     MLA_KV_INT2_ROT = 2,       /* rotated latent as grouped INT2 + bf16 rope key   */
-    MLA_KV_INT2_ROT_QR = 3     /* rotated latent and the (unrotated) rope key, both
+    MLA_KV_INT2_ROT_QR = 3,    /* rotated latent and the (unrotated) rope key, both
                                   as grouped INT2: [c . R ; k_R] in (r + d_R) /
                                   group_size groups; d_R a multiple of group_size */
+    MLA_KV_INT2_JOINT = 4      /* the whole row rotated by one eigenbasis R_j of
+                                  [c ; k_R] ((r + d_R) x (r + d_R)) and stored as
+                                  grouped INT2: [c ; k_R] . R_j in (r + d_R) /
+                                  group_size groups; generic kernel only */
 } mla_kv_kind;
 
 typedef enum {
@@ -121,6 +127,7 @@ typedef enum {
  *   INT2_ROT_QR: codes      [num_blocks, block_size, (r + d_R) / 4] uint8 and
  *               scale_zero [num_blocks, block_size, (r + d_R) / group_size, 2]
  *                          fp16, as above over the row [c . R ; k_R]; rope unused
+ *   INT2_JOINT: codes and scale_zero as INT2_ROT_QR, over the row [c ; k_R] . R_j
  * Unused members are NULL. */
 typedef struct {
     void *latent;
@@ -143,16 +150,18 @@ size_t mla_workspace_bytes(const mla_shape *shape, int32_t B, int32_t q_len);
  *   c_kv        [num_new, r]   bf16 (FP32 kind: fp32)
  *   k_rope      [num_new, d_R] bf16 (FP32 kind: fp32)
  *   R           INT2 kinds: [r, r] fp32 row-major, y = c . R (column j is the
- *               j-th eigenvector in ascending eigenvalue order); else NULL.
+ *               j-th eigenvector in ascending eigenvalue order); INT2_JOINT:
+ *               [r + d_R, r + d_R], y = [c ; k_R] . R_j; else NULL.
  *   clip        INT2 kinds: [r / group_size] fp32 clip thresholds (INT2_ROT_QR:
- *               [(r + d_R) / group_size], the rope groups' after the latent's);
- *               else NULL.
+ *               [(r + d_R) / group_size], the rope groups' after the latent's;
+ *               INT2_JOINT: [(r + d_R) / group_size]); else NULL.
  *   status      optional [1] int32 device word; flags are OR-ed into it.
  * INT2 encoding per token and group g of group_size dims: y = fp32 fmaf chain
  * over k ascending; y clipped to [-clip[g], clip[g]]; scale =
  * fp16_rne((max - min) / 3), zero = fp16_rne(min); code = clamp(rint((y -
  * zero) / scale), 0, 3), 0 when scale == 0. INT2_ROT_QR: the rope groups encode
  * k_R as given (bf16 widened to fp32, not rotated) with their own thresholds.
+ * INT2_JOINT: y = [c ; k_R] . R_j by the same fp32 chain over all r + d_R inputs.
  *   Source: OSCAR issue #10, maintainer reply (rotated + quantised latent in
  *   the cache, thresholds fit on the rotated latent). */
 mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache,
@@ -166,7 +175,9 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache,
  *   seq_lens   [B] int32: tokens in the cache per sequence (>= 1).
  *   q          [B, 1, H, r + d_R] absorbed query, bf16 (FP32 kind: fp32).
  *   W_UV       [H, r, d_v] bf16 (FP32 kind: fp32).
- *   R          INT2 kinds: [r, r] fp32 (as in append); else NULL.
+ *   R          INT2 kinds: [r, r] fp32 (as in append; INT2_JOINT: [r + d_R,
+ *              r + d_R], the query is rotated over all its dims and the output
+ *              is (o_j . R_j^T)[0:r] before W_UV); else NULL.
  *   scale      softmax scale applied to q . k.
  *   out        [B, 1, H, d_v] bf16 (FP32 kind: fp32).
  *   lse        [B, 1, H] fp32, natural log of the softmax denominator.

@@ -30,6 +30,7 @@ MLA_KV_BF16 = 0
 MLA_KV_FP32 = 1
 MLA_KV_INT2_ROT = 2
 MLA_KV_INT2_ROT_QR = 3
+MLA_KV_INT2_JOINT = 4
 
 MLA_IMPL_AUTO = 0
 MLA_IMPL_SIMT = 1
@@ -191,7 +192,7 @@ class Cache:
                        codes=alloc((nb, bs, r // 4), dtype=torch.uint8, device=device),
                        scale_zero=alloc((nb, bs, r // shape.group_size, 2), dtype=torch.float16, device=device),
                        rope=alloc((nb, bs, dR), dtype=torch.bfloat16, device=device))
-        if shape.kind == MLA_KV_INT2_ROT_QR:      # the rope key's codes follow the latent's
+        if shape.kind in (MLA_KV_INT2_ROT_QR, MLA_KV_INT2_JOINT):   # codes over the whole row
             return cls(shape,
                        codes=alloc((nb, bs, (r + dR) // 4), dtype=torch.uint8, device=device),
                        scale_zero=alloc((nb, bs, (r + dR) // shape.group_size, 2), dtype=torch.float16,
@@ -203,7 +204,7 @@ class Cache:
         s = self.shape
         if s.kind == MLA_KV_INT2_ROT:
             return s.kv_lora_rank // 4 + (s.kv_lora_rank // s.group_size) * 4 + 2 * s.rope_dim
-        if s.kind == MLA_KV_INT2_ROT_QR:
+        if s.kind in (MLA_KV_INT2_ROT_QR, MLA_KV_INT2_JOINT):
             qd = s.kv_lora_rank + s.rope_dim
             return qd // 4 + (qd // s.group_size) * 4
         return (4 if s.kind == MLA_KV_FP32 else 2) * (s.kv_lora_rank + s.rope_dim + s.index_dim)

@@ -60,11 +60,14 @@ static mla_status check_shape(const mla_shape *s) {
     if (s->index_dim < 0 || s->index_dim % 8 || s->index_dim > 1024) return MLA_ERR_INVALID;
     if (is_int2(s->kind) && s->index_dim != 0) return MLA_ERR_INVALID;
     if (s->flags & ~(int32_t)MLA_FLAG_WUV_FOLDED) return MLA_ERR_INVALID;
-    if ((s->flags & MLA_FLAG_WUV_FOLDED) && !is_int2(s->kind)) return MLA_ERR_INVALID;
+    // the joint kind's folded up-projection would be [H, r + d_R, d_v]: not offered
+    if ((s->flags & MLA_FLAG_WUV_FOLDED) && (!is_int2(s->kind) || s->kind == MLA_KV_INT2_JOINT))
+        return MLA_ERR_INVALID;
     if (is_int2(s->kind)) {
         if (s->group_size < 4 || s->group_size % 4 || s->kv_lora_rank % s->group_size) return MLA_ERR_INVALID;
         if (s->rope_dim < 8) return MLA_ERR_INVALID;
-        if (s->kind == MLA_KV_INT2_ROT_QR && s->rope_dim % s->group_size) return MLA_ERR_INVALID;
+        if ((s->kind == MLA_KV_INT2_ROT_QR || s->kind == MLA_KV_INT2_JOINT) && s->rope_dim % s->group_size)
+            return MLA_ERR_INVALID;
     }
     // generic kernel limits (shared-memory tiles sized from r and d_R)
     if (s->kv_lora_rank > 1024 || s->rope_dim > 128) return MLA_ERR_UNSUPPORTED;
@@ -127,7 +130,7 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
     w.work = off;          off = up256(off + sizeof(WorkItem) * (size_t)w.max_work);
     w.split_start = off;   off = up256(off + sizeof(int32_t) * ((size_t)B + 1));
     w.stream_start = off;  off = up256(off + sizeof(int32_t) * ((size_t)target + 1));
-    w.part_o = off;        off = up256(off + sizeof(float) * (size_t)w.max_work * rows * s->kv_lora_rank);
+    w.part_o = off;        off = up256(off + sizeof(float) * (size_t)w.max_work * rows * shape_args(s).OD());
     w.part_lse = off;      off = up256(off + sizeof(float) * (size_t)w.max_work * rows);
     w.q_prep = off;
     if (is_int2(s->kind)) {
@@ -417,7 +420,8 @@ mla_status mla_fold_rotation(const mla_shape *shape, const float *R, const void 
                              void *stream) {
     mla_status st = check_shape(shape);
     if (st != MLA_OK) return st;
-    if (!is_int2(shape->kind) || !R || !W_UV || !W_folded || W_UV == W_folded) return MLA_ERR_INVALID;
+    if (!is_int2(shape->kind) || shape->kind == MLA_KV_INT2_JOINT || !R || !W_UV || !W_folded || W_UV == W_folded)
+        return MLA_ERR_INVALID;
     if (launch_fold_rotation(shape_args(shape), R, W_UV, W_folded, (cudaStream_t)stream) != cudaSuccess)
         return MLA_ERR_CUDA;
     prof_kernels(1);

@@ -55,12 +55,19 @@ struct ShapeArgs {
     int32_t ix;                  // extra per-token key after the rope key (BF16/FP32 kinds)
     __host__ __device__ int32_t D() const { return r + dR; }        // elements attention reads
     __host__ __device__ int32_t E() const { return r + dR + ix; }   // cache row stride (BF16/FP32)
-    // INT2 kinds: dims held as codes per token (the latent; INT2_ROT_QR: + the rope key)
-    __host__ __device__ int32_t QD() const { return kind == MLA_KV_INT2_ROT_QR ? r + dR : r; }
+    // INT2 kinds: dims held as codes per token (the latent; INT2_ROT_QR and INT2_JOINT:
+    // + the rope key)
+    __host__ __device__ int32_t QD() const { return kind == MLA_KV_INT2_ROT_QR || kind == MLA_KV_INT2_JOINT ? r + dR : r; }
+    // INT2 kinds: dims the rotation acts on (R is [RD, RD]): the latent, or for
+    // INT2_JOINT the whole row [c ; k_R]
+    __host__ __device__ int32_t RD() const { return kind == MLA_KV_INT2_JOINT ? r + dR : r; }
+    // dims of the attention's latent-space output (the split partials): r, or for
+    // INT2_JOINT all r + d_R rotated dims (rotated back and cut to r in the combine)
+    __host__ __device__ int32_t OD() const { return kind == MLA_KV_INT2_JOINT ? r + dR : r; }
 };
 
 __host__ __device__ constexpr bool is_int2(int32_t kind) {
-    return kind == MLA_KV_INT2_ROT || kind == MLA_KV_INT2_ROT_QR;
+    return kind == MLA_KV_INT2_ROT || kind == MLA_KV_INT2_ROT_QR || kind == MLA_KV_INT2_JOINT;
 }
 
 // Everything a decode kernel reads.

@@ -169,12 +169,12 @@ cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st
 // OUT: 0 fp32 (CUDA-core decode), 1 fp16 (tensor-core decode of the INT2 cache).
 template <int NC, int OUT>
 __global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float *R, void *q_prep, int rows) {
-    extern __shared__ float sq[];                 // [32][r]
-    const int r = p.s.r, D = p.s.D();
+    extern __shared__ float sq[];                 // [32][RD]
+    const int RD = p.s.RD(), D = p.s.D();         // rotated dims (r, or all D for INT2_JOINT)
     const int row0 = blockIdx.x * 32;
     const __nv_bfloat16 *q = (const __nv_bfloat16 *)p.q;
-    for (int idx = threadIdx.x; idx < 32 * r; idx += blockDim.x) {
-        int rr = idx / r, k = idx % r, row = row0 + rr;
+    for (int idx = threadIdx.x; idx < 32 * RD; idx += blockDim.x) {
+        int rr = idx / RD, k = idx % RD, row = row0 + rr;
         sq[idx] = row < rows ? __bfloat162float(q[(size_t)row * D + k]) : 0.f;
     }
     __syncthreads();
@@ -183,16 +183,16 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float 
     for (int rr = 0; rr < 32; ++rr)
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[rr][c] = 0.f;
-    for (int k = 0; k < r; ++k) {
+    for (int k = 0; k < RD; ++k) {
         float Rk[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             int j = threadIdx.x + 256 * c;
-            Rk[c] = j < r ? __ldg(R + (size_t)k * r + j) : 0.f;
+            Rk[c] = j < RD ? __ldg(R + (size_t)k * RD + j) : 0.f;
         }
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr) {
-            float qv = sq[rr * r + k];
+            float qv = sq[rr * RD + k];
 #pragma unroll
             for (int c = 0; c < NC; ++c) acc[rr][c] = fmaf(qv, Rk[c], acc[rr][c]);
         }
@@ -204,15 +204,16 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float 
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             int j = threadIdx.x + 256 * c;
-            if (j < r) {
+            if (j < RD) {
                 if (OUT == 1) ((__half *)q_prep)[(size_t)row * D + j] = __float2half_rn(acc[rr][c]);
                 else ((float *)q_prep)[(size_t)row * D + j] = acc[rr][c];
             }
         }
-        for (int j = threadIdx.x; j < p.s.dR; j += blockDim.x) {
-            const float v = __bfloat162float(q[(size_t)row * D + r + j]);
-            if (OUT == 1) ((__half *)q_prep)[(size_t)row * D + r + j] = __float2half_rn(v);
-            else ((float *)q_prep)[(size_t)row * D + r + j] = v;
+        // the dims outside the rotation (the rope part, unless INT2_JOINT) as given
+        for (int j = RD + threadIdx.x; j < D; j += blockDim.x) {
+            const float v = __bfloat162float(q[(size_t)row * D + j]);
+            if (OUT == 1) ((__half *)q_prep)[(size_t)row * D + j] = __float2half_rn(v);
+            else ((float *)q_prep)[(size_t)row * D + j] = v;
         }
     }
 }
@@ -220,14 +221,18 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeParams p, const float 
 template <int OUT>
 static cudaError_t launch_qprep_t(const DecodeParams &p, const float *R, void *q_prep, cudaStream_t st) {
     const int rows = p.B * p.q_len * p.s.H;
-    const size_t smem = (size_t)32 * p.s.r * sizeof(float);
+    const int RD = p.s.RD();
+    const size_t smem = (size_t)32 * RD * sizeof(float);
     dim3 grid((rows + 31) / 32);
-    if (p.s.r <= 256) {
+    if (RD <= 256) {
         cudaFuncSetAttribute(qprep_kernel<1, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         qprep_kernel<1, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
-    } else if (p.s.r <= 512) {
+    } else if (RD <= 512) {
         cudaFuncSetAttribute(qprep_kernel<2, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         qprep_kernel<2, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
+    } else if (RD <= 768) {
+        cudaFuncSetAttribute(qprep_kernel<3, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        qprep_kernel<3, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
     } else {
         cudaFuncSetAttribute(qprep_kernel<4, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         qprep_kernel<4, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
@@ -338,7 +343,8 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
     if (w >= p.num_work[0]) return;
     const WorkItem item = p.work[w];
     const int b = item.b, t0 = item.t0, t1 = item.t1, slot = w;
-    const int H = p.s.H, r = p.s.r, D = p.s.D(), Dp = D + 1;
+    const int H = p.s.H, D = p.s.D(), Dp = D + 1;
+    const int r = p.s.OD();               // dims of the latent-space output (INT2_JOINT: all D)
     const int rows_total = p.q_len * H;
     const int row0 = blockIdx.y * kRB;
     if (row0 >= rows_total) return;
@@ -471,12 +477,15 @@ static cudaError_t launch_decode_kind(const DecodeParams &p, int32_t max_work, c
     const size_t smem = sizeof(float) * ((size_t)kRB * D + (size_t)kTT * (D + 1) + kRB * kTT + 3 * kRB) +
                         sizeof(int) * kTT;
     dim3 grid(max_work, (p.q_len * p.s.H + kRB - 1) / kRB);
-    if (p.s.r <= 256) {
+    if (p.s.OD() <= 256) {
         cudaFuncSetAttribute(decode_simt_kernel<KIND, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         decode_simt_kernel<KIND, 1><<<grid, 256, smem, st>>>(p);
-    } else if (p.s.r <= 512) {
+    } else if (p.s.OD() <= 512) {
         cudaFuncSetAttribute(decode_simt_kernel<KIND, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         decode_simt_kernel<KIND, 2><<<grid, 256, smem, st>>>(p);
+    } else if (p.s.OD() <= 768) {
+        cudaFuncSetAttribute(decode_simt_kernel<KIND, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_simt_kernel<KIND, 3><<<grid, 256, smem, st>>>(p);
     } else {
         cudaFuncSetAttribute(decode_simt_kernel<KIND, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         decode_simt_kernel<KIND, 4><<<grid, 256, smem, st>>>(p);
@@ -503,11 +512,12 @@ template <bool FP32IO>
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     extern __shared__ float cs[];
     const int H = p.s.H, r = p.s.r, dv = p.s.dv;
+    const int od = p.s.OD();              // partial dims: r, or r + d_R (INT2_JOINT)
     const int h = blockIdx.x;
     const int nrows = p.B * p.q_len;
     const int rb0 = blockIdx.y * kCR;
-    float *so = cs;                       // [kCR][r]
-    float *st = so + kCR * r;             // [kCR][r] (INT2 rotation target)
+    float *so = cs;                       // [kCR][od]
+    float *st = so + kCR * od;            // [kCR][r] (INT2 rotation target)
     float *slse = st + kCR * r;           // [kCR]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rows_total = p.q_len * H;
@@ -515,7 +525,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     // warp w merges row rb0 + w
     if (warp < kCR) {
         const int rb = rb0 + warp;
-        float *dst = so + warp * r;
+        float *dst = so + warp * od;
         if (rb < nrows) {
             const int b = rb / p.q_len, i = rb % p.q_len;
             const int s0 = p.split_start[b], s1 = p.split_start[b + 1];
@@ -533,12 +543,12 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
                 tot += (v == -CUDART_INF_F) ? 0.f : exp2f(v - M);
             }
             const float inv = tot > 0.f ? 1.f / tot : 0.f;
-            for (int d = lane; d < r; d += 32) {
+            for (int d = lane; d < od; d += 32) {
                 float a = 0.f;
                 for (int s = s0; s < s1; ++s) {
                     float v = p.part_lse[(size_t)s * rows_total + row];
                     float wgt = (v == -CUDART_INF_F) ? 0.f : exp2f(v - M) * inv;
-                    const size_t at = ((size_t)s * rows_total + row) * r + d;
+                    const size_t at = ((size_t)s * rows_total + row) * od + d;
                     const float pv = p.part_bf16 ? __bfloat162float(((const __nv_bfloat16 *)p.part_o)[at])
                                                  : ((const float *)p.part_o)[at];
                     a = fmaf(wgt, pv, a);
@@ -547,24 +557,26 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
             }
             if (lane == 0) slse[warp] = nan ? CUDART_NAN_F : (M + log2f(tot)) * kLn2;
         } else {
-            for (int d = lane; d < r; d += 32) dst[d] = 0.f;
+            for (int d = lane; d < od; d += 32) dst[d] = 0.f;
         }
     }
     __syncthreads();
     const float *src = so;
     if (p.R) {
-        // o_lat[j] = sum_k R[j][k] o_rot[k]: a warp per (row, j), lanes over k.
+        // o_lat[j] = sum_k R[j][k] o_rot[k] for j < r (R is [od, od]; INT2_JOINT keeps
+        // the first r of the r + d_R rotated-back dims): a warp per (row, j), lanes over k.
         for (int job = warp; job < kCR * r; job += 8) {
             const int rr = job / r, j = job % r;
-            const float *Rj = p.R + (size_t)j * r;
+            const float *Rj = p.R + (size_t)j * od;
             float a = 0.f;
-            for (int k = lane; k < r; k += 32) a = fmaf(__ldg(Rj + k), so[rr * r + k], a);
+            for (int k = lane; k < od; k += 32) a = fmaf(__ldg(Rj + k), so[rr * od + k], a);
             a = warp_sum(a);
             if (lane == 0) st[rr * r + j] = a;
         }
         __syncthreads();
         src = st;
     }
+    const int ss = p.R ? r : od;          // row stride of the up-projection's input
     // out[v] = sum_k o_lat[k] W_UV[h][k][v]; thread -> (v, k-phase)
     for (int v0 = 0; v0 < dv; v0 += 256) {
         const int v = v0 + tid;
@@ -577,7 +589,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
                 if (FP32IO) wv = __ldg((const float *)p.W_UV + ((size_t)h * r + k) * dv + v);
                 else wv = __bfloat162float(((const __nv_bfloat16 *)p.W_UV)[((size_t)h * r + k) * dv + v]);
 #pragma unroll
-                for (int rr = 0; rr < kCR; ++rr) a[rr] = fmaf(src[rr * r + k], wv, a[rr]);
+                for (int rr = 0; rr < kCR; ++rr) a[rr] = fmaf(src[rr * ss + k], wv, a[rr]);
             }
 #pragma unroll
             for (int rr = 0; rr < kCR; ++rr) {
@@ -597,7 +609,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
 }
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st) {
-    const size_t smem = sizeof(float) * ((size_t)2 * kCR * p.s.r + kCR);
+    const size_t smem = sizeof(float) * ((size_t)kCR * (p.s.OD() + p.s.r) + kCR);
     dim3 grid(p.s.H, (p.B * p.q_len + kCR - 1) / kCR);
     if (p.s.kind == MLA_KV_FP32) {
         cudaFuncSetAttribute(combine_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -681,22 +693,27 @@ constexpr int kAT = 16;   // tokens per INT2 append CTA
 template <int NC>
 __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
     extern __shared__ float sa[];
-    const int r = p.s.r, dR = p.s.dR, gs = p.s.gs, ng = r / gs;
-    const bool rope_codes = p.s.kind == MLA_KV_INT2_ROT_QR;   // the rope key as INT2 groups too
+    const int r = p.s.r, dR = p.s.dR, gs = p.s.gs;
+    const int RD = p.s.RD();          // rotated dims: r, or r + d_R (INT2_JOINT: [c ; k_R])
+    const int ng = RD / gs;
+    const bool rope_codes = p.s.kind == MLA_KV_INT2_ROT_QR;   // the rope key as unrotated INT2 groups
     const int QD = p.s.QD(), ng_all = QD / gs;
-    float *sc = sa;                   // [kAT][r] latent (fp32)
-    float *sy = sc + kAT * r;         // [kAT][r] rotated
-    float *sr = sy + kAT * r;         // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
+    float *sc = sa;                   // [kAT][RD] rotation input (fp32)
+    float *sy = sc + kAT * RD;        // [kAT][RD] rotated
+    float *sr = sy + kAT * RD;        // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
     __shared__ long long s_row[kAT];
     const int n0 = blockIdx.x * kAT;
     const int tid = threadIdx.x;
     if (tid < kAT) s_row[tid] = (n0 + tid < p.num_new) ? locate_slot(p, n0 + tid) : -1;
     const __nv_bfloat16 *c = (const __nv_bfloat16 *)p.c_kv;
-    for (int idx = tid; idx < kAT * r; idx += blockDim.x) {
-        int t = idx / r, k = idx % r;
-        sc[idx] = (n0 + t < p.num_new) ? __bfloat162float(c[(size_t)(n0 + t) * r + k]) : 0.f;
-    }
     const __nv_bfloat16 *kr = (const __nv_bfloat16 *)p.k_rope;
+    for (int idx = tid; idx < kAT * RD; idx += blockDim.x) {
+        int t = idx / RD, k = idx % RD;
+        float v = 0.f;
+        if (n0 + t < p.num_new)
+            v = k < r ? __bfloat162float(c[(size_t)(n0 + t) * r + k]) : __bfloat162float(kr[(size_t)(n0 + t) * dR + k - r]);
+        sc[idx] = v;
+    }
     if (rope_codes)
         for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
             int t = idx / dR, d = idx % dR;
@@ -708,16 +725,16 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
     for (int t = 0; t < kAT; ++t)
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc) acc[t][cc] = 0.f;
-    for (int k = 0; k < r; ++k) {
+    for (int k = 0; k < RD; ++k) {
         float Rk[NC];
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc) {
             int j = tid + 256 * cc;
-            Rk[cc] = j < r ? __ldg(p.R + (size_t)k * r + j) : 0.f;
+            Rk[cc] = j < RD ? __ldg(p.R + (size_t)k * RD + j) : 0.f;
         }
 #pragma unroll
         for (int t = 0; t < kAT; ++t) {
-            const float cv = sc[t * r + k];
+            const float cv = sc[t * RD + k];
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc[t][cc] = __fmaf_rn(cv, Rk[cc], acc[t][cc]);
         }
@@ -727,16 +744,16 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc) {
             int j = tid + 256 * cc;
-            if (j < r) sy[t * r + j] = acc[t][cc];
+            if (j < RD) sy[t * RD + j] = acc[t][cc];
         }
     __syncthreads();
-    // groups 0..ng-1: the rotated latent; INT2_ROT_QR: then the rope key's groups
+    // groups 0..ng-1: the rotated row; INT2_ROT_QR: then the rope key's groups
     for (int job = tid; job < kAT * ng_all; job += blockDim.x) {
         const int t = job / ng_all, g = job % ng_all;
         const long long row = s_row[t];
         if (row < 0) continue;
         const float thr = p.clip[g];
-        const float *y = g < ng ? sy + t * r + g * gs : sr + t * dR + (g - ng) * gs;
+        const float *y = g < ng ? sy + t * RD + g * gs : sr + t * dR + (g - ng) * gs;
         float lo = CUDART_INF_F, hi = -CUDART_INF_F;
         for (int j = 0; j < gs; ++j) {
             float v = fminf(fmaxf(y[j], -thr), thr);
@@ -765,7 +782,7 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
         szp[0] = s16;
         szp[1] = z16;
     }
-    if (!rope_codes)
+    if (p.s.kind == MLA_KV_INT2_ROT)   // the rope key kept in bf16
         for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
             const int t = idx / dR, d = idx % dR;
             const long long row = s_row[t];
@@ -787,14 +804,17 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
     } else if (p.s.kind == MLA_KV_FP32) {
         return launch_pdl(append_copy_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     } else {
-        const size_t smem = sizeof(float) * kAT * (2 * (size_t)p.s.r + (p.s.kind == MLA_KV_INT2_ROT_QR ? p.s.dR : 0));
+        const size_t smem = sizeof(float) * kAT * (2 * (size_t)p.s.RD() + (p.s.kind == MLA_KV_INT2_ROT_QR ? p.s.dR : 0));
         dim3 grid((p.num_new + kAT - 1) / kAT);
-        if (p.s.r <= 256) {
+        if (p.s.RD() <= 256) {
             cudaFuncSetAttribute(append_int2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             append_int2_kernel<1><<<grid, 256, smem, st>>>(p);
-        } else if (p.s.r <= 512) {
+        } else if (p.s.RD() <= 512) {
             cudaFuncSetAttribute(append_int2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             append_int2_kernel<2><<<grid, 256, smem, st>>>(p);
+        } else if (p.s.RD() <= 768) {
+            cudaFuncSetAttribute(append_int2_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<3><<<grid, 256, smem, st>>>(p);
         } else {
             cudaFuncSetAttribute(append_int2_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             append_int2_kernel<4><<<grid, 256, smem, st>>>(p);

@@ -995,7 +995,7 @@ static bool make_out_map(CUtensorMap *map, void *base, int r, int rows_seq, int 
 
 bool tc_shape_supported(const ShapeArgs &s) {
     if (s.r != 512 || s.dR != 64 || s.bs != tc::kTile) return false;
-    return s.kind == MLA_KV_BF16 || (is_int2(s.kind) && s.gs == 32);
+    return s.kind == MLA_KV_BF16 || ((s.kind == MLA_KV_INT2_ROT || s.kind == MLA_KV_INT2_ROT_QR) && s.gs == 32);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st) {

@@ -61,6 +61,12 @@ def test_shape_validation(lib):
     assert mla.mla_resolve_impl(_shape(flags=2)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(flags=mla.MLA_FLAG_WUV_FOLDED)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, flags=mla.MLA_FLAG_WUV_FOLDED)) >= 0
+    # the joint rope/nope kind: generic kernel only, no folded up-projection, whole row in groups
+    joint = mla.MLA_KV_INT2_JOINT
+    assert mla.mla_resolve_impl(_shape(kind=joint)) == mla.MLA_IMPL_SIMT
+    assert mla.mla_resolve_impl(_shape(kind=joint, impl=mla.MLA_IMPL_TCGEN05)) == mla.MLA_ERR_UNSUPPORTED
+    assert mla.mla_resolve_impl(_shape(kind=joint, flags=mla.MLA_FLAG_WUV_FOLDED)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=joint, rope_dim=48)) == mla.MLA_ERR_INVALID
     # the extra per-token key: a multiple of 8 up to 1024, BF16/FP32 kinds only
     assert mla.mla_resolve_impl(_shape(index_dim=64)) in (mla.MLA_IMPL_SIMT, mla.MLA_IMPL_TCGEN05)
     assert mla.mla_resolve_impl(_shape(index_dim=12)) == mla.MLA_ERR_INVALID

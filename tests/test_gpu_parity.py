@@ -602,3 +602,48 @@ def test_int2_decode_with_folded_up_projection(gpu_lib, kind_name, impl_name, H)
             Y = oint2.decode(codes, sz).astype(np.float64)
             ro, rl = oint2.attention_rope_int2(w.q[b], Y, R32, w.W_UV, w.scale)
         _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
+# ------------------------------------------------------------ joint rope/nope kind
+
+@pytest.mark.parametrize("H", [32, 128])
+def test_int2_joint_codes_append_and_decode(gpu_lib, H):
+    """INT2_JOINT ([c ; k_R] rotated by one 576-dim eigenbasis, 18 INT2 groups): the
+    appended codes and scale/zero of every token bit-exact against the oracle's
+    encoding (the fp32 rotation chain over all 576 inputs), and the decode against the
+    oracle's joint attention over the dequantised rows."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, _, _ = _int2_setup(B=3, H=H, len_range=(40, 300))
+    rng = np.random.default_rng(12)
+    KRcal = workloads.bf16_round(rng.standard_normal((w.calib.shape[0], 64)).astype(np.float32)).astype(np.float64)
+    Xj = np.concatenate([w.calib, KRcal], axis=1)
+    Rj, _ = oint2.fit_rotation(Xj)
+    Tj = oint2.clip_thresholds(Xj, Rj)
+    Rj32, Tj32 = Rj.astype(np.float32), Tj.astype(np.float32)
+    shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_JOINT)
+    assert mla.mla_resolve_impl(shape) == mla.MLA_IMPL_SIMT
+    cache = mla.Cache.allocate(shape)
+    assert cache.rope is None and cache.bytes_per_token() == 216
+    st0 = gu.append_tokens(cache, w, w.latent, w.rope, np.zeros(w.B, np.int32), Rj32, Tj32)
+    st1 = gu.append_tokens(cache, w, w.new_latent, w.new_rope, w.start_pos, Rj32, Tj32)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st0)[0] == mla.MLA_OK and mla.mla_read_status_word(st1)[0] == mla.MLA_OK
+    ref = []
+    for b in range(w.B):
+        K = np.concatenate([np.concatenate([w.latent[b], w.new_latent[b]]),
+                            np.concatenate([w.rope[b], w.new_rope[b]])], axis=1)
+        ref.append(oint2.quantize(K, Rj32, Tj32))
+    nb = w.num_blocks
+    ref_codes = layout.write_paged(nb, 64, 144, w.block_table, [x[0] for x in ref], [0] * w.B, np.uint8)
+    ref_sz = layout.write_paged(nb, 64, 36, w.block_table, [x[1].reshape(-1, 36) for x in ref], [0] * w.B, np.uint16)
+    np.testing.assert_array_equal(cache.codes.cpu().numpy(), ref_codes)
+    np.testing.assert_array_equal(cache.scale_zero.cpu().view(torch.int16).numpy().view(np.uint16).reshape(nb, 64, 36),
+                                  ref_sz)
+    w.seq_lens = (w.seq_lens + 32).astype(np.int32)
+    out, lse, ws = gu.attend(w, shape, cache, w.q, R=Rj32)
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    for b in range(w.B):
+        Y = oint2.decode(ref[b][0], ref[b][1]).astype(np.float64)
+        ro, rl = oint2.attention_joint(w.q[b], Y, Rj32, w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
