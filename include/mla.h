@@ -298,6 +298,52 @@ mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cach
 mla_status mla_fold_rotation(const mla_shape *shape, const float *R, const void *W_UV, void *W_folded,
                              void *stream);
 
+/* ---- Calibration of the rotated-INT2 cache (once per layer, off the decode path).
+ *   Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10),
+ *   maintainer reply, "How the rotation adapts to the latent": Sigma = c^T c over
+ *   calibration latents, its eigenvectors in ascending eigenvalue order (so that
+ *   low-variance directions share INT2 groups) as R, clip thresholds fit on the
+ *   rotated latent; and the "open refinement" paragraph after it, weighting latent
+ *   directions by what the up-projection does with them (mla_calib_eigh_weighted).
+ * Device calls are stream-ordered like the attention calls; host calls run on the
+ * calling thread and touch no device. */
+typedef enum { MLA_DTYPE_F64 = 0, MLA_DTYPE_F32 = 1, MLA_DTYPE_BF16 = 2 } mla_dtype;
+
+/* sigma [d, d] fp64 (device) = X^T X, uncentred and unscaled, for calibration rows
+ * X [n, d] (device, mla_dtype), accumulated in fp64. d <= 4096. */
+mla_status mla_calib_covariance(const void *X, int64_t n, int32_t d, int32_t dtype, double *sigma, void *stream);
+
+/* M [r, r] fp64 (device) = sum_h (W_UK[h]^T W_UK[h] + W_UV[h] W_UV[h]^T) for
+ * W_UK [H, d_n, r] and W_UV [H, r, d_v] (device, both mla_dtype): how strongly each
+ * latent direction reaches the keys and the values. */
+mla_status mla_calib_projection_energy(const void *W_UK, const void *W_UV, int32_t H, int32_t d_n, int32_t r,
+                                       int32_t d_v, int32_t dtype, double *M, void *stream);
+
+/* HOST. Eigen-decomposition of the symmetric A [d, d] (host fp64; the lower triangle
+ * is read): eigvals [d] ascending; the columns of R (R64 fp64 and/or R32 fp32
+ * [d, d] row-major, either may be NULL) are the eigenvectors in that order, each
+ * with its largest-magnitude entry (the first on ties) positive, so that y = c . R
+ * as in mla_latent_append. MLA_ERR_UNSUPPORTED if the iteration fails to converge. */
+mla_status mla_calib_eigh(const double *A, int32_t d, double *eigvals, double *R64, float *R32);
+
+/* HOST. The up-projection-aware basis: as mla_calib_eigh for G = S^1/2 M S^1/2
+ * (S^1/2 from the eigen-decomposition of S, negative eigenvalues taken as 0), with
+ * S = mla_calib_covariance and M = mla_calib_projection_energy (host copies). With
+ * M a multiple of the identity it is the basis of S itself. */
+mla_status mla_calib_eigh_weighted(const double *S, const double *M, int32_t d, double *eigvals, double *R64,
+                                   float *R32);
+
+/* absY [n, d] fp64 (device) = |X . R| for calibration rows X [n, d] (device,
+ * mla_dtype) and R [d, d] fp64 (device). */
+mla_status mla_calib_project_abs(const void *X, int64_t n, int32_t d, int32_t dtype, const double *R, double *absY,
+                                 void *stream);
+
+/* HOST. Clip thresholds: clip[g] (fp32) = the pct-th percentile of absY[:, g*gs ..
+ * g*gs + gs - 1] over all n rows, linearly interpolated between the two order
+ * statistics around (n * gs - 1) * pct / 100. absY [n, d] host fp64 (e.g. a copy of
+ * mla_calib_project_abs's output). d a multiple of group_size, 0 <= pct <= 100. */
+mla_status mla_calib_thresholds(double *absY, int64_t n, int32_t d, int32_t group_size, double pct, float *clip);
+
 /* Library ABI version (major * 100 + minor). */
 int32_t mla_version(void);
 

@@ -36,6 +36,7 @@ MLA_IMPL_AUTO = 0
 MLA_IMPL_SIMT = 1
 MLA_IMPL_TCGEN05 = 2
 MLA_FLAG_WUV_FOLDED = 1
+MLA_DTYPE_F64, MLA_DTYPE_F32, MLA_DTYPE_BF16 = 0, 1, 2
 
 # Every symbol include/mla.h declares.
 EXPORTED = (
@@ -43,6 +44,8 @@ EXPORTED = (
     "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
     "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc", "mla_selftest_wait_timeout",
     "mla_latent_append_index", "mla_fold_rotation",
+    "mla_calib_covariance", "mla_calib_projection_energy", "mla_calib_eigh", "mla_calib_eigh_weighted",
+    "mla_calib_project_abs", "mla_calib_thresholds",
 )
 
 
@@ -104,6 +107,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_selftest_wait_timeout.restype = i32
     lib.mla_fold_rotation.argtypes = [sp, vp, vp, vp, vp]
     lib.mla_fold_rotation.restype = i32
+    i64 = ctypes.c_int64
+    lib.mla_calib_covariance.argtypes = [vp, i64, i32, i32, vp, vp]
+    lib.mla_calib_projection_energy.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    lib.mla_calib_eigh.argtypes = [vp, i32, vp, vp, vp]
+    lib.mla_calib_eigh_weighted.argtypes = [vp, vp, i32, vp, vp, vp]
+    lib.mla_calib_project_abs.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+    lib.mla_calib_thresholds.argtypes = [vp, i64, i32, i32, ctypes.c_double, vp]
+    for name in ("mla_calib_covariance", "mla_calib_projection_energy", "mla_calib_eigh", "mla_calib_eigh_weighted",
+                 "mla_calib_project_abs", "mla_calib_thresholds"):
+        getattr(lib, name).restype = i32
     lib.mla_profile_enable.argtypes = [i32]
     lib.mla_profile_enable.restype = i32
     lib.mla_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), i32p, i32p]
@@ -332,3 +345,102 @@ def mla_profile_read():
     _check(load_library().mla_profile_read(ctypes.byref(ms), ctypes.byref(n_att), ctypes.byref(n_all)),
            "mla_profile_read")
     return float(ms.value), int(n_att.value), int(n_all.value)
+
+
+# ---------------------------------------------------------------- calibration
+
+def _np_ptr(a):
+    return a.ctypes.data if a is not None else None
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.float64: MLA_DTYPE_F64, torch.float32: MLA_DTYPE_F32, torch.bfloat16: MLA_DTYPE_BF16}[t.dtype]
+
+
+def calib_covariance(X, stream=None):
+    """Sigma = X^T X (fp64, device) for calibration rows X [n, d] on the device."""
+    import torch
+    n, d = X.shape
+    sigma = torch.empty((d, d), dtype=torch.float64, device=X.device)
+    _check(load_library().mla_calib_covariance(_ptr(X), int(n), int(d), _dtype_code(X), _ptr(sigma), _stream(stream)),
+           "mla_calib_covariance")
+    return sigma
+
+
+def calib_projection_energy(W_UK, W_UV, stream=None):
+    """M = sum_h W_UK[h]^T W_UK[h] + W_UV[h] W_UV[h]^T (fp64, device)."""
+    import torch
+    H, dn, r = W_UK.shape
+    dv = W_UV.shape[2]
+    M = torch.empty((r, r), dtype=torch.float64, device=W_UK.device)
+    _check(load_library().mla_calib_projection_energy(_ptr(W_UK), _ptr(W_UV), int(H), int(dn), int(r), int(dv),
+                                                      _dtype_code(W_UK), _ptr(M), _stream(stream)),
+           "mla_calib_projection_energy")
+    return M
+
+
+def calib_eigh(A):
+    """Host eigenbasis of a symmetric fp64 matrix: (eigenvalues ascending, R fp64, R fp32)."""
+    import numpy as np
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    d = A.shape[0]
+    w = np.empty(d, np.float64)
+    R64 = np.empty((d, d), np.float64)
+    R32 = np.empty((d, d), np.float32)
+    _check(load_library().mla_calib_eigh(_np_ptr(A), d, _np_ptr(w), _np_ptr(R64), _np_ptr(R32)), "mla_calib_eigh")
+    return w, R64, R32
+
+
+def calib_eigh_weighted(S, M):
+    """Host eigenbasis of S^1/2 M S^1/2: (eigenvalues ascending, R fp64, R fp32)."""
+    import numpy as np
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    M = np.ascontiguousarray(M, dtype=np.float64)
+    d = S.shape[0]
+    w = np.empty(d, np.float64)
+    R64 = np.empty((d, d), np.float64)
+    R32 = np.empty((d, d), np.float32)
+    _check(load_library().mla_calib_eigh_weighted(_np_ptr(S), _np_ptr(M), d, _np_ptr(w), _np_ptr(R64), _np_ptr(R32)),
+           "mla_calib_eigh_weighted")
+    return w, R64, R32
+
+
+def calib_project_abs(X, R64, stream=None):
+    """|X . R| (fp64, device) for calibration rows X [n, d] and R [d, d] fp64, both on the device."""
+    import torch
+    n, d = X.shape
+    out = torch.empty((n, d), dtype=torch.float64, device=X.device)
+    _check(load_library().mla_calib_project_abs(_ptr(X), int(n), int(d), _dtype_code(X), _ptr(R64), _ptr(out),
+                                                _stream(stream)), "mla_calib_project_abs")
+    return out
+
+
+def calib_thresholds(absY, group_size: int = 32, pct: float = 99.0):
+    """Host clip thresholds (fp32 [d / group_size]) from |X . R| [n, d] (host fp64,
+    reordered in place)."""
+    import numpy as np
+    absY = np.ascontiguousarray(absY, dtype=np.float64)
+    n, d = absY.shape
+    clip = np.empty(d // group_size, np.float32)
+    _check(load_library().mla_calib_thresholds(_np_ptr(absY), int(n), int(d), int(group_size), float(pct),
+                                               _np_ptr(clip)), "mla_calib_thresholds")
+    return clip
+
+
+def calibrate_rotation(X, group_size: int = 32, pct: float = 99.0, W_UK=None, W_UV=None):
+    """The per-layer calibration of a rotated-INT2 cache from calibration rows X [n, d]
+    on the device: Sigma on the GPU, its eigenbasis on the host (the up-projection-aware
+    one when W_UK and W_UV are given), |X . R| on the GPU and the clip thresholds on the
+    host. Returns (R fp32 [d, d], clip fp32 [d / group_size], eigenvalues, R fp64) as
+    numpy arrays."""
+    import torch
+    S = calib_covariance(X).cpu().numpy()
+    if W_UK is not None:
+        M = calib_projection_energy(W_UK, W_UV).cpu().numpy()
+        w, R64, R32 = calib_eigh_weighted(S, M)
+    else:
+        w, R64, R32 = calib_eigh(S)
+    absY = calib_project_abs(X, torch.from_numpy(R64).to(X.device)).cpu().numpy()
+    clip = calib_thresholds(absY, group_size, pct)
+    return R32, clip, w, R64
