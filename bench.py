@@ -44,7 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--configs", action="store_true",
-                    help="time the four parity workloads (one JSON line each) instead of the bench step")
+                    help="time the other workloads only (one JSON line each) instead of the bench step")
+    ap.add_argument("--no-configs", action="store_true", help="leave the per-workload record out of the bench line")
     return ap.parse_args(argv)
 
 
@@ -162,20 +163,23 @@ def recorded_traffic(kernel: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    """nvidia-smi clock / throttle-reason sampling, timestamped, so that the samples
+    of each measured window (the timed steps, the other legs) can be summarised."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index=0):
-        self.samples = []
+    def __init__(self, device_index=0, interval_ms=20):
+        self.samples = []          # (host time, fields)
         self.proc = None
         self.dev = device_index
+        self.interval_ms = interval_ms
 
     def start(self):
         try:
-            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", str(self.interval_ms)]
             vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
             first = vis.split(",")[0].strip() if vis else str(self.dev)
             if first:
@@ -190,23 +194,31 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
-                self.samples.append(parts)
+                self.samples.append((time.perf_counter(), parts))
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         time.sleep(0.12)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+
+    def summary(self, t0=None, t1=None, slack=0.06):
+        """Median SM clock, max clock, power and the throttle reasons seen between t0
+        and t1 (host perf_counter seconds; widened by `slack` on both sides so that a
+        short window still holds the samples taken while it ran)."""
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, mx, reasons = [], [], set()
-        for p in self.samples:
+        sm, mx, pw, reasons = [], [], [], set()
+        for ts, p in self.samples:
+            if t0 is not None and (ts < t0 - slack or ts > t1 + slack):
+                continue
             try:
                 sm.append(float(p[0]))
                 mx.append(float(p[1]))
+                pw.append(float(p[2]))
             except ValueError:
                 continue
             for n, v in zip(names, p[4:8]):
@@ -215,7 +227,26 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, then /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -334,6 +365,11 @@ def run_gb300(args):
         mla.mla_latent_append(cache, bt, start, cu1, cc, rr, stream=stream)
         mla.mla_decode(cache, bt, seq_lens, qq, W_UV, w.scale, out, lse, ws, stream=stream)
 
+    # clocks are sampled from the warm-up on, through every leg; each leg's window is
+    # summarised on its own
+    sampler = ClockSampler(local)
+    sampler.start()
+    windows = {}
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -343,11 +379,10 @@ def run_gb300(args):
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    sampler.start()
+    t_a = time.perf_counter()
     mla.mla_profile_enable(2)          # launch counting only in this loop (no events)
     for k in range(K):
         flush.zero_()
@@ -355,21 +390,32 @@ def run_gb300(args):
         step()
         ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
+    windows["timed_steps"] = (t_a, time.perf_counter())
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
     _, _, n_kernels = mla.mla_profile_read()
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    # the same steps, untimed, for about 0.4 s: the clock record of this load when the
+    # timed region is shorter than a few sampling periods
+    t_a = time.perf_counter()
+    while time.perf_counter() - t_a < 0.4:
+        for _ in range(50):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+    windows["soak"] = (t_a, time.perf_counter())
     # the attention kernel's own duration, in separate steps: the library's event pair
     # around it would otherwise sit between the kernels of the timed steps
+    t_a = time.perf_counter()
     mla.mla_profile_enable(1)
-    for k in range(max(3, K // 4)):
+    for k in range(max(20, K // 4)):
         flush.zero_()
         step()
     torch.cuda.synchronize(dev)
     att_ms, att_n, _ = mla.mla_profile_read()
     mla.mla_profile_enable(False)
     att_avg_ms = att_ms / max(att_n, 1)
+    windows["roofline"] = (t_a, time.perf_counter())
 
     e2e = None
     if not args.no_e2e:
@@ -423,17 +469,19 @@ def run_gb300(args):
         for _ in range(3):
             e2e_run()
         torch.cuda.synchronize(dev)
-        ke = max(3, K // 4)
+        ke = max(20, K)
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        t_a = time.perf_counter()
         for k in range(ke):
             flush.zero_()
             ev2[k][0].record(stream)
             e2e_run()
             ev2[k][1].record(stream)
         torch.cuda.synchronize(dev)
+        windows["e2e"] = (t_a, time.perf_counter())
         e2e_ms = sum(a.elapsed_time(b) for a, b in ev2) / ke
         code, flags = mla.mla_get_status(ws)
         if code != mla.MLA_OK:
@@ -442,6 +490,64 @@ def run_gb300(args):
         d2h = hout.numel() * 2 + hlse.numel() * 4
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h,
                "mode": "CUDA graph replay" if graph is not None else "eager launches"}
+        # Overlapped variant: the inputs of step k + 1 are uploaded (on a second stream)
+        # while step k computes, into the other of two device buffers; step k's
+        # result is read back as before. One graph per buffer parity; the timed region
+        # starts with the upload of step 0's inputs, so every step's copies are in it.
+        if graph is not None:
+            try:
+                bufs = [(torch.empty_like(q), torch.empty_like(new_c), torch.empty_like(new_r)) for _ in range(2)]
+                cstream = torch.cuda.Stream(dev)
+
+                def upload(buf, st):
+                    with torch.cuda.stream(st):
+                        buf[0].copy_(hq, non_blocking=True)
+                        buf[1].copy_(hc, non_blocking=True)
+                        buf[2].copy_(hr, non_blocking=True)
+
+                def overlapped_step(par):
+                    cur, nxt = bufs[par], bufs[1 - par]
+                    cstream.wait_stream(side)           # fork the copy branch off the step
+                    upload(nxt, cstream)
+                    mla.mla_latent_append(cache, bt, start, cu1, cur[1], cur[2], stream=side)
+                    mla.mla_decode(cache, bt, seq_lens, cur[0], W_UV, w.scale, out, lse, ws, stream=side)
+                    hout.copy_(out, non_blocking=True)
+                    hlse.copy_(lse, non_blocking=True)
+                    side.wait_stream(cstream)           # join: the next inputs have landed
+
+                graphs = []
+                for par in range(2):
+                    side.wait_stream(stream)
+                    with torch.cuda.stream(side):
+                        overlapped_step(par)
+                    side.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=side):
+                        overlapped_step(par)
+                    torch.cuda.synchronize(dev)
+                    graphs.append(g)
+                upload(bufs[0], stream)
+                for k in range(4):
+                    graphs[k & 1].replay()
+                torch.cuda.synchronize(dev)
+                ev3 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                torch.cuda.synchronize(dev)
+                ev3[0].record(stream)
+                upload(bufs[0], stream)
+                for k in range(ke):
+                    graphs[k & 1].replay()
+                ev3[1].record(stream)
+                torch.cuda.synchronize(dev)
+                e2e["overlapped_ms"] = ev3[0].elapsed_time(ev3[1]) / ke
+                e2e["overlapped_note"] = ("inputs of step k+1 uploaded on a second stream during step k, two "
+                                          "device buffers; L2 not flushed between these steps")
+                code, flags = mla.mla_get_status(ws)
+                if code != mla.MLA_OK:
+                    raise RuntimeError(f"device status {code} flags {flags} after the overlapped steps")
+            except RuntimeError:
+                raise
+            except Exception as exc:   # noqa: BLE001 - the serial number stands alone
+                print(f"e2e: overlapped variant not measured ({exc})", file=sys.stderr)
 
     if world > 1:
         step_ms, att_avg_ms, e2e_max = max_over_ranks([step_ms, att_avg_ms, e2e["ms"] if e2e else 0.0], world, dev)
@@ -449,6 +555,7 @@ def run_gb300(args):
             e2e["ms"] = e2e_max
 
     if rank != 0:
+        sampler.stop()
         if world > 1:
             dist.destroy_process_group()
         return 0
@@ -460,10 +567,18 @@ def run_gb300(args):
     achieved = kb / (att_avg_ms * 1e-3) / 1e9
     kernel_name = {mla.MLA_IMPL_SIMT: "decode_simt_kernel", mla.MLA_IMPL_TCGEN05: "decode_tc_kernel"}[
         mla.mla_resolve_impl(shape, 1)]
+    configs = None
+    if not args.no_configs:
+        t_a = time.perf_counter()
+        configs = measure_configs(mla, dev, peaks, flush)
+        windows["configs"] = (t_a, time.perf_counter())
+    sampler.stop()
+    clocks = sampler.summary(*windows["timed_steps"])
+    clock_legs = {k: sampler.summary(*v) for k, v in windows.items() if k != "timed_steps"}
     cpu = None
     if not args.no_cpu_baseline:
         rate, tok, secs, calls = oracle_throughput(w, 12.0)
-        cpu = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "cpu_model": cpu_model(), "kind": "oracle",
                "sample": f"{calls} whole sequences of this workload ({tok} cached tokens, all heads), "
                          f"fp64 numpy, {secs:.1f} s"}
     line = {
@@ -484,45 +599,78 @@ def run_gb300(args):
                      "tensor_tflops": kf / (att_avg_ms * 1e-3) / 1e12},
         "gpu_launches": int(n_kernels),
         "clocks": clocks,
+        "clocks_legs": clock_legs,
         "cpu_baseline": cpu,
     }
     if e2e:
         line["e2e"] = {"value": tokens / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                        "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"], "launch": e2e["mode"]}
+        if "overlapped_ms" in e2e:
+            line["e2e"]["overlapped"] = {"value": tokens / (e2e["overlapped_ms"] * 1e-3),
+                                         "ms_per_step": e2e["overlapped_ms"], "note": e2e["overlapped_note"]}
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
 
 
-def run_configs(args):
-    """One line per workload: a decode (or verify) call timed as a whole (no event
-    pairs inside), then the attention kernel alone in separate calls."""
+def measure_configs(mla, dev, peaks, flush):
+    """The other workloads of the parity suite, each timed as whole calls (plan,
+    attention kernel, combine; INT2: and the query rotation) and its attention kernel
+    alone in separate calls (the library's event pair around it), L2 flushed before
+    every call. Each entry: algorithmic bytes (cache read once + the query) and flops
+    (QK^T + PV) of the attention kernel, their ratio, the bound it implies against the
+    measured peaks (burst figures: every kernel here is timed alone) and the
+    fraction reached. The rotated-INT2 workloads are calibrated with the library's
+    own calibration; their up-projection is folded (MLA_FLAG_WUV_FOLDED)."""
     import numpy as np
     import torch
-    from mla_latent_kv_08_gb300 import build as _build
-    _build.build()
-    import mla_latent_kv_08_gb300 as mla
     import workloads
-    dev = torch.device("cuda", 0)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     bf = torch.bfloat16
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    res = {}
 
     def t(x, dtype=None):
         tt = torch.from_numpy(np.ascontiguousarray(x))
         return (tt.to(dtype) if dtype is not None else tt).to(dev)
 
-    def run(name, w, kind, q_len, R=None, T=None, n=20, fold=False):
+    def timed(fn, n):
+        tot = 0.0
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            tot += e0.elapsed_time(e1)
+        return tot / n
+
+    def run(key, desc, w, kind, q_len, R=None, T=None, n=20, fold=False, append=False):
         shape = mla.Shape(num_heads=w.H, kv_lora_rank=w.r, rope_dim=w.d_rope, v_head_dim=w.d_v,
                           block_size=w.block_size, num_blocks=w.num_blocks, kind=kind,
                           flags=mla.MLA_FLAG_WUV_FOLDED if fold else 0)
         cache = mla.Cache.allocate(shape, dev)
         cu = t(np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32))
         Rd = None if R is None else t(R.astype(np.float32))
-        mla.mla_latent_append(cache, t(w.block_table), t(np.zeros(w.B, np.int32)), cu,
-                              t(np.concatenate(w.latent), bf), t(np.concatenate(w.rope), bf), R=Rd,
-                              clip=None if T is None else t(T.astype(np.float32)))
+        Td = None if T is None else t(T.astype(np.float32))
         bt, sl = t(w.block_table), t(w.seq_lens.astype(np.int32))
+        mla.mla_latent_append(cache, bt, t(np.zeros(w.B, np.int32)), cu, t(np.concatenate(w.latent), bf),
+                              t(np.concatenate(w.rope), bf), R=Rd, clip=Td)
+        entry = {"workload": desc}
+        if append:
+            # the workload's 1024 appended tokens (32 per sequence) rotated and quantised
+            nc, nr = t(np.concatenate(w.new_latent), bf), t(np.concatenate(w.new_rope), bf)
+            cun = t(np.arange(0, 32 * w.B + 1, 32, dtype=np.int32))
+            sp = t(w.start_pos.astype(np.int32))
+            app_ms = timed(lambda: mla.mla_latent_append(cache, bt, sp, cun, nc, nr, R=Rd, clip=Td), n)
+            D = w.r + w.d_rope
+            qd = D if kind == mla.MLA_KV_INT2_JOINT else w.r
+            abytes = (int(nc.numel()) + int(nr.numel())) * 2 + int(nc.shape[0]) * cache.bytes_per_token() + qd * qd * 4
+            entry["append"] = {"tokens": int(nc.shape[0]), "us": app_ms * 1e3,
+                               "algorithmic_bytes": abytes, "GBs": abytes / (app_ms * 1e-3) / 1e9}
         q, W = t(w.q, bf), t(w.W_UV, bf)
         if fold:                    # once per layer: W'_UV = R^T . W_UV
             Wf = torch.empty_like(W)
@@ -532,60 +680,78 @@ def run_configs(args):
         lse = torch.empty((w.B, q_len, w.H), dtype=torch.float32, device=dev)
         ws = mla.alloc_workspace(shape, w.B, q_len, dev)
         call = mla.mla_decode if q_len == 1 else mla.mla_verify
+        go = lambda: call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)   # noqa: E731
         for _ in range(3):
-            call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)
+            go()
         torch.cuda.synchronize(dev)
-        tot = 0.0
-        for _ in range(n):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)
-            e1.record()
-            torch.cuda.synchronize(dev)
-            tot += e0.elapsed_time(e1)
+        call_ms = timed(go, n)
         mla.mla_profile_enable(1)
         for _ in range(n):
             flush.zero_()
-            call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)
+            go()
         torch.cuda.synchronize(dev)
         ms, na, _ = mla.mla_profile_read()
         mla.mla_profile_enable(0)
         code, flags = mla.mla_get_status(ws)
         tok = int(w.seq_lens.sum())
         D = w.r + w.d_rope
-        if kind == mla.MLA_KV_BF16:
-            per_tok = D * 2
-        elif kind == mla.MLA_KV_INT2_ROT:
-            per_tok = w.r // 4 + (w.r // 32) * 4 + 2 * w.d_rope
-        else:                                   # the rope key held as codes as well
-            per_tok = D // 4 + (D // 32) * 4
-        kb = tok * per_tok + w.B * q_len * w.H * D * 2
-        fl = 2 * tok * q_len * w.H * (D + w.r)
-        att = ms / na
-        print(json.dumps({"config": name, "tokens": tok, "call_us": tot / n * 1e3, "attention_us": att * 1e3,
-                          "attention_GBs": kb / (att * 1e-3) / 1e9, "attention_TFLOPs": fl / (att * 1e-3) / 1e12,
-                          "call_KV_tokens_per_s": tok / (tot / n * 1e-3), "status": [code, flags],
-                          "impl": mla.mla_resolve_impl(shape, q_len)}), flush=True)
+        kb = tok * cache.bytes_per_token() + w.B * q_len * w.H * D * 2
+        kf = 2 * tok * q_len * w.H * (D + w.r)
+        att = ms / max(na, 1)
+        ai = kf / kb
+        bound = "tensor" if ai > ridge else "hbm"
+        gbs, tfs = kb / (att * 1e-3) / 1e9, kf / (att * 1e-3) / 1e12
+        entry.update({
+            "tokens": tok, "q_len": q_len, "impl": "tcgen05" if mla.mla_resolve_impl(shape, q_len) == 2 else "simt",
+            "call_us": call_ms * 1e3, "attention_us": att * 1e3, "KV_tokens_per_s": tok / (call_ms * 1e-3),
+            "algorithmic_bytes": kb, "algorithmic_flops": kf, "arithmetic_intensity": ai, "bound": bound,
+            "attention_GBs": gbs, "attention_TFLOPs": tfs,
+            "frac": (gbs / peaks["hbm_gbs"]) if bound == "hbm" else (tfs / peaks["bf16_tflops"]),
+            "frac_of": "measured HBM GB/s" if bound == "hbm" else "measured bf16 TFLOP/s (burst)",
+            "status": [int(code), int(flags)]})
+        res[key] = entry
+        del cache, ws
+        torch.cuda.empty_cache()
 
-    w = workloads.dsv3(1)
-    run("C1 DeepSeek-V3 decode, B=32, L~U[1024,8192]", w, mla.MLA_KV_BF16, 1)
     w = workloads.long_context(2)
-    run("C2 long context, H=64, L=32768/131072", w, mla.MLA_KV_BF16, 1)
+    run("C2", "long context: B=2, L=32768/131072, H=64, bf16", w, mla.MLA_KV_BF16, 1)
     w = workloads.verify(3)
-    run("C3 speculative verify, q_len=8, L~U[4096,32768]", w, mla.MLA_KV_BF16, 8, n=5)
-    # NEXT: one 512-token prefill chunk in latent form (the verify call, causal window)
+    run("C3", "speculative verify: B=16, q_len=8, L~U[4096,32768], H=128, bf16", w, mla.MLA_KV_BF16, 8, n=5)
     w = workloads.verify(5, B=1, q_len=512, len_range=(8192, 8192))
-    run("C5 chunked prefill, one 512-token chunk at L=8192, H=128", w, mla.MLA_KV_BF16, 512, n=3)
+    run("C5", "chunked prefill: one 512-token chunk at L=8192, H=128, bf16", w, mla.MLA_KV_BF16, 512, n=3)
+    del w
+    # rotated INT2: the workload's 65536 calibration latents through the library's own calibration
     w = workloads.int2_rotated(4)
-    # timing only: any orthogonal R and positive thresholds exercise the same kernels
-    R = workloads.haar_orthogonal(np.random.Generator(np.random.PCG64(5)), w.r)
-    run("C4 rotated-INT2 decode, W_UV folded with R^T", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0),
-        fold=True)
-    run("C4 rotated-INT2 decode, o.R^T per call", w, mla.MLA_KV_INT2_ROT, 1, R=R, T=np.full(w.r // 32, 4.0))
-    # next-2: the same workload with the rope key held as two more INT2 groups (216 B a token)
-    run("C6 rotated-INT2 decode, rope key as INT2 too, W_UV folded", w, mla.MLA_KV_INT2_ROT_QR, 1, R=R,
-        T=np.full((w.r + w.d_rope) // 32, 4.0), fold=True)
+    X = torch.from_numpy(np.asarray(w.calib)).to(dev)
+    R32, clip, _, _ = mla.calibrate_rotation(X)
+    run("C4", "rotated INT2 (DeepSeek-V3 shapes, 320 B/token), calibrated by the library, W_UV folded",
+        w, mla.MLA_KV_INT2_ROT, 1, R=R32, T=clip, fold=True, append=True)
+    # the two rope/nope variants: the rope key's thresholds from calibration rope keys
+    # of the cache's rope law (N(0,1) rounded to bf16)
+    rng = np.random.Generator(np.random.PCG64(11))
+    KRcal = workloads.bf16_round(rng.standard_normal((X.shape[0], w.d_rope)).astype(np.float32)).astype(np.float64)
+    clip_r = mla.calib_thresholds(np.abs(KRcal), 32, 99.0)
+    run("C6", "rotated INT2 with the rope key as two more INT2 groups (216 B/token), W_UV folded",
+        w, mla.MLA_KV_INT2_ROT_QR, 1, R=R32, T=np.concatenate([clip, clip_r]), fold=True, append=True)
+    Xj = torch.cat([X, torch.from_numpy(KRcal).to(dev)], dim=1).contiguous()
+    del X
+    Rj32, clip_j, _, _ = mla.calibrate_rotation(Xj)
+    del Xj
+    run("C7", "joint INT2: [c ; k_R] rotated by one 576-dim basis (216 B/token), generic kernel",
+        w, mla.MLA_KV_INT2_JOINT, 1, R=Rj32, T=clip_j, n=3, append=True)
+    return res
+
+
+def run_configs(args):
+    """--configs: the other workloads only, one JSON line each."""
+    import torch
+    from mla_latent_kv_08_gb300 import build as _build
+    _build.build()
+    import mla_latent_kv_08_gb300 as mla
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for key, entry in measure_configs(mla, dev, load_peaks(), flush).items():
+        print(json.dumps(dict(config=key, **entry)), flush=True)
     return 0
 
 
