@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--configs", action="store_true",
                     help="time the other workloads only (one JSON line each) instead of the bench step")
     ap.add_argument("--no-configs", action="store_true", help="leave the per-workload record out of the bench line")
+    ap.add_argument("--only", default="", help="with --configs: comma-separated workload keys (e.g. C3,C4)")
+    ap.add_argument("--reps", type=int, default=0, help="with --configs: timed calls per workload (0: defaults)")
     return ap.parse_args(argv)
 
 
@@ -616,7 +618,7 @@ def run_gb300(args):
     return 0
 
 
-def measure_configs(mla, dev, peaks, flush):
+def measure_configs(mla, dev, peaks, flush, only=(), reps=0):
     """The other workloads of the parity suite, each timed as whole calls (plan,
     attention kernel, combine; INT2: and the query rotation) and its attention kernel
     alone in separate calls (the library's event pair around it), L2 flushed before
@@ -637,18 +639,33 @@ def measure_configs(mla, dev, peaks, flush):
         return (tt.to(dtype) if dtype is not None else tt).to(dev)
 
     def timed(fn, n):
+        """Device time of fn: captured once as a CUDA graph, replayed n times right
+        after an L2 flush, so that the host's launch latency is not in the number."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        torch.cuda.synchronize(dev)
         tot = 0.0
         for _ in range(n):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            fn()
+            g.replay()
             e1.record()
             torch.cuda.synchronize(dev)
             tot += e0.elapsed_time(e1)
         return tot / n
 
     def run(key, desc, w, kind, q_len, R=None, T=None, n=20, fold=False, append=False):
+        if only and key not in only:
+            return
+        if reps:
+            n = reps
         shape = mla.Shape(num_heads=w.H, kv_lora_rank=w.r, rope_dim=w.d_rope, v_head_dim=w.d_v,
                           block_size=w.block_size, num_blocks=w.num_blocks, kind=kind,
                           flags=mla.MLA_FLAG_WUV_FOLDED if fold else 0)
@@ -666,10 +683,11 @@ def measure_configs(mla, dev, peaks, flush):
             cun = t(np.arange(0, 32 * w.B + 1, 32, dtype=np.int32))
             sp = t(w.start_pos.astype(np.int32))
             app_ms = timed(lambda: mla.mla_latent_append(cache, bt, sp, cun, nc, nr, R=Rd, clip=Td), n)
+            entry_note = "device time of one call, captured as a CUDA graph and replayed after an L2 flush"
             D = w.r + w.d_rope
             qd = D if kind == mla.MLA_KV_INT2_JOINT else w.r
             abytes = (int(nc.numel()) + int(nr.numel())) * 2 + int(nc.shape[0]) * cache.bytes_per_token() + qd * qd * 4
-            entry["append"] = {"tokens": int(nc.shape[0]), "us": app_ms * 1e3,
+            entry["append"] = {"tokens": int(nc.shape[0]), "us": app_ms * 1e3, "timing": entry_note,
                                "algorithmic_bytes": abytes, "GBs": abytes / (app_ms * 1e-3) / 1e9}
         q, W = t(w.q, bf), t(w.W_UV, bf)
         if fold:                    # once per layer: W'_UV = R^T . W_UV
@@ -703,7 +721,8 @@ def measure_configs(mla, dev, peaks, flush):
         gbs, tfs = kb / (att * 1e-3) / 1e9, kf / (att * 1e-3) / 1e12
         entry.update({
             "tokens": tok, "q_len": q_len, "impl": "tcgen05" if mla.mla_resolve_impl(shape, q_len) == 2 else "simt",
-            "call_us": call_ms * 1e3, "attention_us": att * 1e3, "KV_tokens_per_s": tok / (call_ms * 1e-3),
+            "call_us": call_ms * 1e3, "call_timing": "device time of one call (CUDA graph replay after an L2 flush)",
+            "attention_us": att * 1e3, "KV_tokens_per_s": tok / (call_ms * 1e-3),
             "algorithmic_bytes": kb, "algorithmic_flops": kf, "arithmetic_intensity": ai, "bound": bound,
             "attention_GBs": gbs, "attention_TFLOPs": tfs,
             "frac": (gbs / peaks["hbm_gbs"]) if bound == "hbm" else (tfs / peaks["bf16_tflops"]),
@@ -713,13 +732,18 @@ def measure_configs(mla, dev, peaks, flush):
         del cache, ws
         torch.cuda.empty_cache()
 
-    w = workloads.long_context(2)
-    run("C2", "long context: B=2, L=32768/131072, H=64, bf16", w, mla.MLA_KV_BF16, 1)
-    w = workloads.verify(3)
-    run("C3", "speculative verify: B=16, q_len=8, L~U[4096,32768], H=128, bf16", w, mla.MLA_KV_BF16, 8, n=5)
-    w = workloads.verify(5, B=1, q_len=512, len_range=(8192, 8192))
-    run("C5", "chunked prefill: one 512-token chunk at L=8192, H=128, bf16", w, mla.MLA_KV_BF16, 512, n=3)
-    del w
+    want = lambda *keys: not only or any(k in only for k in keys)   # noqa: E731
+    if want("C2"):
+        w = workloads.long_context(2)
+        run("C2", "long context: B=2, L=32768/131072, H=64, bf16", w, mla.MLA_KV_BF16, 1)
+    if want("C3"):
+        w = workloads.verify(3)
+        run("C3", "speculative verify: B=16, q_len=8, L~U[4096,32768], H=128, bf16", w, mla.MLA_KV_BF16, 8, n=5)
+    if want("C5"):
+        w = workloads.verify(5, B=1, q_len=512, len_range=(8192, 8192))
+        run("C5", "chunked prefill: one 512-token chunk at L=8192, H=128, bf16", w, mla.MLA_KV_BF16, 512, n=3)
+    if not want("C4", "C6", "C7"):
+        return res
     # rotated INT2: the workload's 65536 calibration latents through the library's own calibration
     w = workloads.int2_rotated(4)
     X = torch.from_numpy(np.asarray(w.calib)).to(dev)
@@ -750,7 +774,8 @@ def run_configs(args):
     import mla_latent_kv_08_gb300 as mla
     dev = torch.device("cuda", 0)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    for key, entry in measure_configs(mla, dev, load_peaks(), flush).items():
+    only = tuple(k.strip() for k in args.only.split(",") if k.strip())
+    for key, entry in measure_configs(mla, dev, load_peaks(), flush, only, args.reps).items():
         print(json.dumps(dict(config=key, **entry)), flush=True)
     return 0
 
