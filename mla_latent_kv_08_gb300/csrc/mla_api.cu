@@ -64,7 +64,8 @@ static mla_status check_shape(const mla_shape *s) {
     if ((s->flags & MLA_FLAG_WUV_FOLDED) && (!is_int2(s->kind) || s->kind == MLA_KV_INT2_JOINT))
         return MLA_ERR_INVALID;
     if (is_int2(s->kind)) {
-        if (s->group_size < 4 || s->group_size % 4 || s->kv_lora_rank % s->group_size) return MLA_ERR_INVALID;
+        if (s->group_size < 4 || s->group_size > 128 || s->group_size % 4 || s->kv_lora_rank % s->group_size)
+            return MLA_ERR_INVALID;
         if (s->rope_dim < 8) return MLA_ERR_INVALID;
         if ((s->kind == MLA_KV_INT2_ROT_QR || s->kind == MLA_KV_INT2_JOINT) && s->rope_dim % s->group_size)
             return MLA_ERR_INVALID;
@@ -141,6 +142,7 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
         w.lse2 = off;   off = up256(off + sizeof(float) * nrow);
         w.ident = off;  off = up256(off + sizeof(int32_t) * ((size_t)B + 1));
         w.r16 = off;    off = up256(off + sizeof(__half) * (size_t)s->kv_lora_rank * s->kv_lora_rank);
+        w.rsplit = off; off = up256(off + 2 * sizeof(__nv_bfloat16) * (size_t)s->kv_lora_rank * s->kv_lora_rank);
     }
     w.total = off;
     return w;
@@ -204,7 +206,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         // of this cache kind) from the tensor-core GEMM for the tensor-core kernel,
         // which then reads it in place of q
         if (tc) {
-            if (launch_rot_query(R, (__half *)(ws + w.r16), q, ws + w.q_prep, B * q_len * s->num_heads,
+            if (launch_rot_query(R, (__nv_bfloat16 *)(ws + w.rsplit), q, ws + w.q_prep, B * q_len * s->num_heads,
                                  s->kv_lora_rank + s->rope_dim, p.status, stream_) != cudaSuccess)
                 return MLA_ERR_CUDA;
             p.q = ws + w.q_prep;
@@ -239,7 +241,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         // W_UV up-projection reads the merged rows as one-split partials
         float *o_rot = (float *)(ws + w.o_rot), *o_lat = (float *)(ws + w.o_lat), *lse2 = (float *)(ws + w.lse2);
         int32_t *ident = (int32_t *)(ws + w.ident);
-        if (launch_rot_output(c, (const __half *)(ws + w.r16), o_rot, o_lat, lse2, ident, p.status, stream_) !=
+        if (launch_rot_output(c, (__half *)(ws + w.r16), o_rot, o_lat, lse2, ident, p.status, stream_) !=
             cudaSuccess)
             return MLA_ERR_CUDA;
         c.split_start = ident;
@@ -248,10 +250,11 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         c.part_lse = lse2;
         c.R = nullptr;
         if (launch_combine_tc(c, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-        prof_kernels(6);
+        prof_kernels(8);            // plan, R split, q . R, decode, merge, R to fp16, o . R^T, combine
     } else {
         if ((comb_tc ? launch_combine_tc(c, stream_) : launch_combine(c, stream_)) != cudaSuccess) return MLA_ERR_CUDA;
-        prof_kernels(int2 ? 4 : 3);
+        // plan, decode, combine; INT2 adds the query rotation (tensor cores: R split + GEMM)
+        prof_kernels(int2 ? (tc ? 5 : 4) : 3);
     }
     return MLA_OK;
 }

@@ -44,7 +44,8 @@ struct WsLayout {
     size_t o_lat;         // fp32 [B * q_len * H][r]  o_rot . R^T
     size_t lse2;          // fp32 [B * q_len * H]     merged log2-sum-exp
     size_t ident;         // int32 [B + 1]           one slot per sequence
-    size_t r16;           // fp16 [r][r]             R as the rotation GEMMs' operand (INT2, tensor cores)
+    size_t r16;           // fp16 [r][r]             R as the output rotation's operand (INT2, tensor cores)
+    size_t rsplit;        // bf16 [2][r][r]          R as two bf16 halves for the query rotation
     size_t total;
     int32_t max_work;     // upper bound of schedule length (streams + B)
     int32_t target;       // number of work streams
@@ -166,11 +167,11 @@ bool combine_tc_supported(const ShapeArgs &s);
 cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st);
 // ---- tensor-core rotations of the rotated-INT2 cache (defined in mla_rot_tc.cu)
 bool rot_tc_supported(const ShapeArgs &s);
-// launch_rot_query also writes R16 = fp16(R) ([r][r], 16-byte aligned), which
-// launch_rot_output then reads.
-cudaError_t launch_rot_query(const float *R, __half *R16, const void *q_bf16, void *q_rot_f16, int rows, int D,
-                             int32_t *status, cudaStream_t st);
-cudaError_t launch_rot_output(const CombineParams &c, const __half *R16, float *o_rot, float *o_lat, float *lse2,
+// launch_rot_query writes Rsplit = [bf16(R) ; bf16(R - bf16(R))] ([2][r][r]) first;
+// launch_rot_output writes R16 = fp16(R) ([r][r]) first. Both 16-byte aligned.
+cudaError_t launch_rot_query(const float *R, __nv_bfloat16 *Rsplit, const void *q_bf16, void *q_rot_f16, int rows,
+                             int D, int32_t *status, cudaStream_t st);
+cudaError_t launch_rot_output(const CombineParams &c, __half *R16, float *o_rot, float *o_lat, float *lse2,
                               int32_t *ident, int32_t *status, cudaStream_t st);
 
 // ---- small device helpers ---------------------------------------------------

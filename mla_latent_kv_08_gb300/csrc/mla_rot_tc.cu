@@ -1,15 +1,16 @@
-// The two rotations of the rotated-INT2 cache on the tensor cores:
-//   q_rot[m, :] = q_lat[m, :] . R          (query prep, before attention)
-//   o_lat[m, :] = o_rot[m, :] . R^T        (after the split merge, before W_UV)
-// as one GEMM kernel Y[M x 512] = X[M x 512] . op(R), op = identity or transpose,
-// with kv_lora_rank 512. R is first converted once per call to fp16 (R16); the
-// GEMM's B tiles come from R16 by TMA, the A tiles (bf16 query rows or fp32
-// merged outputs) are converted to fp16 by the threads that stage them in
-// shared memory, and the MMA accumulates in fp32 in tensor memory. A CTA
-// computes a [128 x 128] tile of Y over eight 64-wide K chunks: warps 1..7 convert
-// the whole A tile into shared memory chunk by chunk (one chunk of loads in flight
-// ahead), while warp 0 streams B through four stages and issues each chunk's MMAs
-// as soon as its A and B are there.
+// The two rotations of the rotated-INT2 cache on the tensor cores, kv_lora_rank 512:
+//   q_rot[m, :] = q_lat[m, :] . R          (query prep, before attention): qrot_kernel,
+//                                          below, with R split into two bf16 halves
+//   o_lat[m, :] = o_rot[m, :] . R^T        (after the split merge, before W_UV, when the
+//                                          up-projection is not folded): rot_gemm_kernel
+// rot_gemm_kernel computes Y[M x 512] = X[M x 512] . op(R), op = identity or
+// transpose. R is first converted per call to fp16 (R16); the GEMM's B tiles come
+// from R16 by TMA, the A tiles (fp32 merged outputs) are converted to fp16 by the
+// threads that stage them in shared memory, and the MMA accumulates in fp32 in
+// tensor memory. A CTA computes a [128 x 128] tile of Y over eight 64-wide K chunks:
+// warps 1..7 convert the whole A tile into shared memory chunk by chunk (one chunk of
+// loads in flight ahead), while warp 0 streams B through four stages and issues each
+// chunk's MMAs as soon as its A and B are there.
 //
 // Also here: the merge of split partials into one latent row per (sequence,
 // draft position, head), which precedes the second rotation.
@@ -56,6 +57,38 @@ __device__ __forceinline__ uint4 pack8_f16(const float *v) {
     const __half2 h2 = __floats2half2_rn(v[4], v[5]);
     const __half2 h3 = __floats2half2_rn(v[6], v[7]);
     return make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1, *(const uint32_t *)&h2, *(const uint32_t *)&h3);
+}
+
+// Y[m, 512 + d] = fp16(X[m, 512 + d]) for the copy_rope dims of rows m0 .. m0 + 127
+// (bf16 X): 16-byte vectors, a thread's loads all issued before its stores.
+__device__ __forceinline__ void copy_rope_f16(const RotParams &rp, int m0, int tid, int nthreads) {
+    if (rp.copy_rope <= 0) return;
+    const int vec = rp.copy_rope / 8;            // 8-element vectors per row
+    const int total = kTm * vec;
+    constexpr int kMaxPer = 8;
+    for (int job0 = tid; job0 < total; job0 += kMaxPer * nthreads) {
+    uint4 v[kMaxPer];
+    int at[kMaxPer];
+    int n = 0;
+    for (int job = job0; job < total && n < kMaxPer; job += nthreads) {
+        const int r = job / vec, c = job % vec, m = m0 + r;
+        if (m >= rp.M) continue;
+        v[n] = __ldg((const uint4 *)((const __nv_bfloat16 *)rp.X + (size_t)m * rp.ldx + kK) + c);
+        at[n++] = job;
+    }
+    for (int i = 0; i < n; ++i) {
+        const int r = at[i] / vec, c = at[i] % vec, m = m0 + r;
+        const __nv_bfloat162 *h = (const __nv_bfloat162 *)&v[i];
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(h[e]);
+            f[2 * e] = x.x;
+            f[2 * e + 1] = x.y;
+        }
+        *((uint4 *)((__half *)rp.Y + (size_t)m * rp.ldy + kK) + c) = pack8_f16(f);
+    }
+    }
 }
 
 // R16 = fp16(R), round to nearest even, eight elements per thread.
@@ -262,15 +295,149 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const __grid_cons
         }
     }
     // the query's rope part passes through unrotated (bf16 -> fp16)
-    if (rp.copy_rope > 0 && blockIdx.y == 0) {
-        for (int job = tid; job < kTm * rp.copy_rope; job += kThreads) {
-            const int r = job / rp.copy_rope, d = job % rp.copy_rope, m = m0 + r;
-            if (m < rp.M) {
-                const float f = __bfloat162float(((const __nv_bfloat16 *)rp.X)[(size_t)m * rp.ldx + kK + d]);
-                ((__half *)rp.Y)[(size_t)m * rp.ldy + kK + d] = __float2half_rn(f);
+    if (blockIdx.y == 0) copy_rope_f16(rp, m0, tid, kThreads);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTn) : "memory");
+    }
+}
+
+// ---- the query rotation, q_rot = q_lat . R, without converting the query --------
+// R is split into two bf16 matrices, R = R_hi + R_lo + e with R_hi = bf16(R) and R_lo
+// = bf16(R - R_hi) (|e| <= 2^-17 |R|, finer than one fp16 rounding of R), so that the
+// bf16 query rows feed the tensor cores straight from TMA: per K-step two MMAs (with
+// R_hi and with R_lo) accumulate into the same fp32 tile. A CTA computes a [128 x 128]
+// tile of q_rot over eight 64-wide K chunks in four TMA stages (A: [128 rows x 64 k]
+// query box; B: [64 k x 128 j] of R_hi and of R_lo, MN-major); lane 0 of warp 0
+// issues the copies and the MMAs, four warps read the tile out as fp16.
+constexpr int kQThreads = 128;
+constexpr int kQStages = 4;
+constexpr uint32_t kQStageBytes = kABytes + 2 * kBBytes;          // 48 KB
+constexpr uint32_t kQOffBar = kQStages * kQStageBytes;            // 192 KB
+constexpr uint32_t kQSmemBytes = kQOffBar + 256 + 1024;
+
+__global__ void __launch_bounds__(256) r_split_bf16_kernel(const float *R, __nv_bfloat16 *Rhi, __nv_bfloat16 *Rlo, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const float v = R[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        Rhi[i] = hi;
+        Rlo[i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
+}
+
+__global__ void __launch_bounds__(kQThreads, 1) qrot_kernel(const __grid_constant__ CUtensorMap q_map,
+                                                            const __grid_constant__ CUtensorMap rhi_map,
+                                                            const __grid_constant__ CUtensorMap rlo_map,
+                                                            const RotParams rp) {
+    const int m0 = blockIdx.x * kTm, j0 = blockIdx.y * kTn;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + kQOffBar);      // [kQStages] chunk landed
+    uint64_t *freed = full + kQStages;                   // [kQStages] MMAs reading the stage done
+    uint64_t *mma_fin = freed + kQStages;
+    uint32_t *tmem_slot = (uint32_t *)(mma_fin + 1);
+    int32_t *abort_flag = (int32_t *)(mma_fin + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    if (tid == 0) {
+        for (int i = 0; i < kQStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&freed[i], 1);
+        }
+        mbar_init(mma_fin, 1);
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTn)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    if (warp == 0 && lane == 0) {
+        // bf16 A and B, fp32 D, M 128, N 128, B MN-major (R's rows are k)
+        constexpr uint32_t idesc = idesc_bf16(kTm, kTn, true);
+        int last[kQStages];
+        auto issue = [&](int kc) {           // chunk kc's A and B boxes into stage kc % kQStages
+            const int st = kc % kQStages;
+            uint8_t *S = smem + st * kQStageBytes;
+            last[st] = kc;
+            mbar_expect_tx(&full[st], kQStageBytes);
+            tma_load_2d(S, &q_map, kc * kKc, m0, &full[st]);
+            for (int atom = 0; atom < kTn / 64; ++atom) {
+                tma_load_2d(S + kABytes + atom * (kKc * 128), &rhi_map, j0 + 64 * atom, kc * kKc, &full[st]);
+                tma_load_2d(S + kABytes + kBBytes + atom * (kKc * 128), &rlo_map, j0 + 64 * atom, kc * kKc, &full[st]);
+            }
+        };
+        for (int st = 0; st < kQStages; ++st) {
+            last[st] = -1;
+            if (st < kChunks) issue(st);
+        }
+        bool ok = true;
+        for (int kc = 0; kc < kChunks && ok; ++kc) {
+            const int st = kc % kQStages;
+            ok = mbar_wait_bounded(&full[st], (kc / kQStages) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint8_t *S = smem + st * kQStageBytes;
+            const uint64_t a0 = sdesc(smem_u32(S), 16, 1024);
+            const uint64_t bh = sdesc(smem_u32(S + kABytes), kKc * 128, 1024);
+            const uint64_t bl = sdesc(smem_u32(S + kABytes + kBBytes), kKc * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kKc / 16; ++kk) {
+                const uint64_t a = a0 + (uint64_t)((32 * kk) >> 4);
+                mma_ss(tmem, a, bh + (uint64_t)((2048 * kk) >> 4), idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                mma_ss(tmem, a, bl + (uint64_t)((2048 * kk) >> 4), idesc, 1u);
+            }
+            mma_commit(&freed[st]);
+            if (kc + kQStages < kChunks) {      // refill the stage once its MMAs are done
+                ok = mbar_wait_bounded(&freed[st], (kc / kQStages) & 1, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs);
+                if (ok) issue(kc + kQStages);
+            }
+        }
+        mma_commit(mma_fin);
+        if (!ok) {
+            // never leave a copy in flight into this CTA's shared memory (bounded waits)
+            for (int st = 0; st < kQStages; ++st)
+                if (last[st] >= 0)
+                    mbar_wait_bounded(&full[st], (last[st] / kQStages) & 1, abort_flag + 1, nullptr, 0, kTimeoutNs);
+        }
+    }
+    __syncwarp();
+    bool ok = mbar_wait_bounded(mma_fin, 0, abort_flag, rp.status, FLAG_TIMEOUT, kTimeoutNs) &&
+              *(volatile int32_t *)abort_flag == 0;
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+    {
+        const int m = m0 + 32 * warp + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+        for (int c = 0; c < kTn / 32; ++c) {
+            uint32_t v[32];
+            if (ok) {
+                TMEM_LD32(taddr + 32 * c, v);
+                tmem_wait_ld();
+            }
+            if (m >= rp.M) continue;
+            __half *dst = (__half *)rp.Y + (size_t)m * rp.ldy + j0 + 32 * c;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = ok ? __uint_as_float(v[8 * q + e]) : CUDART_NAN_F;
+                *(uint4 *)(dst + 8 * q) = pack8_f16(f);
             }
         }
     }
+    // the query's rope part passes through unrotated (bf16 -> fp16)
+    if (blockIdx.y == 0) copy_rope_f16(rp, m0, tid, kQThreads);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -370,12 +537,36 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(CombineParams c, float 
 
 bool rot_tc_supported(const ShapeArgs &s) { return s.r == rot::kK; }
 
-cudaError_t launch_rot_query(const float *R, __half *R16, const void *q_bf16, void *q_rot_f16, int rows, int D,
-                             int32_t *status, cudaStream_t st) {
-    const int n8 = rot::kK * rot::kK / 8;
-    rot::r_to_f16_kernel<<<(n8 + 255) / 256, 256, 0, st>>>(R, R16, n8);
+cudaError_t launch_rot_query(const float *R, __nv_bfloat16 *Rsplit, const void *q_bf16, void *q_rot_f16, int rows,
+                             int D, int32_t *status, cudaStream_t st) {
+    const int n = rot::kK * rot::kK;
+    __nv_bfloat16 *Rhi = Rsplit, *Rlo = Rsplit + n;
+    rot::r_split_bf16_kernel<<<(n + 255) / 256, 256, 0, st>>>(R, Rhi, Rlo, n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    auto fn = rot::encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    CUtensorMap qm, hm, lm;
+    memset(&qm, 0, sizeof qm);
+    cuuint32_t estr[2] = {1, 1};
+    {   // the query rows [rows, D] bf16: boxes of [64 k x 128 rows], rows past the end read 0
+        cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)rot::kTm};
+        if (fn(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q_bf16), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int which = 0; which < 2; ++which) {   // R_hi, R_lo [512 k, 512 j] bf16: boxes of [64 j x 64 k]
+        cuuint64_t dims[2] = {(cuuint64_t)rot::kK, (cuuint64_t)rot::kK};
+        cuuint64_t strides[1] = {(cuuint64_t)rot::kK * 2};
+        cuuint32_t box[2] = {64, 64};
+        if (fn(which ? &lm : &hm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, which ? (void *)Rlo : (void *)Rhi, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     rot::RotParams rp;
     rp.X = q_bf16;
     rp.ldx = D;
@@ -384,12 +575,18 @@ cudaError_t launch_rot_query(const float *R, __half *R16, const void *q_bf16, vo
     rp.M = rows;
     rp.copy_rope = D - rot::kK;
     rp.status = status;
-    return rot::launch_t<false, false, true>(R16, rp, st);
+    e = cudaFuncSetAttribute(rot::qrot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rot::kQSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((rows + rot::kTm - 1) / rot::kTm, rot::kK / rot::kTn);
+    return launch_pdl(rot::qrot_kernel, grid, dim3(rot::kQThreads), rot::kQSmemBytes, st, qm, hm, lm, rp);
 }
 
-cudaError_t launch_rot_output(const CombineParams &c, const __half *R16, float *o_rot, float *o_lat, float *lse2,
+cudaError_t launch_rot_output(const CombineParams &c, __half *R16, float *o_rot, float *o_lat, float *lse2,
                               int32_t *ident, int32_t *status, cudaStream_t st) {
     const int rows = c.B * c.q_len * c.s.H;
+    const int n8 = rot::kK * rot::kK / 8;
+    rot::r_to_f16_kernel<<<(n8 + 255) / 256, 256, 0, st>>>(c.R, R16, n8);
+    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
     rot::merge_rows_kernel<<<min((rows + 7) / 8, 4096), 256, 0, st>>>(c, o_rot, lse2, ident);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

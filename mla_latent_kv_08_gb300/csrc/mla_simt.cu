@@ -690,70 +690,92 @@ __global__ void __launch_bounds__(256) append_index_kernel(AppendParams p) {
 
 constexpr int kAT = 16;   // tokens per INT2 append CTA
 
-template <int NC>
-__global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
+// One CTA: kAT tokens x one block of kAC output columns (a whole number of groups,
+// at most 128). Thread (column c, token half th) runs the fp32 fmaf chains of its
+// column for 8 tokens, k ascending from +0 (the encoding definition's order), with R
+// staged through shared memory 32 rows at a time; then one thread per (token, group)
+// clips, ranges, rounds scale/zero to fp16 and packs the codes.
+constexpr int kAKC = 32;  // R rows staged per step
+template <int COLS>   // COLS: columns per CTA (128 when group_size divides 128, else 0: read `cols`)
+__global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p, int cols_rt) {
     extern __shared__ float sa[];
+    const int cols = COLS ? COLS : cols_rt;
     const int r = p.s.r, dR = p.s.dR, gs = p.s.gs;
     const int RD = p.s.RD();          // rotated dims: r, or r + d_R (INT2_JOINT: [c ; k_R])
+    const int RDp = (RD + 3) & ~3;    // row stride of the staged inputs (float4 reads)
     const int ng = RD / gs;
     const bool rope_codes = p.s.kind == MLA_KV_INT2_ROT_QR;   // the rope key as unrotated INT2 groups
     const int QD = p.s.QD(), ng_all = QD / gs;
-    float *sc = sa;                   // [kAT][RD] rotation input (fp32)
-    float *sy = sc + kAT * RD;        // [kAT][RD] rotated
-    float *sr = sy + kAT * RD;        // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
+    const int j0 = blockIdx.y * cols;                          // first output column of this CTA
+    const int ncol = min(cols, RD - j0);
+    float *sc = sa;                   // [kAT][RDp] rotation input (fp32)
+    float *sR = sc + kAT * RDp;       // [kAKC][cols] rows of R, this CTA's columns
+    float *sy = sR + kAKC * cols;     // [kAT][cols] rotated
+    float *sr = sy + kAT * cols;      // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
     __shared__ long long s_row[kAT];
     const int n0 = blockIdx.x * kAT;
     const int tid = threadIdx.x;
     if (tid < kAT) s_row[tid] = (n0 + tid < p.num_new) ? locate_slot(p, n0 + tid) : -1;
     const __nv_bfloat16 *c = (const __nv_bfloat16 *)p.c_kv;
     const __nv_bfloat16 *kr = (const __nv_bfloat16 *)p.k_rope;
-    for (int idx = tid; idx < kAT * RD; idx += blockDim.x) {
-        int t = idx / RD, k = idx % RD;
-        float v = 0.f;
-        if (n0 + t < p.num_new)
-            v = k < r ? __bfloat162float(c[(size_t)(n0 + t) * r + k]) : __bfloat162float(kr[(size_t)(n0 + t) * dR + k - r]);
-        sc[idx] = v;
-    }
-    if (rope_codes)
+    for (int t = 0; t < kAT; ++t)
+        for (int k = tid; k < RDp; k += blockDim.x) {
+            float v = 0.f;
+            if (n0 + t < p.num_new && k < RD)
+                v = k < r ? __bfloat162float(c[(size_t)(n0 + t) * r + k]) : __bfloat162float(kr[(size_t)(n0 + t) * dR + k - r]);
+            sc[t * RDp + k] = v;
+        }
+    if (rope_codes && blockIdx.y == 0)
         for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
             int t = idx / dR, d = idx % dR;
             sr[idx] = (n0 + t < p.num_new) ? __bfloat162float(kr[(size_t)(n0 + t) * dR + d]) : 0.f;
         }
-    __syncthreads();
-    float acc[kAT][NC];
+    const int col = tid & 127, th = tid >> 7;                 // column, token half (tokens 8*th..8*th+7)
+    const bool act = col < ncol;
+    float acc[8];
 #pragma unroll
-    for (int t = 0; t < kAT; ++t)
-#pragma unroll
-        for (int cc = 0; cc < NC; ++cc) acc[t][cc] = 0.f;
-    for (int k = 0; k < RD; ++k) {
-        float Rk[NC];
-#pragma unroll
-        for (int cc = 0; cc < NC; ++cc) {
-            int j = tid + 256 * cc;
-            Rk[cc] = j < RD ? __ldg(p.R + (size_t)k * RD + j) : 0.f;
+    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+    const float *scb = sc + (8 * th) * RDp;
+    for (int k0 = 0; k0 < RD; k0 += kAKC) {
+        __syncthreads();              // previous chunk consumed (and sc ready on the first pass)
+        for (int kk = tid / cols, cc = tid % cols; kk < kAKC; kk += 256 / cols) {
+            // 256 / cols rows of the chunk per pass (cols divides 256 for every allowed cols)
+            sR[kk * cols + cc] = (k0 + kk < RD && cc < ncol) ? __ldg(p.R + (size_t)(k0 + kk) * RD + j0 + cc) : 0.f;
         }
+        __syncthreads();
+        if (act) {
+            const int kn = min(kAKC, RD - k0);      // a multiple of 4 (RD is)
+            for (int kk = 0; kk < kn; kk += 4) {
+                const float r0 = sR[kk * cols + col], r1 = sR[(kk + 1) * cols + col];
+                const float r2 = sR[(kk + 2) * cols + col], r3 = sR[(kk + 3) * cols + col];
 #pragma unroll
-        for (int t = 0; t < kAT; ++t) {
-            const float cv = sc[t * RD + k];
-#pragma unroll
-            for (int cc = 0; cc < NC; ++cc) acc[t][cc] = __fmaf_rn(cv, Rk[cc], acc[t][cc]);
+                for (int t = 0; t < 8; ++t) {
+                    const float4 x = *(const float4 *)(scb + t * RDp + k0 + kk);
+                    float a = acc[t];
+                    a = __fmaf_rn(x.x, r0, a);      // k ascending: the definition's chain
+                    a = __fmaf_rn(x.y, r1, a);
+                    a = __fmaf_rn(x.z, r2, a);
+                    a = __fmaf_rn(x.w, r3, a);
+                    acc[t] = a;
+                }
+            }
         }
     }
+    if (act)
 #pragma unroll
-    for (int t = 0; t < kAT; ++t)
-#pragma unroll
-        for (int cc = 0; cc < NC; ++cc) {
-            int j = tid + 256 * cc;
-            if (j < RD) sy[t * RD + j] = acc[t][cc];
-        }
+        for (int t = 0; t < 8; ++t) sy[(8 * th + t) * cols + col] = acc[t];
     __syncthreads();
-    // groups 0..ng-1: the rotated row; INT2_ROT_QR: then the rope key's groups
-    for (int job = tid; job < kAT * ng_all; job += blockDim.x) {
-        const int t = job / ng_all, g = job % ng_all;
+    // this CTA's groups of the rotated row; INT2_ROT_QR: the rope key's groups in the
+    // first column block
+    const int g0 = j0 / gs, gn = ncol / gs;
+    const int extra = (rope_codes && blockIdx.y == 0) ? ng_all - ng : 0;
+    for (int job = tid; job < kAT * (gn + extra); job += blockDim.x) {
+        const int t = job / (gn + extra), gl = job % (gn + extra);
         const long long row = s_row[t];
         if (row < 0) continue;
+        const int g = gl < gn ? g0 + gl : ng + (gl - gn);
         const float thr = p.clip[g];
-        const float *y = g < ng ? sy + t * RD + g * gs : sr + t * dR + (g - ng) * gs;
+        const float *y = gl < gn ? sy + t * cols + gl * gs : sr + t * dR + (g - ng) * gs;
         float lo = CUDART_INF_F, hi = -CUDART_INF_F;
         for (int j = 0; j < gs; ++j) {
             float v = fminf(fmaxf(y[j], -thr), thr);
@@ -782,7 +804,7 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p) {
         szp[0] = s16;
         szp[1] = z16;
     }
-    if (p.s.kind == MLA_KV_INT2_ROT)   // the rope key kept in bf16
+    if (p.s.kind == MLA_KV_INT2_ROT && blockIdx.y == 0)   // the rope key kept in bf16
         for (int idx = tid; idx < kAT * dR; idx += blockDim.x) {
             const int t = idx / dR, d = idx % dR;
             const long long row = s_row[t];
@@ -804,20 +826,18 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
     } else if (p.s.kind == MLA_KV_FP32) {
         return launch_pdl(append_copy_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     } else {
-        const size_t smem = sizeof(float) * kAT * (2 * (size_t)p.s.RD() + (p.s.kind == MLA_KV_INT2_ROT_QR ? p.s.dR : 0));
-        dim3 grid((p.num_new + kAT - 1) / kAT);
-        if (p.s.RD() <= 256) {
-            cudaFuncSetAttribute(append_int2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            append_int2_kernel<1><<<grid, 256, smem, st>>>(p);
-        } else if (p.s.RD() <= 512) {
-            cudaFuncSetAttribute(append_int2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            append_int2_kernel<2><<<grid, 256, smem, st>>>(p);
-        } else if (p.s.RD() <= 768) {
-            cudaFuncSetAttribute(append_int2_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            append_int2_kernel<3><<<grid, 256, smem, st>>>(p);
+        // column blocks of whole groups, at most 128 columns (group_size <= 128)
+        const int cols = (128 / p.s.gs) * p.s.gs;
+        const int RDp = (p.s.RD() + 3) & ~3;
+        const size_t smem = sizeof(float) * ((size_t)kAT * RDp + (size_t)kAKC * cols + (size_t)kAT * cols +
+                                             (p.s.kind == MLA_KV_INT2_ROT_QR ? (size_t)kAT * p.s.dR : 0));
+        dim3 grid((p.num_new + kAT - 1) / kAT, (p.s.RD() + cols - 1) / cols);
+        if (cols == 128) {
+            cudaFuncSetAttribute(append_int2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<128><<<grid, 256, smem, st>>>(p, cols);
         } else {
-            cudaFuncSetAttribute(append_int2_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            append_int2_kernel<4><<<grid, 256, smem, st>>>(p);
+            cudaFuncSetAttribute(append_int2_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<0><<<grid, 256, smem, st>>>(p, cols);
         }
     }
     return cudaGetLastError();
