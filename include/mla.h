@@ -94,7 +94,8 @@ typedef struct {
     int32_t block_size;        /* tokens per cache block                          */
     int32_t num_blocks;        /* physical blocks in the pool                     */
     int32_t group_size;        /* INT2 group length along r (and d_R for
-                                  INT2_ROT_QR), e.g. 32; else ignored             */
+                                  INT2_ROT_QR / INT2_JOINT), a multiple of 4 in
+                                  [4, 128], e.g. 32; else ignored                 */
     int32_t kind;              /* mla_kv_kind                                     */
     int32_t impl;              /* mla_impl                                        */
     int32_t num_splits_hint;   /* 0: planner's choice; k>0: aim for about k split-

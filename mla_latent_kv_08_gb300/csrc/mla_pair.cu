@@ -306,6 +306,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
                 if (valid < kTile && vrole) {
                     if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs], (T / kNV) & 1, bars, p.status))) {
                         ok = false;
+                        ++T;                   // this tile's boxes are in flight: drained below
                         break;
                     }
                     for (int jb = lane; jb < (kTile - valid) * 4 * 8; jb += 32) {
@@ -320,6 +321,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
                     if (own) {
                         if (!__all_sync(0xffffffffu, mbar_wait(&bars->t_full[ts], (k / kNT) & 1, bars, p.status))) {
                             ok = false;
+                            ++T;                   // this tile's boxes are in flight: drained below
                             break;
                         }
                         for (int jb = lane; jb < (kTile - valid) * 5 * 8; jb += 32) {
@@ -340,10 +342,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
         // drain: never leave a copy in flight into this CTA's shared memory
         if (vrole) {
             for (int u = T - kNV; u < T; ++u)
-                if (u >= 0) mbar_wait(&bars->v_full[u % kNV], (u / kNV) & 1, bars, p.status);
+                if (u >= 0) mbar_drain(&bars->v_full[u % kNV], (u / kNV) & 1);
         } else {
             for (int u = T - 2 * kNT; u < T; ++u)
-                if (u >= 0 && owned(u)) mbar_wait(&bars->t_full[(u >> 1) % kNT], ((u >> 1) / kNT) & 1, bars, p.status);
+                if (u >= 0 && owned(u)) mbar_drain(&bars->t_full[(u >> 1) % kNT], ((u >> 1) / kNT) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {

@@ -74,6 +74,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Wait for copies already issued into shared memory before a CTA exits, also
+// after an abort (the abort flag is not consulted), bounded by `timeout_ns`.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity,
+                                           unsigned long long timeout_ns = 2000000000ull) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_suspend(bar, parity, 1000u))
+        if (globaltimer() - t0 > timeout_ns) return false;
+    return true;
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"

@@ -77,25 +77,25 @@ constexpr uint32_t kStageBytes = kKvBlocks * kKvBlockBytes;         // 72 KB
 constexpr uint32_t kQBlockBytes = kRows * 128;                      // 16 KB
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
-// INT2 raw stage: one block's codes [64 x 128 B], scale/zero [64 x 64 B] and
-// rope keys [64 x 128 B], copied verbatim and expanded into a stage by the
-// dequantising warps.
-constexpr uint32_t kRawCodes = kTile * 128, kRawSz = kTile * 64, kRawRope = kTile * 128;
-constexpr uint32_t kRawBytes = kRawCodes + kRawSz + kRawRope;       // 20 KB (the larger of the two kinds)
-// Raw stage per INT2 kind, bytes per token: codes, scale/zero pairs, bf16 rope key.
-// INT2_ROT_QR holds the rope key as two more groups of codes (none in bf16).
+// INT2 raw stages (two): one block's codes and scale/zero pairs, copied verbatim and
+// expanded into an operand stage by the dequantising warps. The bf16 rope key of
+// INT2_ROT is not staged here: it is loaded by TMA straight into the operand stage's
+// rope block (bf16 and fp16 share the 16-bit swizzled layout) and converted in place.
+// Bytes per token: codes, scale/zero pairs; INT2_ROT_QR holds the rope key as two
+// more groups of codes.
 template <int KIND> struct Raw {
     static constexpr bool kQR = KIND == MLA_KV_INT2_ROT_QR;
+    static constexpr bool kRopeTma = KIND == MLA_KV_INT2_ROT;         // bf16 rope key by TMA
     static constexpr uint32_t kGroups = kQR ? 18 : 16;               // groups of 32 per token
-    static constexpr uint32_t kCodesRow = 8 * kGroups, kSzRow = 4 * kGroups, kRopeRow = kQR ? 0 : 128;
-    static constexpr uint32_t kCodes = kTile * kCodesRow, kSz = kTile * kSzRow, kRope = kTile * kRopeRow;
-    static constexpr uint32_t kBytes = kCodes + kSz + kRope;
+    static constexpr uint32_t kCodesRow = 8 * kGroups, kSzRow = 4 * kGroups;
+    static constexpr uint32_t kCodes = kTile * kCodesRow, kSz = kTile * kSzRow;
+    static constexpr uint32_t kBytes = kCodes + kSz;
 };
-static_assert(Raw<MLA_KV_INT2_ROT>::kBytes == kRawBytes && Raw<MLA_KV_INT2_ROT_QR>::kBytes <= kRawBytes,
-              "raw stage sizes");
+constexpr uint32_t kRawStage = Raw<MLA_KV_INT2_ROT_QR>::kBytes;      // 13.5 KB (the larger kind)
+static_assert(Raw<MLA_KV_INT2_ROT>::kBytes <= kRawStage && kRawStage % 16 == 0, "raw stage sizes");
 constexpr uint32_t kOffRaw = kOffQ + 3 * kQBlockBytes;              // 192 KB (INT2: after 3 Q blocks)
 constexpr uint32_t kOffBar = kOffQ + kMaxQSmemBlocks * kQBlockBytes; // 224 KB
-static_assert(kOffRaw + kRawBytes <= kOffBar, "INT2 raw stage must fit beside its Q blocks");
+static_assert(kOffRaw + 2 * kRawStage <= kOffBar, "two INT2 raw stages must fit beside the Q blocks");
 constexpr uint32_t kOffXchg = kOffBar + 256;                        // [2][128] fp32 row values
 constexpr uint32_t kSmemBytes = kOffXchg + 1024 + 1024;             // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -178,8 +178,9 @@ struct Bars {
     uint64_t xchg_full;       // both halves of every row wrote their value
     uint64_t xchg_read;       // both halves read the other's value
     uint64_t tail_done[kStages];  // bf16: the producer zeroed a partial tile's slots past the end
-    uint64_t raw_full;        // INT2: raw block landed
-    uint64_t raw_empty;       // INT2: raw block expanded
+    uint64_t raw_full[2];     // INT2: raw block landed (raw stage T % 2)
+    uint64_t raw_empty[2];    // INT2: raw block read by every dequantising thread
+    uint64_t rope_full[kStages];  // INT2_ROT: the bf16 rope block landed in the operand stage
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -222,7 +223,8 @@ constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2
 template <int KIND>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                 const __grid_constant__ CUtensorMap o_map, const TcParams tp) {
+                 const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap rope_map,
+                 const TcParams tp) {
     constexpr bool kInt2 = is_int2(KIND);
     using RW = Raw<KIND>;
     constexpr int kSBufs = Layout<KIND>::kSBufs;
@@ -255,9 +257,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             mbar_init(&bars->full[s], kInt2 ? kDequantThreads : 1);
             mbar_init(&bars->empty[s], 1);
             mbar_init(&bars->tail_done[s], 1);
+            mbar_init(&bars->rope_full[s], 1);
         }
-        mbar_init(&bars->raw_full, 1);
-        mbar_init(&bars->raw_empty, kDequantThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->raw_full[i], 1);
+            mbar_init(&bars->raw_empty[i], kDequantThreads);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_free[i], kSoftmaxThreads);
@@ -317,7 +322,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (kInt2) {
                         prefetch_l2(p.codes + (size_t)blk * RW::kCodes, RW::kCodes);
                         prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz);
-                        if (RW::kRope) prefetch_l2((const uint8_t *)p.rope + (size_t)blk * RW::kRope, RW::kRope);
+                        if (RW::kRopeTma)
+                            prefetch_l2((const uint8_t *)p.rope + (size_t)blk * kKvBlockBytes, kKvBlockBytes);
                     } else {
                         // the block's rows (index keys included: one contiguous range)
                         prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * p.s.E(),
@@ -343,20 +349,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     blk = 0;
                 }
                 if (kInt2) {
-                    if (T >= 1 && !__all_sync(0xffffffffu, mbar_wait(&bars->raw_empty, (T - 1) & 1, bars, p.status))) {
+                    // raw stage T % 2 is free once every dequantising thread read tile T - 2
+                    const int rs = T & 1;
+                    if (T >= 2 &&
+                        !__all_sync(0xffffffffu, mbar_wait(&bars->raw_empty[rs], ((T - 2) >> 1) & 1, bars, p.status))) {
                         ok = false;
                         break;
                     }
-                    uint8_t *raw = smem + kOffRaw;
-                    if (lane == 0) mbar_expect_tx(&bars->raw_full, RW::kBytes);
+                    uint8_t *raw = smem + kOffRaw + rs * kRawStage;
+                    if (lane == 0) mbar_expect_tx(&bars->raw_full[rs], RW::kBytes);
                     __syncwarp();
-                    if (lane == 0) bulk_load(raw, p.codes + (size_t)blk * RW::kCodes, RW::kCodes, &bars->raw_full);
+                    if (lane == 0) bulk_load(raw, p.codes + (size_t)blk * RW::kCodes, RW::kCodes, &bars->raw_full[rs]);
                     if (lane == 1)
                         bulk_load(raw + RW::kCodes, (const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz,
-                                  &bars->raw_full);
-                    if (RW::kRope && lane == 2)
-                        bulk_load(raw + RW::kCodes + RW::kSz, (const uint8_t *)p.rope + (size_t)blk * RW::kRope,
-                                  RW::kRope, &bars->raw_full);
+                                  &bars->raw_full[rs]);
                     if (lane == 0) MLA_TRACE_POINT(24, T);
                 } else {
                     const int s = T % kStages;
@@ -378,6 +384,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (valid < kTile) {
                         if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status))) {
                             ok = false;
+                            ++T;                   // this tile's boxes are in flight: drained below
                             break;
                         }
                         const int jobs = (kTile - valid) * kKvBlocks * 8;
@@ -399,10 +406,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         }
         // drain: never leave a copy in flight into this CTA's shared memory
         if (kInt2) {
-            if (T >= 1) mbar_wait(&bars->raw_full, (T - 1) & 1, bars, p.status);
+            for (int u = T - 2; u < T; ++u)
+                if (u >= 0) mbar_drain(&bars->raw_full[u & 1], (u >> 1) & 1);
         } else {
             for (int u = T - kStages; u < T; ++u)
-                if (u >= 0) mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, bars, p.status);
+                if (u >= 0) mbar_drain(&bars->full[u % kStages], (u / kStages) & 1);
         }
         __syncwarp();
     } else if (kInt2 && (warp == 2 || warp == 3 || warp >= 12)) {
@@ -414,28 +422,39 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         const int dw = warp < 4 ? warp - 2 : warp - 10;   // dequantising warp 0..5
         const __half2 k1024 = __float2half2_rn(1024.f);
         const int dt = 32 * dw + lane;
-        int T = 0;
+        int T = 0, rope_pending = -1;              // dt 0: tile whose rope copy is in flight
         bool ok = true;
         for (int i = i0; i < i1 && ok; ++i) {
             const WorkItem it = p.work[i];
             const int L = p.seq_lens[it.b];
             const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
             for (int t = 0; t < nt; ++t, ++T) {
-                const int s = T % kStages;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->raw_full, T & 1, bars, p.status))) { ok = false; break; }
-                if (dt == 0) MLA_TRACE_POINT(25, T);
+                const int s = T % kStages, rs = T & 1;
                 if (T >= kStages &&
                     !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
                     ok = false;
                     break;
                 }
                 if (dt == 0) MLA_TRACE_POINT(26, T);
+                uint8_t *stage = smem + kOffStage + s * kStageBytes;
+                // the operand stage is free: its bf16 rope block comes by TMA while the
+                // latent part is expanded
+                if (RW::kRopeTma && dt == 0) {
+                    int blk = block_of(p, it.b, it.t0 / kTile + t);
+                    if (blk < 0) blk = 0;                  // the softmax marks the item's rows NaN
+                    mbar_expect_tx(&bars->rope_full[s], kKvBlockBytes);
+                    tma_load_2d(stage + 8 * kKvBlockBytes, &rope_map, 0, blk * kTile, &bars->rope_full[s]);
+                    rope_pending = T;
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->raw_full[rs], (T >> 1) & 1, bars, p.status))) {
+                    ok = false;
+                    break;
+                }
+                if (dt == 0) MLA_TRACE_POINT(25, T);
                 const int valid = min(kTile, L - (it.t0 + t * kTile));
-                const uint8_t *raw = smem + kOffRaw;
-                const uint4 *rope = (const uint4 *)(raw + RW::kCodes + RW::kSz);
+                const uint8_t *raw = smem + kOffRaw + rs * kRawStage;
                 const uint8_t *codes = raw;
                 const __half *sz = (const __half *)(raw + RW::kCodes);
-                uint8_t *stage = smem + kOffStage + s * kStageBytes;
                 // One 32-dim group of row rr (8 code bytes, one scale/zero pair) into four
                 // 16-byte chunks of fp16; zeros for slots past the sequence end.
                 auto expand_group = [&](int rr, int g, uint4 (&outc)[4]) {
@@ -485,13 +504,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * gr + q4)) = outc[q4];
                     }
-                } else {
-                    // rope key: bf16 -> fp16 (exact for values inside fp16's range), 8 chunks a row
+                }
+                mbar_arrive(&bars->raw_empty[rs]);    // this thread is done with the raw stage
+                if (RW::kRopeTma) {
+                    // the rope block landed as bf16: to fp16 in place (exact for values inside
+                    // fp16's range), 16-byte chunks; slots past the sequence end become zeros
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bars->rope_full[s], (T / kStages) & 1, bars, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    rope_pending = -1;
                     for (int job = dt; job < kTile * 8; job += kDequantThreads) {
                         const int rr = job >> 3, ch = job & 7;
+                        uint4 *at = (uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch));
                         uint4 out = make_uint4(0, 0, 0, 0);
                         if (rr < valid) {
-                            const uint4 u = rope[rr * 8 + ch];
+                            const uint4 u = *at;
                             const __nv_bfloat162 *bh = (const __nv_bfloat162 *)&u;
                             __half2 hh[4];
 #pragma unroll
@@ -499,15 +527,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                             out = make_uint4(*(const uint32_t *)&hh[0], *(const uint32_t *)&hh[1], *(const uint32_t *)&hh[2],
                                              *(const uint32_t *)&hh[3]);
                         }
-                        *(uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch)) = out;
+                        *at = out;
                     }
                 }
                 fence_proxy_async();
-                mbar_arrive(&bars->raw_empty);
                 mbar_arrive(&bars->full[s]);
                 if (dt == 0) MLA_TRACE_POINT(27, T);
             }
         }
+        // an aborted pass never leaves its rope copy in flight
+        if (rope_pending >= 0) mbar_drain(&bars->rope_full[rope_pending % kStages], (rope_pending / kStages) & 1);
     } else if (warp == 1) {
         // ================================================= MMA issuer: lane 0 alone runs
         // the loop (plain bounded waits, no warp-wide votes or syncs per tile)
@@ -960,14 +989,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over the first 576 columns of a row-major [rows, row_elems] matrix of
-// 16-bit elements (bf16 or fp16), 128-byte swizzled boxes of [box_rows, 64]. Rows
-// past the end read as zero.
+// 2-D map over the first `cols` columns (576 by default) of a row-major
+// [rows, row_elems] matrix of 16-bit elements (bf16 or fp16), 128-byte swizzled
+// boxes of [box_rows, 64]. Rows past the end read as zero.
 static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows,
-                     CUtensorMapDataType dtype, uint64_t row_elems = kD) {
+                     CUtensorMapDataType dtype, uint64_t row_elems = kD, uint64_t cols = kD) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
@@ -1009,11 +1038,17 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     // MN-major V operand: 64-dim atoms 8 KB apart, 8-token groups 1 KB apart.
     tp.v_lbo = tc::kKvBlockBytes;
     tp.v_sbo = 1024;
-    CUtensorMap kv_map, q_map, o_map;
+    CUtensorMap kv_map, q_map, o_map, rope_map;
     memset(&kv_map, 0, sizeof kv_map);
+    memset(&rope_map, 0, sizeof rope_map);
     const bool int2 = is_int2(p.s.kind);
     if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile,
                                CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)p.s.E()))
+        return cudaErrorInvalidValue;
+    // INT2_ROT: the bf16 rope keys [num_blocks * block_size, d_R], one 64-row box a tile
+    if (p.s.kind == MLA_KV_INT2_ROT &&
+        !tc::make_map(&rope_map, p.rope, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      (uint64_t)p.s.dR, (uint64_t)p.s.dR))
         return cudaErrorInvalidValue;
     // the query: bf16 as given, or the fp16 rotated query of the INT2 cache
     const int rows_seq = p.q_len * p.s.H;
@@ -1028,7 +1063,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);
     const int threads = int2 ? tc::threads_of<MLA_KV_INT2_ROT>() : tc::threads_of<MLA_KV_BF16>();
-    return launch_pdl(kern, grid, dim3(threads), tc::kSmemBytes, st, kv_map, q_map, o_map, tp);
+    return launch_pdl(kern, grid, dim3(threads), tc::kSmemBytes, st, kv_map, q_map, o_map, rope_map, tp);
 }
 
 }  // namespace mla
