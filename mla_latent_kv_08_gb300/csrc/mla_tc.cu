@@ -14,7 +14,7 @@
 // Per CTA, per 64-token tile (one cache block):
 //   TMA     9 loads of [64 tokens x 64 dims], 128B-swizzled, into a stage (INT2:
 //           a bulk copy of the block's codes, scale/zero pairs and rope keys,
-//           expanded into the stage by six dequantising warps)
+//           expanded into the stage by eight dequantising warps)
 //   MMA     S[128 x 64]  = Q[128 x 576] . K[64 x 576]^T   (36 x M128 N64 K16, in
 //           two issue groups; the first K-steps read Q from tensor memory)
 //   softmax two warps per 32-row lane quarter, one per half of the tile's
@@ -49,8 +49,8 @@ namespace mla {
 namespace tc {
 
 // Threads per CTA: warps 0..3 control (producer, MMA, two dequantisers), 4..11
-// softmax; the INT2 kind adds dequantising warps 12..15.
-template <int KIND> constexpr int threads_of() { return is_int2(KIND) ? 512 : 384; }
+// softmax; the INT2 kind adds dequantising warps 12..17.
+template <int KIND> constexpr int threads_of() { return is_int2(KIND) ? 576 : 384; }
 constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
@@ -96,14 +96,16 @@ static_assert(Raw<MLA_KV_INT2_ROT>::kBytes <= kRawStage && kRawStage % 16 == 0, 
 constexpr uint32_t kOffRaw = kOffQ + 3 * kQBlockBytes;              // 192 KB (INT2: after 3 Q blocks)
 constexpr uint32_t kOffBar = kOffQ + kMaxQSmemBlocks * kQBlockBytes; // 224 KB
 static_assert(kOffRaw + 2 * kRawStage <= kOffBar, "two INT2 raw stages must fit beside the Q blocks");
-constexpr uint32_t kOffXchg = kOffBar + 256;                        // [2][128] fp32 row values
+constexpr uint32_t kOffXchg = kOffBar + 512;                        // [2][128] fp32 row values
 constexpr uint32_t kSmemBytes = kOffXchg + 1024 + 1024;             // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 // P (bf16 [128 rows x 64 tokens], 16 KB) of tile T is written into two column
 // blocks of tile T's own stage that only QK reads (the other half's V dims),
 // once QK(T) is done; PV(T) is their last reader.
 __host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u; }
-constexpr int kDequantWarps = 6;      // warps 2, 3, 12..15 (rotated-INT2 cache)
+// rotated-INT2 cache: warps 2, 3, 12..17, two on each SM sub-partition (warp w runs
+// on sub-partition w % 4), beside two softmax warps on each
+constexpr int kDequantWarps = 8;
 constexpr int kDequantThreads = 32 * kDequantWarps;
 constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 64 dims] bf16
 // QK K-steps in two issue groups: [0,16) (Q from tensor memory in the bf16 kind)
@@ -161,7 +163,9 @@ __device__ unsigned long long g_cta_wait[4096];   // after the grid dependency w
 //         17 first QK MMA issued, 18 about to issue it, 19 second issued, 20 tail
 //         handled, 21 after the tcgen05 fence, 22 descriptors ready (MMA),
 //         INT2: 24 raw block copy issued (producer), 25 raw block seen, 26 stage
-//         free seen, 27 stage expanded (dequantising warp 2)
+//         free seen, 27 stage expanded (dequantising warp 2), 28 latent part
+//         expanded (warp 2), 29 rope block landed (warp 2), 30 latent part
+//         expanded (the last dequantising warp), 31 P complete (MMA)
 
 struct Bars {
     uint64_t full[kStages];       // bf16: tile landed; INT2: stage expanded
@@ -175,8 +179,8 @@ struct Bars {
     uint64_t q_tmem;          // the tensor-memory part of Q is stored
     uint64_t qreg_free;       // every softmax thread is done with the Q region
     uint64_t mma_fin;
-    uint64_t xchg_full;       // both halves of every row wrote their value
-    uint64_t xchg_read;       // both halves read the other's value
+    uint64_t xchg_full[4];    // lane quarter q: both halves of its rows wrote their value
+    uint64_t xchg_read[4];    // lane quarter q: both halves read the other's value
     uint64_t tail_done[kStages];  // bf16: the producer zeroed a partial tile's slots past the end
     uint64_t raw_full[2];     // INT2: raw block landed (raw stage T % 2)
     uint64_t raw_empty[2];    // INT2: raw block read by every dequantising thread
@@ -185,7 +189,7 @@ struct Bars {
     int32_t abort_flag;
 };
 
-static_assert(sizeof(Bars) <= 256, "barriers must fit below the exchange area");
+static_assert(sizeof(Bars) <= 512, "barriers must fit below the exchange area");
 
 struct TcParams {
     DecodeParams p;
@@ -276,8 +280,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         mbar_init(&bars->q_tmem, kSoftmaxThreads);
         mbar_init(&bars->qreg_free, kSoftmaxThreads);
         mbar_init(&bars->mma_fin, 1);
-        mbar_init(&bars->xchg_full, kSoftmaxThreads);
-        mbar_init(&bars->xchg_read, kSoftmaxThreads);
+        for (int q = 0; q < 4; ++q) {          // the two softmax warps of a lane quarter
+            mbar_init(&bars->xchg_full[q], 64);
+            mbar_init(&bars->xchg_read[q], 64);
+        }
         bars->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -308,8 +314,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         // ================================================= producer (+ L2 prefetch)
         // bf16 cache: the warp runs converged; lane 0 waits and arms the stage
         // barrier, lanes 0..8 each issue one of the tile's nine TMA boxes.
-        // INT2 cache: lanes 0..2 copy the block's codes, scale/zero pairs and rope
-        // keys into the raw stage for the dequantising warps.
+        // INT2 cache: lanes 0 and 1 copy the block's codes and scale/zero pairs into
+        // a raw stage for the dequantising warps.
         const bool prefetcher = kPrefetchAhead > 0 && half == 0 && g == 0;
         int pi = i0, pt = 0, ahead = 0;        // L2 prefetch cursor, kPrefetchAhead tiles ahead
         auto advance_prefetch = [&]() {
@@ -419,7 +425,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         // this cache kind), written in the 128B-swizzled layout the MMAs
         // read; the bf16 rope key is converted to fp16; slots past the sequence end
         // are zeroed.
-        const int dw = warp < 4 ? warp - 2 : warp - 10;   // dequantising warp 0..5
+        const int dw = warp < 4 ? warp - 2 : warp - 10;   // dequantising warp 0..7
         const __half2 k1024 = __float2half2_rn(1024.f);
         const int dt = 32 * dw + lane;
         int T = 0, rope_pending = -1;              // dt 0: tile whose rope copy is in flight
@@ -455,57 +461,92 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 const uint8_t *raw = smem + kOffRaw + rs * kRawStage;
                 const uint8_t *codes = raw;
                 const __half *sz = (const __half *)(raw + RW::kCodes);
-                // One 32-dim group of row rr (8 code bytes, one scale/zero pair) into four
-                // 16-byte chunks of fp16; zeros for slots past the sequence end.
-                auto expand_group = [&](int rr, int g, uint4 (&outc)[4]) {
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) outc[q4] = make_uint4(0, 0, 0, 0);
-                    if (rr >= valid) return;
-                    const uint2 cb = *(const uint2 *)(codes + rr * RW::kCodesRow + 8 * g);
-                    const __half2 szp = *(const __half2 *)(sz + (rr * RW::kGroups + g) * 2);
+                // One 32-dim group (8 code bytes, one scale/zero pair) into four 16-byte
+                // chunks of fp16.
+                auto expand_group = [&](uint2 cb, __half2 szp, uint4 (&outc)[4]) {
                     const __half2 s2 = __half2half2(__low2half(szp)), z2 = __half2half2(__high2half(szp));
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const unsigned two = ((q4 < 2 ? cb.x : cb.y) >> (16 * (q4 & 1))) & 0xffffu;
-                        // two codes at a time in half2: 1024 + c has the bits 0x6400 | c,
-                        // so subtracting 1024 gives c exactly; then one fused c * s + z
-                        // rounded once to fp16 (the operand type)
-                        __half2 hh[4];
+                    for (int wd = 0; wd < 2; ++wd) {
+                        // 16 codes, element i at bits 2i: elements i and i + 8 sit 16 bits
+                        // apart, so one mask gives the half2 (1024 + c_i, 1024 + c_{i+8})
+                        // (1024 + c has the bits 0x6400 | c); subtracting 1024 gives the
+                        // codes exactly, then one fused c * s + z rounded once to fp16
+                        // (the operand type); byte permutes pair the values up in order.
+                        const unsigned w = wd ? cb.y : cb.x;
+                        uint32_t a[8];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const unsigned pr = (two >> (4 * e)) & 0xFu;
-                            const unsigned wv = 0x64006400u | (pr & 3u) | ((pr & 0xCu) << 14);
-                            const __half2 c2 = __hsub2(*(const __half2 *)&wv, k1024);
-                            hh[e] = __hfma2(c2, s2, z2);
+                        for (int i = 0; i < 8; ++i) {
+                            const unsigned wv = ((w >> (2 * i)) & 0x00030003u) | 0x64006400u;
+                            const __half2 v = __hfma2(__hsub2(*(const __half2 *)&wv, k1024), s2, z2);
+                            a[i] = *(const uint32_t *)&v;
                         }
-                        const __half2 h0 = hh[0], h1 = hh[1], h2 = hh[2], h3 = hh[3];
-                        outc[q4] = make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1, *(const uint32_t *)&h2,
-                                              *(const uint32_t *)&h3);
+                        outc[2 * wd] = make_uint4(__byte_perm(a[0], a[1], 0x5410), __byte_perm(a[2], a[3], 0x5410),
+                                                  __byte_perm(a[4], a[5], 0x5410), __byte_perm(a[6], a[7], 0x5410));
+                        outc[2 * wd + 1] = make_uint4(__byte_perm(a[0], a[1], 0x7632), __byte_perm(a[2], a[3], 0x7632),
+                                                      __byte_perm(a[4], a[5], 0x7632), __byte_perm(a[6], a[7], 0x7632));
                     }
                 };
-                // latent: a lane expands one group of one row; a warp covers two rows per
-                // pass, so its code reads are contiguous.
-                const int half_lane = lane >> 4, grp = lane & 15;
-                for (int rr = 2 * dw + half_lane; rr < kTile; rr += 2 * kDequantWarps) {
+                // latent: a lane expands one group of one row. A warp pass covers half of
+                // a row octet: lane l takes group l % 16 (distinct groups in a half-warp:
+                // conflict-free code reads) of the octet's row (a + 4 (l / 16) + j) % 8,
+                // a = (l / 2) % 4, pass j = 0..3 (each quarter-warp's 16-byte stores then
+                // fall on eight distinct swizzled chunks: conflict-free). All four passes'
+                // codes and scale/zero pairs are read first, so that the shared-memory
+                // latency is paid once; the raw stage is then released.
+                static_assert(kTile / 2 == 4 * kDequantWarps, "four latent passes per dequantising warp");
+                static_assert(kTile * 2 <= kDequantThreads, "one rope-group job per dequantising thread");
+                const int grp = lane & 15, rho0 = ((lane >> 1) & 3) + 4 * (lane >> 4);
+                auto row_of = [&](int k) {
+                    const int u = dw + kDequantWarps * k;
+                    return 8 * (u >> 2) + ((rho0 + (u & 3)) & 7);
+                };
+                uint2 cbv[4];
+                __half2 szv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = row_of(k);
+                    cbv[k] = *(const uint2 *)(codes + rr * RW::kCodesRow + 8 * grp);
+                    szv[k] = *(const __half2 *)(sz + (rr * RW::kGroups + grp) * 2);
+                }
+                // INT2_ROT_QR: the rope key held as codes, groups 16 and 17 of the row
+                const int rr_q = dt >> 1, gr_q = dt & 1;
+                const bool rope_job = RW::kQR && dt < kTile * 2;
+                uint2 cb_q = make_uint2(0, 0);
+                __half2 sz_q = __float2half2_rn(0.f);
+                if (rope_job) {
+                    cb_q = *(const uint2 *)(codes + rr_q * RW::kCodesRow + 8 * (16 + gr_q));
+                    sz_q = *(const __half2 *)(sz + (rr_q * RW::kGroups + 16 + gr_q) * 2);
+                }
+                mbar_arrive(&bars->raw_empty[rs]);    // this thread is done with the raw stage
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = row_of(k);
                     uint4 outc[4];
-                    expand_group(rr, grp, outc);
+                    if (rr < valid) {
+                        expand_group(cbv[k], szv[k], outc);
+                    } else {                           // slots past the sequence end: zeros
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) outc[q4] = make_uint4(0, 0, 0, 0);
+                    }
                     // group grp = latent chunks 4*grp .. 4*grp+3 = column block grp/2, chunks 4*(grp%2)..
                     uint8_t *blk = stage + (grp >> 1) * kKvBlockBytes;
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * (grp & 1) + q4)) = outc[q4];
                 }
-                if (RW::kQR) {
-                    // rope key held as codes: groups 16 and 17 of the row -> the rope block
-                    for (int job = dt; job < kTile * 2; job += kDequantThreads) {
-                        const int rr = job >> 1, gr = job & 1;
-                        uint4 outc[4];
-                        expand_group(rr, 16 + gr, outc);
-                        uint8_t *blk = stage + 8 * kKvBlockBytes;
+                if (rope_job) {                        // -> the rope block
+                    uint4 outc[4];
+                    if (rr_q < valid) {
+                        expand_group(cb_q, sz_q, outc);
+                    } else {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * gr + q4)) = outc[q4];
+                        for (int q4 = 0; q4 < 4; ++q4) outc[q4] = make_uint4(0, 0, 0, 0);
                     }
+                    uint8_t *blk = stage + 8 * kKvBlockBytes;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr_q, 4 * gr_q + q4)) = outc[q4];
                 }
-                mbar_arrive(&bars->raw_empty[rs]);    // this thread is done with the raw stage
+                if (dt == 0) MLA_TRACE_POINT(28, T);
+                if (dt == kDequantThreads - 32) MLA_TRACE_POINT(30, T);
                 if (RW::kRopeTma) {
                     // the rope block landed as bf16: to fp16 in place (exact for values inside
                     // fp16's range), 16-byte chunks; slots past the sequence end become zeros
@@ -514,6 +555,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         break;
                     }
                     rope_pending = -1;
+                    if (dt == 0) MLA_TRACE_POINT(29, T);
                     for (int job = dt; job < kTile * 8; job += kDequantThreads) {
                         const int rr = job >> 3, ch = job & 7;
                         uint4 *at = (uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch));
@@ -548,6 +590,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             auto issue_pv = [&](int Tp, bool first_of_item) -> bool {
                 const int pb = Tp & 1;
                 if (!mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, p.status)) return false;
+                MLA_TRACE_POINT(31, Tp);
                 tc_fence_after();
                 const int s = Tp % kStages;
                 const uint64_t a0 =
@@ -586,6 +629,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                             if (mbar_test(&bars->p_full[pbp], ((T - 1) >> 1) & 1)) { st = 2; break; }
                             if (mbar_test(&bars->full[s], (T / kStages) & 1)) { st = 1; break; }
                             if ((it2 & 63u) == 63u && (aborted(bars) || globaltimer() - tw0 > kTimeoutNs)) break;
+                            __nanosleep(32);         // leave issue slots to the sub-partition's other warps
                         }
                         if (st == 2) {
                             if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
@@ -693,12 +737,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         int nstage = 0;                                 // q_stage phases consumed
         // Swap one value per row with the other half of the row (bounded waits).
         auto exchange = [&](float v, float &other) -> bool {
-            if (nx > 0 && !mbar_wait(&bars->xchg_read, (nx - 1) & 1, bars, p.status)) return false;
+            if (nx > 0 && !mbar_wait(&bars->xchg_read[wq], (nx - 1) & 1, bars, p.status)) return false;
             xchg[hs * 128 + row] = v;
-            mbar_arrive(&bars->xchg_full);
-            if (!mbar_wait(&bars->xchg_full, nx & 1, bars, p.status)) return false;
+            mbar_arrive(&bars->xchg_full[wq]);
+            if (!mbar_wait(&bars->xchg_full[wq], nx & 1, bars, p.status)) return false;
             other = xchg[(hs ^ 1) * 128 + row];
-            mbar_arrive(&bars->xchg_read);
+            mbar_arrive(&bars->xchg_read[wq]);
             ++nx;
             return true;
         };
