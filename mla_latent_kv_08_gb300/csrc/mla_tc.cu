@@ -490,40 +490,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 // a row octet: lane l takes group l % 16 (distinct groups in a half-warp:
                 // conflict-free code reads) of the octet's row (a + 4 (l / 16) + j) % 8,
                 // a = (l / 2) % 4, pass j = 0..3 (each quarter-warp's 16-byte stores then
-                // fall on eight distinct swizzled chunks: conflict-free). All four passes'
-                // codes and scale/zero pairs are read first, so that the shared-memory
-                // latency is paid once; the raw stage is then released.
+                // fall on eight distinct swizzled chunks: conflict-free). Each pass reads
+                // its own codes (reading all four passes' first measured slower).
                 static_assert(kTile / 2 == 4 * kDequantWarps, "four latent passes per dequantising warp");
                 static_assert(kTile * 2 <= kDequantThreads, "one rope-group job per dequantising thread");
                 const int grp = lane & 15, rho0 = ((lane >> 1) & 3) + 4 * (lane >> 4);
-                auto row_of = [&](int k) {
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {
                     const int u = dw + kDequantWarps * k;
-                    return 8 * (u >> 2) + ((rho0 + (u & 3)) & 7);
-                };
-                uint2 cbv[4];
-                __half2 szv[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rr = row_of(k);
-                    cbv[k] = *(const uint2 *)(codes + rr * RW::kCodesRow + 8 * grp);
-                    szv[k] = *(const __half2 *)(sz + (rr * RW::kGroups + grp) * 2);
-                }
-                // INT2_ROT_QR: the rope key held as codes, groups 16 and 17 of the row
-                const int rr_q = dt >> 1, gr_q = dt & 1;
-                const bool rope_job = RW::kQR && dt < kTile * 2;
-                uint2 cb_q = make_uint2(0, 0);
-                __half2 sz_q = __float2half2_rn(0.f);
-                if (rope_job) {
-                    cb_q = *(const uint2 *)(codes + rr_q * RW::kCodesRow + 8 * (16 + gr_q));
-                    sz_q = *(const __half2 *)(sz + (rr_q * RW::kGroups + 16 + gr_q) * 2);
-                }
-                mbar_arrive(&bars->raw_empty[rs]);    // this thread is done with the raw stage
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rr = row_of(k);
+                    const int rr = 8 * (u >> 2) + ((rho0 + (u & 3)) & 7);
+                    const uint2 cb = *(const uint2 *)(codes + rr * RW::kCodesRow + 8 * grp);
+                    const __half2 szp = *(const __half2 *)(sz + (rr * RW::kGroups + grp) * 2);
                     uint4 outc[4];
                     if (rr < valid) {
-                        expand_group(cbv[k], szv[k], outc);
+                        expand_group(cb, szp, outc);
                     } else {                           // slots past the sequence end: zeros
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) outc[q4] = make_uint4(0, 0, 0, 0);
@@ -533,18 +513,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * (grp & 1) + q4)) = outc[q4];
                 }
-                if (rope_job) {                        // -> the rope block
+                if (RW::kQR && dt < kTile * 2) {
+                    // the rope key held as codes: groups 16 and 17 of the row -> the rope block
+                    const int rr = dt >> 1, gr = dt & 1;
+                    const uint2 cb = *(const uint2 *)(codes + rr * RW::kCodesRow + 8 * (16 + gr));
+                    const __half2 szp = *(const __half2 *)(sz + (rr * RW::kGroups + 16 + gr) * 2);
                     uint4 outc[4];
-                    if (rr_q < valid) {
-                        expand_group(cb_q, sz_q, outc);
+                    if (rr < valid) {
+                        expand_group(cb, szp, outc);
                     } else {
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) outc[q4] = make_uint4(0, 0, 0, 0);
                     }
                     uint8_t *blk = stage + 8 * kKvBlockBytes;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr_q, 4 * gr_q + q4)) = outc[q4];
+                    for (int q4 = 0; q4 < 4; ++q4) *(uint4 *)(blk + sw128(rr, 4 * gr + q4)) = outc[q4];
                 }
+                mbar_arrive(&bars->raw_empty[rs]);    // this thread is done with the raw stage
                 if (dt == 0) MLA_TRACE_POINT(28, T);
                 if (dt == kDequantThreads - 32) MLA_TRACE_POINT(30, T);
                 if (RW::kRopeTma) {
