@@ -31,7 +31,13 @@ constexpr uint32_t kOffW = 0;
 constexpr uint32_t kOffO = kWBytes;                  // o_lat: 8 column blocks of [kMaxRows x 128 B]
 constexpr uint32_t kOBlockBytes = kMaxRows * 128;
 constexpr uint32_t kOffBar = kOffO + 8 * kOBlockBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 8 * kMaxRows + 1024;
+constexpr int kWarps = kThreads / 32;
+// rows with many splits, few rows: each warp's partial merge of its share of a row's
+// splits (max, sum, 512 unnormalised dims), merged once more per row
+constexpr uint32_t kOffPart = kOffBar + 64 + 8 * kMaxRows;
+constexpr uint32_t kPartBytes = kWarps * (8 + kR * 4);
+constexpr uint32_t kSmemBytes = kOffPart + kPartBytes + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 struct CombTcParams {
@@ -108,7 +114,91 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
         s_range[tid] = make_int2(c.split_start[b], c.split_start[b + 1]);
     }
     __syncthreads();
-    for (int rr = warp; rr < NR; rr += kThreads / 32) {
+    // Rows of 8 or fewer: each row's splits are dealt to wpr = 16 / rows warps (split
+    // sb + wpr k to warp sub of the row), each merging its share; the row's warp then
+    // merges the wpr partials. More rows: one warp per row merges all of its splits.
+    const int wpr = nrows <= kWarps / 2 ? kWarps / nrows : 1;
+    // one split batch (up to four splits, stride `step`) merged into (M, tot, acc)
+    auto merge_splits = [&](int row, int s_first, int s_end, int step, float &M, float &tot, float (&acc)[16],
+                            bool &nan) {
+        for (int sb = s_first; sb < s_end; sb += 4 * step) {
+            float4 f[4][4];
+            float v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int sp = sb + k * step;
+                v[k] = -CUDART_INF_F;
+                if (sp < s_end) {
+                    const size_t at = ((size_t)sp * rows_seq + row) * kR;
+                    if (c.part_bf16) {      // 4 bf16 per (lane, q): half the bytes of fp32
+                        const uint2 *po = (const uint2 *)((const __nv_bfloat16 *)c.part_o + at);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) f[k][q] = bf16x4_to_float4(po[lane + 32 * q]);
+                    } else {
+                        const float4 *po = (const float4 *)((const float *)c.part_o + at);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) f[k][q] = po[lane + 32 * q];
+                    }
+                    v[k] = c.part_lse[(size_t)sp * rows_seq + row];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) f[k][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            float Mn = M;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                nan |= isnan(v[k]);
+                Mn = fmaxf(Mn, v[k]);
+            }
+            // rescale what was merged so far (nothing, or the earlier splits)
+            const float a = M == -CUDART_INF_F ? 0.f : exp2f(M - Mn);
+            tot *= a;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] *= a;
+            M = Mn;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float wgt = v[k] == -CUDART_INF_F ? 0.f : exp2f(v[k] - M);
+                tot += wgt;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[4 * q + 0] = fmaf(wgt, f[k][q].x, acc[4 * q + 0]);
+                    acc[4 * q + 1] = fmaf(wgt, f[k][q].y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(wgt, f[k][q].z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(wgt, f[k][q].w, acc[4 * q + 3]);
+                }
+            }
+        }
+    };
+    float *part_ms = (float *)(smem + kOffPart);                  // [kWarps][2]: M, tot
+    float *part_acc = (float *)(smem + kOffPart + 8 * kWarps);    // [kWarps][kR]
+    int *part_nan = (int *)(smem + kOffBar + 48);                 // rows whose splits hold a NaN
+    if (wpr > 1) {
+        if (tid == 0) *part_nan = 0;
+        __syncthreads();
+        const int rr = warp / wpr, sub = warp % wpr;
+        float M = -CUDART_INF_F, tot = 0.f, acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+        bool nan = false;
+        if (rr < nrows) {
+            const int2 sr = s_range[rr];
+            const int row = ((row0 + rr) % c.q_len) * H + h;
+            merge_splits(row, sr.x + sub, sr.y, wpr, M, tot, acc, nan);
+        }
+        if (lane == 0) {
+            part_ms[2 * warp] = M;
+            part_ms[2 * warp + 1] = tot;
+            if (nan) atomicOr(part_nan, 1 << rr);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *(float4 *)(part_acc + warp * kR + 4 * (lane + 32 * q)) =
+                make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        __syncthreads();
+    }
+    for (int rr = warp; rr < NR; rr += kWarps) {
         const int grow = row0 + rr;
         float acc[16];
 #pragma unroll
@@ -117,56 +207,27 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
         if (rr < nrows) {
             const int i = grow % c.q_len;
             const int2 sr = s_range[rr];
-            const int s0 = sr.x, s1 = sr.y;
             const int row = i * H + h;
-            bool nan = s1 <= s0;
+            bool nan = sr.y <= sr.x;
             float M = -CUDART_INF_F, tot = 0.f;
-            for (int sb = s0; sb < s1; sb += 4) {
-                float4 f[4][4];
-                float v[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int sp = sb + k;
-                    v[k] = -CUDART_INF_F;
-                    if (sp < s1) {
-                        const size_t at = ((size_t)sp * rows_seq + row) * kR;
-                        if (c.part_bf16) {      // 4 bf16 per (lane, q): half the bytes of fp32
-                            const uint2 *po = (const uint2 *)((const __nv_bfloat16 *)c.part_o + at);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) f[k][q] = bf16x4_to_float4(po[lane + 32 * q]);
-                        } else {
-                            const float4 *po = (const float4 *)((const float *)c.part_o + at);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) f[k][q] = po[lane + 32 * q];
-                        }
-                        v[k] = c.part_lse[(size_t)sp * rows_seq + row];
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) f[k][q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-                float Mn = M;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    nan |= isnan(v[k]);
-                    Mn = fmaxf(Mn, v[k]);
-                }
-                // rescale what was merged so far (nothing, or the earlier splits)
-                const float a = M == -CUDART_INF_F ? 0.f : exp2f(M - Mn);
-                tot *= a;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) acc[k] *= a;
-                M = Mn;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float wgt = v[k] == -CUDART_INF_F ? 0.f : exp2f(v[k] - M);
-                    tot += wgt;
+            if (wpr == 1) {
+                merge_splits(row, sr.x, sr.y, 1, M, tot, acc, nan);
+            } else {
+                // the row's wpr partials, each weighted by 2^(M_j - M)
+                nan |= ((*part_nan >> rr) & 1) != 0;
+                for (int j = 0; j < wpr; ++j) M = fmaxf(M, part_ms[2 * (rr * wpr + j)]);
+                for (int j = 0; j < wpr; ++j) {
+                    const int w = rr * wpr + j;
+                    const float Mj = part_ms[2 * w];
+                    const float wgt = Mj == -CUDART_INF_F ? 0.f : exp2f(Mj - M);
+                    tot = fmaf(wgt, part_ms[2 * w + 1], tot);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        acc[4 * q + 0] = fmaf(wgt, f[k][q].x, acc[4 * q + 0]);
-                        acc[4 * q + 1] = fmaf(wgt, f[k][q].y, acc[4 * q + 1]);
-                        acc[4 * q + 2] = fmaf(wgt, f[k][q].z, acc[4 * q + 2]);
-                        acc[4 * q + 3] = fmaf(wgt, f[k][q].w, acc[4 * q + 3]);
+                        const float4 a = *(const float4 *)(part_acc + w * kR + 4 * (lane + 32 * q));
+                        acc[4 * q + 0] = fmaf(wgt, a.x, acc[4 * q + 0]);
+                        acc[4 * q + 1] = fmaf(wgt, a.y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(wgt, a.z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(wgt, a.w, acc[4 * q + 3]);
                     }
                 }
             }

@@ -166,6 +166,20 @@ def test_split_count_does_not_change_result(gpu_lib):
     _check_seq(res[2][0], res[2][1], w, 0, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+@pytest.mark.parametrize("B", [1, 5, 8, 9])
+def test_combine_shares_splits_across_warps(gpu_lib, B):
+    """Up to 8 rows per combine CTA deal each row's splits to several warps (16 / rows
+    of them) and merge their partials; 9 rows take one warp per row. Every row must
+    match the oracle whichever way its splits were merged."""
+    w = workloads.dsv3(11 + B, B=B, H=16, len_range=(3000, 5000))
+    shape = gu.shape_for(w, splits=48)
+    cache, _ = gu.fill_cache(w, shape)
+    out, lse, _ = gu.attend(w, shape, cache, w.q)
+    for b in range(w.B):
+        ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 def test_verify_causal_window(gpu_lib):
     w = workloads.verify(3, B=4, q_len=8, len_range=(8, 400), H=32)
     w.seq_lens[0] = 8          # first draft row sees exactly one token
