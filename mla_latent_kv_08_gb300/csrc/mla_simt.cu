@@ -69,6 +69,12 @@ extern "C" int mla_plan_trace_read(unsigned long long *host) {
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_work) {
     __shared__ int s_warp[33];
     __shared__ long long s_tiles;
+    // per sequence slot of the current chunk (dynamic shared memory, blockDim slots):
+    // cost position of the first tile, first stream, first item (chunk-local), tiles,
+    // length
+    extern __shared__ long long plan_slots[];
+    long long *s_tb = plan_slots, *s_first = plan_slots + blockDim.x;
+    int *s_loc = (int *)(plan_slots + 2 * blockDim.x), *s_n = s_loc + blockDim.x, *s_len = s_n + blockDim.x;
 #ifdef MLA_TRACE
     if (threadIdx.x == 0) g_plan_time[0] = ptx_globaltimer();
 #endif
@@ -115,30 +121,78 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
         const long long first = tb / T;
         const long long last = n > 0 ? (tb + n - 1) / T : first - 1;
         const int cnt = (int)(last - first + 1);
-        const int start = item_carry + block_exclusive_scan(cnt, s_warp, tot_items);
-        if (b < p.B) {
-            ((int32_t *)p.split_start)[b] = start;
-            for (int k = 0; k < cnt && start + k < max_work; ++k) {
-                const long long s = first + k;
-                const long long lo = (s * T > tb ? s * T : tb) - tb;
-                const long long hi = ((s + 1) * T < tb + n ? (s + 1) * T : tb + n) - tb;
+        const int loc = block_exclusive_scan(cnt, s_warp, tot_items);   // first item, within this chunk
+        if (b < p.B) ((int32_t *)p.split_start)[b] = item_carry + loc;
+        // One item of sequence slot i: the work item (within max_work) and
+        // stream_start[s] = index of the first item whose stream is >= s, for the
+        // item's own stream and, for a sequence's first item, also the streams from
+        // the one after the stream holding the cost position just before the
+        // sequence's start charge.
+        auto write_item = [&](int slot, int k, int idx, long long tbi, long long first_i, int ni, int Li) {
+            const long long sgi = first_i + k;
+            if (idx < max_work) {
+                const long long lo = (sgi * T > tbi ? sgi * T : tbi) - tbi;
+                const long long hi = ((sgi + 1) * T < tbi + ni ? (sgi + 1) * T : tbi + ni) - tbi;
                 WorkItem it;
-                it.b = b;
+                it.b = base + slot;
                 it.t0 = (int)(lo * kPlanTile);
-                it.t1 = (int)min((long long)L, hi * kPlanTile);
-                it.stream = (int)s;
-                ((WorkItem *)p.work)[start + k] = it;
+                it.t1 = (int)min((long long)Li, hi * kPlanTile);
+                it.stream = (int)sgi;
+                ((WorkItem *)p.work)[idx] = it;
             }
-            // stream_start[s] = index of the first item whose stream is >= s. It lies
-            // in this sequence for the streams after the one holding the cost position
-            // just before the sequence, up to the sequence's last stream.
-            if (n > 0) {
-                const long long cb = tb - ic;
-                const long long prev = cb > 0 ? (cb - 1) / T : -1;
-                for (long long s = prev + 1; s <= last && s < P; ++s)
-                    ((int32_t *)p.stream_start)[s] = min(start + (int)(s > first ? s - first : 0), max_work);
+            long long s_lo = sgi;
+            if (k == 0) {
+                const long long cb = tbi - ic;
+                s_lo = cb > 0 ? (cb - 1) / T + 1 : 0;
+            }
+            for (long long st = s_lo; st <= sgi && st < P; ++st) ((int32_t *)p.stream_start)[st] = min(idx, max_work);
+        };
+        // a thread writes its own sequence's items unless some sequence has many (the
+        // per-item path below pays a search and a barrier: measured slower for a
+        // DeepSeek-V3 batch of 32 sequences of up to 6 items, faster for two sequences
+        // of about 38)
+        if (!__syncthreads_or(cnt > 12)) {
+            if (b < p.B) {
+                const int start = item_carry + loc;
+                for (int k = 0; k < cnt && start + k < max_work; ++k) {
+                    const long long sg = first + k;
+                    const long long lo = (sg * T > tb ? sg * T : tb) - tb;
+                    const long long hi = ((sg + 1) * T < tb + n ? (sg + 1) * T : tb + n) - tb;
+                    WorkItem it;
+                    it.b = b;
+                    it.t0 = (int)(lo * kPlanTile);
+                    it.t1 = (int)min((long long)L, hi * kPlanTile);
+                    it.stream = (int)sg;
+                    ((WorkItem *)p.work)[start + k] = it;
+                }
+                if (n > 0) {
+                    const long long cb = tb - ic;
+                    const long long prev = cb > 0 ? (cb - 1) / T : -1;
+                    for (long long st = prev + 1; st <= last && st < P; ++st)
+                        ((int32_t *)p.stream_start)[st] = min(start + (int)(st > first ? st - first : 0), max_work);
+                }
+            }
+        } else {
+            // many (a few long sequences): the chunk's items one per thread; item j
+            // belongs to the last slot whose first item is <= j (slots without items
+            // share the next one's start)
+            s_loc[tid] = loc;
+            s_tb[tid] = tb;
+            s_first[tid] = first;
+            s_n[tid] = n;
+            s_len[tid] = L;
+            __syncthreads();
+            for (int j = tid; j < tot_items; j += blockDim.x) {
+                int lo_i = 0, hi_i = blockDim.x - 1;
+                while (lo_i < hi_i) {
+                    const int mid = (lo_i + hi_i + 1) >> 1;
+                    if (s_loc[mid] <= j) lo_i = mid;
+                    else hi_i = mid - 1;
+                }
+                write_item(lo_i, j - s_loc[lo_i], item_carry + j, s_tb[lo_i], s_first[lo_i], s_n[lo_i], s_len[lo_i]);
             }
         }
+        __syncthreads();                     // the slots are rewritten by the next chunk
         tile_carry += tot_tiles;
         item_carry += tot_items;
     }
@@ -148,8 +202,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
         ((int32_t *)p.num_work)[0] = total;
     }
     // streams past the last sequence's last stream, and the end marker stream_start[P]
-    for (long long s = (NC > 0 ? (NC - 1) / T : -1) + 1 + tid; s <= P; s += blockDim.x)
-        ((int32_t *)p.stream_start)[s] = total;
+    for (long long st = (NC > 0 ? (NC - 1) / T : -1) + 1 + tid; st <= P; st += blockDim.x)
+        ((int32_t *)p.stream_start)[st] = total;
 #ifdef MLA_TRACE
     __syncthreads();
     if (tid == 0) g_plan_time[2] = ptx_globaltimer();
@@ -159,7 +213,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
     // one thread per sequence (whole warps, at most 1024): fewer threads, cheaper barriers
     const int threads = p.B >= 1024 ? 1024 : ((p.B + 31) / 32) * 32;
-    return launch_pdl(plan_kernel, dim3(1), dim3(threads > 0 ? threads : 32), 0, st, p, max_work);
+    const int nt = threads > 0 ? threads : 32;
+    return launch_pdl(plan_kernel, dim3(1), dim3(nt), (size_t)nt * 28, st, p, max_work);
 }
 
 // ============================================================================
