@@ -10,8 +10,9 @@
 // N), and reading every tile in both CTAs doubles the L2 -> SM traffic. Here the tiles
 // of a stream alternate: tile T is "owned" by CTA T % 2, which alone loads all of the
 // tile and computes S, the softmax and P; the other CTA loads only its 256 V dims of
-// the tile and receives P (bf16 [128 x 64], 16 KB) by a bulk shared-memory copy into
-// its own shared memory. Both then accumulate O += P . V for their own dims.
+// the tile and receives P (bf16 [128 x 64], 16 KB) in its own shared memory, written
+// by the softmax threads with 16-byte st.async stores that complete transaction bytes
+// on the receiver's barrier. Both then accumulate O += P . V for their own dims.
 //
 // The softmax base. Both CTAs accumulate into outputs that must share one running
 // maximum per row. The owner of tile T derives it from the base after tile T-1 (held
@@ -29,8 +30,8 @@
 //   MMA     S[128 x 64] = Q[128 x 576] . K[64 x 576]^T  (24 K-steps with Q in tensor
 //           memory, 12 with Q in shared memory)
 //   softmax S -> registers, causal/length mask, row max (two warps per row), base,
-//           P = 2^(s*scale*log2e - base) rounded to bf16 into the CTA's P buffer,
-//           bulk copy of P to the other CTA
+//           P = 2^(s*scale*log2e - base) rounded to bf16 into the CTA's P buffer
+//           and (st.async) into the other CTA's
 //   MMA     O[128 x 256] += P[128 x 64] . V[64 x 256]  (8 M128 N128 K16 MMAs)
 // and per tile it does not own: TMA of its 4 V boxes, the base message (rescale),
 // then the same PV from the received P.
