@@ -50,7 +50,14 @@ namespace tc {
 
 // Threads per CTA: warps 0..3 control (producer, MMA, two dequantisers), 4..11
 // softmax; the INT2 kind adds dequantising warps 12..17.
-template <int KIND> constexpr int threads_of() { return is_int2(KIND) ? 576 : 384; }
+// PV MMAs from a warp of their own (the score MMAs' issuer then never holds them back)
+#ifndef MLA_SPLIT_PV
+#define MLA_SPLIT_PV 1
+#endif
+constexpr bool kSplitPv = MLA_SPLIT_PV != 0;
+template <int KIND> constexpr int threads_of() { return is_int2(KIND) ? (kSplitPv ? 608 : 576) : 384; }
+// the PV issuer: warp 2 (idle in the bf16 kind), warp 18 for the INT2 kinds
+template <int KIND> __host__ __device__ constexpr int pv_warp() { return is_int2(KIND) ? 18 : 2; }
 constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
@@ -179,6 +186,7 @@ struct Bars {
     uint64_t q_tmem;          // the tensor-memory part of Q is stored
     uint64_t qreg_free;       // every softmax thread is done with the Q region
     uint64_t mma_fin;
+    uint64_t pv_fin;          // the PV issuer's MMAs are complete
     uint64_t xchg_full[4];    // lane quarter q: both halves of its rows wrote their value
     uint64_t xchg_read[4];    // lane quarter q: both halves read the other's value
     uint64_t tail_done[kStages];  // bf16: the producer zeroed a partial tile's slots past the end
@@ -224,12 +232,41 @@ __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
 #endif
 constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2 ahead of the TMA loads
 
+// PV(Tp): O[128 x 256] += P(Tp) . V(Tp) from tile Tp's stage (4 x M128 N256 K16; P in
+// the two column blocks of the other half's V dims), once the softmax has stored P;
+// then commits pv_done and the stage's empty barrier. Issued by one thread.
+template <int KIND>
+__device__ __forceinline__ bool issue_pv(Bars *bars, uint8_t *smem, int half, const TcParams &tp, uint32_t d_o, int Tp,
+                                         bool first_of_item, int32_t *status) {
+    constexpr bool kInt2 = is_int2(KIND);
+    const int pb = Tp & 1;
+    if (!mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, status)) return false;
+    MLA_TRACE_POINT(31, Tp);
+    tc_fence_after();
+    const int s = Tp % kStages;
+    const uint64_t a0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes + p_block(half) * kKvBlockBytes), 16, 1024);
+    const uint64_t b0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes, tp.v_lbo, tp.v_sbo);
+    // INT2 cache: the operands are fp16 (the dequantised latent, P); bf16 otherwise
+    constexpr uint32_t kIdPv = kInt2 ? idesc_f16(128, 256, true) : idesc_bf16(128, 256, true);
+    // descriptor start addresses advance in 16-byte units
+    if (first_of_item) mma_ss_k<kIdPv, 0>(d_o, a0, b0);
+    else mma_ss_k<kIdPv, 1>(d_o, a0, b0);
+    mma_ss_k<kIdPv, 1>(d_o, a0 + 2, b0 + 128);
+    mma_ss_k<kIdPv, 1>(d_o, a0 + 4, b0 + 256);
+    mma_ss_k<kIdPv, 1>(d_o, a0 + 6, b0 + 384);
+    mma_commit(&bars->pv_done[pb]);
+    mma_commit(&bars->empty[s]);
+    MLA_TRACE_POINT(5, Tp);
+    return true;
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                  const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap rope_map,
                  const TcParams tp) {
     constexpr bool kInt2 = is_int2(KIND);
+    constexpr int kPvWarp = pv_warp<KIND>();
     using RW = Raw<KIND>;
     constexpr int kSBufs = Layout<KIND>::kSBufs;
     constexpr int kQTmemBlocks = Layout<KIND>::kQTmemBlocks;
@@ -280,6 +317,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         mbar_init(&bars->q_tmem, kSoftmaxThreads);
         mbar_init(&bars->qreg_free, kSoftmaxThreads);
         mbar_init(&bars->mma_fin, 1);
+        mbar_init(&bars->pv_fin, 1);
         for (int q = 0; q < 4; ++q) {          // the two softmax warps of a lane quarter
             mbar_init(&bars->xchg_full[q], 64);
             mbar_init(&bars->xchg_read[q], 64);
@@ -419,7 +457,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 if (u >= 0) mbar_drain(&bars->full[u % kStages], (u / kStages) & 1);
         }
         __syncwarp();
-    } else if (kInt2 && (warp == 2 || warp == 3 || warp >= 12)) {
+    } else if (kInt2 && (warp == 2 || warp == 3 || (warp >= 12 && warp < 12 + kDequantWarps - 2))) {
         // ================================================= INT2 expansion into the stage
         // value = code * scale + zero, rounded once to fp16 (the MMA operand type of
         // this cache kind), written in the 128B-swizzled layout the MMAs
@@ -564,36 +602,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         }
         // an aborted pass never leaves its rope copy in flight
         if (rope_pending >= 0) mbar_drain(&bars->rope_full[rope_pending % kStages], (rope_pending / kStages) & 1);
+    } else if (kSplitPv && warp == kPvWarp) {
+        // ================================================= PV issuer: lane 0 issues
+        // O += P(T) . V(T) for every tile in order as soon as the softmax has stored
+        // P(T), so that the stage is released without waiting for the score MMAs of
+        // the next tile to be issued; it commits its own MMAs (pv_done, empty).
+        if (lane == 0) {
+            const uint32_t d_o = tmem + kColO;
+            bool ok = true;
+            int T = 0;
+            for (int i = i0; i < i1 && ok; ++i) {
+                const WorkItem it = p.work[i];
+                const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+                for (int t = 0; t < nt; ++t, ++T) {
+                    if (!issue_pv<KIND>(bars, smem, half, tp, d_o, T, t == 0, p.status)) { ok = false; break; }
+                }
+            }
+            mma_commit(&bars->pv_fin);
+            mbar_wait(&bars->pv_fin, 0, bars, p.status);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ================================================= MMA issuer: lane 0 alone runs
-        // the loop (plain bounded waits, no warp-wide votes or syncs per tile)
+        // the loop (plain bounded waits, no warp-wide votes or syncs per tile); with a
+        // PV issuer warp, the score MMAs alone
         if (lane == 0) {
             const uint32_t d_o = tmem + kColO;
             bool ok = true;
             int T = 0;
             uint32_t tail_par = 0;                 // bit s: parity of the partial tiles seen in stage s
-            auto issue_pv = [&](int Tp, bool first_of_item) -> bool {
-                const int pb = Tp & 1;
-                if (!mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, p.status)) return false;
-                MLA_TRACE_POINT(31, Tp);
-                tc_fence_after();
-                const int s = Tp % kStages;
-                const uint64_t a0 =
-                    sdesc(smem_u32(smem + kOffStage + s * kStageBytes + p_block(half) * kKvBlockBytes), 16, 1024);
-                const uint64_t b0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes,
-                                          tp.v_lbo, tp.v_sbo);
-                // INT2 cache: the operands are fp16 (the dequantised latent, P); bf16 otherwise
-                constexpr uint32_t kIdPv = kInt2 ? idesc_f16(128, 256, true) : idesc_bf16(128, 256, true);
-                // descriptor start addresses advance in 16-byte units
-                if (first_of_item) mma_ss_k<kIdPv, 0>(d_o, a0, b0);
-                else mma_ss_k<kIdPv, 1>(d_o, a0, b0);
-                mma_ss_k<kIdPv, 1>(d_o, a0 + 2, b0 + 128);
-                mma_ss_k<kIdPv, 1>(d_o, a0 + 4, b0 + 256);
-                mma_ss_k<kIdPv, 1>(d_o, a0 + 6, b0 + 384);
-                mma_commit(&bars->pv_done[pb]);
-                mma_commit(&bars->empty[s]);
-                MLA_TRACE_POINT(5, Tp);
-                return true;
+            auto issue_pv_here = [&](int Tp, bool first_of_item) -> bool {
+                return issue_pv<KIND>(bars, smem, half, tp, d_o, Tp, first_of_item, p.status);
             };
             int item_no = 0;
             for (int i = i0; i < i1 && ok; ++i, ++item_no) {
@@ -606,7 +645,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     // Wait for this tile's stage; meanwhile issue the previous tile's PV as
                     // soon as its P is ready, so that its stage is released early.
                     bool pv_early = false;
-                    if (t > 0) {
+                    if (!kSplitPv && t > 0) {
                         const int pbp = (T - 1) & 1;
                         int st = 0;                  // 1 = stage landed, 2 = P ready
                         const unsigned long long tw0 = globaltimer();
@@ -617,7 +656,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                             __nanosleep(32);         // leave issue slots to the sub-partition's other warps
                         }
                         if (st == 2) {
-                            if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
+                            if (!issue_pv_here(T - 1, t == 1)) { ok = false; break; }
                             pv_early = true;
                         }
                     }
@@ -638,7 +677,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     // QK(T) in kQkGroups issue groups. PV(T-1) of the same item is
                     // slipped in between groups as soon as its P is ready, so that the
                     // stage it reads is released early; otherwise it follows QK(T).
-                    bool pv_pending = t > 0 && !pv_early;
+                    bool pv_pending = !kSplitPv && t > 0 && !pv_early;
                     const int pb_prev = (T - 1) & 1;
                     MLA_TRACE_POINT(20, T);
                     tc_fence_after();
@@ -678,16 +717,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         MLA_TRACE_POINT(10 + grp, T);
                         if (MLA_PV_SLIP && pv_pending && grp < kQkGroups - 1 &&
                             mbar_test(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1)) {
-                            if (!issue_pv(T - 1, t == 1)) { ok = false; break; }
+                            if (!issue_pv_here(T - 1, t == 1)) { ok = false; break; }
                             pv_pending = false;
                         }
                     }
                     if (!ok) break;
                     mma_commit(&bars->s_full[T % kSBufs]);
                     MLA_TRACE_POINT(2, T);
-                    if (pv_pending && !issue_pv(T - 1, t == 1)) { ok = false; break; }
+                    if (pv_pending && !issue_pv_here(T - 1, t == 1)) { ok = false; break; }
                 }
-                if (ok && nt > 0 && !issue_pv(T - 1, nt == 1)) ok = false;
+                if (!kSplitPv && ok && nt > 0 && !issue_pv_here(T - 1, nt == 1)) ok = false;
             }
             mma_commit(&bars->mma_fin);
             mbar_wait(&bars->mma_fin, 0, bars, p.status);
