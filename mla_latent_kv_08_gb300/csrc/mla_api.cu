@@ -187,6 +187,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.scale_zero = (const __half *)cache->scale_zero;
     p.rope = (const __nv_bfloat16 *)cache->rope;
     p.q = q;
+    p.q_rope = q;
     p.q_prep = int2 ? (const float *)(ws + w.q_prep) : nullptr;
     p.scale_log2 = scale * kLog2e;
     p.status = (int32_t *)(ws + w.status);

@@ -82,6 +82,8 @@ struct DecodeParams {
     const __half *scale_zero;    // INT2
     const __nv_bfloat16 *rope;   // INT2
     const void *q;               // caller's absorbed query
+    const void *q_rope;          // the caller's bf16 query, whose rope dims the tensor-core
+                                 // INT2_ROT decode reads as they are (the query itself)
     const float *q_prep;         // INT2: rotated query (fp32), else nullptr
     float scale_log2;            // scale * log2(e)
     int32_t *status;             // -> flags word

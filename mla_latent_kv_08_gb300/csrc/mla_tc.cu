@@ -13,8 +13,8 @@
 //
 // Per CTA, per 64-token tile (one cache block):
 //   TMA     9 loads of [64 tokens x 64 dims], 128B-swizzled, into a stage (INT2:
-//           a bulk copy of the block's codes, scale/zero pairs and rope keys,
-//           expanded into the stage by eight dequantising warps)
+//           a bulk copy of the block's codes and scale/zero pairs, expanded into
+//           the stage by eight dequantising warps; INT2_ROT's bf16 rope key by TMA)
 //   MMA     S[128 x 64]  = Q[128 x 576] . K[64 x 576]^T   (36 x M128 N64 K16, in
 //           two issue groups; the first K-steps read Q from tensor memory)
 //   softmax two warps per 32-row lane quarter, one per half of the tile's
@@ -87,7 +87,7 @@ constexpr uint32_t kOffQ = kOffStage + kStages * kStageBytes;       // 144 KB
 // INT2 raw stages (two): one block's codes and scale/zero pairs, copied verbatim and
 // expanded into an operand stage by the dequantising warps. The bf16 rope key of
 // INT2_ROT is not staged here: it is loaded by TMA straight into the operand stage's
-// rope block (bf16 and fp16 share the 16-bit swizzled layout) and converted in place.
+// rope block and stays bf16 (its score K-steps take the caller's bf16 query rope dims).
 // Bytes per token: codes, scale/zero pairs; INT2_ROT_QR holds the rope key as two
 // more groups of codes.
 template <int KIND> struct Raw {
@@ -264,7 +264,7 @@ template <int KIND>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                  const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap rope_map,
-                 const TcParams tp) {
+                 const __grid_constant__ CUtensorMap qr_map, const TcParams tp) {
     constexpr bool kInt2 = is_int2(KIND);
     constexpr int kPvWarp = pv_warp<KIND>();
     using RW = Raw<KIND>;
@@ -461,8 +461,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         // ================================================= INT2 expansion into the stage
         // value = code * scale + zero, rounded once to fp16 (the MMA operand type of
         // this cache kind), written in the 128B-swizzled layout the MMAs
-        // read; the bf16 rope key is converted to fp16; slots past the sequence end
-        // are zeroed.
+        // read; the bf16 rope key (INT2_ROT) lands by TMA and stays bf16; slots past
+        // the sequence end are zeroed.
         const int dw = warp < 4 ? warp - 2 : warp - 10;   // dequantising warp 0..7
         const __half2 k1024 = __float2half2_rn(1024.f);
         const int dt = 32 * dw + lane;
@@ -571,29 +571,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 if (dt == 0) MLA_TRACE_POINT(28, T);
                 if (dt == kDequantThreads - 32) MLA_TRACE_POINT(30, T);
                 if (RW::kRopeTma) {
-                    // the rope block landed as bf16: to fp16 in place (exact for values inside
-                    // fp16's range), 16-byte chunks; slots past the sequence end become zeros
+                    // the rope block landed as bf16, the MMA operand type of its score
+                    // K-steps: only a sequence's final partial block has slots past the
+                    // end to zero (stale, possibly non-finite, cache bytes)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bars->rope_full[s], (T / kStages) & 1, bars, p.status))) {
                         ok = false;
                         break;
                     }
                     rope_pending = -1;
                     if (dt == 0) MLA_TRACE_POINT(29, T);
-                    for (int job = dt; job < kTile * 8; job += kDequantThreads) {
-                        const int rr = job >> 3, ch = job & 7;
-                        uint4 *at = (uint4 *)(stage + 8 * kKvBlockBytes + sw128(rr, ch));
-                        uint4 out = make_uint4(0, 0, 0, 0);
-                        if (rr < valid) {
-                            const uint4 u = *at;
-                            const __nv_bfloat162 *bh = (const __nv_bfloat162 *)&u;
-                            __half2 hh[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) hh[e] = __float22half2_rn(__bfloat1622float2(bh[e]));
-                            out = make_uint4(*(const uint32_t *)&hh[0], *(const uint32_t *)&hh[1], *(const uint32_t *)&hh[2],
-                                             *(const uint32_t *)&hh[3]);
-                        }
-                        *at = out;
-                    }
+                    for (int job = dt; job < (kTile - valid) * 8; job += kDequantThreads)
+                        *(uint4 *)(stage + 8 * kKvBlockBytes + sw128(valid + (job >> 3), job & 7)) = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async();
                 mbar_arrive(&bars->full[s]);
@@ -709,6 +697,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                                 MLA_TRACE_POINT(19, T);
                             } else if (j < 4 * kQTmemBlocks) {
                                 mma_ts_k<kIdQk, 1>(d_s, qt + 8 * j, bd);
+                            } else if (RW::kRopeTma && j >= 4 * (kKvBlocks - 1)) {
+                                // INT2_ROT: the rope block is bf16 on both sides (the key as
+                                // cached, the caller's query); the same fp32 accumulator
+                                constexpr uint32_t kIdRope = idesc_bf16(128, 64, false);
+                                mma_ss_k<kIdRope, 1>(
+                                    d_s, qd + (uint64_t)((((j >> 2) - kQTmemBlocks) * kQBlockBytes + 32 * (j & 3)) >> 4), bd);
                             } else {
                                 mma_ss_k<kIdQk, 1>(
                                     d_s, qd + (uint64_t)((((j >> 2) - kQTmemBlocks) * kQBlockBytes + 32 * (j & 3)) >> 4), bd);
@@ -789,7 +783,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 bar = &bars->q_smem;
             }
             mbar_expect_tx(bar, (uint32_t)n * kQBlockBytes);
-            for (int k = 0; k < n; ++k) tma_load_2d(smem + kOffQ + k * kQBlockBytes, &q_map, 64 * (first + k), qrow, bar);
+            for (int k = 0; k < n; ++k) {
+                // INT2_ROT: the rope block (8) straight from the caller's bf16 query
+                const bool rope_bf16 = RW::kRopeTma && first + k == kKvBlocks - 1;
+                tma_load_2d(smem + kOffQ + k * kQBlockBytes, rope_bf16 ? &qr_map : &q_map, 64 * (first + k), qrow, bar);
+            }
             return true;
         };
         // Staged round -> tensor memory: each thread moves its row's 64-dim
@@ -1113,6 +1111,12 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile,
                                CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)p.s.E()))
         return cudaErrorInvalidValue;
+    // INT2_ROT: the caller's bf16 query, read for its rope block only
+    CUtensorMap qr_map;
+    memset(&qr_map, 0, sizeof qr_map);
+    if (p.s.kind == MLA_KV_INT2_ROT &&
+        !tc::make_map(&qr_map, p.q_rope, (uint64_t)p.B * p.q_len * p.s.H, tc::kRows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return cudaErrorInvalidValue;
     // INT2_ROT: the bf16 rope keys [num_blocks * block_size, d_R], one 64-row box a tile
     if (p.s.kind == MLA_KV_INT2_ROT &&
         !tc::make_map(&rope_map, p.rope, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -1131,7 +1135,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);
     const int threads = int2 ? tc::threads_of<MLA_KV_INT2_ROT>() : tc::threads_of<MLA_KV_BF16>();
-    return launch_pdl(kern, grid, dim3(threads), tc::kSmemBytes, st, kv_map, q_map, o_map, rope_map, tp);
+    return launch_pdl(kern, grid, dim3(threads), tc::kSmemBytes, st, kv_map, q_map, o_map, rope_map, qr_map, tp);
 }
 
 }  // namespace mla
