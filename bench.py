@@ -661,14 +661,14 @@ def measure_configs(mla, dev, peaks, flush, only=(), reps=0):
             tot += e0.elapsed_time(e1)
         return tot / n
 
-    def run(key, desc, w, kind, q_len, R=None, T=None, n=20, fold=False, append=False):
+    def run(key, desc, w, kind, q_len, R=None, T=None, n=20, fold=False, append=False, q_rotated=False):
         if only and key not in only:
             return
         if reps:
             n = reps
         shape = mla.Shape(num_heads=w.H, kv_lora_rank=w.r, rope_dim=w.d_rope, v_head_dim=w.d_v,
                           block_size=w.block_size, num_blocks=w.num_blocks, kind=kind,
-                          flags=mla.MLA_FLAG_WUV_FOLDED if fold else 0)
+                          flags=(mla.MLA_FLAG_WUV_FOLDED if fold else 0) | (mla.MLA_FLAG_Q_ROTATED if q_rotated else 0))
         cache = mla.Cache.allocate(shape, dev)
         cu = t(np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32))
         Rd = None if R is None else t(R.astype(np.float32))
@@ -694,11 +694,19 @@ def measure_configs(mla, dev, peaks, flush, only=(), reps=0):
             Wf = torch.empty_like(W)
             mla.mla_fold_rotation(shape, Rd, W, Wf)
             W = Wf
+        Rcall = Rd
+        if q_rotated:
+            # the caller's query projection carries R (folded once, like W_UV): its
+            # latent dims arrive as bf16(q_lat . R), and R is not passed at all
+            qf = t(w.q)
+            qf[..., :w.r] = qf[..., :w.r] @ Rd
+            q = qf.to(bf)
+            Rcall = None
         out = torch.empty((w.B, q_len, w.H, w.d_v), dtype=bf, device=dev)
         lse = torch.empty((w.B, q_len, w.H), dtype=torch.float32, device=dev)
         ws = mla.alloc_workspace(shape, w.B, q_len, dev)
         call = mla.mla_decode if q_len == 1 else mla.mla_verify
-        go = lambda: call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rd)   # noqa: E731
+        go = lambda: call(cache, bt, sl, q, W, w.scale, out, lse, ws, R=Rcall)   # noqa: E731
         for _ in range(3):
             go()
         torch.cuda.synchronize(dev)
@@ -742,7 +750,7 @@ def measure_configs(mla, dev, peaks, flush, only=(), reps=0):
     if want("C5"):
         w = workloads.verify(5, B=1, q_len=512, len_range=(8192, 8192))
         run("C5", "chunked prefill: one 512-token chunk at L=8192, H=128, bf16", w, mla.MLA_KV_BF16, 512, n=3)
-    if not want("C4", "C6", "C7"):
+    if not want("C4", "C4q", "C6", "C7"):
         return res
     # rotated INT2: the workload's 65536 calibration latents through the library's own calibration
     w = workloads.int2_rotated(4)
@@ -750,6 +758,8 @@ def measure_configs(mla, dev, peaks, flush, only=(), reps=0):
     R32, clip, _, _ = mla.calibrate_rotation(X)
     run("C4", "rotated INT2 (DeepSeek-V3 shapes, 320 B/token), calibrated by the library, W_UV folded",
         w, mla.MLA_KV_INT2_ROT, 1, R=R32, T=clip, fold=True, append=True)
+    run("C4q", "rotated INT2 as C4, R folded into both W_UV and the query's projection (query given rotated)",
+        w, mla.MLA_KV_INT2_ROT, 1, R=R32, T=clip, fold=True, q_rotated=True)
     # the two rope/nope variants: the rope key's thresholds from calibration rope keys
     # of the cache's rope law (N(0,1) rounded to bf16)
     rng = np.random.Generator(np.random.PCG64(11))

@@ -109,12 +109,17 @@ typedef struct {
 } mla_shape;
 
 typedef enum {
-    /* INT2 kinds only: the W_UV given to mla_decode / mla_verify is already the
-     * folded W'_UV[h] = R^T . W_UV[h] of mla_fold_rotation, so the latent-space
+    /* INT2_ROT / INT2_ROT_QR: the W_UV given to mla_decode / mla_verify is already
+     * the folded W'_UV[h] = R^T . W_UV[h] of mla_fold_rotation, so the latent-space
      * output stays in the rotated basis and no o . R^T product is formed per call
-     * (out = o_rot . R^T . W_UV[h] = o_rot . W'_UV[h]). R is still required: the
-     * query is rotated by it on every call. */
-    MLA_FLAG_WUV_FOLDED = 1
+     * (out = o_rot . R^T . W_UV[h] = o_rot . W'_UV[h]). */
+    MLA_FLAG_WUV_FOLDED = 1,
+    /* INT2_ROT / INT2_ROT_QR: the query's first r dims are already in the rotated
+     * basis (q_lat . R, e.g. with R folded into the query's absorbed projection
+     * once, as W_UV is folded by mla_fold_rotation), so the library does not rotate
+     * the query; the rope dims are as always. With both flags set R is not read and
+     * may be NULL. */
+    MLA_FLAG_Q_ROTATED = 2
 } mla_flag;
 
 /* The paged cache. Block p, slot j is token row p*block_size + j.
@@ -178,7 +183,8 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache,
  *   W_UV       [H, r, d_v] bf16 (FP32 kind: fp32).
  *   R          INT2 kinds: [r, r] fp32 (as in append; INT2_JOINT: [r + d_R,
  *              r + d_R], the query is rotated over all its dims and the output
- *              is (o_j . R_j^T)[0:r] before W_UV); else NULL.
+ *              is (o_j . R_j^T)[0:r] before W_UV); else NULL. May be NULL with
+ *              MLA_FLAG_WUV_FOLDED | MLA_FLAG_Q_ROTATED (not read).
  *   scale      softmax scale applied to q . k.
  *   out        [B, 1, H, d_v] bf16 (FP32 kind: fp32).
  *   lse        [B, 1, H] fp32, natural log of the softmax denominator.

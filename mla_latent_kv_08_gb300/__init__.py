@@ -36,6 +36,7 @@ MLA_IMPL_AUTO = 0
 MLA_IMPL_SIMT = 1
 MLA_IMPL_TCGEN05 = 2
 MLA_FLAG_WUV_FOLDED = 1
+MLA_FLAG_Q_ROTATED = 2
 MLA_DTYPE_F64, MLA_DTYPE_F32, MLA_DTYPE_BF16 = 0, 1, 2
 
 # Every symbol include/mla.h declares.

@@ -59,9 +59,9 @@ static mla_status check_shape(const mla_shape *s) {
         return MLA_ERR_INVALID;
     if (s->index_dim < 0 || s->index_dim % 8 || s->index_dim > 1024) return MLA_ERR_INVALID;
     if (is_int2(s->kind) && s->index_dim != 0) return MLA_ERR_INVALID;
-    if (s->flags & ~(int32_t)MLA_FLAG_WUV_FOLDED) return MLA_ERR_INVALID;
+    if (s->flags & ~(int32_t)(MLA_FLAG_WUV_FOLDED | MLA_FLAG_Q_ROTATED)) return MLA_ERR_INVALID;
     // the joint kind's folded up-projection would be [H, r + d_R, d_v]: not offered
-    if ((s->flags & MLA_FLAG_WUV_FOLDED) && (!is_int2(s->kind) || s->kind == MLA_KV_INT2_JOINT))
+    if ((s->flags & (MLA_FLAG_WUV_FOLDED | MLA_FLAG_Q_ROTATED)) && (!is_int2(s->kind) || s->kind == MLA_KV_INT2_JOINT))
         return MLA_ERR_INVALID;
     if (is_int2(s->kind)) {
         if (s->group_size < 4 || s->group_size > 128 || s->group_size % 4 || s->kv_lora_rank % s->group_size)
@@ -160,7 +160,11 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     const bool int2 = is_int2(s->kind);
     const bool rope_bf16 = s->kind == MLA_KV_INT2_ROT;      // INT2_ROT_QR holds the rope key as codes
     if (int2) {
-        if (!cache->codes || !cache->scale_zero || (rope_bf16 && !cache->rope) || !R) return MLA_ERR_INVALID;
+        // R is read for the query (unless it comes rotated) and for the output (unless
+        // W_UV comes folded)
+        const bool r_unused = (s->flags & MLA_FLAG_WUV_FOLDED) && (s->flags & MLA_FLAG_Q_ROTATED);
+        if (!cache->codes || !cache->scale_zero || (rope_bf16 && !cache->rope) || (!R && !r_unused))
+            return MLA_ERR_INVALID;
         if (!aligned16(cache->codes) || !aligned16(cache->scale_zero) || (rope_bf16 && !aligned16(cache->rope)))
             return MLA_ERR_INVALID;
     } else {
@@ -206,7 +210,14 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         // the rotated query: fp32 for the CUDA-core kernel; fp16 (the MMA operand type
         // of this cache kind) from the tensor-core GEMM for the tensor-core kernel,
         // which then reads it in place of q
-        if (tc) {
+        if (s->flags & MLA_FLAG_Q_ROTATED) {
+            // already rotated: only widened to the operand type (fp16 for the tensor
+            // cores, fp32 for the CUDA-core kernel)
+            if (launch_convert_query(q, ws + w.q_prep, (size_t)B * q_len * s->num_heads * p.s.D(), tc, stream_) !=
+                cudaSuccess)
+                return MLA_ERR_CUDA;
+            if (tc) p.q = ws + w.q_prep;
+        } else if (tc) {
             if (launch_rot_query(R, (__nv_bfloat16 *)(ws + w.rsplit), q, ws + w.q_prep, B * q_len * s->num_heads,
                                  s->kv_lora_rank + s->rope_dim, p.status, stream_) != cudaSuccess)
                 return MLA_ERR_CUDA;
@@ -432,6 +443,6 @@ mla_status mla_fold_rotation(const mla_shape *shape, const float *R, const void 
     return MLA_OK;
 }
 
-int32_t mla_version(void) { return 102; }
+int32_t mla_version(void) { return 103; }
 
 }  // extern "C"

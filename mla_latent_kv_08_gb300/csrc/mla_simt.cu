@@ -10,6 +10,8 @@
 
 #include <math_constants.h>
 
+#include <algorithm>
+
 namespace mla {
 
 // ============================================================================
@@ -293,6 +295,41 @@ static cudaError_t launch_qprep_t(const DecodeParams &p, const float *R, void *q
         qprep_kernel<4, OUT><<<grid, 256, smem, st>>>(p, R, q_prep, rows);
     }
     return cudaGetLastError();
+}
+
+// A query that comes in the rotated basis: bf16 -> the decode kernels' operand type,
+// 8 elements (16 bytes in) per thread step.
+template <int OUT>
+__global__ void __launch_bounds__(256) convert_query_kernel(const __nv_bfloat16 *q, void *out, size_t n8) {
+    pdl_trigger();
+    pdl_wait();
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const uint4 u = ((const uint4 *)q)[i];
+        const __nv_bfloat162 *h = (const __nv_bfloat162 *)&u;
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(h[e]);
+            f[2 * e] = x.x;
+            f[2 * e + 1] = x.y;
+        }
+        if (OUT == 1) {
+            __half2 o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
+            ((uint4 *)out)[i] = *(const uint4 *)o;
+        } else {
+            ((float4 *)out)[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+            ((float4 *)out)[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+}
+
+cudaError_t launch_convert_query(const void *q, void *out, size_t n, bool out_f16, cudaStream_t st) {
+    const size_t n8 = n / 8;                      // n = rows * (r + d_R), a multiple of 8
+    const int blocks = (int)std::min<size_t>((n8 + 255) / 256, 2048);
+    return out_f16 ? launch_pdl(convert_query_kernel<1>, dim3(blocks), dim3(256), 0, st, (const __nv_bfloat16 *)q, out, n8)
+                   : launch_pdl(convert_query_kernel<0>, dim3(blocks), dim3(256), 0, st, (const __nv_bfloat16 *)q, out, n8);
 }
 
 cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bool out_f16, cudaStream_t st) {

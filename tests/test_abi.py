@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     import mla_latent_kv_08_gb300 as mla
-    assert mla.mla_version() == 102
+    assert mla.mla_version() == 103
     for code in range(-6, 1):
         assert mla.status_string(code) != "unknown status"
     assert mla.status_string(-99) == "unknown status"
@@ -57,15 +57,21 @@ def test_shape_validation(lib):
     assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, group_size=6)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kv_lora_rank=2048)) == mla.MLA_ERR_UNSUPPORTED
     assert mla.mla_resolve_impl(_shape(), q_len=0) == mla.MLA_ERR_INVALID
-    # flags: only MLA_FLAG_WUV_FOLDED exists, and it belongs to the INT2 kinds
-    assert mla.mla_resolve_impl(_shape(flags=2)) == mla.MLA_ERR_INVALID
+    # flags: MLA_FLAG_WUV_FOLDED and MLA_FLAG_Q_ROTATED, for the rotated INT2 kinds only
+    both = mla.MLA_FLAG_WUV_FOLDED | mla.MLA_FLAG_Q_ROTATED
+    assert mla.mla_resolve_impl(_shape(flags=4)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, flags=4)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(flags=mla.MLA_FLAG_WUV_FOLDED)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(flags=mla.MLA_FLAG_Q_ROTATED)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, flags=mla.MLA_FLAG_WUV_FOLDED)) >= 0
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT, flags=mla.MLA_FLAG_Q_ROTATED)) >= 0
+    assert mla.mla_resolve_impl(_shape(kind=mla.MLA_KV_INT2_ROT_QR, flags=both)) >= 0
     # the joint rope/nope kind: generic kernel only, no folded up-projection, whole row in groups
     joint = mla.MLA_KV_INT2_JOINT
     assert mla.mla_resolve_impl(_shape(kind=joint)) == mla.MLA_IMPL_SIMT
     assert mla.mla_resolve_impl(_shape(kind=joint, impl=mla.MLA_IMPL_TCGEN05)) == mla.MLA_ERR_UNSUPPORTED
     assert mla.mla_resolve_impl(_shape(kind=joint, flags=mla.MLA_FLAG_WUV_FOLDED)) == mla.MLA_ERR_INVALID
+    assert mla.mla_resolve_impl(_shape(kind=joint, flags=mla.MLA_FLAG_Q_ROTATED)) == mla.MLA_ERR_INVALID
     assert mla.mla_resolve_impl(_shape(kind=joint, rope_dim=48)) == mla.MLA_ERR_INVALID
     # the extra per-token key: a multiple of 8 up to 1024, BF16/FP32 kinds only
     assert mla.mla_resolve_impl(_shape(index_dim=64)) in (mla.MLA_IMPL_SIMT, mla.MLA_IMPL_TCGEN05)

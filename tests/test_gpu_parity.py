@@ -618,6 +618,63 @@ def test_int2_decode_with_folded_up_projection(gpu_lib, kind_name, impl_name, H)
         _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+@pytest.mark.parametrize("kind_name,impl_name,H,fold", [("rot", "tcgen05", 128, True), ("rot", "simt", 32, True),
+                                                        ("rope", "tcgen05", 128, True), ("rope", "simt", 32, True),
+                                                        ("rot", "tcgen05", 64, False), ("rope", "simt", 32, False)])
+def test_int2_decode_with_query_given_rotated(gpu_lib, kind_name, impl_name, H, fold):
+    """MLA_FLAG_Q_ROTATED: the caller passes q with its latent dims already in the
+    rotated basis (bf16(q_lat . R)); with W_UV folded too, R is not passed at all. The
+    oracle gets the same query expressed back in the unrotated basis (q_rot . R^T, fp64),
+    so that its own q . R reproduces the caller's rotated dims."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=3, H=H, len_range=(60, 700))
+    kind = mla.MLA_KV_INT2_ROT if kind_name == "rot" else mla.MLA_KV_INT2_ROT_QR
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    T = T32
+    if kind_name == "rope":
+        rng = np.random.default_rng(12)
+        KRcal = workloads.bf16_round(rng.standard_normal((8192, 64)).astype(np.float32)).astype(np.float64)
+        TR32 = oint2.rope_thresholds(KRcal).astype(np.float32)
+        T = np.concatenate([T32, TR32])
+    shape = gu.shape_for(w, kind=kind, impl=impl)
+    cache, st = gu.fill_cache(w, shape, R32, T)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    r = w.r
+    q_rot = np.array(w.q, dtype=np.float64)
+    q_rot[..., :r] = workloads.bf16_round((q_rot[..., :r] @ R32.astype(np.float64)).astype(np.float32))
+    q_back = q_rot.copy()
+    q_back[..., :r] = q_rot[..., :r] @ R32.astype(np.float64).T
+    W = gu.dev(w.W_UV, torch.bfloat16)
+    fshape = gu.shape_for(w, kind=kind, impl=impl)
+    fshape.flags = mla.MLA_FLAG_Q_ROTATED
+    if fold:
+        fshape.flags |= mla.MLA_FLAG_WUV_FOLDED
+        Wf = torch.empty((w.H, w.r, w.d_v), dtype=torch.bfloat16, device="cuda")
+        mla.mla_fold_rotation(shape, gu.dev(R32), W, Wf)
+        W = Wf
+    out = torch.empty((w.B, 1, w.H, w.d_v), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, 1, w.H), dtype=torch.float32, device="cuda")
+    ws = mla.alloc_workspace(fshape, w.B, 1)
+    mla.mla_decode(cache, gu.dev(w.block_table), gu.dev(w.seq_lens.astype(np.int32)),
+                   gu.dev(q_rot.astype(np.float32), torch.bfloat16), W, w.scale, out, lse, ws,
+                   R=None if fold else gu.dev(R32), shape=fshape)
+    torch.cuda.synchronize()
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    for b in range(w.B):
+        if kind_name == "rot":
+            codes, sz = oint2.quantize(w.latent[b], R32, T32)
+            ro, rl = oint2.attention_rotated(q_back[b], oint2.decode(codes, sz), w.rope[b], R32, w.W_UV, w.scale)
+        else:
+            codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
+            Y = oint2.decode(codes, sz).astype(np.float64)
+            ro, rl = oint2.attention_rope_int2(q_back[b], Y, R32, w.W_UV, w.scale)
+        _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 # ------------------------------------------------------------ joint rope/nope kind
 
 @pytest.mark.parametrize("H", [32, 128])
