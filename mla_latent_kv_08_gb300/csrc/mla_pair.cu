@@ -36,8 +36,9 @@
 // and per tile it does not own: TMA of its 4 V boxes, the base message (rescale),
 // then the same PV from the received P.
 //
-// Roles: warp 0 = TMA producer (+ L2 prefetch, + zeroing of a partial tile's slots
-// past the end); warp 1 = TMEM owner, lane 0 issues every MMA; warps 2..9 = Q loads,
+// Roles: warp 0 = V producer (+ L2 prefetch, + zeroing of a partial tile's slots past
+// the end), warp 10 = score-only producer; warp 1 = TMEM owner, lane 0 issues the
+// score MMAs; warp 11, lane 0, the PV MMAs; warps 2..9 = Q loads,
 // softmax, messages and the epilogue (warp w reads TMEM lanes 32*(w%4)..+31, half
 // (w-2)/4 of each row). Every wait is bounded (2 s); a wait that gives up records
 // FLAG_TIMEOUT and the CTA winds down without trapping. Both CTAs wait for every
@@ -56,7 +57,9 @@ namespace pair {
 
 using namespace ptx;
 
-constexpr int kThreads = 352;          // warp 0 V producer, 1 MMA, 2..9 softmax, 10 score-only producer
+constexpr int kThreads = 384;          // warp 0 V producer, 1 score MMAs, 2..9 softmax, 10 score-only
+                                       // producer, 11 PV MMAs
+constexpr int kPvWarp = 11;
 constexpr int kTWarp = 10;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kTile = 64;              // tokens per tile == cache block size
@@ -127,8 +130,9 @@ struct Bars {
     uint64_t bmsg;            // the other CTA's base for one of its tiles landed
     uint64_t lmsg[2];         // the other CTA's row sums at the end of a work item (item % 2)
     uint64_t q_stage, q_smem, q_tmem, qreg_free;
-    uint64_t mma_fin;
+    uint64_t mma_fin, pv_fin;
     uint64_t xchg_full, xchg_read;
+    int32_t pv_issued;        // tiles whose PV MMAs have been issued (PV issuer -> score issuer)
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -201,6 +205,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
         mbar_init(&bars->q_tmem, kSoftmaxThreads);
         mbar_init(&bars->qreg_free, kSoftmaxThreads);
         mbar_init(&bars->mma_fin, 1);
+        mbar_init(&bars->pv_fin, 1);
+        bars->pv_issued = 0;
         mbar_init(&bars->xchg_full, kSoftmaxThreads);
         mbar_init(&bars->xchg_read, kSoftmaxThreads);
         bars->abort_flag = 0;
@@ -349,71 +355,50 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
                 if (u >= 0 && owned(u)) mbar_drain(&bars->t_full[(u >> 1) % kNT], ((u >> 1) / kNT) & 1);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ================================================= MMA issuer (lane 0)
-        // An event loop over two cursors: the PV of every tile, in tile order, and the
-        // QK of this CTA's next owned tile, in two halves. Each pass issues whatever of
-        // the two is ready; nothing is issued out of its cursor's order.
+    } else if (warp == 1 || warp == kPvWarp) {
+        // ================================================= MMA issuers (lane 0 of each)
+        // Warp 1 issues the score MMAs of this CTA's owned tiles, warp kPvWarp the PV of
+        // every tile, each in tile order as soon as its inputs are there (one issuer
+        // for both held the PV of a tile back behind the next tile's score MMAs). Every
+        // barrier phase is observed in order, each right after the one before it
+        // completed, so a parity test never sees a barrier two phases away: a V slot's
+        // phases are observed alternately by the two issuers (the scores of an owned
+        // tile, the PV of the other CTA's), and the scores of tile T wait until PV(T-3),
+        // the slot's previous user, was issued (published in pv_issued). Each issuer
+        // toggles its own parity bit of a slot's tail barrier for every partial tile that
+        // passes through the slot, observed by it or not.
         if (lane == 0) {
+            const bool is_pv = warp == kPvWarp;
             const uint32_t d_o = tmem + kColO, d_s = tmem + kColS, qt = tmem + kColQ;
             constexpr uint32_t kIdQk = idesc_bf16(128, 64, false);
             constexpr uint32_t kIdPv = idesc_bf16(128, 128, true);
+            volatile int32_t *pv_issued = &bars->pv_issued;
             bool ok = true;
-            // Every barrier phase is observed in order, each right after the one before it
-            // completed, so a parity test never sees a barrier two phases away: the V slot
-            // of a tile is observed by the QK of an owned tile or by the PV of another
-            // tile, and the QK of tile T waits until PV(T-3), the slot's previous user, was
-            // issued (its V load could not have started earlier anyway).
-            uint32_t vt_par = 0, tt_par = 0;      // bit s: parity of the partial tiles seen in slot s
-            struct Cursor {
-                int i, t, T, nt, L, t0;
-                int own_items;                    // items with an owned tile before this one
-                bool has_own;                     // this CTA owns a tile of this item
-            };
-            auto load_item = [&](Cursor &c) {
-                if (c.i < i1) {
-                    const WorkItem it = p.work[c.i];
-                    c.nt = (it.t1 - it.t0 + kTile - 1) / kTile;
-                    c.L = p.seq_lens[it.b];
-                    c.t0 = it.t0;
-                    c.has_own = c.nt >= 2 || owned(c.T);
-                }
-            };
-            auto advance = [&](Cursor &c) {
-                ++c.T;
-                if (++c.t >= c.nt) {
-                    c.own_items += c.has_own ? 1 : 0;
-                    ++c.i;
-                    c.t = 0;
-                    load_item(c);
-                }
-            };
-            auto valid_of = [&](const Cursor &c) { return min(kTile, c.L - (c.t0 + c.t * kTile)); };
-            Cursor pv{i0, 0, 0, 0, 0, 0, 0, false}, qk{i0, 0, 0, 0, 0, 0, 0, false};
-            load_item(pv);
-            load_item(qk);
-            while (qk.i < i1 && !owned(qk.T)) advance(qk);
-            int qk_half = 0;                      // 0: next is the first half of the owned tile's QK
-            int q_obs = 0;                        // owned items whose Q (TMEM and smem parts) was observed
-            unsigned long long t_last = globaltimer();
-            uint32_t spins = 0;
-            while (ok && pv.i < i1) {
-                bool did = false;
-                // ---- PV of tile pv.T
-                {
-                    const int T = pv.T;
+            uint32_t vt_par = 0, tt_par = 0;      // bit s: parity of the partial tiles passed in slot s
+            int T = 0, own_items = 0;
+            for (int i = i0; i < i1 && ok; ++i) {
+                const WorkItem it = p.work[i];
+                const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
+                const int L = p.seq_lens[it.b];
+                const bool has_own = nt >= 2 || owned(T);
+                bool q_seen = false;              // this item's Q observed (score issuer)
+                for (int t = 0; t < nt && ok; ++t, ++T) {
                     const bool own = owned(T);
                     const int vs = T % kNV;
-                    const int valid = valid_of(pv);
-                    bool rdy = mbar_test(&bars->ready[T & 1], (T >> 1) & 1);
-                    if (rdy && !own) {
-                        rdy = mbar_test(&bars->p_rx, (T >> 1) & 1) && mbar_test(&bars->v_full[vs], (T / kNV) & 1);
-                        if (rdy && valid < kTile) rdy = mbar_test(&bars->v_tail[vs], (vt_par >> vs) & 1u);
-                    }
-                    if (rdy) {
+                    const int valid = min(kTile, L - (it.t0 + t * kTile));
+                    const bool partial = valid < kTile;
+                    if (is_pv) {
+                        // ---- PV of tile T
+                        ok = mbar_wait(&bars->ready[T & 1], (T >> 1) & 1, bars, p.status);
+                        if (ok && !own) {
+                            ok = mbar_wait(&bars->p_rx, (T >> 1) & 1, bars, p.status) &&
+                                 mbar_wait(&bars->v_full[vs], (T / kNV) & 1, bars, p.status);
+                            if (ok && partial) ok = mbar_wait(&bars->v_tail[vs], (vt_par >> vs) & 1u, bars, p.status);
+                        }
+                        if (partial) vt_par ^= 1u << vs;
+                        if (!ok) break;
                         if (!own) {
                             mbar_expect_tx(&bars->p_rx, kPBytes);   // arm the next copy's phase
-                            if (valid < kTile) vt_par ^= 1u << vs;
                             // P arrived by the other CTA's generic-proxy remote stores; the MMAs
                             // read it through the async proxy
                             fence_proxy_async();
@@ -425,7 +410,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint64_t a = a0 + (uint64_t)(2 * k), b = b0 + (uint64_t)(128 * k);
-                            if (pv.t == 0 && k == 0) {
+                            if (t == 0 && k == 0) {
                                 mma_ss_k<kIdPv, 0>(d_o, a, b);
                                 mma_ss_k<kIdPv, 0>(d_o + 128, a, b + 1024);
                             } else {
@@ -436,32 +421,46 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
                         mma_commit(&bars->pv_done[T & 1]);
                         mma_commit(&bars->v_empty[vs]);
                         if (!own) mma_commit_mc(&bars->rbuf_free, (uint16_t)(1u << peer));
+                        *pv_issued = T + 1;
                         PTRACE(4, T);
-                        advance(pv);
-                        did = true;
-                    }
-                }
-                // ---- QK of the owned tile qk.T (one half per pass, also right after a PV:
-                // keeping the scores ahead measured faster than giving the PVs priority)
-                if (qk.i < i1) {
-                    const int T = qk.T, k = T >> 1, ts = k % kNT, vs = T % kNV;
-                    bool rdy = true;
-                    if (qk_half == 0) {
-                        if (q_obs == qk.own_items &&
-                            mbar_test(&bars->q_tmem, qk.own_items & 1) && mbar_test(&bars->q_smem, qk.own_items & 1))
-                            ++q_obs;
-                        rdy = q_obs > qk.own_items && pv.T > T - kNV;
-                        rdy = rdy && mbar_test(&bars->t_full[ts], (k / kNT) & 1) && mbar_test(&bars->v_full[vs], (T / kNV) & 1);
-                        rdy = rdy && (k == 0 || mbar_test(&bars->s_free, (k - 1) & 1));
-                        if (rdy && valid_of(qk) < kTile)
-                            rdy = mbar_test(&bars->t_tail[ts], (tt_par >> ts) & 1u) &&
-                                  mbar_test(&bars->v_tail[vs], (vt_par >> vs) & 1u);
-                        if (rdy && valid_of(qk) < kTile) {
+                    } else {
+                        // ---- QK of tile T, if this CTA owns it
+                        const int k = T >> 1, ts = k % kNT;
+                        if (!own) {
+                            if (partial) vt_par ^= 1u << vs;
+                            continue;
+                        }
+                        if (!q_seen) {
+                            ok = mbar_wait(&bars->q_tmem, own_items & 1, bars, p.status) &&
+                                 mbar_wait(&bars->q_smem, own_items & 1, bars, p.status);
+                            q_seen = true;
+                        }
+                        // the V slot's previous user, PV(T - 3), was issued
+                        if (ok && *pv_issued <= T - kNV) {
+                            const unsigned long long tw0 = globaltimer();
+                            for (uint32_t it2 = 0; *pv_issued <= T - kNV; ++it2) {
+                                if ((it2 & 63u) == 63u && (aborted(bars) || globaltimer() - tw0 > kTimeoutNs)) {
+                                    if (!aborted(bars)) {
+                                        atomicExch(&bars->abort_flag, 1);
+                                        raise_flag(p.status, FLAG_TIMEOUT);
+                                    }
+                                    ok = false;
+                                    break;
+                                }
+                                __nanosleep(32);
+                            }
+                        }
+                        ok = ok && mbar_wait(&bars->t_full[ts], (k / kNT) & 1, bars, p.status) &&
+                             mbar_wait(&bars->v_full[vs], (T / kNV) & 1, bars, p.status) &&
+                             (k == 0 || mbar_wait(&bars->s_free, (k - 1) & 1, bars, p.status));
+                        if (ok && partial)
+                            ok = mbar_wait(&bars->t_tail[ts], (tt_par >> ts) & 1u, bars, p.status) &&
+                                 mbar_wait(&bars->v_tail[vs], (vt_par >> vs) & 1u, bars, p.status);
+                        if (partial) {
                             tt_par ^= 1u << ts;
                             vt_par ^= 1u << vs;
                         }
-                    }
-                    if (rdy) {
+                        if (!ok) break;
                         tc_fence_after();
                         const uint64_t vd = sdesc(smem_u32(smem + kOffV + vs * kVSeg), 16, 1024);
                         const uint64_t td = sdesc(smem_u32(smem + kOffT + ts * kTSeg), 16, 1024);
@@ -475,42 +474,24 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
                             const int ti = d < 8 ? (d & 3) : 4;
                             return td + (uint64_t)((ti * kBox + off) >> 4);
                         };
-                        if (qk_half == 0) {
-                            mma_ts_k<kIdQk, 0>(d_s, qt, kdesc(0));
+                        mma_ts_k<kIdQk, 0>(d_s, qt, kdesc(0));
 #pragma unroll
-                            for (int j = 1; j < kQkSplit; ++j) mma_ts_k<kIdQk, 1>(d_s, qt + 8 * j, kdesc(j));
-                            PTRACE(2, T);
-                            qk_half = 1;
-                        } else {
+                        for (int j = 1; j < kQkSplit; ++j) mma_ts_k<kIdQk, 1>(d_s, qt + 8 * j, kdesc(j));
+                        PTRACE(2, T);
 #pragma unroll
-                            for (int j = kQkSplit; j < 36; ++j)
-                                mma_ss_k<kIdQk, 1>(
-                                    d_s, qd + (uint64_t)((((j >> 2) - kQTmemBlocks) * kQBlock + 32 * (j & 3)) >> 4), kdesc(j));
-                            mma_commit(&bars->s_full);
-                            mma_commit(&bars->t_empty[ts]);
-                            PTRACE(3, T);
-                            qk_half = 0;
-                            do advance(qk);
-                            while (qk.i < i1 && !owned(qk.T));
-                        }
-                        did = true;
+                        for (int j = kQkSplit; j < 36; ++j)
+                            mma_ss_k<kIdQk, 1>(
+                                d_s, qd + (uint64_t)((((j >> 2) - kQTmemBlocks) * kQBlock + 32 * (j & 3)) >> 4), kdesc(j));
+                        mma_commit(&bars->s_full);
+                        mma_commit(&bars->t_empty[ts]);
+                        PTRACE(3, T);
                     }
                 }
-                if (did) {
-                    spins = 0;
-                    t_last = globaltimer();
-                } else if ((++spins & 63u) == 0) {
-                    if (aborted(bars)) {
-                        ok = false;
-                    } else if (globaltimer() - t_last > kTimeoutNs) {
-                        atomicExch(&bars->abort_flag, 1);
-                        raise_flag(p.status, FLAG_TIMEOUT);
-                        ok = false;
-                    }
-                }
+                if (has_own) ++own_items;
             }
-            mma_commit(&bars->mma_fin);
-            mbar_wait(&bars->mma_fin, 0, bars, p.status);
+            uint64_t *fin = is_pv ? &bars->pv_fin : &bars->mma_fin;
+            mma_commit(fin);
+            mbar_wait(fin, 0, bars, p.status);
         }
         __syncwarp();
     } else {
