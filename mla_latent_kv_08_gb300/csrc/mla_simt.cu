@@ -782,14 +782,17 @@ __global__ void __launch_bounds__(256) append_index_kernel(AppendParams p) {
 
 constexpr int kAT = 16;   // tokens per INT2 append CTA
 
-// One CTA: kAT tokens x one block of kAC output columns (a whole number of groups,
-// at most 128). Thread (column c, token half th) runs the fp32 fmaf chains of its
-// column for 8 tokens, k ascending from +0 (the encoding definition's order), with R
-// staged through shared memory 32 rows at a time; then one thread per (token, group)
-// clips, ranges, rounds scale/zero to fp16 and packs the codes.
+// One CTA: kAT tokens x one block of output columns (a whole number of groups, at
+// most 128), 128 threads. Thread (token quad tq, column quad cq) runs the 16 fp32 fmaf
+// chains of tokens 4 tq .. 4 tq + 3 x columns 4 cq .. 4 cq + 3, each k ascending from
+// +0 (the encoding definition's order), reading R as 16-byte rows of its four columns
+// and the inputs as 16-byte runs of four k, with R staged through shared memory 32 rows
+// at a time; then one thread per (token, group) clips, ranges, rounds scale/zero to
+// fp16 and packs the codes.
 constexpr int kAKC = 32;  // R rows staged per step
-template <int COLS>   // COLS: columns per CTA (128 when group_size divides 128, else 0: read `cols`)
-__global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p, int cols_rt) {
+constexpr int kAThreads = 128;
+template <int COLS>   // COLS: columns per CTA (128, 96 or 64; 0: read `cols`)
+__global__ void __launch_bounds__(kAThreads) append_int2_kernel(AppendParams p, int cols_rt) {
     extern __shared__ float sa[];
     const int cols = COLS ? COLS : cols_rt;
     const int r = p.s.r, dR = p.s.dR, gs = p.s.gs;
@@ -801,9 +804,11 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p, int co
     const int j0 = blockIdx.y * cols;                          // first output column of this CTA
     const int ncol = min(cols, RD - j0);
     float *sc = sa;                   // [kAT][RDp] rotation input (fp32)
-    float *sR = sc + kAT * RDp;       // [kAKC][cols] rows of R, this CTA's columns
-    float *sy = sR + kAKC * cols;     // [kAT][cols] rotated
-    float *sr = sy + kAT * cols;      // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
+    float *sR = sc + kAT * RDp;       // [2][kAKC][cols] rows of R, this CTA's columns
+    const int ys = cols + 1;          // row stride of sy: a (token, group) job per lane reads
+                                      // 16 tokens' rows on 16 different banks
+    float *sy = sR + 2 * kAKC * cols; // [kAT][ys] rotated
+    float *sr = sy + kAT * ys;        // INT2_ROT_QR: [kAT][d_R] rope key (fp32)
     __shared__ long long s_row[kAT];
     const int n0 = blockIdx.x * kAT;
     const int tid = threadIdx.x;
@@ -822,52 +827,90 @@ __global__ void __launch_bounds__(256) append_int2_kernel(AppendParams p, int co
             int t = idx / dR, d = idx % dR;
             sr[idx] = (n0 + t < p.num_new) ? __bfloat162float(kr[(size_t)(n0 + t) * dR + d]) : 0.f;
         }
-    const int col = tid & 127, th = tid >> 7;                 // column, token half (tokens 8*th..8*th+7)
-    const bool act = col < ncol;
-    float acc[8];
+    static_assert(kAT == 16 && kAThreads == 128, "four token quads x 32 column quads");
+    const int cq = tid & 31, tq = tid >> 5;                   // column quad, token quad
+    const bool act = 4 * cq < ncol;                           // ncol is a multiple of 4
+    float acc[4][4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-    const float *scb = sc + (8 * th) * RDp;
-    for (int k0 = 0; k0 < RD; k0 += kAKC) {
-        __syncthreads();              // previous chunk consumed (and sc ready on the first pass)
-        for (int kk = tid / cols, cc = tid % cols; kk < kAKC; kk += 256 / cols) {
-            // 256 / cols rows of the chunk per pass (cols divides 256 for every allowed cols)
-            sR[kk * cols + cc] = (k0 + kk < RD && cc < ncol) ? __ldg(p.R + (size_t)(k0 + kk) * RD + j0 + cc) : 0.f;
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) acc[t][c4] = 0.f;
+    const float *scb = sc + (4 * tq) * RDp;
+    // R chunks of kAKC rows, double-buffered: chunk c + 1 is read from global memory
+    // into registers while chunk c is used, then stored into the other buffer
+    constexpr int kPer = kAKC * 128 / kAThreads;              // chunk elements per thread (cols <= 128)
+    const int nchunks = (RD + kAKC - 1) / kAKC;
+    float pre[kPer];
+    auto load_chunk = [&](int k0) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int idx = tid + e * kAThreads, kk = idx / cols, cc = idx % cols;
+            pre[e] = (idx < kAKC * cols && k0 + kk < RD && cc < ncol) ? __ldg(p.R + (size_t)(k0 + kk) * RD + j0 + cc) : 0.f;
         }
-        __syncthreads();
+    };
+    auto store_chunk = [&](float *dst) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int idx = tid + e * kAThreads;
+            if (idx < kAKC * cols) dst[idx] = pre[e];
+        }
+    };
+    load_chunk(0);
+    store_chunk(sR);
+    for (int ch = 0; ch < nchunks; ++ch) {
+        __syncthreads();              // chunk ch stored (and sc ready on the first pass)
+        if (ch + 1 < nchunks) load_chunk((ch + 1) * kAKC);
+        const float *sRc = sR + (ch & 1) * kAKC * cols;
+        const int k0 = ch * kAKC;
         if (act) {
             const int kn = min(kAKC, RD - k0);      // a multiple of 4 (RD is)
+#pragma unroll 2
             for (int kk = 0; kk < kn; kk += 4) {
-                const float r0 = sR[kk * cols + col], r1 = sR[(kk + 1) * cols + col];
-                const float r2 = sR[(kk + 2) * cols + col], r3 = sR[(kk + 3) * cols + col];
+                float4 rr4[4];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
+                for (int u = 0; u < 4; ++u) rr4[u] = *(const float4 *)(sRc + (kk + u) * cols + 4 * cq);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
                     const float4 x = *(const float4 *)(scb + t * RDp + k0 + kk);
-                    float a = acc[t];
-                    a = __fmaf_rn(x.x, r0, a);      // k ascending: the definition's chain
-                    a = __fmaf_rn(x.y, r1, a);
-                    a = __fmaf_rn(x.z, r2, a);
-                    a = __fmaf_rn(x.w, r3, a);
-                    acc[t] = a;
+                    // k ascending within each column's chain: the definition's order
+                    acc[t][0] = __fmaf_rn(x.x, rr4[0].x, acc[t][0]);
+                    acc[t][1] = __fmaf_rn(x.x, rr4[0].y, acc[t][1]);
+                    acc[t][2] = __fmaf_rn(x.x, rr4[0].z, acc[t][2]);
+                    acc[t][3] = __fmaf_rn(x.x, rr4[0].w, acc[t][3]);
+                    acc[t][0] = __fmaf_rn(x.y, rr4[1].x, acc[t][0]);
+                    acc[t][1] = __fmaf_rn(x.y, rr4[1].y, acc[t][1]);
+                    acc[t][2] = __fmaf_rn(x.y, rr4[1].z, acc[t][2]);
+                    acc[t][3] = __fmaf_rn(x.y, rr4[1].w, acc[t][3]);
+                    acc[t][0] = __fmaf_rn(x.z, rr4[2].x, acc[t][0]);
+                    acc[t][1] = __fmaf_rn(x.z, rr4[2].y, acc[t][1]);
+                    acc[t][2] = __fmaf_rn(x.z, rr4[2].z, acc[t][2]);
+                    acc[t][3] = __fmaf_rn(x.z, rr4[2].w, acc[t][3]);
+                    acc[t][0] = __fmaf_rn(x.w, rr4[3].x, acc[t][0]);
+                    acc[t][1] = __fmaf_rn(x.w, rr4[3].y, acc[t][1]);
+                    acc[t][2] = __fmaf_rn(x.w, rr4[3].z, acc[t][2]);
+                    acc[t][3] = __fmaf_rn(x.w, rr4[3].w, acc[t][3]);
                 }
             }
         }
+        if (ch + 1 < nchunks) store_chunk(sR + ((ch + 1) & 1) * kAKC * cols);
     }
     if (act)
 #pragma unroll
-        for (int t = 0; t < 8; ++t) sy[(8 * th + t) * cols + col] = acc[t];
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) sy[(4 * tq + t) * ys + 4 * cq + c4] = acc[t][c4];
     __syncthreads();
     // this CTA's groups of the rotated row; INT2_ROT_QR: the rope key's groups in the
     // first column block
     const int g0 = j0 / gs, gn = ncol / gs;
     const int extra = (rope_codes && blockIdx.y == 0) ? ng_all - ng : 0;
     for (int job = tid; job < kAT * (gn + extra); job += blockDim.x) {
-        const int t = job / (gn + extra), gl = job % (gn + extra);
+        const int t = job % kAT, gl = job / kAT;            // lanes: consecutive tokens
         const long long row = s_row[t];
         if (row < 0) continue;
         const int g = gl < gn ? g0 + gl : ng + (gl - gn);
         const float thr = p.clip[g];
-        const float *y = gl < gn ? sy + t * cols + gl * gs : sr + t * dR + (g - ng) * gs;
+        const float *y = gl < gn ? sy + t * ys + gl * gs : sr + t * dR + (g - ng) * gs;
         float lo = CUDART_INF_F, hi = -CUDART_INF_F;
         for (int j = 0; j < gs; ++j) {
             float v = fminf(fmaxf(y[j], -thr), thr);
@@ -918,18 +961,32 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
     } else if (p.s.kind == MLA_KV_FP32) {
         return launch_pdl(append_copy_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     } else {
-        // column blocks of whole groups, at most 128 columns (group_size <= 128)
-        const int cols = (128 / p.s.gs) * p.s.gs;
-        const int RDp = (p.s.RD() + 3) & ~3;
-        const size_t smem = sizeof(float) * ((size_t)kAT * RDp + (size_t)kAKC * cols + (size_t)kAT * cols +
+        // column blocks of whole groups, at most 128 columns (group_size <= 128): 128,
+        // 96 or 64 where that splits the rotated row into whole blocks (compiled), else
+        // the largest multiple of the group size up to 128
+        const int RD = p.s.RD(), gs = p.s.gs;
+        int cols = (128 / gs) * gs;
+        for (int c : {128, 96, 64})
+            if (c % gs == 0 && RD % c == 0) {
+                cols = c;
+                break;
+            }
+        const int RDp = (RD + 3) & ~3;
+        const size_t smem = sizeof(float) * ((size_t)kAT * RDp + (size_t)2 * kAKC * cols + (size_t)kAT * (cols + 1) +
                                              (p.s.kind == MLA_KV_INT2_ROT_QR ? (size_t)kAT * p.s.dR : 0));
         dim3 grid((p.num_new + kAT - 1) / kAT, (p.s.RD() + cols - 1) / cols);
         if (cols == 128) {
             cudaFuncSetAttribute(append_int2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            append_int2_kernel<128><<<grid, 256, smem, st>>>(p, cols);
+            append_int2_kernel<128><<<grid, kAThreads, smem, st>>>(p, cols);
+        } else if (cols == 96) {
+            cudaFuncSetAttribute(append_int2_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<96><<<grid, kAThreads, smem, st>>>(p, cols);
+        } else if (cols == 64) {
+            cudaFuncSetAttribute(append_int2_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            append_int2_kernel<64><<<grid, kAThreads, smem, st>>>(p, cols);
         } else {
             cudaFuncSetAttribute(append_int2_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            append_int2_kernel<0><<<grid, 256, smem, st>>>(p, cols);
+            append_int2_kernel<0><<<grid, kAThreads, smem, st>>>(p, cols);
         }
     }
     return cudaGetLastError();
