@@ -421,23 +421,34 @@ def run_gb300(args):
 
     e2e = None
     if not args.no_e2e:
-        hq = torch.from_numpy(np.ascontiguousarray(w.q)).to(bf).pin_memory()
-        hc = new_c.cpu().pin_memory()
-        hr = new_r.cpu().pin_memory()
-        hout = torch.empty(out.shape, dtype=bf).pin_memory()
-        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        q_d = torch.empty_like(q)
-        c_d = torch.empty_like(new_c)
-        r_d = torch.empty_like(new_r)
+        # The step's inputs (query, new latents, new rope keys) sit in one pinned host
+        # buffer and one device buffer, and its results (out, lse) in one device buffer
+        # read back into one pinned buffer: one copy each way per step, as a caller
+        # would lay them out. Tensors are views at 256-byte-aligned offsets.
+        def packed(parts, device, pin):
+            offs, n = [], 0
+            for t in parts:
+                offs.append(n)
+                n += (t.numel() * t.element_size() + 255) // 256 * 256
+            raw = torch.empty(n, dtype=torch.uint8, device=device)
+            if pin:
+                raw = raw.pin_memory()
+            views = [raw[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, parts)]
+            return raw, views
+        q_host = torch.from_numpy(np.ascontiguousarray(w.q)).to(bf)
+        hin, (hq, hc, hr) = packed([q_host, new_c, new_r], "cpu", True)
+        hq.copy_(q_host)
+        hc.copy_(new_c.cpu())
+        hr.copy_(new_r.cpu())
+        din, (q_d, c_d, r_d) = packed([q, new_c, new_r], dev, False)
+        dres, (out_d, lse_d) = packed([out, lse], dev, False)
+        hres = torch.empty(dres.shape, dtype=torch.uint8).pin_memory()
 
         def e2e_step(st):
-            q_d.copy_(hq, non_blocking=True)
-            c_d.copy_(hc, non_blocking=True)
-            r_d.copy_(hr, non_blocking=True)
+            din.copy_(hin, non_blocking=True)
             mla.mla_latent_append(cache, bt, start, cu1, c_d, r_d, stream=st)
-            mla.mla_decode(cache, bt, seq_lens, q_d, W_UV, w.scale, out, lse, ws, stream=st)
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+            mla.mla_decode(cache, bt, seq_lens, q_d, W_UV, w.scale, out_d, lse_d, ws, stream=st)
+            hres.copy_(dres, non_blocking=True)
 
         # The whole step (copies from and to pinned host memory, append, decode) is
         # captured once as a CUDA graph and replayed: its copies read and write the
@@ -488,8 +499,8 @@ def run_gb300(args):
         code, flags = mla.mla_get_status(ws)
         if code != mla.MLA_OK:
             raise RuntimeError(f"device status {code} flags {flags} after the end-to-end steps")
-        h2d = hq.numel() * 2 + hc.numel() * 2 + hr.numel() * 2
-        d2h = hout.numel() * 2 + hlse.numel() * 4
+        h2d = hin.numel()
+        d2h = hres.numel()
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h,
                "mode": "CUDA graph replay" if graph is not None else "eager launches"}
         # Overlapped variant: the inputs of step k + 1 are uploaded (on a second stream)
@@ -498,23 +509,21 @@ def run_gb300(args):
         # starts with the upload of step 0's inputs, so every step's copies are in it.
         if graph is not None:
             try:
-                bufs = [(torch.empty_like(q), torch.empty_like(new_c), torch.empty_like(new_r)) for _ in range(2)]
+                bufs = [packed([q, new_c, new_r], dev, False) for _ in range(2)]
                 cstream = torch.cuda.Stream(dev)
 
                 def upload(buf, st):
                     with torch.cuda.stream(st):
-                        buf[0].copy_(hq, non_blocking=True)
-                        buf[1].copy_(hc, non_blocking=True)
-                        buf[2].copy_(hr, non_blocking=True)
+                        buf[0].copy_(hin, non_blocking=True)
 
                 def overlapped_step(par):
                     cur, nxt = bufs[par], bufs[1 - par]
                     cstream.wait_stream(side)           # fork the copy branch off the step
                     upload(nxt, cstream)
-                    mla.mla_latent_append(cache, bt, start, cu1, cur[1], cur[2], stream=side)
-                    mla.mla_decode(cache, bt, seq_lens, cur[0], W_UV, w.scale, out, lse, ws, stream=side)
-                    hout.copy_(out, non_blocking=True)
-                    hlse.copy_(lse, non_blocking=True)
+                    qv, cv, rv = cur[1]
+                    mla.mla_latent_append(cache, bt, start, cu1, cv, rv, stream=side)
+                    mla.mla_decode(cache, bt, seq_lens, qv, W_UV, w.scale, out_d, lse_d, ws, stream=side)
+                    hres.copy_(dres, non_blocking=True)
                     side.wait_stream(cstream)           # join: the next inputs have landed
 
                 graphs = []
