@@ -432,6 +432,58 @@ def test_tcgen05_and_simt_agree_with_oracle(gpu_lib, H, q_len, lens):
             _check_seq(o, l, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+def _shorten(w, lens):
+    """Cut each sequence of a workload to the given length (its blocks stay valid)."""
+    for b, L in enumerate(lens):
+        w.seq_lens[b] = L
+        w.latent[b], w.rope[b] = w.latent[b][:L], w.rope[b][:L]
+
+
+@pytest.mark.parametrize("kind_name,q_len", [("bf16", 1), ("bf16", 2), ("int2", 1), ("rope", 1)])
+def test_lengths_at_tile_boundaries(gpu_lib, kind_name, q_len):
+    """Sequence lengths on both sides of the 64-token tile (and block) boundaries, one
+    token, and two tiles and a bit, on the tensor-core kernels: the decode (bf16, rotated
+    INT2, rope-INT2) and the paired verify kernel (bf16, q_len 2)."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    lens = [max(q_len, 1), 63, 64, 65, 127, 128, 129, 191]
+    if kind_name == "bf16":
+        w = workloads.dsv3(77 + q_len, B=len(lens), H=128, len_range=(200, 260), q_len=q_len)
+        _shorten(w, lens)
+        shape = gu.shape_for(w, impl=mla.MLA_IMPL_TCGEN05)
+        cache, _ = gu.fill_cache(w, shape)
+        out, lse, ws = gu.attend(w, shape, cache, w.q, q_len=q_len)
+        assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+        for b in range(w.B):
+            ro, rl = attention.absorbed(w.q[b], w.latent[b], w.rope[b], w.W_UV, w.scale)
+            _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+        return
+    w, R32, T32 = _int2_setup(B=len(lens), H=128, len_range=(200, 260))
+    _shorten(w, lens)
+    kind = mla.MLA_KV_INT2_ROT if kind_name == "int2" else mla.MLA_KV_INT2_ROT_QR
+    T = T32
+    if kind_name == "rope":
+        rng = np.random.default_rng(12)
+        KRcal = workloads.bf16_round(rng.standard_normal((8192, 64)).astype(np.float32)).astype(np.float64)
+        TR32 = oint2.rope_thresholds(KRcal).astype(np.float32)
+        T = np.concatenate([T32, TR32])
+    shape = gu.shape_for(w, kind=kind, impl=mla.MLA_IMPL_TCGEN05)
+    cache, st = gu.fill_cache(w, shape, R32, T)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    out, lse, ws = gu.attend(w, shape, cache, w.q, R=R32)
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    for b in range(w.B):
+        if kind_name == "int2":
+            codes, sz = oint2.quantize(w.latent[b], R32, T32)
+            ro, rl = oint2.attention_rotated(w.q[b], oint2.decode(codes, sz), w.rope[b], R32, w.W_UV, w.scale)
+        else:
+            codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
+            Y = oint2.decode(codes, sz).astype(np.float64)
+            ro, rl = oint2.attention_rope_int2(w.q[b], Y, R32, w.W_UV, w.scale)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+
+
 def test_auto_picks_tensor_cores_for_dsv3(gpu_lib):
     import mla_latent_kv_08_gb300 as mla
     w = workloads.dsv3(1, B=2, H=128, len_range=(64, 64))
