@@ -473,15 +473,31 @@ def test_lengths_at_tile_boundaries(gpu_lib, kind_name, q_len):
     assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
     out, lse, ws = gu.attend(w, shape, cache, w.q, R=R32)
     assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    f16 = lambda x: np.asarray(x, np.float64).astype(np.float16).astype(np.float64)   # noqa: E731
     for b in range(w.B):
         if kind_name == "int2":
             codes, sz = oint2.quantize(w.latent[b], R32, T32)
-            ro, rl = oint2.attention_rotated(w.q[b], oint2.decode(codes, sz), w.rope[b], R32, w.W_UV, w.scale)
+            K = oint2.decode(codes, sz).astype(np.float64)
+            ro, rl = oint2.attention_rotated(w.q[b], K, w.rope[b], R32, w.W_UV, w.scale)
         else:
             codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
             Y = oint2.decode(codes, sz).astype(np.float64)
             ro, rl = oint2.attention_rope_int2(w.q[b], Y, R32, w.W_UV, w.scale)
-        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+        if w.seq_lens[b] > 1:
+            _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+            continue
+        # One token: the LSE is that token's score itself, with no averaging of the
+        # fp16 operand roundings of the rotated query and the dequantised key (the INT2
+        # kernels' operand type). The kernel must match the score formed from those
+        # fp16 operands to the usual bar, and the definition within twice it.
+        q = np.asarray(w.q[b], np.float64)[0]                        # [H, r + d_R]
+        if kind_name == "int2":
+            qk = f16(q[:, :w.r] @ R32.astype(np.float64)) @ f16(K[0, :w.r]) + q[:, w.r:] @ w.rope[b][0].astype(np.float64)
+        else:
+            qy = np.concatenate([q[:, :w.r] @ R32.astype(np.float64), q[:, w.r:]], axis=1)
+            qk = f16(qy) @ f16(Y[0])
+        assert float(np.max(np.abs(lse[b, 0] - w.scale * qk))) <= gu.BF16_LSE_TOL
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, 2 * gu.BF16_LSE_TOL)
 
 
 def test_auto_picks_tensor_cores_for_dsv3(gpu_lib):
