@@ -132,9 +132,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-# the files that define the tensor-core decode kernel (its DRAM counters are recorded
-# against their hash; host-side changes elsewhere do not invalidate them)
-KERNEL_SOURCES = ("mla_tc.cu", "mla_ptx.cuh", "mla_internal.cuh")
+# the files that define the bf16 tensor-core decode kernel (its DRAM counters are
+# recorded against their hash; host-side changes elsewhere do not invalidate them)
+KERNEL_SOURCES = ("mla_wide.cu", "mla_ptx.cuh", "mla_internal.cuh")
 
 
 def kernel_source_hash():
@@ -576,7 +576,7 @@ def run_gb300(args):
     tokens = w.total_tokens * world
     value = job_throughput(w.total_tokens, world, step_ms)
     achieved = kb / (att_avg_ms * 1e-3) / 1e9
-    kernel_name = {mla.MLA_IMPL_SIMT: "decode_simt_kernel", mla.MLA_IMPL_TCGEN05: "decode_tc_kernel"}[
+    kernel_name = {mla.MLA_IMPL_SIMT: "decode_simt_kernel", mla.MLA_IMPL_TCGEN05: "decode_wide_kernel"}[
         mla.mla_resolve_impl(shape, 1)]
     configs = None
     if not args.no_configs:

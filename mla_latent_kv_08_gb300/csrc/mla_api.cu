@@ -99,9 +99,14 @@ int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
     return tc_ok ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
 }
 
-// Tiles the planner charges per sequence start on the tensor-core path (a work item's
-// query load and epilogue cost about as much as two to three 64-token tiles).
+// Units the planner charges per sequence start on the tensor-core path (a work item's
+// query load and epilogue cost about as much as two to three 64-token tiles, or one
+// to two 128-token steps of the bf16 decode that scores two blocks per MMA).
 constexpr int kItemCostTc = 3;
+#ifndef MLA_ITEM_COST_WIDE
+#define MLA_ITEM_COST_WIDE 2
+#endif
+constexpr int kItemCostWide = MLA_ITEM_COST_WIDE;
 
 static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {
     WsLayout w;
@@ -196,7 +201,11 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.scale_log2 = scale * kLog2e;
     p.status = (int32_t *)(ws + w.status);
     p.num_work = (const int32_t *)(ws + w.status + sizeof(int32_t));
-    p.item_cost = impl == MLA_IMPL_TCGEN05 ? kItemCostTc : 0;
+    // the bf16 decode that scores two blocks per MMA plans in 128-token steps, so that
+    // only a sequence's last work item can end with an unpaired block
+    const bool wide = impl == MLA_IMPL_TCGEN05 && s->kind == MLA_KV_BF16 && q_len == 1 && kDecodeWide;
+    p.item_cost = impl == MLA_IMPL_TCGEN05 ? (wide ? kItemCostWide : kItemCostTc) : 0;
+    p.plan_tile = wide ? 128 : 64;
     p.work = (const WorkItem *)(ws + w.work);
     p.split_start = (const int32_t *)(ws + w.split_start);
     p.stream_start = (const int32_t *)(ws + w.stream_start);

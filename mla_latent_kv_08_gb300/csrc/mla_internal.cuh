@@ -92,7 +92,8 @@ struct DecodeParams {
     const int32_t *split_start;
     const int32_t *stream_start;
     int32_t streams;
-    int32_t item_cost;           // planner: tiles charged per sequence start (its Q load, epilogue)
+    int32_t item_cost;           // planner: units charged per sequence start (its Q load, epilogue)
+    int32_t plan_tile;           // planner: tokens per cost unit; work items start at multiples of it
     float *part_o;
     float *part_lse;
 };
@@ -166,6 +167,12 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
 // ---- paired tensor-core decode of the bf16 cache (defined in mla_pair.cu) ----
 cudaError_t launch_decode_pair(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 int pair_max_clusters();   // 2-CTA clusters resident at once on the current device (0: unknown)
+// ---- bf16 decode scoring two cache blocks per MMA (mla_wide.cu) -----------------
+#ifndef MLA_DECODE_WIDE
+#define MLA_DECODE_WIDE 1
+#endif
+constexpr bool kDecodeWide = MLA_DECODE_WIDE != 0;   // one query row per sequence: decode_wide_kernel
+cudaError_t launch_decode_wide(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 // ---- tensor-core combine + W_UV (defined in mla_combine_tc.cu) --------------
 bool combine_tc_supported(const ShapeArgs &s);
 cudaError_t launch_combine_tc(const CombineParams &c, cudaStream_t st);

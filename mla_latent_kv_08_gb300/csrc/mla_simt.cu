@@ -97,10 +97,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
     // load and epilogue of a new work item) followed by one unit per tile; streams
     // take equal cost ranges, so a stream that starts more sequences gets fewer tiles.
     const int ic = p.item_cost;
+    const int PT = p.plan_tile > 0 ? p.plan_tile : kPlanTile;
     long long local = 0;
     for (int b = tid; b < p.B; b += blockDim.x) {
         const int L = p.seq_lens[b];
-        if (L >= p.q_len && L <= cap) local += (L + kPlanTile - 1) / kPlanTile + ic;
+        if (L >= p.q_len && L <= cap) local += (L + PT - 1) / PT + ic;
         else raise_flag(p.status, FLAG_BAD_LENGTH);
     }
 #pragma unroll
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
         int n = 0, L = 0;
         if (b < p.B) {
             L = p.seq_lens[b];
-            if (L >= p.q_len && L <= cap) n = (L + kPlanTile - 1) / kPlanTile;
+            if (L >= p.q_len && L <= cap) n = (L + PT - 1) / PT;
         }
         int tot_tiles, tot_items;
         // tb: cost position of the sequence's first tile (after its start charge)
@@ -137,8 +138,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
                 const long long hi = ((sgi + 1) * T < tbi + ni ? (sgi + 1) * T : tbi + ni) - tbi;
                 WorkItem it;
                 it.b = base + slot;
-                it.t0 = (int)(lo * kPlanTile);
-                it.t1 = (int)min((long long)Li, hi * kPlanTile);
+                it.t0 = (int)(lo * PT);
+                it.t1 = (int)min((long long)Li, hi * PT);
                 it.stream = (int)sgi;
                 ((WorkItem *)p.work)[idx] = it;
             }
@@ -162,8 +163,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
                     const long long hi = ((sg + 1) * T < tb + n ? (sg + 1) * T : tb + n) - tb;
                     WorkItem it;
                     it.b = b;
-                    it.t0 = (int)(lo * kPlanTile);
-                    it.t1 = (int)min((long long)L, hi * kPlanTile);
+                    it.t0 = (int)(lo * PT);
+                    it.t1 = (int)min((long long)L, hi * PT);
                     it.stream = (int)sg;
                     ((WorkItem *)p.work)[start + k] = it;
                 }

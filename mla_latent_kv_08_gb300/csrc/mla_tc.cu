@@ -1098,6 +1098,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
     // CTAs that take turns computing the scores (mla_pair.cu); one row per sequence
     // (decode) measured faster on the kernel below, whose CTAs both score every tile
     if (p.s.kind == MLA_KV_BF16 && p.q_len > 1) return launch_decode_pair(p, max_work, st);
+    // one row per sequence: two cache blocks per score MMA (mla_wide.cu)
+    if (p.s.kind == MLA_KV_BF16 && kDecodeWide) return launch_decode_wide(p, max_work, st);
     tc::TcParams tp;
     tp.p = p;
     tp.row_tiles = (p.q_len * p.s.H + tc::kRows - 1) / tc::kRows;
