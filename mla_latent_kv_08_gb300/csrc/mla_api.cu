@@ -103,10 +103,7 @@ int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
 // query load and epilogue cost about as much as two to three 64-token tiles, or one
 // to two 128-token steps of the bf16 decode that scores two blocks per MMA).
 constexpr int kItemCostTc = 3;
-#ifndef MLA_ITEM_COST_WIDE
-#define MLA_ITEM_COST_WIDE 2
-#endif
-constexpr int kItemCostWide = MLA_ITEM_COST_WIDE;
+constexpr int kItemCostWide = 2;
 
 static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {
     WsLayout w;
@@ -117,12 +114,6 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
         // one wave of persistent CTAs: 2 per stream per 128-row tile
         const int row_tiles = (q_len * s->num_heads + 127) / 128;
         target = sms / (2 * row_tiles);
-        // the bf16 cache with q_len > 1 runs on 2-CTA clusters: no more streams than
-        // pairs that fit at once
-        if (s->kind == MLA_KV_BF16 && q_len > 1) {
-            const int pairs = pair_max_clusters();
-            if (pairs > 0 && pairs / row_tiles < target) target = pairs / row_tiles;
-        }
         if (target < 1) target = 1;
         if (s->num_splits_hint > 0 && s->num_splits_hint < target) target = s->num_splits_hint;
     } else {
@@ -203,7 +194,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.num_work = (const int32_t *)(ws + w.status + sizeof(int32_t));
     // the bf16 decode that scores two blocks per MMA plans in 128-token steps, so that
     // only a sequence's last work item can end with an unpaired block
-    const bool wide = impl == MLA_IMPL_TCGEN05 && s->kind == MLA_KV_BF16 && q_len == 1 && kDecodeWide;
+    const bool wide = impl == MLA_IMPL_TCGEN05 && s->kind == MLA_KV_BF16;
     p.item_cost = impl == MLA_IMPL_TCGEN05 ? (wide ? kItemCostWide : kItemCostTc) : 0;
     p.plan_tile = wide ? 128 : 64;
     p.work = (const WorkItem *)(ws + w.work);

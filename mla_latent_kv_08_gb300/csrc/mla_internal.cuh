@@ -164,14 +164,7 @@ cudaError_t launch_fold_rotation(const ShapeArgs &s, const float *R, const void 
 // ---- tensor-core decode (defined in mla_tc.cu) -----------------------------
 bool tc_shape_supported(const ShapeArgs &s);
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st);
-// ---- paired tensor-core decode of the bf16 cache (defined in mla_pair.cu) ----
-cudaError_t launch_decode_pair(const DecodeParams &p, int32_t max_work, cudaStream_t st);
-int pair_max_clusters();   // 2-CTA clusters resident at once on the current device (0: unknown)
-// ---- bf16 decode scoring two cache blocks per MMA (mla_wide.cu) -----------------
-#ifndef MLA_DECODE_WIDE
-#define MLA_DECODE_WIDE 1
-#endif
-constexpr bool kDecodeWide = MLA_DECODE_WIDE != 0;   // one query row per sequence: decode_wide_kernel
+// ---- bf16 tensor-core decode, two cache blocks per score MMA (mla_wide.cu) ----
 cudaError_t launch_decode_wide(const DecodeParams &p, int32_t max_work, cudaStream_t st);
 // ---- tensor-core combine + W_UV (defined in mla_combine_tc.cu) --------------
 bool combine_tc_supported(const ShapeArgs &s);

@@ -1,6 +1,7 @@
-// Tensor-core (tcgen05 / TMEM / TMA) split-KV decode for the DeepSeek-V3 latent
-// shape: kv_lora_rank 512, rope 64, block size 64; bf16 cache, or the rotated-INT2
-// cache expanded into fp16 operands on the fly.
+// Tensor-core (tcgen05 / TMEM / TMA) split-KV decode of the rotated-INT2 caches
+// (INT2_ROT, INT2_ROT_QR) of the DeepSeek-V3 latent shape: kv_lora_rank 512, rope 64,
+// block size 64, the codes expanded into fp16 operands on the fly. (The bf16 cache has
+// its own kernel, mla_wide.cu.)
 //
 // Work decomposition. The planner cuts the concatenated 64-token tiles of all
 // sequences into equal runs ("streams"); a work item is one sequence's part of
@@ -12,29 +13,29 @@
 // the scores S = Q K^T on its own (the pair shares the KV tiles through L2).
 //
 // Per CTA, per 64-token tile (one cache block):
-//   TMA     9 loads of [64 tokens x 64 dims], 128B-swizzled, into a stage (INT2:
-//           a bulk copy of the block's codes and scale/zero pairs, expanded into
-//           the stage by eight dequantising warps; INT2_ROT's bf16 rope key by TMA)
+//   copy    a bulk copy of the block's codes and scale/zero pairs into a raw stage,
+//           expanded into an operand stage by eight dequantising warps (INT2_ROT's
+//           bf16 rope key by TMA into the stage's rope block)
 //   MMA     S[128 x 64]  = Q[128 x 576] . K[64 x 576]^T   (36 x M128 N64 K16, in
 //           two issue groups; the first K-steps read Q from tensor memory)
 //   softmax two warps per 32-row lane quarter, one per half of the tile's
 //           columns: tcgen05.ld of S, causal/length mask, row max shared through
 //           an mbarrier exchange, running max in log2 units with a lazy rescale
-//           (only when the max grows by more than 8, so P <= 2^8), P -> the two
-//           stage blocks only QK reads (swizzled)
-//   MMA     O[128 x 256] += P[128 x 64] . V[64 x 256]     (4 x M128 N256 K16)
-//           V is the same smem tile read as an MN-major operand; PV(T-1) is
-//           slipped between the QK groups of tile T as soon as P(T-1) is ready
+//           (only when the max grows by more than 8, so P <= 2^8), P (fp16) -> the
+//           two stage blocks only QK reads (swizzled)
+//   MMA     O[128 x 256] += P[128 x 64] . V[64 x 256]     (4 x M128 N256 K16,
+//           issued by a warp of their own); V is the same stage read as an
+//           MN-major operand
 // Per work item: Q arrives by TMA (its tensor-memory part staged through the Q
 // region of shared memory); the epilogue writes O / l to the bf16 partial
 // buffer by TMA stores and the log2-sum-exp to the partial LSE; the combine
 // kernel merges splits and applies W_UV.
 //
-// Tensor memory columns: O [0,256), S [256,256+64*kSBufs), Q after S.
-// Roles: warp 0 = TMA producer (+ L2 prefetch, + zeroing of a partial tile's
-// slots past the end); warp 1 = TMEM owner, its lane 0 runs the MMA loop; warps
-// 2,3 (+12..15 for INT2) = dequantisers; warps 4..11 = Q loads, softmax,
-// correction and epilogue (warp w reads TMEM lanes 32*(w%4)..+31). All waits are
+// Tensor memory columns: O [0,256), S [256,320), Q after S.
+// Roles: warp 0 = raw-block copies (+ L2 prefetch); warp 1 = TMEM owner, its lane 0
+// issues the score MMAs; warps 2, 3, 12..17 = dequantisers; warps 4..11 = Q loads,
+// softmax, correction and epilogue (warp w reads TMEM lanes 32*(w%4)..+31); warp 18,
+// lane 0, the PV MMAs. All waits are
 // bounded: a wait that gives up records FLAG_TIMEOUT and the CTA winds down
 // without trapping.
 #include "mla_internal.cuh"
@@ -48,35 +49,21 @@
 namespace mla {
 namespace tc {
 
-// Threads per CTA: warps 0..3 control (producer, MMA, two dequantisers), 4..11
-// softmax; the INT2 kind adds dequantising warps 12..17.
-// PV MMAs from a warp of their own (the score MMAs' issuer then never holds them back)
-#ifndef MLA_SPLIT_PV
-#define MLA_SPLIT_PV 1
-#endif
-constexpr bool kSplitPv = MLA_SPLIT_PV != 0;
-template <int KIND> constexpr int threads_of() { return is_int2(KIND) ? (kSplitPv ? 608 : 576) : 384; }
-// the PV issuer: warp 2 (idle in the bf16 kind), warp 18 for the INT2 kinds
-template <int KIND> __host__ __device__ constexpr int pv_warp() { return is_int2(KIND) ? 18 : 2; }
+// Threads per CTA: warp 0 producer, 1 score MMAs, 2, 3 and 12..17 dequantisers,
+// 4..11 softmax, 18 PV MMAs (from a warp of their own, the score MMAs' issuer never
+// holds them back).
+constexpr int kThreads = 608;
+constexpr int kPvWarp = 18;
 constexpr int kTile = 64;             // tokens per tile == cache block size
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kD = 576;               // r + d_R
 constexpr int kKvBlocks = 9;          // 64-dim column blocks per token row
 constexpr int kStages = 2;
 constexpr uint32_t kColO = 0, kColS = 256;
-// Tensor-memory layout per cache kind. bf16: two S buffers (QK of the next tile
-// does not wait for the softmax of this one), Q dims 0..255 in TMEM, 256..575 in
-// smem. INT2 (whose raw stage needs shared memory): one S buffer, Q dims 0..383
-// in TMEM, 384..575 in smem.
-template <int KIND> struct Layout;
-template <> struct Layout<MLA_KV_BF16> {
-    static constexpr int kSBufs = 2, kQTmemBlocks = 4, kQSmemBlocks = 5;
-};
-template <> struct Layout<MLA_KV_INT2_ROT> {
-    static constexpr int kSBufs = 1, kQTmemBlocks = 6, kQSmemBlocks = 3;
-};
-template <> struct Layout<MLA_KV_INT2_ROT_QR> : Layout<MLA_KV_INT2_ROT> {};
-constexpr int kMaxQSmemBlocks = 5;
+// Tensor-memory layout: one S buffer, Q dims 0..383 in TMEM, 384..575 in smem (the
+// raw stages take the rest of the shared memory).
+constexpr int kSBufs = 1, kQTmemBlocks = 6, kQSmemBlocks = 3;
+constexpr int kMaxQSmemBlocks = 5;    // the Q region's size (the raw stages sit in its last two blocks)
 constexpr int kSoftmaxThreads = 256;  // warps 4..11: two warps per 32-row lane quarter
 
 constexpr uint32_t kKvBlockBytes = kTile * 128;                     // 8 KB
@@ -115,8 +102,7 @@ __host__ __device__ constexpr uint32_t p_block(int half) { return half ? 0u : 4u
 constexpr int kDequantWarps = 8;
 constexpr int kDequantThreads = 32 * kDequantWarps;
 constexpr uint32_t kEpiBoxBytes = 32 * 128;   // epilogue box: [32 rows x 64 dims] bf16
-// QK K-steps in two issue groups: [0,16) (Q from tensor memory in the bf16 kind)
-// and [16,36). Every group boundary costs the MMA warp a warp sync and a barrier
+// QK K-steps in two issue groups: [0,16) (Q from tensor memory) and [16,36). Every group boundary costs the MMA warp a warp sync and a barrier
 // probe; with more, finer groups the decode ran slower.
 constexpr int kQkGroups = 2;
 __host__ __device__ constexpr int grp_start(int grp) {
@@ -175,7 +161,7 @@ __device__ unsigned long long g_cta_wait[4096];   // after the grid dependency w
 //         expanded (the last dequantising warp), 31 P complete (MMA)
 
 struct Bars {
-    uint64_t full[kStages];       // bf16: tile landed; INT2: stage expanded
+    uint64_t full[kStages];       // stage expanded (and its rope block landed)
     uint64_t empty[kStages];
     uint64_t s_full[2];
     uint64_t s_free[2];
@@ -189,7 +175,6 @@ struct Bars {
     uint64_t pv_fin;          // the PV issuer's MMAs are complete
     uint64_t xchg_full[4];    // lane quarter q: both halves of its rows wrote their value
     uint64_t xchg_read[4];    // lane quarter q: both halves read the other's value
-    uint64_t tail_done[kStages];  // bf16: the producer zeroed a partial tile's slots past the end
     uint64_t raw_full[2];     // INT2: raw block landed (raw stage T % 2)
     uint64_t raw_empty[2];    // INT2: raw block read by every dequantising thread
     uint64_t rope_full[kStages];  // INT2_ROT: the bf16 rope block landed in the operand stage
@@ -227,9 +212,6 @@ __device__ __forceinline__ int block_of(const DecodeParams &p, int b, int lb) {
 #ifndef MLA_PREFETCH_AHEAD
 #define MLA_PREFETCH_AHEAD 2
 #endif
-#ifndef MLA_PV_SLIP
-#define MLA_PV_SLIP 1
-#endif
 constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2 ahead of the TMA loads
 
 // PV(Tp): O[128 x 256] += P(Tp) . V(Tp) from tile Tp's stage (4 x M128 N256 K16; P in
@@ -238,7 +220,6 @@ constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;   // tiles prefetched into L2
 template <int KIND>
 __device__ __forceinline__ bool issue_pv(Bars *bars, uint8_t *smem, int half, const TcParams &tp, uint32_t d_o, int Tp,
                                          bool first_of_item, int32_t *status) {
-    constexpr bool kInt2 = is_int2(KIND);
     const int pb = Tp & 1;
     if (!mbar_wait(&bars->p_full[pb], (Tp >> 1) & 1, bars, status)) return false;
     MLA_TRACE_POINT(31, Tp);
@@ -246,8 +227,8 @@ __device__ __forceinline__ bool issue_pv(Bars *bars, uint8_t *smem, int half, co
     const int s = Tp % kStages;
     const uint64_t a0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes + p_block(half) * kKvBlockBytes), 16, 1024);
     const uint64_t b0 = sdesc(smem_u32(smem + kOffStage + s * kStageBytes) + 4 * half * kKvBlockBytes, tp.v_lbo, tp.v_sbo);
-    // INT2 cache: the operands are fp16 (the dequantised latent, P); bf16 otherwise
-    constexpr uint32_t kIdPv = kInt2 ? idesc_f16(128, 256, true) : idesc_bf16(128, 256, true);
+    // the operands are fp16 (the dequantised latent, P)
+    constexpr uint32_t kIdPv = idesc_f16(128, 256, true);
     // descriptor start addresses advance in 16-byte units
     if (first_of_item) mma_ss_k<kIdPv, 0>(d_o, a0, b0);
     else mma_ss_k<kIdPv, 1>(d_o, a0, b0);
@@ -261,16 +242,11 @@ __device__ __forceinline__ bool issue_pv(Bars *bars, uint8_t *smem, int half, co
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(threads_of<KIND>(), 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                  const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap rope_map,
                  const __grid_constant__ CUtensorMap qr_map, const TcParams tp) {
-    constexpr bool kInt2 = is_int2(KIND);
-    constexpr int kPvWarp = pv_warp<KIND>();
     using RW = Raw<KIND>;
-    constexpr int kSBufs = Layout<KIND>::kSBufs;
-    constexpr int kQTmemBlocks = Layout<KIND>::kQTmemBlocks;
-    constexpr int kQSmemBlocks = Layout<KIND>::kQSmemBlocks;
     constexpr uint32_t kColQ = kColS + 64 * kSBufs;
     constexpr int kQRounds = (kQTmemBlocks + kQSmemBlocks - 1) / kQSmemBlocks;   // staging rounds of the TMEM part
     constexpr int kEpiBoxes = (int)((kQSmemBlocks * kQBlockBytes) / (8 * kEpiBoxBytes));   // per warp at a time
@@ -295,9 +271,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->full[s], kInt2 ? kDequantThreads : 1);
+            mbar_init(&bars->full[s], kDequantThreads);
             mbar_init(&bars->empty[s], 1);
-            mbar_init(&bars->tail_done[s], 1);
             mbar_init(&bars->rope_full[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -350,10 +325,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 
     if (warp == 0) {
         // ================================================= producer (+ L2 prefetch)
-        // bf16 cache: the warp runs converged; lane 0 waits and arms the stage
-        // barrier, lanes 0..8 each issue one of the tile's nine TMA boxes.
-        // INT2 cache: lanes 0 and 1 copy the block's codes and scale/zero pairs into
-        // a raw stage for the dequantising warps.
+        // Lanes 0 and 1 copy the block's codes and scale/zero pairs into a raw stage
+        // for the dequantising warps.
         const bool prefetcher = kPrefetchAhead > 0 && half == 0 && g == 0;
         int pi = i0, pt = 0, ahead = 0;        // L2 prefetch cursor, kPrefetchAhead tiles ahead
         auto advance_prefetch = [&]() {
@@ -363,16 +336,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 if (pt >= nt) { ++pi; pt = 0; continue; }
                 const int blk = block_of(p, it.b, it.t0 / kTile + pt);
                 if (blk >= 0) {
-                    if (kInt2) {
-                        prefetch_l2(p.codes + (size_t)blk * RW::kCodes, RW::kCodes);
-                        prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz);
-                        if (RW::kRopeTma)
-                            prefetch_l2((const uint8_t *)p.rope + (size_t)blk * kKvBlockBytes, kKvBlockBytes);
-                    } else {
-                        // the block's rows (index keys included: one contiguous range)
-                        prefetch_l2((const __nv_bfloat16 *)p.latent + (size_t)blk * kTile * p.s.E(),
-                                    (uint32_t)kTile * p.s.E() * 2);
-                    }
+                    prefetch_l2(p.codes + (size_t)blk * RW::kCodes, RW::kCodes);
+                    prefetch_l2((const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz);
+                    if (RW::kRopeTma)
+                        prefetch_l2((const uint8_t *)p.rope + (size_t)blk * kKvBlockBytes, kKvBlockBytes);
                 }
                 ++pt;
                 ++ahead;
@@ -392,7 +359,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     if (lane == 0) raise_flag(p.status, FLAG_BAD_BLOCK);
                     blk = 0;
                 }
-                if (kInt2) {
+                {
                     // raw stage T % 2 is free once every dequantising thread read tile T - 2
                     const int rs = T & 1;
                     if (T >= 2 &&
@@ -408,38 +375,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         bulk_load(raw + RW::kCodes, (const uint8_t *)p.scale_zero + (size_t)blk * RW::kSz, RW::kSz,
                                   &bars->raw_full[rs]);
                     if (lane == 0) MLA_TRACE_POINT(24, T);
-                } else {
-                    const int s = T % kStages;
-                    if (T >= kStages &&
-                        !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ((T - kStages) / kStages) & 1, bars, p.status))) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) MLA_TRACE_POINT(6, T);
-                    uint8_t *stage = smem + kOffStage + s * kStageBytes;
-                    if (lane == 0) mbar_expect_tx(&bars->full[s], kStageBytes);
-                    __syncwarp();
-                    if (lane < kKvBlocks)
-                        tma_load_2d(stage + lane * kKvBlockBytes, &kv_map, lane * 64, blk * kTile, &bars->full[s]);
-                    // a sequence's final partial block: once it has landed, zero the slots
-                    // past the end so that P = 0 never meets stale (possibly non-finite)
-                    // cache bytes; the MMA thread waits for this on partial tiles only
-                    const int valid = min(kTile, L - (it.t0 + t * kTile));
-                    if (valid < kTile) {
-                        if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status))) {
-                            ok = false;
-                            ++T;                   // this tile's boxes are in flight: drained below
-                            break;
-                        }
-                        const int jobs = (kTile - valid) * kKvBlocks * 8;
-                        for (int jb = lane; jb < jobs; jb += 32) {
-                            const int rr = valid + jb / (kKvBlocks * 8), rem = jb % (kKvBlocks * 8);
-                            *(uint4 *)(stage + (rem >> 3) * kKvBlockBytes + sw128(rr, rem & 7)) = make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars->tail_done[s]);
-                    }
                 }
                 if (lane == 0) {                 // L2 prefetch after this tile's own loads
                     MLA_TRACE_POINT(0, T);
@@ -449,15 +384,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             }
         }
         // drain: never leave a copy in flight into this CTA's shared memory
-        if (kInt2) {
-            for (int u = T - 2; u < T; ++u)
-                if (u >= 0) mbar_drain(&bars->raw_full[u & 1], (u >> 1) & 1);
-        } else {
-            for (int u = T - kStages; u < T; ++u)
-                if (u >= 0) mbar_drain(&bars->full[u % kStages], (u / kStages) & 1);
-        }
+        for (int u = T - 2; u < T; ++u)
+            if (u >= 0) mbar_drain(&bars->raw_full[u & 1], (u >> 1) & 1);
         __syncwarp();
-    } else if (kInt2 && (warp == 2 || warp == 3 || (warp >= 12 && warp < 12 + kDequantWarps - 2))) {
+    } else if (warp == 2 || warp == 3 || (warp >= 12 && warp < 12 + kDequantWarps - 2)) {
         // ================================================= INT2 expansion into the stage
         // value = code * scale + zero, rounded once to fp16 (the MMA operand type of
         // this cache kind), written in the 128B-swizzled layout the MMAs
@@ -590,7 +520,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         }
         // an aborted pass never leaves its rope copy in flight
         if (rope_pending >= 0) mbar_drain(&bars->rope_full[rope_pending % kStages], (rope_pending / kStages) & 1);
-    } else if (kSplitPv && warp == kPvWarp) {
+    } else if (warp == kPvWarp) {
         // ================================================= PV issuer: lane 0 issues
         // O += P(T) . V(T) for every tile in order as soon as the softmax has stored
         // P(T), so that the stage is released without waiting for the score MMAs of
@@ -611,43 +541,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ================================================= MMA issuer: lane 0 alone runs
-        // the loop (plain bounded waits, no warp-wide votes or syncs per tile); with a
-        // PV issuer warp, the score MMAs alone
+        // ================================================= score MMAs: lane 0 alone runs
+        // the loop (plain bounded waits, no warp-wide votes or syncs per tile)
         if (lane == 0) {
-            const uint32_t d_o = tmem + kColO;
             bool ok = true;
             int T = 0;
-            uint32_t tail_par = 0;                 // bit s: parity of the partial tiles seen in stage s
-            auto issue_pv_here = [&](int Tp, bool first_of_item) -> bool {
-                return issue_pv<KIND>(bars, smem, half, tp, d_o, Tp, first_of_item, p.status);
-            };
             int item_no = 0;
             for (int i = i0; i < i1 && ok; ++i, ++item_no) {
                 const WorkItem it = p.work[i];
-                const int L = p.seq_lens[it.b];
                 const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
                 if (!mbar_wait(&bars->q_tmem, item_no & 1, bars, p.status)) { ok = false; break; }
                 for (int t = 0; t < nt; ++t, ++T) {
                     const int s = T % kStages;
-                    // Wait for this tile's stage; meanwhile issue the previous tile's PV as
-                    // soon as its P is ready, so that its stage is released early.
-                    bool pv_early = false;
-                    if (!kSplitPv && t > 0) {
-                        const int pbp = (T - 1) & 1;
-                        int st = 0;                  // 1 = stage landed, 2 = P ready
-                        const unsigned long long tw0 = globaltimer();
-                        for (uint32_t it2 = 0;; ++it2) {
-                            if (mbar_test(&bars->p_full[pbp], ((T - 1) >> 1) & 1)) { st = 2; break; }
-                            if (mbar_test(&bars->full[s], (T / kStages) & 1)) { st = 1; break; }
-                            if ((it2 & 63u) == 63u && (aborted(bars) || globaltimer() - tw0 > kTimeoutNs)) break;
-                            __nanosleep(32);         // leave issue slots to the sub-partition's other warps
-                        }
-                        if (st == 2) {
-                            if (!issue_pv_here(T - 1, t == 1)) { ok = false; break; }
-                            pv_early = true;
-                        }
-                    }
                     if (!mbar_wait(&bars->full[s], (T / kStages) & 1, bars, p.status)) { ok = false; break; }
                     MLA_TRACE_POINT(1, T);
                     // the S buffer this QK writes was read out by the softmax kSBufs tiles ago
@@ -657,16 +562,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                         break;
                     }
                     MLA_TRACE_POINT(16, T);
-                    // a partial tile: the producer zeroes its slots past the end first
-                    if (!kInt2 && min(kTile, L - (it.t0 + t * kTile)) < kTile) {
-                        if (!mbar_wait(&bars->tail_done[s], (tail_par >> s) & 1u, bars, p.status)) { ok = false; break; }
-                        tail_par ^= 1u << s;
-                    }
-                    // QK(T) in kQkGroups issue groups. PV(T-1) of the same item is
-                    // slipped in between groups as soon as its P is ready, so that the
-                    // stage it reads is released early; otherwise it follows QK(T).
-                    bool pv_pending = !kSplitPv && t > 0 && !pv_early;
-                    const int pb_prev = (T - 1) & 1;
+                    // QK(T) in kQkGroups issue groups (the dequantising warps zero a
+                    // partial tile's slots past the end before they complete full[s])
                     MLA_TRACE_POINT(20, T);
                     tc_fence_after();
                     MLA_TRACE_POINT(21, T);
@@ -675,7 +572,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                     const uint32_t qt = tmem + kColQ;
                     const uint32_t d_s = tmem + kColS + 64 * (T % kSBufs);
                     MLA_TRACE_POINT(22, T);
-                    constexpr uint32_t kIdQk = kInt2 ? idesc_f16(128, 64, false) : idesc_bf16(128, 64, false);
+                    constexpr uint32_t kIdQk = idesc_f16(128, 64, false);
 #pragma unroll
                     for (int grp = 0; grp < kQkGroups; ++grp) {
                         // the item's first tile: its shared-memory Q part may still be landing
@@ -709,18 +606,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                             }
                         }
                         MLA_TRACE_POINT(10 + grp, T);
-                        if (MLA_PV_SLIP && pv_pending && grp < kQkGroups - 1 &&
-                            mbar_test(&bars->p_full[pb_prev], ((T - 1) >> 1) & 1)) {
-                            if (!issue_pv_here(T - 1, t == 1)) { ok = false; break; }
-                            pv_pending = false;
-                        }
                     }
                     if (!ok) break;
                     mma_commit(&bars->s_full[T % kSBufs]);
                     MLA_TRACE_POINT(2, T);
-                    if (pv_pending && !issue_pv_here(T - 1, t == 1)) { ok = false; break; }
                 }
-                if (!kSplitPv && ok && nt > 0 && !issue_pv_here(T - 1, nt == 1)) ok = false;
             }
             mma_commit(&bars->mma_fin);
             mbar_wait(&bars->mma_fin, 0, bars, p.status);
@@ -899,13 +789,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
                 for (int j = 0; j < 16; ++j) {
                     const float a = ex2(fmaf(__uint_as_float(sv[2 * j]), cs, nmb));
                     const float c = ex2(fmaf(__uint_as_float(sv[2 * j + 1]), cs, nmb));
-                    if (kInt2) {
-                        const __half2 h = __floats2half2_rn(a, c);
-                        pk[j] = *(const uint32_t *)&h;
-                    } else {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
-                        pk[j] = *(const uint32_t *)&h;
-                    }
+                    const __half2 h = __floats2half2_rn(a, c);     // P: fp16, the PV operand type
+                    pk[j] = *(const uint32_t *)&h;
                     sum0 += a;             // fp32 row sum: the LSE does not see the rounding of P
                     sum1 += c;
                 }
@@ -1094,25 +979,16 @@ bool tc_shape_supported(const ShapeArgs &s) {
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
-    // bf16 cache with several query rows per sequence (verify, prefill chunks): pairs of
-    // CTAs that take turns computing the scores (mla_pair.cu); one row per sequence
-    // (decode) measured faster on the kernel below, whose CTAs both score every tile
-    if (p.s.kind == MLA_KV_BF16 && p.q_len > 1) return launch_decode_pair(p, max_work, st);
-    // one row per sequence: two cache blocks per score MMA (mla_wide.cu)
-    if (p.s.kind == MLA_KV_BF16 && kDecodeWide) return launch_decode_wide(p, max_work, st);
+    // the bf16 cache: two cache blocks per score MMA (mla_wide.cu)
+    if (p.s.kind == MLA_KV_BF16) return launch_decode_wide(p, max_work, st);
     tc::TcParams tp;
     tp.p = p;
     tp.row_tiles = (p.q_len * p.s.H + tc::kRows - 1) / tc::kRows;
     // MN-major V operand: 64-dim atoms 8 KB apart, 8-token groups 1 KB apart.
     tp.v_lbo = tc::kKvBlockBytes;
     tp.v_sbo = 1024;
-    CUtensorMap kv_map, q_map, o_map, rope_map;
-    memset(&kv_map, 0, sizeof kv_map);
+    CUtensorMap q_map, o_map, rope_map;
     memset(&rope_map, 0, sizeof rope_map);
-    const bool int2 = is_int2(p.s.kind);
-    if (!int2 && !tc::make_map(&kv_map, p.latent, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile,
-                               CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)p.s.E()))
-        return cudaErrorInvalidValue;
     // INT2_ROT: the caller's bf16 query, read for its rope block only
     CUtensorMap qr_map;
     memset(&qr_map, 0, sizeof qr_map);
@@ -1124,20 +1000,17 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int32_t max_work, cudaStream
         !tc::make_map(&rope_map, p.rope, (uint64_t)p.s.num_blocks * p.s.bs, tc::kTile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       (uint64_t)p.s.dR, (uint64_t)p.s.dR))
         return cudaErrorInvalidValue;
-    // the query: bf16 as given, or the fp16 rotated query of the INT2 cache
+    // the fp16 rotated query
     const int rows_seq = p.q_len * p.s.H;
-    if (!tc::make_map(&q_map, p.q, (uint64_t)p.B * rows_seq, tc::kRows,
-                      int2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+    if (!tc::make_map(&q_map, p.q, (uint64_t)p.B * rows_seq, tc::kRows, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return cudaErrorInvalidValue;
     if (!tc::make_out_map(&o_map, p.part_o, p.s.r, rows_seq, max_work)) return cudaErrorInvalidValue;
     auto kern = p.s.kind == MLA_KV_INT2_ROT_QR ? tc::decode_tc_kernel<MLA_KV_INT2_ROT_QR>
-                : int2                        ? tc::decode_tc_kernel<MLA_KV_INT2_ROT>
-                                              : tc::decode_tc_kernel<MLA_KV_BF16>;
+                                              : tc::decode_tc_kernel<MLA_KV_INT2_ROT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2, tp.row_tiles, p.streams);
-    const int threads = int2 ? tc::threads_of<MLA_KV_INT2_ROT>() : tc::threads_of<MLA_KV_BF16>();
-    return launch_pdl(kern, grid, dim3(threads), tc::kSmemBytes, st, kv_map, q_map, o_map, rope_map, qr_map, tp);
+    return launch_pdl(kern, grid, dim3(tc::kThreads), tc::kSmemBytes, st, q_map, o_map, rope_map, qr_map, tp);
 }
 
 }  // namespace mla
