@@ -350,7 +350,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         for (int i = i0; i < i1 && ok; ++i) {
             const WorkItem it = p.work[i];
             const int nt = (it.t1 - it.t0 + kTile - 1) / kTile;
-            const int L = p.seq_lens[it.b];
             int next_blk = block_of(p, it.b, it.t0 / kTile);     // loaded one tile ahead
             for (int t = 0; t < nt; ++t, ++T) {
                 int blk = next_blk;

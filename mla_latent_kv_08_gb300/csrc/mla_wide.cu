@@ -99,6 +99,8 @@ __device__ __forceinline__ int score_only_block(int half, int k) { return k < 4 
 #endif
 constexpr int kTraceSteps = 64;
 __device__ long long g_wtrace[12][kTraceSteps];
+// per CTA (globaltimer): entry, after the grid dependency wait, end
+__device__ unsigned long long g_wcta[2048][3];
 #define WTRACE(ev, step)                                                                                          \
     do {                                                                                                          \
         if (blockIdx.x == MLA_TRACE_HALF && blockIdx.y == 0 && blockIdx.z == MLA_TRACE_STREAM && (step) < kTraceSteps) \
@@ -168,6 +170,10 @@ decode_wide_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
     Bars *bars = (Bars *)(smem + kOffBar);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) WTRACE(11, 0);
+#ifdef MLA_TRACE
+    const unsigned cta_id = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    if (tid == 0 && cta_id < 2048) g_wcta[cta_id][0] = globaltimer();
+#endif
 
     if (tid == 0) {
         mbar_init(&bars->full_a, 1);
@@ -204,6 +210,9 @@ decode_wide_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
     const uint32_t tmem = bars->tmem_base;
     // the set-up above overlaps the planner; its schedule is read only from here on
     pdl_wait();
+#ifdef MLA_TRACE
+    if (tid == 0 && cta_id < 2048) g_wcta[cta_id][1] = globaltimer();
+#endif
     const int i0 = p.stream_start[stream], i1 = p.stream_start[stream + 1];
     if (i0 >= i1) {                          // no work for this stream (CTA-uniform)
         if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
@@ -635,6 +644,9 @@ decode_wide_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
+#ifdef MLA_TRACE
+    if (tid == 0 && cta_id < 2048) g_wcta[cta_id][2] = globaltimer();
+#endif
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
@@ -710,5 +722,8 @@ cudaError_t launch_decode_wide(const DecodeParams &p, int32_t max_work, cudaStre
 #ifdef MLA_TRACE
 extern "C" int mla_wide_trace_read(long long *events) {
     return (int)cudaMemcpyFromSymbol(events, mla::wide::g_wtrace, sizeof(mla::wide::g_wtrace));
+}
+extern "C" int mla_wide_cta_read(unsigned long long *times) {
+    return (int)cudaMemcpyFromSymbol(times, mla::wide::g_wcta, sizeof(mla::wide::g_wcta));
 }
 #endif
