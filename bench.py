@@ -363,9 +363,11 @@ def run_gb300(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # one step: this step's new token of every sequence appended, then the decode, in
+    # one call (mla_append_decode: the copy rides on the planner's launch)
     def step(qq=q, cc=new_c, rr=new_r):
-        mla.mla_latent_append(cache, bt, start, cu1, cc, rr, stream=stream)
-        mla.mla_decode(cache, bt, seq_lens, qq, W_UV, w.scale, out, lse, ws, stream=stream)
+        mla.mla_append_decode(cache, bt, start, cu1, cc, rr, seq_lens, qq, W_UV, w.scale, out, lse, ws,
+                              stream=stream)
 
     # clocks are sampled from the warm-up on, through every leg; each leg's window is
     # summarised on its own
@@ -446,8 +448,8 @@ def run_gb300(args):
 
         def e2e_step(st):
             din.copy_(hin, non_blocking=True)
-            mla.mla_latent_append(cache, bt, start, cu1, c_d, r_d, stream=st)
-            mla.mla_decode(cache, bt, seq_lens, q_d, W_UV, w.scale, out_d, lse_d, ws, stream=st)
+            mla.mla_append_decode(cache, bt, start, cu1, c_d, r_d, seq_lens, q_d, W_UV, w.scale, out_d, lse_d, ws,
+                                  stream=st)
             hres.copy_(dres, non_blocking=True)
 
         # The whole step (copies from and to pinned host memory, append, decode) is
@@ -521,8 +523,8 @@ def run_gb300(args):
                     cstream.wait_stream(side)           # fork the copy branch off the step
                     upload(nxt, cstream)
                     qv, cv, rv = cur[1]
-                    mla.mla_latent_append(cache, bt, start, cu1, cv, rv, stream=side)
-                    mla.mla_decode(cache, bt, seq_lens, qv, W_UV, w.scale, out_d, lse_d, ws, stream=side)
+                    mla.mla_append_decode(cache, bt, start, cu1, cv, rv, seq_lens, qv, W_UV, w.scale, out_d, lse_d,
+                                          ws, stream=side)
                     hres.copy_(dres, non_blocking=True)
                     side.wait_stream(cstream)           # join: the next inputs have landed
 

@@ -196,6 +196,29 @@ mla_status mla_decode(const mla_shape *shape, const mla_cache *cache,
                       const void *W_UV, const float *R, float scale, void *out,
                       float *lse, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Append then decode in one call: the same work and the same results as
+ * mla_latent_append(shape, cache, block_table, max_blocks_per_seq, B, start_pos,
+ * cu_new, num_new, c_kv, k_rope, R, clip, append_status, stream) followed by
+ * mla_decode(shape, cache, block_table, max_blocks_per_seq, seq_lens, B, q, W_UV,
+ * R, scale, out, lse, workspace, workspace_bytes, stream), every argument meaning
+ * what it means there (seq_lens counts the appended tokens). For the bf16 and fp32
+ * kinds the new tokens are copied by the launch that plans the decode, so the
+ * copy adds no launch of its own to the step; for the INT2 kinds the append runs
+ * as its own kernel first. Flags of the append (bad block or position) go to
+ * append_status (may be NULL), those of the decode to the workspace
+ * (mla_get_status). Argument errors of either part are returned before anything
+ * is launched.
+ *   Source: "MLA model support (GLM-5.1 / DeepSeek-style)" (OSCAR issue #10), the
+ *   decode step of a serving loop: each step's new latent rows are cached, then
+ *   the step's query attends over the whole cache. */
+mla_status mla_append_decode(const mla_shape *shape, const mla_cache *cache,
+                             const int32_t *block_table, int32_t max_blocks_per_seq, int32_t B,
+                             const int32_t *start_pos, const int32_t *cu_new, int32_t num_new,
+                             const void *c_kv, const void *k_rope, const float *clip,
+                             int32_t *append_status, const int32_t *seq_lens, const void *q,
+                             const void *W_UV, const float *R, float scale, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
 /* Speculative verify: q_len >= 1 draft rows per sequence, already appended, so
  * row i of sequence b sees positions 0 .. seq_lens[b] - q_len + i. Arguments as
  * mla_decode with q [B, q_len, H, r + d_R], out [B, q_len, H, d_v], lse

@@ -44,7 +44,7 @@ EXPORTED = (
     "mla_workspace_bytes", "mla_latent_append", "mla_decode", "mla_verify", "mla_get_status",
     "mla_read_status_word", "mla_status_string", "mla_resolve_impl", "mla_version",
     "mla_profile_enable", "mla_profile_read", "mla_decode_noalloc", "mla_selftest_wait_timeout",
-    "mla_latent_append_index", "mla_fold_rotation",
+    "mla_latent_append_index", "mla_fold_rotation", "mla_append_decode",
     "mla_calib_covariance", "mla_calib_projection_energy", "mla_calib_eigh", "mla_calib_eigh_weighted",
     "mla_calib_project_abs", "mla_calib_thresholds",
 )
@@ -89,6 +89,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_latent_append_index.argtypes = [sp, cp, vp, i32, i32, vp, vp, i32, vp, vp, vp]
     lib.mla_latent_append_index.restype = i32
     lib.mla_decode.argtypes = [sp, cp, vp, i32, vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.mla_append_decode.argtypes = [sp, cp, vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.mla_append_decode.restype = i32
     lib.mla_decode.restype = i32
     lib.mla_verify.argtypes = [sp, cp, vp, i32, vp, i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
     lib.mla_verify.restype = i32
@@ -271,6 +274,21 @@ def mla_decode(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, 
                           _ptr(W_UV), _ptr(R), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
                           int(workspace.numel() * workspace.element_size()), _stream(stream))
     _check(code, "mla_decode")
+
+
+def mla_append_decode(cache: Cache, block_table, start_pos, cu_new, c_kv, k_rope, seq_lens, q, W_UV,
+                      scale: float, out, lse, workspace, R=None, clip=None, append_status=None, stream=None,
+                      shape: Optional[Shape] = None) -> None:
+    """mla_latent_append of len(c_kv) new tokens, then mla_decode over the cache that
+    holds them, in one call (see include/mla.h)."""
+    lib = load_library()
+    code = lib.mla_append_decode(ctypes.byref((shape or cache.shape).c()), ctypes.byref(cache.c()),
+                                 _ptr(block_table), int(block_table.shape[1]), int(seq_lens.shape[0]),
+                                 _ptr(start_pos), _ptr(cu_new), int(c_kv.shape[0]), _ptr(c_kv), _ptr(k_rope),
+                                 _ptr(clip), _ptr(append_status), _ptr(seq_lens), _ptr(q), _ptr(W_UV), _ptr(R),
+                                 float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                 int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check(code, "mla_append_decode")
 
 
 def mla_verify(cache: Cache, block_table, seq_lens, q, W_UV, scale: float, out, lse, workspace,

@@ -104,6 +104,8 @@ int32_t resolve_impl(const mla_shape *s, int32_t q_len) {
 // to two 128-token steps of the bf16 decode that scores two blocks per MMA).
 constexpr int kItemCostTc = 3;
 constexpr int kItemCostWide = 2;
+// mla_append_decode: new tokens up to this count are copied by the planner's launch
+constexpr int32_t kFusedAppendMax = 4096;
 
 static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t impl) {
     WsLayout w;
@@ -144,10 +146,13 @@ static WsLayout ws_layout(const mla_shape *s, int32_t B, int32_t q_len, int32_t 
     return w;
 }
 
+// `fuse`: the step's new tokens, appended before the attention (mla_append_decode);
+// nullptr for a plain decode or verify. Its arguments are checked by the caller.
 static mla_status run_attention(const mla_shape *s, const mla_cache *cache, const int32_t *block_table,
                                 int32_t max_blocks, const int32_t *seq_lens, int32_t B, int32_t q_len,
                                 const void *q, const void *W_UV, const float *R, float scale, void *out,
-                                float *lse, void *workspace, size_t ws_bytes, void *stream) {
+                                float *lse, void *workspace, size_t ws_bytes, void *stream,
+                                const AppendParams *fuse = nullptr) {
     mla_status st = check_shape(s);
     if (st != MLA_OK) return st;
     if (!cache || !block_table || !seq_lens || !q || !W_UV || !out || !lse || !workspace) return MLA_ERR_INVALID;
@@ -204,7 +209,18 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.part_o = (float *)(ws + w.part_o);
     p.part_lse = (float *)(ws + w.part_lse);
 
-    if (launch_plan(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    // A decode step's few new tokens (bf16 / fp32 cache) are copied by the planner's
+    // launch; otherwise the append runs as its own kernel first.
+    int launches = 0;
+    if (fuse && !int2 && fuse->num_new <= kFusedAppendMax) {
+        if (launch_plan_append(p, w.max_work, *fuse, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    } else {
+        if (fuse) {
+            if (launch_append(*fuse, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+            ++launches;
+        }
+        if (launch_plan(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    }
     const bool tc = impl == MLA_IMPL_TCGEN05;
     if (int2) {
         // the rotated query: fp32 for the CUDA-core kernel; fp16 (the MMA operand type
@@ -262,12 +278,15 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
         c.part_lse = lse2;
         c.R = nullptr;
         if (launch_combine_tc(c, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-        prof_kernels(8);            // plan, R split, q . R, decode, merge, R to fp16, o . R^T, combine
+        launches += 3;              // merge, R to fp16, o . R^T
     } else {
         if ((comb_tc ? launch_combine_tc(c, stream_) : launch_combine(c, stream_)) != cudaSuccess) return MLA_ERR_CUDA;
-        // plan, decode, combine; INT2 adds the query rotation (tensor cores: R split + GEMM)
-        prof_kernels(int2 ? (tc ? 5 : 4) : 3);
     }
+    // plan, decode, combine; INT2 adds the query preparation: the tensor-core rotation
+    // (R split + GEMM), the CUDA-core one, or the conversion of a query given rotated
+    launches += 3;
+    if (int2) launches += (s->flags & MLA_FLAG_Q_ROTATED) ? 1 : (tc ? 2 : 1);
+    prof_kernels(launches);
     return MLA_OK;
 }
 
@@ -284,15 +303,11 @@ size_t mla_workspace_bytes(const mla_shape *shape, int32_t B, int32_t q_len) {
     return ws_layout(shape, B, q_len, impl).total;
 }
 
-mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
-                             int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
-                             const int32_t *cu_new, int32_t num_new, const void *c_kv, const void *k_rope,
-                             const float *R, const float *clip, int32_t *status, void *stream) {
-    mla_status st = check_shape(shape);
-    if (st != MLA_OK) return st;
-    if (!cache || !block_table || !start_pos || !cu_new || B < 1 || max_blocks_per_seq < 1 || num_new < 0)
-        return MLA_ERR_INVALID;
-    if (num_new == 0) return MLA_OK;
+// Checks of mla_latent_append's arguments (num_new > 0) and its kernel parameters.
+static mla_status append_params(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
+                                const int32_t *cu_new, int32_t num_new, const void *c_kv, const void *k_rope,
+                                const float *R, const float *clip, int32_t *status, AppendParams &p) {
     if (!c_kv || !k_rope || !aligned16(c_kv) || !aligned16(k_rope)) return MLA_ERR_INVALID;
     const bool int2 = is_int2(shape->kind);
     if (int2) {
@@ -301,7 +316,6 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, con
     } else {
         if (!cache->latent || !aligned16(cache->latent)) return MLA_ERR_INVALID;
     }
-    AppendParams p;
     memset(&p, 0, sizeof p);
     p.s = shape_args(shape);
     p.B = B;
@@ -319,9 +333,45 @@ mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, con
     p.scale_zero = (__half *)cache->scale_zero;
     p.rope = (__nv_bfloat16 *)cache->rope;
     p.status = status;
+    return MLA_OK;
+}
+
+mla_status mla_latent_append(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                             int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
+                             const int32_t *cu_new, int32_t num_new, const void *c_kv, const void *k_rope,
+                             const float *R, const float *clip, int32_t *status, void *stream) {
+    mla_status st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    if (!cache || !block_table || !start_pos || !cu_new || B < 1 || max_blocks_per_seq < 1 || num_new < 0)
+        return MLA_ERR_INVALID;
+    if (num_new == 0) return MLA_OK;
+    AppendParams p;
+    st = append_params(shape, cache, block_table, max_blocks_per_seq, B, start_pos, cu_new, num_new, c_kv, k_rope,
+                       R, clip, status, p);
+    if (st != MLA_OK) return st;
     if (launch_append(p, (cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
     prof_kernels(1);
     return MLA_OK;
+}
+
+mla_status mla_append_decode(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
+                             int32_t max_blocks_per_seq, int32_t B, const int32_t *start_pos,
+                             const int32_t *cu_new, int32_t num_new, const void *c_kv, const void *k_rope,
+                             const float *clip, int32_t *append_status, const int32_t *seq_lens, const void *q,
+                             const void *W_UV, const float *R, float scale, void *out, float *lse, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    mla_status st = check_shape(shape);
+    if (st != MLA_OK) return st;
+    if (!cache || !block_table || !start_pos || !cu_new || B < 1 || max_blocks_per_seq < 1 || num_new < 0)
+        return MLA_ERR_INVALID;
+    AppendParams a;
+    if (num_new > 0) {
+        st = append_params(shape, cache, block_table, max_blocks_per_seq, B, start_pos, cu_new, num_new, c_kv,
+                           k_rope, R, clip, append_status, a);
+        if (st != MLA_OK) return st;
+    }
+    return run_attention(shape, cache, block_table, max_blocks_per_seq, seq_lens, B, 1, q, W_UV, R, scale, out, lse,
+                         workspace, workspace_bytes, stream, num_new > 0 ? &a : nullptr);
 }
 
 mla_status mla_latent_append_index(const mla_shape *shape, const mla_cache *cache, const int32_t *block_table,
@@ -443,6 +493,6 @@ mla_status mla_fold_rotation(const mla_shape *shape, const float *R, const void 
     return MLA_OK;
 }
 
-int32_t mla_version(void) { return 103; }
+int32_t mla_version(void) { return 104; }
 
 }  // extern "C"

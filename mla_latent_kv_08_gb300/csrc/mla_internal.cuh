@@ -153,6 +153,8 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st);
+// The planner and the bf16 / fp32 copy of a step's new tokens in one launch.
+cudaError_t launch_plan_append(const DecodeParams &p, int32_t max_work, const AppendParams &a, cudaStream_t st);
 // q (bf16) -> fp16 (out_f16) or fp32, n elements, for a query that comes rotated.
 cudaError_t launch_convert_query(const void *q, void *out, size_t n, bool out_f16, cudaStream_t st);
 cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bool out_f16, cudaStream_t st);

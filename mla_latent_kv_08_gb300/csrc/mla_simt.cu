@@ -68,7 +68,7 @@ extern "C" int mla_plan_trace_read(unsigned long long *host) {
     return (int)cudaMemcpyFromSymbol(host, g_plan_time, sizeof g_plan_time);
 }
 #endif
-__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_work) {
+__device__ __forceinline__ void plan_body(const DecodeParams &p, int32_t max_work) {
     __shared__ int s_warp[33];
     __shared__ long long s_tiles;
     // per sequence slot of the current chunk (dynamic shared memory, blockDim slots):
@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_
     if (tid == 0) g_plan_time[2] = ptx_globaltimer();
 #endif
 }
+
+__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int32_t max_work) { plan_body(p, max_work); }
 
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st) {
     // one thread per sequence (whole warps, at most 1024): fewer threads, cheaper barriers
@@ -741,11 +743,9 @@ __device__ __forceinline__ long long locate_slot(const AppendParams &p, int n) {
     return (long long)blk * p.s.bs + pos % p.s.bs;
 }
 
+// New token n into its slot: one warp, 16-byte vectors.
 template <typename T>
-__global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
-    pdl_trigger();
-    pdl_wait();
-    const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+__device__ __forceinline__ void copy_token(const AppendParams &p, int n) {
     const int lane = threadIdx.x & 31;
     if (n >= p.num_new) return;
     long long row = 0;
@@ -759,6 +759,27 @@ __global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
     const uint4 *src_r = (const uint4 *)((const T *)p.k_rope + (size_t)n * dR);
     for (int v = lane; v < r / E; v += 32) dst[v] = src_c[v];
     for (int v = lane; v < dR / E; v += 32) dst[r / E + v] = src_r[v];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
+    pdl_trigger();
+    pdl_wait();
+    copy_token<T>(p, blockIdx.x * 8 + (threadIdx.x >> 5));
+}
+
+// The decode's planner (block 0) and the copy of the step's new tokens (the other
+// blocks, a warp per token) in one launch: both wait for the previous kernel of the
+// stream first, as the two separate kernels do.
+template <typename T>
+__global__ void __launch_bounds__(1024) plan_append_kernel(DecodeParams p, int32_t max_work, AppendParams a) {
+    if (blockIdx.x == 0) {
+        plan_body(p, max_work);
+        return;
+    }
+    pdl_wait();
+    pdl_trigger();
+    copy_token<T>(a, (blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5));
 }
 
 // The extra per-token key (index_dim elements) into elements [r + d_R, E) of each
@@ -953,6 +974,15 @@ cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st) {
     if (p.s.kind == MLA_KV_BF16)
         return launch_pdl(append_index_kernel<__nv_bfloat16>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
     return launch_pdl(append_index_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
+}
+
+cudaError_t launch_plan_append(const DecodeParams &p, int32_t max_work, const AppendParams &a, cudaStream_t st) {
+    const int threads = p.B >= 1024 ? 1024 : ((p.B + 31) / 32) * 32;
+    const int nt = threads > 0 ? threads : 32;
+    const int warps = nt / 32;
+    const int blocks = 1 + (a.num_new + warps - 1) / warps;
+    auto kern = a.s.kind == MLA_KV_FP32 ? plan_append_kernel<float> : plan_append_kernel<__nv_bfloat16>;
+    return launch_pdl(kern, dim3(blocks), dim3(nt), (size_t)nt * 28, st, p, max_work, a);
 }
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {

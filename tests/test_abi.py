@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     import mla_latent_kv_08_gb300 as mla
-    assert mla.mla_version() == 103
+    assert mla.mla_version() == 104
     for code in range(-6, 1):
         assert mla.status_string(code) != "unknown status"
     assert mla.status_string(-99) == "unknown status"
@@ -112,6 +112,10 @@ def test_null_arguments_rejected_before_launch(lib):
     assert rc == mla.MLA_ERR_INVALID
     rc = lib.mla_decode(None, ctypes.byref(cache), None, 4, None, 2, None, None, None,
                         ctypes.c_float(0.1), None, None, None, 0, None)
+    assert rc == mla.MLA_ERR_INVALID
+    # append then decode: either part's missing arguments are refused before any launch
+    rc = lib.mla_append_decode(ctypes.byref(s), ctypes.byref(cache), None, 4, 2, None, None, 5, None, None,
+                               None, None, None, None, None, None, ctypes.c_float(0.1), None, None, None, 0, None)
     assert rc == mla.MLA_ERR_INVALID
     assert lib.mla_get_status(None, None, None) == mla.MLA_ERR_INVALID
 
