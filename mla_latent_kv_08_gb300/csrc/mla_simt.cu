@@ -15,16 +15,17 @@
 namespace mla {
 
 // ============================================================================
-// Planner. The cache of every valid sequence is cut into 64-token tiles (one
-// cache block); the concatenation of all sequences' tiles is split into
-// `streams` contiguous runs of T = ceil(total_tiles / streams) tiles. A work
-// item is the intersection of one sequence with one run, so every stream gets
-// the same number of tiles (the last tile of a sequence may be short) and the
-// schedule has at most streams + B items. Items are listed sequence by
+// Planner. The cache of every valid sequence is cut into units of plan_tile tokens
+// (64: one cache block; 128: the two blocks the bf16 tensor-core kernel scores per
+// MMA); each sequence is also charged item_cost units for its start. The
+// concatenation of all sequences' costs is split into `streams` contiguous runs of
+// equal cost. A work item is the intersection of one sequence with one run, so
+// every stream gets the same cost (the last unit of a sequence may be short) and
+// the schedule has at most streams + B items. Items are listed sequence by
 // sequence, which also lists them stream by stream. One CTA; the schedule lives
 // in the workspace, so no launch needs the lengths on the host.
 // ============================================================================
-constexpr int kPlanTile = 64;
+constexpr int kPlanTile = 64;      // plan_tile when the caller leaves it 0
 
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, at
 // most 1024).
