@@ -262,6 +262,9 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     c.out = out;
     c.lse = lse;
     const bool comb_tc = tc && combine_tc_supported(p.s);
+    // the tensor-core decode kernels release the combine only after their own wait for
+    // the planner, whose split ranges the combine may then read before its wait
+    c.ranges_early = tc ? 1 : 0;
     const bool folded = int2 && (s->flags & MLA_FLAG_WUV_FOLDED);
     if (folded) c.R = nullptr;                 // W_UV already carries R^T
     if (int2 && comb_tc && !folded) {
@@ -273,6 +276,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
             cudaSuccess)
             return MLA_ERR_CUDA;
         c.split_start = ident;
+        c.ranges_early = 0;                    // written by the merge, two kernels back
         c.part_bf16 = 0;                       // o_lat is fp32
         c.part_o = o_lat;
         c.part_lse = lse2;

@@ -101,18 +101,22 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, const CombTcParams 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // ---- merge split partials: warp per row, each lane owns 16 latent dims. Every
+    // row's split range is read first (before the dependency wait when the planner
+    // that wrote them is known to have completed); then a row costs one round trip:
+    // its log2-sum-exps and partials (up to four splits at a time) are loaded together
+    // and merged with a running maximum.
+    int2 *s_range = (int2 *)(smem + kOffBar + 64);   // [kMaxRows] split ranges
+    auto read_ranges = [&]() {
+        if (tid < nrows) {
+            const int b = (row0 + tid) / c.q_len;
+            s_range[tid] = make_int2(c.split_start[b], c.split_start[b + 1]);
+        }
+    };
+    if (c.ranges_early) read_ranges();
     pdl_wait();                      // the split partials are complete from here on
     COMB_TRACE(1);
-
-    // ---- merge split partials: warp per row, each lane owns 16 latent dims. Every
-    // row's split range is read first; then a row costs one round trip: its log2-sum-
-    // exps and partials (up to four splits at a time) are loaded together and merged
-    // with a running maximum.
-    int2 *s_range = (int2 *)(smem + kOffBar + 64);   // [kMaxRows] split ranges
-    if (tid < nrows) {
-        const int b = (row0 + tid) / c.q_len;
-        s_range[tid] = make_int2(c.split_start[b], c.split_start[b + 1]);
-    }
+    if (!c.ranges_early) read_ranges();
     __syncthreads();
     // Rows of 8 or fewer: each row's splits are dealt to wpr = 16 / rows warps (split
     // sb + wpr k to warp sub of the row), each merging its share; the row's warp then

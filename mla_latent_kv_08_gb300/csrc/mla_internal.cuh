@@ -105,6 +105,9 @@ struct CombineParams {
     const int32_t *split_start;
     const void *part_o;
     const float *part_lse;
+    int32_t ranges_early;        // split_start comes from the planner and the kernel before the
+                                 // combine released it only after its own dependency wait, so
+                                 // the planner's writes may be read before the combine's wait
     const float *R;              // INT2: [r, r], else nullptr
     const void *W_UV;            // [H, r, dv]
     void *out;                   // [B, q_len, H, dv]

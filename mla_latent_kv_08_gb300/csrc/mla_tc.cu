@@ -257,7 +257,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     const int half = blockIdx.x;            // 0/1: which 256 latent output dims
     const int g = blockIdx.y;               // query row tile
     const int stream = blockIdx.z;          // work stream (persistent over its items)
-    pdl_trigger();
     const int rows_seq = p.q_len * p.s.H;
 #ifdef MLA_TRACE
     const unsigned cta_id = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
@@ -312,8 +311,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    // the set-up above overlaps the planner; its schedule is read only from here on
+    // the set-up above overlaps the planner; its schedule is read only from here on.
+    // The combine may launch from here: the planner has completed, so the combine can
+    // read the schedule's split ranges before its own wait.
     pdl_wait();
+    pdl_trigger();
 #ifdef MLA_TRACE
     if (threadIdx.x == 0 && cta_id < 4096) g_cta_wait[cta_id] = globaltimer();
 #endif

@@ -162,7 +162,6 @@ decode_wide_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
     const int half = blockIdx.x;             // 0/1: which 256 latent output dims
     const int g = blockIdx.y;                // query row tile
     const int stream = blockIdx.z;           // work stream (persistent over its items)
-    pdl_trigger();
     const int rows_seq = p.q_len * p.s.H;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -208,8 +207,11 @@ decode_wide_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    // the set-up above overlaps the planner; its schedule is read only from here on
+    // the set-up above overlaps the planner; its schedule is read only from here on.
+    // The combine may launch from here: the planner has completed, so the combine can
+    // read the schedule's split ranges before its own wait.
     pdl_wait();
+    pdl_trigger();
 #ifdef MLA_TRACE
     if (tid == 0 && cta_id < 2048) g_wcta[cta_id][1] = globaltimer();
 #endif
