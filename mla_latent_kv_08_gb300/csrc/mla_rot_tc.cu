@@ -59,35 +59,29 @@ __device__ __forceinline__ uint4 pack8_f16(const float *v) {
     return make_uint4(*(const uint32_t *)&h0, *(const uint32_t *)&h1, *(const uint32_t *)&h2, *(const uint32_t *)&h3);
 }
 
-// Y[m, 512 + d] = fp16(X[m, 512 + d]) for the copy_rope dims of rows m0 .. m0 + 127
-// (bf16 X): 16-byte vectors, a thread's loads all issued before its stores.
-__device__ __forceinline__ void copy_rope_f16(const RotParams &rp, int m0, int tid, int nthreads) {
+// Y[m, 512 + d] = fp16(X[m, 512 + d]) for the copy_rope dims of part `part` of `nparts`
+// row ranges of rows m0 .. m0 + 127 (bf16 X): 16-byte vectors.
+__device__ __forceinline__ void copy_rope_f16(const RotParams &rp, int m0, int tid, int nthreads, int part,
+                                              int nparts) {
     if (rp.copy_rope <= 0) return;
     const int vec = rp.copy_rope / 8;            // 8-element vectors per row
-    const int total = kTm * vec;
-    constexpr int kMaxPer = 8;
-    for (int job0 = tid; job0 < total; job0 += kMaxPer * nthreads) {
-    uint4 v[kMaxPer];
-    int at[kMaxPer];
-    int n = 0;
-    for (int job = job0; job < total && n < kMaxPer; job += nthreads) {
-        const int r = job / vec, c = job % vec, m = m0 + r;
-        if (m >= rp.M) continue;
-        v[n] = __ldg((const uint4 *)((const __nv_bfloat16 *)rp.X + (size_t)m * rp.ldx + kK) + c);
-        at[n++] = job;
-    }
-    for (int i = 0; i < n; ++i) {
-        const int r = at[i] / vec, c = at[i] % vec, m = m0 + r;
-        const __nv_bfloat162 *h = (const __nv_bfloat162 *)&v[i];
+    const int rows = (kTm + nparts - 1) / nparts;
+    const int r0 = part * rows;
+    const int total = rows * vec;
+#pragma unroll 4
+    for (int job = tid; job < total; job += nthreads) {
+        const int r = r0 + job / vec, c = job % vec, m = m0 + r;
+        if (r >= kTm || m >= rp.M) continue;
+        const uint4 u = __ldg((const uint4 *)((const __nv_bfloat16 *)rp.X + (size_t)m * rp.ldx + kK) + c);
+        const __nv_bfloat162 *hv = (const __nv_bfloat162 *)&u;
         float f[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 x = __bfloat1622float2(h[e]);
+            const float2 x = __bfloat1622float2(hv[e]);
             f[2 * e] = x.x;
             f[2 * e + 1] = x.y;
         }
         *((uint4 *)((__half *)rp.Y + (size_t)m * rp.ldy + kK) + c) = pack8_f16(f);
-    }
     }
 }
 
@@ -295,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) rot_gemm_kernel(const __grid_cons
         }
     }
     // the query's rope part passes through unrotated (bf16 -> fp16)
-    if (blockIdx.y == 0) copy_rope_f16(rp, m0, tid, kThreads);
+    if (blockIdx.y == 0) copy_rope_f16(rp, m0, tid, kThreads, 0, 1);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -416,8 +410,14 @@ __global__ void __launch_bounds__(kQThreads, 1) qrot_kernel(const __grid_constan
               *(volatile int32_t *)abort_flag == 0;
     ok = __syncthreads_and(ok);
     tc_fence_after();
+    // Epilogue: the fp32 tile -> fp16 rows staged in shared memory (the stages are free:
+    // every MMA has completed and every copy into them landed), then stored as whole
+    // 256-byte row segments; rows 272 bytes apart, so that a warp's staging writes fall
+    // on distinct banks.
+    constexpr int kRowB = kTn * 2 + 16;
+    uint8_t *stg = smem;
     {
-        const int m = m0 + 32 * warp + lane;
+        const int r = 32 * warp + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
         for (int c = 0; c < kTn / 32; ++c) {
             uint32_t v[32];
@@ -425,19 +425,25 @@ __global__ void __launch_bounds__(kQThreads, 1) qrot_kernel(const __grid_constan
                 TMEM_LD32(taddr + 32 * c, v);
                 tmem_wait_ld();
             }
-            if (m >= rp.M) continue;
-            __half *dst = (__half *)rp.Y + (size_t)m * rp.ldy + j0 + 32 * c;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float f[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] = ok ? __uint_as_float(v[8 * q + e]) : CUDART_NAN_F;
-                *(uint4 *)(dst + 8 * q) = pack8_f16(f);
+                *(uint4 *)(stg + r * kRowB + (32 * c + 8 * q) * 2) = pack8_f16(f);
             }
         }
     }
-    // the query's rope part passes through unrotated (bf16 -> fp16)
-    if (blockIdx.y == 0) copy_rope_f16(rp, m0, tid, kQThreads);
+    __syncthreads();
+    constexpr int kVecs = kTn / 8;                  // 16-byte vectors a row segment
+    for (int idx = tid; idx < kTm * kVecs; idx += kQThreads) {
+        const int r = idx / kVecs, cv = idx % kVecs, m = m0 + r;
+        if (m < rp.M)
+            *((uint4 *)((__half *)rp.Y + (size_t)m * rp.ldy + j0) + cv) = *(const uint4 *)(stg + r * kRowB + 16 * cv);
+    }
+    // the query's rope part passes through unrotated (bf16 -> fp16), a quarter of the
+    // rows by each of the row tile's column-tile CTAs
+    copy_rope_f16(rp, m0, tid, kQThreads, blockIdx.y, gridDim.y);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
