@@ -209,19 +209,25 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     p.part_o = (float *)(ws + w.part_o);
     p.part_lse = (float *)(ws + w.part_lse);
 
-    // A decode step's few new tokens (bf16 / fp32 cache) are copied by the planner's
-    // launch; otherwise the append runs as its own kernel first.
-    int launches = 0;
-    if (fuse && !int2 && fuse->num_new <= kFusedAppendMax) {
-        if (launch_plan_append(p, w.max_work, *fuse, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-    } else {
-        if (fuse) {
-            if (launch_append(*fuse, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-            ++launches;
-        }
-        if (launch_plan(p, w.max_work, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-    }
     const bool tc = impl == MLA_IMPL_TCGEN05;
+    // Work that needs nothing from the planner rides on its launch: a decode step's few
+    // new tokens (bf16 / fp32 cache; otherwise the append runs as its own kernel first)
+    // and the split of R for the tensor-core query rotation.
+    int launches = 0;
+    const bool copy_fused = fuse && !int2 && fuse->num_new <= kFusedAppendMax;
+    const bool split_fused = int2 && tc && !(s->flags & MLA_FLAG_Q_ROTATED);
+    if (fuse && !copy_fused) {
+        if (launch_append(*fuse, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+        ++launches;
+    }
+    if (copy_fused || split_fused) {
+        if (launch_plan_prep(p, w.max_work, copy_fused ? fuse : nullptr, split_fused ? R : nullptr,
+                             (__nv_bfloat16 *)(ws + w.rsplit), s->kv_lora_rank * s->kv_lora_rank,
+                             stream_) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    } else if (launch_plan(p, w.max_work, stream_) != cudaSuccess) {
+        return MLA_ERR_CUDA;
+    }
     if (int2) {
         // the rotated query: fp32 for the CUDA-core kernel; fp16 (the MMA operand type
         // of this cache kind) from the tensor-core GEMM for the tensor-core kernel,
@@ -235,7 +241,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
             if (tc) p.q = ws + w.q_prep;
         } else if (tc) {
             if (launch_rot_query(R, (__nv_bfloat16 *)(ws + w.rsplit), q, ws + w.q_prep, B * q_len * s->num_heads,
-                                 s->kv_lora_rank + s->rope_dim, p.status, stream_) != cudaSuccess)
+                                 s->kv_lora_rank + s->rope_dim, p.status, stream_, split_fused) != cudaSuccess)
                 return MLA_ERR_CUDA;
             p.q = ws + w.q_prep;
         } else if (launch_qprep(p, R, ws + w.q_prep, false, stream_) != cudaSuccess) {
@@ -289,7 +295,7 @@ static mla_status run_attention(const mla_shape *s, const mla_cache *cache, cons
     // plan, decode, combine; INT2 adds the query preparation: the tensor-core rotation
     // (R split + GEMM), the CUDA-core one, or the conversion of a query given rotated
     launches += 3;
-    if (int2) launches += (s->flags & MLA_FLAG_Q_ROTATED) ? 1 : (tc ? 2 : 1);
+    if (int2) launches += 1;    // the query rotation (R split by the planner's launch) or conversion
     prof_kernels(launches);
     return MLA_OK;
 }

@@ -156,8 +156,11 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 cudaError_t launch_plan(const DecodeParams &p, int32_t max_work, cudaStream_t st);
-// The planner and the bf16 / fp32 copy of a step's new tokens in one launch.
-cudaError_t launch_plan_append(const DecodeParams &p, int32_t max_work, const AppendParams &a, cudaStream_t st);
+// The planner plus, in the same launch, the bf16 / fp32 copy of a step's new tokens
+// (a; nullptr: none) and the split of R ([r_n] fp32) into bf16 halves at Rsplit and
+// Rsplit + r_n (R nullptr: none).
+cudaError_t launch_plan_prep(const DecodeParams &p, int32_t max_work, const AppendParams *a, const float *R,
+                             __nv_bfloat16 *Rsplit, int32_t r_n, cudaStream_t st);
 // q (bf16) -> fp16 (out_f16) or fp32, n elements, for a query that comes rotated.
 cudaError_t launch_convert_query(const void *q, void *out, size_t n, bool out_f16, cudaStream_t st);
 cudaError_t launch_qprep(const DecodeParams &p, const float *R, void *q_prep, bool out_f16, cudaStream_t st);
@@ -179,7 +182,7 @@ bool rot_tc_supported(const ShapeArgs &s);
 // launch_rot_query writes Rsplit = [bf16(R) ; bf16(R - bf16(R))] ([2][r][r]) first;
 // launch_rot_output writes R16 = fp16(R) ([r][r]) first. Both 16-byte aligned.
 cudaError_t launch_rot_query(const float *R, __nv_bfloat16 *Rsplit, const void *q_bf16, void *q_rot_f16, int rows,
-                             int D, int32_t *status, cudaStream_t st);
+                             int D, int32_t *status, cudaStream_t st, bool split_done = false);
 cudaError_t launch_rot_output(const CombineParams &c, __half *R16, float *o_rot, float *o_lat, float *lse2,
                               int32_t *ident, int32_t *status, cudaStream_t st);
 

@@ -544,12 +544,15 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(CombineParams c, float 
 bool rot_tc_supported(const ShapeArgs &s) { return s.r == rot::kK; }
 
 cudaError_t launch_rot_query(const float *R, __nv_bfloat16 *Rsplit, const void *q_bf16, void *q_rot_f16, int rows,
-                             int D, int32_t *status, cudaStream_t st) {
+                             int D, int32_t *status, cudaStream_t st, bool split_done) {
     const int n = rot::kK * rot::kK;
     __nv_bfloat16 *Rhi = Rsplit, *Rlo = Rsplit + n;
-    rot::r_split_bf16_kernel<<<(n + 255) / 256, 256, 0, st>>>(R, Rhi, Rlo, n);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!split_done) {               // (the planner's launch usually splits R already)
+        rot::r_split_bf16_kernel<<<(n + 255) / 256, 256, 0, st>>>(R, Rhi, Rlo, n);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     auto fn = rot::encode_fn();
     if (!fn) return cudaErrorInvalidValue;
     CUtensorMap qm, hm, lm;

@@ -769,18 +769,39 @@ __global__ void __launch_bounds__(256) append_copy_kernel(AppendParams p) {
     copy_token<T>(p, blockIdx.x * 8 + (threadIdx.x >> 5));
 }
 
-// The decode's planner (block 0) and the copy of the step's new tokens (the other
-// blocks, a warp per token) in one launch: both wait for the previous kernel of the
-// stream first, as the two separate kernels do.
+// Work that needs no result of the planner, done by extra blocks of the planner's
+// launch: the copy of a decode step's new tokens (bf16 / fp32 cache) and the split of
+// the INT2 rotation R into bf16 halves for the query rotation.
+struct PrepParams {
+    AppendParams a;              // a.num_new == 0: no copy
+    int32_t copy_blocks;         // blocks 1 .. copy_blocks copy tokens, a warp per token
+    const float *R;              // nullptr: no split
+    __nv_bfloat16 *Rhi, *Rlo;
+    int32_t r_n;                 // elements of R
+};
+
+// The decode's planner (block 0), then the copy blocks, then the R-split blocks. Every
+// block waits for the previous kernel of the stream first, as separate kernels would.
 template <typename T>
-__global__ void __launch_bounds__(1024) plan_append_kernel(DecodeParams p, int32_t max_work, AppendParams a) {
+__global__ void __launch_bounds__(1024) plan_prep_kernel(DecodeParams p, int32_t max_work, PrepParams pp) {
     if (blockIdx.x == 0) {
         plan_body(p, max_work);
         return;
     }
     pdl_wait();
     pdl_trigger();
-    copy_token<T>(a, (blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5));
+    const int bi = blockIdx.x - 1;
+    if (bi < pp.copy_blocks) {
+        copy_token<T>(pp.a, bi * (blockDim.x >> 5) + (threadIdx.x >> 5));
+        return;
+    }
+    const int nsb = gridDim.x - 1 - pp.copy_blocks;
+    for (int i = (bi - pp.copy_blocks) * blockDim.x + threadIdx.x; i < pp.r_n; i += nsb * blockDim.x) {
+        const float v = pp.R[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        pp.Rhi[i] = hi;
+        pp.Rlo[i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
 }
 
 // The extra per-token key (index_dim elements) into elements [r + d_R, E) of each
@@ -977,13 +998,27 @@ cudaError_t launch_append_index(const AppendParams &p, cudaStream_t st) {
     return launch_pdl(append_index_kernel<float>, dim3((p.num_new + 7) / 8), dim3(256), 0, st, p);
 }
 
-cudaError_t launch_plan_append(const DecodeParams &p, int32_t max_work, const AppendParams &a, cudaStream_t st) {
+cudaError_t launch_plan_prep(const DecodeParams &p, int32_t max_work, const AppendParams *a, const float *R,
+                             __nv_bfloat16 *Rsplit, int32_t r_n, cudaStream_t st) {
     const int threads = p.B >= 1024 ? 1024 : ((p.B + 31) / 32) * 32;
-    const int nt = threads > 0 ? threads : 32;
+    int nt = threads > 0 ? threads : 32;
+    if (R && nt < 128) nt = 128;                 // the split blocks: eight elements a thread or so
+    PrepParams pp;
+    memset(&pp, 0, sizeof pp);
+    if (a) pp.a = *a;
     const int warps = nt / 32;
-    const int blocks = 1 + (a.num_new + warps - 1) / warps;
-    auto kern = a.s.kind == MLA_KV_FP32 ? plan_append_kernel<float> : plan_append_kernel<__nv_bfloat16>;
-    return launch_pdl(kern, dim3(blocks), dim3(nt), (size_t)nt * 28, st, p, max_work, a);
+    pp.copy_blocks = a ? (a->num_new + warps - 1) / warps : 0;
+    int split_blocks = 0;
+    if (R) {
+        pp.R = R;
+        pp.Rhi = Rsplit;
+        pp.Rlo = Rsplit + r_n;
+        pp.r_n = r_n;
+        split_blocks = (r_n + nt * 8 - 1) / (nt * 8);
+    }
+    const dim3 grid(1 + pp.copy_blocks + split_blocks);
+    auto kern = (a && a->s.kind == MLA_KV_FP32) ? plan_prep_kernel<float> : plan_prep_kernel<__nv_bfloat16>;
+    return launch_pdl(kern, grid, dim3(nt), (size_t)nt * 28, st, p, max_work, pp);
 }
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
