@@ -207,6 +207,19 @@ decode_wide_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // Each CTA asks L2 for its share of the query (a call input; only a cache hint),
+    // so that the first work item's query load does not wait on DRAM.
+    if (tid == 0) {
+        const size_t q_bytes = (size_t)p.B * rows_seq * kD * 2;
+        const size_t n_ctas = (size_t)gridDim.x * gridDim.y * gridDim.z;
+        const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const size_t share = ((q_bytes + n_ctas - 1) / n_ctas + 15) & ~(size_t)15;
+        const size_t lo = cta * share;
+        if (lo < q_bytes) {
+            const size_t hi = min(q_bytes, lo + share);
+            prefetch_l2((const uint8_t *)p.q + lo, (uint32_t)((hi - lo) & ~(size_t)15));
+        }
+    }
     // the set-up above overlaps the planner; its schedule is read only from here on.
     // The combine may launch from here: the planner has completed, so the combine can
     // read the schedule's split ranges before its own wait.
