@@ -580,6 +580,66 @@ def test_tensor_core_decode_with_the_generic_combine(gpu_lib):
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+@pytest.mark.parametrize("kind_name,impl_name,q_len",
+                         [("rot", "tcgen05", 2), ("rot", "tcgen05", 5), ("rope", "tcgen05", 3), ("rot", "simt", 3)])
+def test_int2_verify_causal_window(gpu_lib, kind_name, impl_name, q_len):
+    """Speculative verify on the rotated-INT2 caches: q_len draft rows a sequence, row i
+    seeing positions 0 .. L - q_len + i, against the oracle's attention over the
+    dequantised rows. At H = 128 a sequence's rows span several 128-row tiles, and
+    sequence 0 holds exactly q_len tokens, so that its first row sees a single one."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=3, H=128, len_range=(q_len, 700))
+    w.seq_lens[0] = q_len
+    w.latent[0], w.rope[0] = w.latent[0][:q_len], w.rope[0][:q_len]
+    rng = np.random.default_rng(40 + q_len)
+    q = workloads.bf16_round(rng.standard_normal((w.B, q_len, w.H, w.r + w.d_rope)).astype(np.float32))
+    impl = mla.MLA_IMPL_SIMT if impl_name == "simt" else mla.MLA_IMPL_TCGEN05
+    if kind_name == "rot":
+        shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT, impl=impl)
+        cache, st = gu.fill_cache(w, shape, R32, T32)
+    else:
+        KRcal = workloads.bf16_round(rng.standard_normal((8192, 64)).astype(np.float32)).astype(np.float64)
+        TR32 = oint2.rope_thresholds(KRcal).astype(np.float32)
+        shape = gu.shape_for(w, kind=mla.MLA_KV_INT2_ROT_QR, impl=impl)
+        cache, st = gu.fill_cache(w, shape, R32, np.concatenate([T32, TR32]))
+    assert mla.mla_resolve_impl(shape) == impl
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    out, lse, ws = gu.attend(w, shape, cache, q, R=R32, q_len=q_len)
+    assert mla.mla_get_status(ws)[0] == mla.MLA_OK
+    f16 = lambda x: np.asarray(x, np.float64).astype(np.float16).astype(np.float64)   # noqa: E731
+    R64 = R32.astype(np.float64)
+    for b in range(w.B):
+        qb = np.asarray(q[b], np.float64)
+        if kind_name == "rot":
+            codes, sz = oint2.quantize(w.latent[b], R32, T32)
+            K = oint2.decode(codes, sz).astype(np.float64)
+            ro, rl = oint2.attention_rotated(q[b], K, w.rope[b], R32, w.W_UV, w.scale)
+            # the tensor-core kernel's operands: q.R and the dequantised key in fp16, the
+            # rope dims bf16 on both sides as given
+            q_op = np.concatenate([f16(qb[..., :w.r] @ R64), qb[..., w.r:]], axis=-1)
+            C_op, KR_op = f16(K), w.rope[b]
+        else:
+            codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
+            Y = oint2.decode(codes, sz).astype(np.float64)
+            ro, rl = oint2.attention_rope_int2(q[b], Y, R32, w.W_UV, w.scale)
+            q_op = f16(np.concatenate([qb[..., :w.r] @ R64, qb[..., w.r:]], axis=-1))
+            C_op, KR_op = f16(Y[:, :w.r]), f16(Y[:, w.r:])
+        if impl_name == "simt":
+            _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+            continue
+        # Rows whose softmax sits on a few tokens see the fp16 roundings of the rotated
+        # query and of the dequantised key (the tensor-core operand type of these kinds)
+        # with little averaging, as a single token does. The kernel must match the
+        # attention formed from those same operands (in fp64) to the usual bars, and the
+        # definition within twice the LSE bar.
+        _, l_op, o_rot = attention.absorbed(q_op, C_op, KR_op, np.zeros((w.H, w.r, 1)), w.scale, return_latent=True)
+        o_op = np.einsum("qhr,hrv->qhv", o_rot @ R64.T, np.asarray(w.W_UV, np.float64))
+        _check_seq(out, lse, w, b, o_op, l_op, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, 2 * gu.BF16_LSE_TOL)
+
+
 @pytest.mark.parametrize("impl_name,H", [("simt", 32), ("tcgen05", 32), ("tcgen05", 128)])
 def test_int2_rope_codes_append_and_decode(gpu_lib, impl_name, H):
     """INT2_ROT_QR (the rope key quantised as two more INT2 groups): codes and
