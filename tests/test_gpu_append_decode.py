@@ -1,7 +1,8 @@
 """mla_append_decode: appending a step's new tokens and decoding in one call gives the
 results of mla_latent_append followed by mla_decode, bit for bit, on every cache kind
-(the bf16 / fp32 copy runs inside the planner's launch, the INT2 append as its own
-kernel), and reports the append's flags through its own status word."""
+(the bf16 / fp32 copy of up to 4096 tokens runs inside the planner's launch; more
+tokens, and the INT2 append, as a kernel of their own), and reports the append's flags
+through its own status word."""
 import numpy as np
 import pytest
 
@@ -20,15 +21,17 @@ def _int2_setup(B, H, len_range, seed=4):
     return w, R.astype(np.float32), T.astype(np.float32)
 
 
-def _last_tokens(w):
-    """Per sequence: its last cached token (latent, rope) and position L - 1."""
-    lat = [x[-1:] for x in w.latent]
-    rope = [x[-1:] for x in w.rope]
-    return lat, rope, (w.seq_lens - 1).astype(np.int32)
+def _last_tokens(w, k=1):
+    """Per sequence: its last k cached tokens (latent, rope) and their first position."""
+    lat = [x[-k:] for x in w.latent]
+    rope = [x[-k:] for x in w.rope]
+    return lat, rope, (w.seq_lens - k).astype(np.int32)
 
 
-@pytest.mark.parametrize("kind_name", ["bf16", "fp32", "int2"])
-def test_append_decode_matches_append_then_decode(gpu_lib, kind_name):
+# k new tokens a sequence: one (a decode step), three, and 6 x 700 = 4200, past the
+# 4096 tokens that the planner's launch copies (the append then runs as its own kernel)
+@pytest.mark.parametrize("kind_name,k", [("bf16", 1), ("fp32", 1), ("int2", 1), ("bf16", 3), ("bf16", 700)])
+def test_append_decode_matches_append_then_decode(gpu_lib, kind_name, k):
     import mla_latent_kv_08_gb300 as mla
     import torch
     if kind_name == "fp32":
@@ -37,7 +40,7 @@ def test_append_decode_matches_append_then_decode(gpu_lib, kind_name):
         R = T = None
         shape = gu.shape_for(w)
     elif kind_name == "bf16":
-        w = workloads.dsv3(31, B=6, H=128, len_range=(60, 400))
+        w = workloads.dsv3(31, B=6, H=128, len_range=(60, 400) if k < 700 else (800, 1000))
         q = w.q
         R = T = None
         shape = gu.shape_for(w)
@@ -49,7 +52,7 @@ def test_append_decode_matches_append_then_decode(gpu_lib, kind_name):
     # last slot overwritten with zeros, so that only the fused call's copy restores it
     cache_a, st_a = gu.fill_cache(w, shape, R, T)
     cache_b, st_b = gu.fill_cache(w, shape, R, T)
-    lat, rope, pos = _last_tokens(w)
+    lat, rope, pos = _last_tokens(w, k)
     zeros_c = [np.zeros_like(x) for x in lat]
     zeros_r = [np.zeros_like(x) for x in rope]
     gu.append_tokens(cache_b, w, zeros_c, zeros_r, pos, R, T)
@@ -63,7 +66,7 @@ def test_append_decode_matches_append_then_decode(gpu_lib, kind_name):
     lse_b = torch.empty((w.B, 1, w.H), dtype=torch.float32, device="cuda")
     ws_b = mla.alloc_workspace(shape, w.B, 1)
     ast = torch.zeros(1, dtype=torch.int32, device="cuda")
-    cu = np.arange(w.B + 1, dtype=np.int32)
+    cu = (k * np.arange(w.B + 1)).astype(np.int32)
     mla.mla_append_decode(cache_b, gu.dev(w.block_table), gu.dev(pos), gu.dev(cu),
                           gu.dev(np.concatenate(lat).astype(np.float32), dt),
                           gu.dev(np.concatenate(rope).astype(np.float32), dt),
