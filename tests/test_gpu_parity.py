@@ -608,24 +608,8 @@ def test_int2_verify_causal_window(gpu_lib, kind_name, impl_name, q_len):
     assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
     out, lse, ws = gu.attend(w, shape, cache, q, R=R32, q_len=q_len)
     assert mla.mla_get_status(ws)[0] == mla.MLA_OK
-    f16 = lambda x: np.asarray(x, np.float64).astype(np.float16).astype(np.float64)   # noqa: E731
-    R64 = R32.astype(np.float64)
     for b in range(w.B):
-        qb = np.asarray(q[b], np.float64)
-        if kind_name == "rot":
-            codes, sz = oint2.quantize(w.latent[b], R32, T32)
-            K = oint2.decode(codes, sz).astype(np.float64)
-            ro, rl = oint2.attention_rotated(q[b], K, w.rope[b], R32, w.W_UV, w.scale)
-            # the tensor-core kernel's operands: q.R and the dequantised key in fp16, the
-            # rope dims bf16 on both sides as given
-            q_op = np.concatenate([f16(qb[..., :w.r] @ R64), qb[..., w.r:]], axis=-1)
-            C_op, KR_op = f16(K), w.rope[b]
-        else:
-            codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
-            Y = oint2.decode(codes, sz).astype(np.float64)
-            ro, rl = oint2.attention_rope_int2(q[b], Y, R32, w.W_UV, w.scale)
-            q_op = f16(np.concatenate([qb[..., :w.r] @ R64, qb[..., w.r:]], axis=-1))
-            C_op, KR_op = f16(Y[:, :w.r]), f16(Y[:, w.r:])
+        ro, rl, o_op, l_op = _int2_references(w, q[b], b, kind_name, R32, T32, TR32 if kind_name == "rope" else None)
         if impl_name == "simt":
             _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
             continue
@@ -634,10 +618,66 @@ def test_int2_verify_causal_window(gpu_lib, kind_name, impl_name, q_len):
         # with little averaging, as a single token does. The kernel must match the
         # attention formed from those same operands (in fp64) to the usual bars, and the
         # definition within twice the LSE bar.
-        _, l_op, o_rot = attention.absorbed(q_op, C_op, KR_op, np.zeros((w.H, w.r, 1)), w.scale, return_latent=True)
-        o_op = np.einsum("qhr,hrv->qhv", o_rot @ R64.T, np.asarray(w.W_UV, np.float64))
         _check_seq(out, lse, w, b, o_op, l_op, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, 2 * gu.BF16_LSE_TOL)
+
+
+def _int2_references(w, qb, b, kind_name, R32, T32, TR32=None):
+    """Sequence b against the oracle: the definition over the oracle's dequantised codes
+    (ro, rl), and the same attention formed in fp64 from the tensor-core kernel's operands
+    (o_op, l_op): q.R and the dequantised key rounded to fp16 (INT2_ROT's rope dims bf16
+    on both sides as given; INT2_ROT_QR's rope dims fp16 like the rest)."""
+    f16 = lambda x: np.asarray(x, np.float64).astype(np.float16).astype(np.float64)   # noqa: E731
+    R64 = R32.astype(np.float64)
+    q64 = np.asarray(qb, np.float64)
+    if kind_name == "rot":
+        codes, sz = oint2.quantize(w.latent[b], R32, T32)
+        K = oint2.decode(codes, sz).astype(np.float64)
+        ro, rl = oint2.attention_rotated(qb, K, w.rope[b], R32, w.W_UV, w.scale)
+        q_op = np.concatenate([f16(q64[..., :w.r] @ R64), q64[..., w.r:]], axis=-1)
+        C_op, KR_op = f16(K), w.rope[b]
+    else:
+        codes, sz = oint2.quantize_rope_int2(w.latent[b], w.rope[b], R32, T32, TR32)
+        Y = oint2.decode(codes, sz).astype(np.float64)
+        ro, rl = oint2.attention_rope_int2(qb, Y, R32, w.W_UV, w.scale)
+        q_op = f16(np.concatenate([q64[..., :w.r] @ R64, q64[..., w.r:]], axis=-1))
+        C_op, KR_op = f16(Y[:, :w.r]), f16(Y[:, w.r:])
+    _, l_op, o_rot = attention.absorbed(q_op, C_op, KR_op, np.zeros((w.H, w.r, 1)), w.scale, return_latent=True)
+    o_op = np.einsum("qhr,hrv->qhv", o_rot @ R64.T, np.asarray(w.W_UV, np.float64))
+    return ro, rl, o_op, l_op
+
+
+def _rope_thresholds(seed):
+    rng = np.random.default_rng(seed)
+    KRcal = workloads.bf16_round(rng.standard_normal((8192, 64)).astype(np.float32)).astype(np.float64)
+    return oint2.rope_thresholds(KRcal).astype(np.float32)
+
+
+@pytest.mark.parametrize("kind_name", ["rot", "rope"])
+def test_int2_split_count_does_not_change_result(gpu_lib, kind_name):
+    """The rotated-INT2 tensor-core decode with the sequences cut 1, 7 and 200 ways
+    (different work items over the 64-token tiles, merged by the combine): the same LSE
+    to 1e-5 and the same output to the bf16 rounding of the split partials; and sequence
+    0 against the oracle as in the INT2 verify test."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=3, H=64, len_range=(2000, 3000))
+    TR32 = _rope_thresholds(12) if kind_name == "rope" else None
+    kind = mla.MLA_KV_INT2_ROT if kind_name == "rot" else mla.MLA_KV_INT2_ROT_QR
+    T = T32 if kind_name == "rot" else np.concatenate([T32, TR32])
+    res = []
+    for hint in (1, 7, 200):
+        shape = gu.shape_for(w, kind=kind, impl=mla.MLA_IMPL_TCGEN05, splits=hint)
+        cache, st = gu.fill_cache(w, shape, R32, T)
+        torch.cuda.synchronize()
+        assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+        res.append(gu.attend(w, shape, cache, w.q, R=R32)[:2])
+    for o, l in res[1:]:
+        assert np.max(np.abs(l - res[0][1])) < 1e-5
+        assert gu.rel_err(o, res[0][0]) < 8e-3      # bf16 output rounding of near-equal fp32 values
+    ro, rl, o_op, l_op = _int2_references(w, w.q[0], 0, kind_name, R32, T32, TR32)
+    _check_seq(res[2][0], res[2][1], w, 0, o_op, l_op, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+    _check_seq(res[2][0], res[2][1], w, 0, ro, rl, gu.BF16_REL_TOL, 2 * gu.BF16_LSE_TOL)
 
 
 @pytest.mark.parametrize("impl_name,H", [("simt", 32), ("tcgen05", 32), ("tcgen05", 128)])
