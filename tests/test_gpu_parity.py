@@ -384,6 +384,31 @@ def test_bad_block_id_sets_flag_and_nan_rows(gpu_lib):
         _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
 
 
+@pytest.mark.parametrize("kind_name", ["rot", "rope"])
+def test_int2_bad_block_id_sets_flag_and_nan_rows(gpu_lib, kind_name):
+    """The rotated-INT2 tensor-core decode with one out-of-range block id: the flag is
+    raised, that sequence's rows are NaN, and the other sequences match the oracle."""
+    import mla_latent_kv_08_gb300 as mla
+    import torch
+    w, R32, T32 = _int2_setup(B=3, H=16, len_range=(100, 200))
+    TR32 = _rope_thresholds(12) if kind_name == "rope" else None
+    kind = mla.MLA_KV_INT2_ROT if kind_name == "rot" else mla.MLA_KV_INT2_ROT_QR
+    shape = gu.shape_for(w, kind=kind, impl=mla.MLA_IMPL_TCGEN05)
+    cache, st = gu.fill_cache(w, shape, R32, T32 if kind_name == "rot" else np.concatenate([T32, TR32]))
+    torch.cuda.synchronize()
+    assert mla.mla_read_status_word(st)[0] == mla.MLA_OK
+    w.block_table = w.block_table.copy()
+    w.block_table[1, 0] = w.num_blocks + 5          # out of range for decode only
+    out, lse, ws = gu.attend(w, shape, cache, w.q, R=R32)
+    code, flags = mla.mla_get_status(ws)
+    assert code == mla.MLA_ERR_BOUNDS and flags & 1
+    assert np.all(np.isnan(out[1])) and np.all(np.isnan(lse[1]))
+    for b in (0, 2):
+        ro, rl, o_op, l_op = _int2_references(w, w.q[b], b, kind_name, R32, T32, TR32)
+        _check_seq(out, lse, w, b, o_op, l_op, gu.BF16_REL_TOL, gu.BF16_LSE_TOL)
+        _check_seq(out, lse, w, b, ro, rl, gu.BF16_REL_TOL, 2 * gu.BF16_LSE_TOL)
+
+
 def test_bad_length_sets_flag(gpu_lib):
     import mla_latent_kv_08_gb300 as mla
     w = workloads.dsv3(14, B=2, H=16, len_range=(100, 120))
